@@ -1,0 +1,203 @@
+"""CPU oracle for fine-grained FP8 quantisation and the block-scaled FP8 GEMM.
+
+TEST INFRASTRUCTURE ONLY.  The product path never imports this package; only
+``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` use it.  It shares no code with the CUDA library.
+
+The arithmetic lives in ``fp8_oracle.c`` (plain C, binary64 where the method
+leaves precision open; see that file's header for the passages of the
+DeepSeek-V3 Technical Report each step follows).  This module only marshals
+numpy arrays into it.
+
+Conventions: bfloat16 tensors are passed as ``uint16`` numpy arrays holding
+the raw bfloat16 bit patterns; E4M3 codes are ``uint8`` arrays.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+from .build import build as _build, LIB_PATH
+
+_lib = None
+
+BSCALE_BLOCK128 = 0    # sb[N/128][K/128]
+BSCALE_ROW1x128 = 1    # sb[K/128][N]
+BSCALE_BLOCK128_T = 2  # sb[K/128][N/128]
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            _build()
+        lib = ctypes.CDLL(LIB_PATH)
+        P = ctypes.c_void_p
+        I64 = ctypes.c_int64
+        lib.fo_e4m3_encode.restype = ctypes.c_uint8
+        lib.fo_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.fo_e4m3_decode.restype = ctypes.c_double
+        lib.fo_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.fo_e4m3_encode_array.argtypes = [P, I64, P]
+        lib.fo_e4m3_decode_array.argtypes = [P, I64, P]
+        lib.fo_round_f32.argtypes = [P, I64, P]
+        lib.fo_round_bf16.argtypes = [P, I64, P]
+        lib.fo_group_scale.restype = ctypes.c_float
+        lib.fo_group_scale.argtypes = [ctypes.c_float]
+        lib.fo_quant_act_1x128.argtypes = [P, I64, I64, I64, P, I64, P]
+        lib.fo_quant_act_128x1.argtypes = [P, I64, I64, I64, P, P]
+        lib.fo_quant_weight_128x128.argtypes = [P, I64, I64, I64, P, P, P]
+        lib.fo_gemm_blockscaled_rows.argtypes = [
+            P, I64, P, I64, P, I64, P, I64, ctypes.c_int, I64, I64, I64, P, I64, P,
+            ctypes.c_int]
+        _lib = lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def _c(a, dtype):
+    return np.ascontiguousarray(a, dtype=dtype)
+
+
+def default_threads() -> int:
+    return max(1, len(os.sched_getaffinity(0)))
+
+
+# ------------------------------------------------------------------ formats --
+def e4m3_encode(x) -> np.ndarray:
+    """E4M3 codes (RNE, saturating at 448) of binary32 values."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, np.uint8)
+    _load().fo_e4m3_encode_array(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def e4m3_decode(c) -> np.ndarray:
+    """binary64 values of E4M3 codes."""
+    c = _c(c, np.uint8)
+    out = np.empty(c.shape, np.float64)
+    _load().fo_e4m3_decode_array(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def round_f32(c) -> np.ndarray:
+    c = _c(c, np.float64)
+    out = np.empty(c.shape, np.float32)
+    _load().fo_round_f32(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def round_bf16(c) -> np.ndarray:
+    """bfloat16 bit patterns of RNE_bf16(fl32(c))."""
+    c = _c(c, np.float64)
+    out = np.empty(c.shape, np.uint16)
+    _load().fo_round_bf16(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def group_scale(amax: float) -> np.float32:
+    return np.float32(_load().fo_group_scale(float(amax)))
+
+
+# ---------------------------------------------------------------- quantisers --
+def quant_act_1x128(x_bf16: np.ndarray):
+    """x: uint16 [M, K] bfloat16 bits -> (codes uint8 [M, K], scales f32 [K/128, M])."""
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    assert K % 128 == 0
+    xq = np.empty((M, K), np.uint8)
+    sx = np.empty((K // 128, M), np.float32)
+    _load().fo_quant_act_1x128(_ptr(x), M, K, K, _ptr(xq), K, _ptr(sx))
+    return xq, sx
+
+
+def quant_act_128x1(x_bf16: np.ndarray):
+    """x: uint16 [M, K] -> (codes uint8 [K, M] transposed, scales f32 [M/128, K])."""
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    assert M % 128 == 0
+    xqT = np.empty((K, M), np.uint8)
+    sxT = np.empty((M // 128, K), np.float32)
+    _load().fo_quant_act_128x1(_ptr(x), M, K, K, _ptr(xqT), _ptr(sxT))
+    return xqT, sxT
+
+
+def quant_weight_128x128(w_bf16: np.ndarray):
+    """w: uint16 [K, N] -> (wq uint8 [N, K], wqT uint8 [K, N], sw f32 [N/128, K/128])."""
+    w = _c(w_bf16, np.uint16)
+    K, N = w.shape
+    assert K % 128 == 0 and N % 128 == 0
+    wq = np.empty((N, K), np.uint8)
+    wqT = np.empty((K, N), np.uint8)
+    sw = np.empty((N // 128, K // 128), np.float32)
+    _load().fo_quant_weight_128x128(_ptr(w), K, N, N, _ptr(wq), _ptr(wqT), _ptr(sw))
+    return wq, wqT, sw
+
+
+# --------------------------------------------------------------------- GEMM --
+def gemm_blockscaled(aq, sa, bq, sb, bmode=BSCALE_BLOCK128, rows=None, nthreads=None):
+    """binary64 C[rows, :] of the block-scaled product.
+
+    aq: uint8 [M, K] codes, sa: f32 [K/128, M]; bq: uint8 [N, K] codes;
+    sb: f32 laid out per ``bmode`` (BLOCK128 [N/128, K/128], ROW1x128
+    [K/128, N], BLOCK128_T [K/128, N/128]).  ``rows``: the rows of C to form
+    (default all).
+    """
+    aq = _c(aq, np.uint8)
+    sa = _c(sa, np.float32)
+    bq = _c(bq, np.uint8)
+    sb = _c(sb, np.float32)
+    M, K = aq.shape
+    N, K2 = bq.shape
+    assert K == K2 and K % 128 == 0 and N % 128 == 0
+    assert sa.shape == (K // 128, M)
+    expect = {BSCALE_BLOCK128: (N // 128, K // 128), BSCALE_ROW1x128: (K // 128, N),
+              BSCALE_BLOCK128_T: (K // 128, N // 128)}[bmode]
+    assert sb.shape == expect, (sb.shape, expect)
+    if rows is None:
+        rows = np.arange(M, dtype=np.int64)
+    rows = _c(rows, np.int64)
+    assert rows.size == 0 or (rows.min() >= 0 and rows.max() < M)
+    out = np.empty((rows.size, N), np.float64)
+    if rows.size:
+        _load().fo_gemm_blockscaled_rows(
+            _ptr(aq), K, _ptr(sa), M, _ptr(bq), K, _ptr(sb), sb.shape[1], bmode, M, N, K,
+            _ptr(rows), rows.size, _ptr(out), nthreads or default_threads())
+    return out
+
+
+def grouped_gemm(aq, sa, bq, sb, offsets, rows=None, nthreads=None):
+    """binary64 Y[rows, :] of the grouped (per-expert) block-scaled product.
+
+    aq: uint8 [T, K] rows grouped by expert; sa: f32 [K/128, T];
+    bq: uint8 [E, N, K]; sb: f32 [E, N/128, K/128];
+    offsets: int [E+1], rows offsets[e]..offsets[e+1]-1 belong to expert e.
+    Each row of Y is the dense product of that row with its expert's weight.
+    """
+    aq = _c(aq, np.uint8)
+    sa = _c(sa, np.float32)
+    bq = _c(bq, np.uint8)
+    sb = _c(sb, np.float32)
+    offsets = np.asarray(offsets, dtype=np.int64)
+    T, K = aq.shape
+    E, N, _ = bq.shape
+    assert offsets.shape == (E + 1,) and offsets[0] == 0 and offsets[-1] == T
+    if rows is None:
+        rows = np.arange(T, dtype=np.int64)
+    rows = np.asarray(rows, dtype=np.int64)
+    out = np.empty((rows.size, N), np.float64)
+    expert_of = np.searchsorted(offsets, rows, side="right") - 1
+    for e in range(E):
+        sel = np.nonzero(expert_of == e)[0]
+        if sel.size == 0:
+            continue
+        # each row only needs its own A row and A scales; pass the whole A
+        # so that the row indices stay global.
+        out[sel] = gemm_blockscaled(aq, sa, bq[e], sb[e], BSCALE_BLOCK128,
+                                    rows=rows[sel], nthreads=nthreads)
+    return out
