@@ -1,0 +1,385 @@
+#!/usr/bin/env python3
+"""Benchmark of the fine-grained FP8 hot path on one (or N independent) B300s.
+
+One step = one pass of the path over one batch of the dense Fprop workload
+X[8192, 2048] (BF16, outlier channels) . W[2048, 7168] (BF16) -> Y (BF16):
+  1. 1x128 activation quantisation of X      (fp8_quant_act_1x128)
+  2. 128x128 weight quantisation of W         (fp8_quant_weight_128x128)
+  3. block-scaled FP8 GEMM with per-128-K FP32 promotion (fp8_gemm_blockscaled)
+The metric is the step's FP8 GEMM throughput, 2*M*N*K / step time (TFLOP/s);
+the JSON line also carries each kernel's own rate and roofline fraction.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own replica of the workload (weak scaling,
+no collective on the data path); rank 0 prints one JSON line.
+`--impl reference` times the CPU oracle on a bounded sample of the same
+workload instead (on rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from fp8_fine_grained_22_b300 import inputs  # noqa: E402
+
+WORKLOAD = "fprop_m8192_n7168_k2048_bf16"
+L2_BYTES = 126 * 2 ** 20
+METRIC = "FP8 block-scaled GEMM TFLOP/s and % of B300 FP8 peak; quantizer GB/s"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemm_fprop_m8192_n7168_k2048.md")
+CSRC = os.path.join(ROOT, "fp8_fine_grained_22_b300", "csrc")
+
+
+# ------------------------------------------------------------------ helpers --
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(CSRC)):
+        with open(os.path.join(CSRC, name), "rb") as f:
+            h.update(name.encode())
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per GEMM launch from the committed ncu summary, if the
+    kernel sources are unchanged since it was taken; else None."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    txt = open(PROFILE_SUMMARY).read()
+    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    m_h = re.search(r"source_sha256:\s*([0-9a-f]+)", txt)
+    if not (m_b and m_h) or m_h.group(1) != source_hash():
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- our path --
+def run_ours(args, rank, world, local):
+    from fp8_fine_grained_22_b300 import fp8fg
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fp8fg.lib()  # fail loudly if the CUDA library is missing
+    wl = inputs.fprop_dense(seed=0, device="cpu")
+    M, N, K = wl.M, wl.N, wl.K
+    flops = 2.0 * M * N * K
+    x = wl.x.to(dev)
+    w = wl.w.to(dev)
+    xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    sx = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+    wq = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        fp8fg.fp8_quant_act_1x128(x, xq, sx, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        fp8fg.fp8_quant_weight_128x128(w, wq=wq, sw=sw, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        fp8fg.fp8_gemm_blockscaled(xq, sx, wq, sw, out_dtype=torch.bfloat16, c=y, stream=stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if fp8fg.device_error() != 0:
+        raise RuntimeError("device-side error during warm-up")
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()  # L2 flush between steps, outside the step's events
+            step(events[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    if world > 1:
+        torch.distributed.barrier()
+    qx = [e[0].elapsed_time(e[1]) for e in events]
+    qw = [e[1].elapsed_time(e[2]) for e in events]
+    gm = [e[2].elapsed_time(e[3]) for e in events]
+    st = [e[0].elapsed_time(e[3]) for e in events]
+    ms_step = statistics.mean(st)
+    if world > 1:
+        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+    gemm_ms = statistics.mean(gm)
+    qx_ms, qw_ms = statistics.mean(qx), statistics.mean(qw)
+
+    # ----- end to end through the public API: pinned host in, host out -----
+    xh = wl.x.pin_memory()
+    wh = wl.w.pin_memory()
+    yh = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    h2d = xh.numel() * 2 + wh.numel() * 2
+    d2h = yh.numel() * 2
+
+    def e2e_step():
+        x.copy_(xh, non_blocking=True)
+        w.copy_(wh, non_blocking=True)
+        step()
+        yh.copy_(y, non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_start.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e_start.elapsed_time(e_end) / args.steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    err = fp8fg.device_error()
+    if err != 0:
+        raise RuntimeError("device-side error status %d" % err)
+
+    peaks, peak_src = measured_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]  # FP8 dense = 2 x BF16 dense (nominal ratio)
+    hbm = peaks["hbm_gbs"]
+    gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
+    qx_bytes = M * K * 2 + M * K + (K // 128) * M * 4
+    qw_bytes = K * N * 2 + K * N + (K // 128) * (N // 128) * 4
+    value = world * flops / (ms_step * 1e-3) / 1e12
+    clocks = clk.summary()
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> f32 accumulate, bf16 out",
+        "data": "synthetic (seeded: N(0,1) activations with 1% x100 outlier channels, "
+                "N(0,0.006^2) weights)",
+        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "global_batch": M * world,
+                   "parallelism": "replicas (dp%d, no collective)" % world,
+                   "l2": "flushed between steps (%d MB write)" % (flush.numel() * 4 >> 20),
+                   "step": ["fp8_quant_act_1x128", "fp8_quant_weight_128x128",
+                            "fp8_gemm_blockscaled"]},
+        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": 3 * args.steps,
+        "roofline": {"kernel": "fp8_gemm_blockscaled", "bound": "tensor",
+                     "achieved": round(gemm_tflops, 2), "peak": round(fp8_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
+                     "peak_source": "%s bf16 burst x 2 (nominal FP8:BF16 dense ratio)" % peak_src,
+                     "traffic": profiled_traffic(),
+                     "algorithmic_bytes": M * K + N * K + M * N * 2 + (K // 128) * (M + N // 128) * 4},
+        "kernels": {
+            "fp8_gemm_blockscaled": {"ms": round(gemm_ms, 5), "tflops": round(gemm_tflops, 2),
+                                     "frac_fp8_peak": round(gemm_tflops / fp8_peak, 4)},
+            "fp8_quant_act_1x128": {"ms": round(qx_ms, 5),
+                                    "gbs": round(qx_bytes / (qx_ms * 1e-3) / 1e9, 1),
+                                    "frac_hbm": round(qx_bytes / (qx_ms * 1e-3) / 1e9 / hbm, 4)},
+            "fp8_quant_weight_128x128": {"ms": round(qw_ms, 5),
+                                         "gbs": round(qw_bytes / (qw_ms * 1e-3) / 1e9, 1),
+                                         "frac_hbm": round(qw_bytes / (qw_ms * 1e-3) / 1e9 / hbm,
+                                                           4)},
+        },
+        "clocks": clocks,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if args.cpu_baseline and rank == 0:
+        line["cpu_baseline"] = cpu_baseline(args.cpu_sample_rows)
+    return line
+
+
+# ------------------------------------------------------- CPU oracle baseline --
+def cpu_baseline(n_rows, wl=None):
+    """The oracle on the host cores: quantise all of W and a sample of X rows,
+    then the binary64 block-scaled GEMM of those rows."""
+    import oracle
+
+    if wl is None:
+        wl = inputs.fprop_dense(seed=0, device="cpu")
+    threads = oracle.default_threads()
+    xb = inputs.bf16_bits(wl.x[:n_rows])
+    wb = inputs.bf16_bits(wl.w)
+    t0 = time.perf_counter()
+    aq, sa = oracle.quant_act_1x128(xb)
+    bq, _, sw = oracle.quant_weight_128x128(wb)
+    c = oracle.gemm_blockscaled(aq, sa, bq, sw, nthreads=threads)
+    oracle.round_bf16(c)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * n_rows * wl.N * wl.K
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": "%d of %d rows of X (all of W quantised), binary64 GEMM" % (n_rows, wl.M)}
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle, timed per step on a bounded sample."""
+    wl = inputs.fprop_dense(seed=0, device="cpu")
+    for _ in range(args.warmup and 1):
+        cpu_baseline(8, wl)
+    times = []
+    res = None
+    for _ in range(args.steps):
+        res = cpu_baseline(args.ref_rows, wl)
+        times.append(res["seconds"])
+    flops = 2.0 * args.ref_rows * wl.N * wl.K
+    ms = statistics.mean(times) * 1e3
+    value = flops / (ms * 1e-3) / 1e12
+    return {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": round(value, 6),
+        "unit": "TFLOP/s",
+        "n_gpus": 1,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 1),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f64 oracle (e4m3 codes, binary64 accumulate)",
+        "data": "synthetic (same seeded workload)",
+        "config": {"workload": WORKLOAD, "M": wl.M, "N": wl.N, "K": wl.K,
+                   "sample_rows": args.ref_rows},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": res["cores"],
+                         "kind": "oracle", "sample": res["sample"]},
+        "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
+    ap.add_argument("--cpu-sample-rows", type=int, default=2048)
+    ap.add_argument("--ref-rows", type=int, default=512)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args)), flush=True)
+        return
+    if world > 1:
+        torch.distributed.init_process_group(
+            backend="nccl" if torch.cuda.is_available() else "gloo")
+    try:
+        line = run_ours(args, rank, world, local)
+        if rank == 0:
+            print(json.dumps(line), flush=True)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

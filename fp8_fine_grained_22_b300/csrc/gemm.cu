@@ -1,0 +1,649 @@
+// gemm.cu -- block-scaled FP8 GEMM with per-128-K FP32 promotion on the
+// sm_103a tensor cores (tcgen05 + tensor memory + TMA).
+//
+// Method (DeepSeek-V3 Technical Report, section 3.3.2 and Figure 7(b)): the
+// tensor cores form the partial sum of each 128-wide K interval; that partial
+// is promoted to FP32, multiplied by the A-row scale and the B scale of the
+// interval, and accumulated in FP32 outside the tensor core.
+//
+// Blackwell mapping (the report's H800 design copied WGMMA register partials
+// to CUDA-core registers; here the partials live in tensor memory):
+//   warp 0      TMA producer: A tile 128x128 and B tile BNx128 (E4M3, 128-byte
+//               swizzle) per K block into a STAGES-deep shared-memory ring.
+//   warp 1      MMA issuer: four tcgen05.mma kind::f8f6f4 (K = 32 each) per K
+//               block into one of two TMEM partial buffers (BN FP32 columns
+//               each), then tcgen05.commit to release the smem stage and to
+//               signal the epilogue.
+//   warps 2..9  promotion epilogue: tcgen05.ld the partial of K block kb,
+//               acc += partial * (sa[m,kb] * sb[kb]) with packed FP32 FMAs
+//               in registers, release the TMEM buffer; after the last K block,
+//               convert and store the tile through a swizzled shared-memory
+//               staging buffer and TMA bulk stores.
+// The kernel is persistent: one CTA per SM walks a static tile schedule.
+// Every barrier wait is bounded; on expiry the kernel records
+// FP8_ERR_TIMEOUT in a device error word, unwinds and frees its TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cudaTypedefs.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+
+namespace fp8fg {
+
+// bit 0: a barrier wait timed out; bit 1: invalid grouped offsets
+__device__ unsigned int g_dev_error;
+
+constexpr int BM = 128;               // rows per tile (TMEM lanes)
+constexpr int BK = 128;               // K block = promotion interval
+constexpr int kEpiWarps = 8;          // 2 per TMEM lane quadrant
+constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr long long kWaitLimit = 1LL << 32;  // cycles (about 2 s at 2 GHz)
+constexpr int kSmemLimit = 232448;    // 227 KB opt-in per CTA
+
+template <int BN, bool ROWSCALE>
+struct Cfg {
+    static constexpr int A_BYTES = BM * BK;
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int COLS = BN / 2;           // columns per epilogue thread
+    static constexpr int TMEM_COLS = 2 * BN;      // two partial buffers
+    static constexpr int CSTAGE_BYTES = kEpiWarps * 4096;
+    static constexpr int RSCALE_BYTES = ROWSCALE ? 2 * BN * 4 : 0;
+    static constexpr int HEADER = 256;            // barriers, TMEM slot, flags
+    static constexpr int FIXED = HEADER + 1023 + CSTAGE_BYTES + RSCALE_BYTES;
+    static constexpr int STAGES_FIT = (kSmemLimit - FIXED) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
+    static constexpr int SMEM = FIXED + STAGES * STAGE_BYTES;
+    static_assert(STAGES >= 2, "pipeline too shallow");
+    static_assert(2 * STAGES + 7 <= 30, "header too small for barriers");
+    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of 2");
+};
+
+struct GemmParams {
+    const float* sa;      // sa[kb * lds_a + row]
+    int64_t lds_a;
+    const float* sb;      // B scales (layout per bmode)
+    int64_t ld_sb;        // ROW1x128: row stride of sb
+    int64_t sb_expert;    // grouped: floats per expert in sb
+    int bmode;            // FP8_BSCALE_*
+    int64_t M;            // dense: rows of A and C; grouped: T
+    int64_t N, K;
+    void* c;
+    int64_t ldc;          // elements
+    const int32_t* offsets;  // grouped only
+    int E;
+};
+
+struct Tile {
+    int64_t row0;     // first row of A / C
+    int64_t row_end;  // rows >= row_end are not this tile's
+    int64_t b_row0;   // first row of B (expert-major for grouped)
+    int64_t n0;       // first output column
+    int expert;
+};
+
+template <int BN, bool GROUPED>
+__device__ __forceinline__ bool get_tile(const GemmParams& p, int64_t t, Tile& ti) {
+    const int64_t nblk = p.N / BN;
+    if (!GROUPED) {
+        const int64_t mblk = (p.M + BM - 1) / BM;
+        if (t >= mblk * nblk) return false;
+        const int64_t mb = t / nblk, nb = t % nblk;
+        ti.row0 = mb * BM;
+        ti.row_end = p.M;
+        ti.n0 = nb * BN;
+        ti.b_row0 = ti.n0;
+        ti.expert = 0;
+        return true;
+    } else {
+        int64_t base = 0;
+        for (int e = 0; e < p.E; ++e) {
+            const int64_t lo = __ldg(p.offsets + e), hi = __ldg(p.offsets + e + 1);
+            const int64_t n_e = ((hi - lo + BM - 1) / BM) * nblk;
+            if (t < base + n_e) {
+                const int64_t local = t - base;
+                const int64_t mb = local / nblk, nb = local % nblk;
+                ti.row0 = lo + mb * BM;
+                ti.row_end = hi;
+                ti.n0 = nb * BN;
+                ti.b_row0 = static_cast<int64_t>(e) * p.N + ti.n0;
+                ti.expert = e;
+                return true;
+            }
+            base += n_e;
+        }
+        return false;
+    }
+}
+
+// Shared-memory matrix descriptor of a K-major operand tile whose rows are
+// 128 bytes (one 128-byte swizzle atom wide), 8-row core groups 1024 bytes
+// apart: start address, leading byte offset 16 (unused for this layout),
+// stride byte offset 1024, descriptor version 1, swizzle mode 128B.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
+    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+           (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+           (static_cast<uint64_t>(2) << 61);
+}
+
+// Instruction descriptor: E4M3 x E4M3 -> FP32, A and B K-major, M = 128, N = BN.
+template <int BN>
+__device__ __forceinline__ uint32_t idesc_e4m3_f32() {
+    return (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) |
+           (static_cast<uint32_t>(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void raise_error(volatile int* abort_flag, unsigned bits) {
+    *abort_flag = 1;
+    atomicOr(&g_dev_error, bits);
+}
+
+// Single-thread bounded wait.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitLimit) {
+            raise_error(abort_flag, 1u);
+            return false;
+        }
+    }
+    return true;
+}
+
+// Whole-warp bounded wait with a warp-uniform outcome.
+__device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag) {
+    const long long t0 = clock64();
+    while (true) {
+        const bool ok = mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, ok)) return true;
+        const bool expired = clock64() - t0 > kWaitLimit;
+        const bool stop = (*abort_flag != 0) || expired;
+        if (__any_sync(0xffffffffu, stop)) {
+            if (expired) raise_error(abort_flag, 1u);
+            return false;
+        }
+    }
+}
+
+__device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
+__device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
+
+__device__ __forceinline__ uint32_t bf16x2(uint64_t pair) {
+    const __nv_bfloat162 h = __floats2bfloat162_rn(u2f(static_cast<uint32_t>(pair)),
+                                                   u2f(static_cast<uint32_t>(pair >> 32)));
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+template <int BN, bool OUT_BF16, bool ROWSCALE, bool GROUPED>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA,
+                            const __grid_constant__ CUtensorMap tmB,
+                            const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+    using C = Cfg<BN, ROWSCALE>;
+    constexpr int S = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + 240);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + 244);
+    uint8_t* base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + C::HEADER + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* stages = base;
+    uint8_t* cstage = base + S * C::STAGE_BYTES;
+    float* rscale = reinterpret_cast<float*>(cstage + C::CSTAGE_BYTES);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    auto full_bar = [&](int s) { return smem_addr(&bars[s]); };
+    auto empty_bar = [&](int s) { return smem_addr(&bars[S + s]); };
+    auto tfull_bar = [&](int b) { return smem_addr(&bars[2 * S + b]); };
+    auto tempty_bar = [&](int b) { return smem_addr(&bars[2 * S + 2 + b]); };
+    const uint32_t drain_bar = smem_addr(&bars[2 * S + 4]);
+    // ROWSCALE: the epilogue warps stage each K block's B-row scales in a
+    // double buffer; this barrier pair (one per buffer) says all warps wrote.
+    auto rs_bar = [&](int b) { return smem_addr(&bars[2 * S + 5 + b]); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), kEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        mbar_init(rs_bar(0), kEpiWarps);
+        mbar_init(rs_bar(1), kEpiWarps);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    if (GROUPED) {
+        // offsets[0] == 0, non-decreasing, offsets[E] <= T; checked by all threads
+        bool bad = false;
+        if (threadIdx.x == 0) bad = (__ldg(p.offsets) != 0) || (__ldg(p.offsets + p.E) > p.M);
+        for (int e = threadIdx.x; e < p.E; e += kThreads)
+            bad |= __ldg(p.offsets + e + 1) < __ldg(p.offsets + e);
+        if (bad) raise_error(abort_flag, 2u);
+        __syncthreads();
+    }
+    const uint32_t tmem_base = *tmem_slot;
+    const int64_t KB = p.K / BK;
+    const bool aborted_at_start = *abort_flag != 0;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0 && !aborted_at_start) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
+                Tile ti;
+                if (!get_tile<BN, GROUPED>(p, t, ti)) break;
+                for (int64_t kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = static_cast<int>(it % S);
+                    const uint32_t ph = (it / S) & 1u;
+                    if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = stages + s * C::STAGE_BYTES;
+                    mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
+                    tma_load_2d(smem_addr(st), &tmA, full_bar(s), static_cast<int>(kb * BK),
+                                static_cast<int>(ti.row0));
+                    tma_load_2d(smem_addr(st + C::A_BYTES), &tmB, full_bar(s),
+                                static_cast<int>(kb * BK), static_cast<int>(ti.b_row0));
+                }
+            }
+            if (!ok) {
+                // let copies already issued land before the CTA can exit
+                const uint32_t n = it < static_cast<uint32_t>(S) ? it : static_cast<uint32_t>(S);
+                for (uint32_t i = it - n; i < it; ++i) {
+                    const long long t0 = clock64();
+                    while (!mbar_try_wait(full_bar(static_cast<int>(i % S)), (i / S) & 1u) &&
+                           clock64() - t0 < (1LL << 24)) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // --------------------------------------------------------- MMA issuer
+        if (lane == 0 && !aborted_at_start) {
+            const uint32_t idesc = idesc_e4m3_f32<BN>();
+            uint32_t it = 0, kbg = 0;
+            bool ok = true, issued = false;
+            for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
+                Tile ti;
+                if (!get_tile<BN, GROUPED>(p, t, ti)) break;
+                for (int64_t kb = 0; kb < KB; ++kb, ++it, ++kbg) {
+                    const int s = static_cast<int>(it % S);
+                    const uint32_t ph = (it / S) & 1u;
+                    const uint32_t buf = kbg & 1u, tph = (kbg >> 1) & 1u;
+                    if (!wait_bar(full_bar(s), ph, abort_flag) ||
+                        !wait_bar(tempty_bar(buf), tph ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a_addr = smem_addr(stages + s * C::STAGE_BYTES);
+                    const uint64_t adesc = smem_desc_sw128(a_addr);
+                    const uint64_t bdesc = smem_desc_sw128(a_addr + C::A_BYTES);
+                    const uint32_t d = tmem_base + buf * BN;
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
+                        mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+                    mma_commit(empty_bar(s));
+                    mma_commit(tfull_bar(buf));
+                    issued = true;
+                }
+            }
+            if (!ok && issued) {
+                // wait (bounded) for every MMA already issued before TMEM is freed
+                mma_commit(drain_bar);
+                const long long t0 = clock64();
+                while (!mbar_try_wait(drain_bar, 0) && clock64() - t0 < (1LL << 24)) {
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------- promotion epilogue
+        constexpr int COLS = C::COLS;
+        constexpr int ELT = OUT_BF16 ? 2 : 4;
+        constexpr int BOX_COLS = 128 / ELT;  // one 128-byte swizzle row per box row
+        const int ew = warp - 2;              // 0..7
+        const int q = warp & 3;               // TMEM lane quadrant of this warp
+        const int cg = ew >> 2;               // column half of the tile
+        uint8_t* my_cstage = cstage + ew * 4096;
+        const int64_t NB = p.N / 128;
+        uint32_t kbg = 0;
+        bool ok = !aborted_at_start;
+        for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
+            Tile ti;
+            if (!get_tile<BN, GROUPED>(p, t, ti)) break;
+            const int64_t row = ti.row0 + q * 32 + lane;
+            const bool row_in_alloc = row < p.M;
+            const int64_t ncol0 = ti.n0 + cg * COLS;
+            const int64_t nb = ncol0 / 128;
+            const float* sb_e = p.sb + (GROUPED ? ti.expert * p.sb_expert : 0);
+            auto b_scale_at = [&](int64_t kb) -> float {
+                return p.bmode == FP8_BSCALE_BLOCK128 ? __ldg(sb_e + nb * KB + kb)
+                                                      : __ldg(sb_e + kb * NB + nb);
+            };
+            const int rcol = ew * 32 + lane;  // ROWSCALE: column this thread stages
+            auto row_scale_at = [&](int64_t kb) -> float {
+                return rcol < BN ? __ldg(p.sb + kb * p.ld_sb + ti.n0 + rcol) : 0.0f;
+            };
+            float sa_next = row_in_alloc ? __ldg(p.sa + row) : 0.0f;
+            float sb_next = ROWSCALE ? row_scale_at(0) : b_scale_at(0);
+
+            uint64_t acc[COLS / 2];
+#pragma unroll
+            for (int i = 0; i < COLS / 2; ++i) acc[i] = 0;
+
+            for (int64_t kb = 0; kb < KB; ++kb, ++kbg) {
+                const float sa_cur = sa_next, sb_cur = sb_next;
+                if (kb + 1 < KB) {
+                    sa_next = row_in_alloc ? __ldg(p.sa + (kb + 1) * p.lds_a + row) : 0.0f;
+                    sb_next = ROWSCALE ? row_scale_at(kb + 1) : b_scale_at(kb + 1);
+                }
+                const uint32_t buf = kbg & 1u, tph = (kbg >> 1) & 1u;
+                if (ROWSCALE) {
+                    // buffer `buf` was last read in K block kbg-2; every warp
+                    // arrived on this buffer's barrier for kbg-1 only after
+                    // finishing that read, so it is free to overwrite here.
+                    if (rcol < BN) rscale[buf * BN + rcol] = sb_cur;
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(rs_bar(buf));
+                    if (!wait_bar_warp(rs_bar(buf), tph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (!wait_bar_warp(tfull_bar(buf), tph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t taddr =
+                    tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + cg * COLS;
+                if (!ROWSCALE) {
+                    const float sc = sa_cur * sb_cur;
+                    const uint64_t sc2 = pack2(f2u(sc), f2u(sc));
+#pragma unroll
+                    for (int ch = 0; ch < COLS / 16; ++ch) {
+                        uint32_t r[16];
+                        tmem_ld16_wait(taddr + ch * 16, r);
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            acc[ch * 8 + i] = ffma2(pack2(r[2 * i], r[2 * i + 1]), sc2, acc[ch * 8 + i]);
+                    }
+                } else {
+                    const uint64_t sa2 = pack2(f2u(sa_cur), f2u(sa_cur));
+                    const float* rs = rscale + buf * BN + cg * COLS;
+#pragma unroll
+                    for (int ch = 0; ch < COLS / 16; ++ch) {
+                        uint32_t r[16];
+                        tmem_ld16_wait(taddr + ch * 16, r);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float4 b4 = *reinterpret_cast<const float4*>(rs + ch * 16 + 4 * i);
+                            const uint64_t p0 =
+                                fmul2(pack2(r[4 * i], r[4 * i + 1]), pack2(f2u(b4.x), f2u(b4.y)));
+                            const uint64_t p1 = fmul2(pack2(r[4 * i + 2], r[4 * i + 3]),
+                                                      pack2(f2u(b4.z), f2u(b4.w)));
+                            acc[ch * 8 + 2 * i] = ffma2(p0, sa2, acc[ch * 8 + 2 * i]);
+                            acc[ch * 8 + 2 * i + 1] = ffma2(p1, sa2, acc[ch * 8 + 2 * i + 1]);
+                        }
+                    }
+                }
+                tc_fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tempty_bar(buf));
+            }
+            if (!ok) break;
+
+            // ---------------------------------------------------- tile store
+            const int64_t wrow0 = ti.row0 + q * 32;
+            if (wrow0 + 32 <= ti.row_end) {
+                // whole 32-row box valid: stage with the 128-byte swizzle, TMA store
+#pragma unroll
+                for (int bx = 0; bx < COLS / BOX_COLS; ++bx) {
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint4 v;
+                        if (OUT_BF16) {
+                            const int a0 = (bx * BOX_COLS + j * 8) / 2;
+                            v = make_uint4(bf16x2(acc[a0]), bf16x2(acc[a0 + 1]), bf16x2(acc[a0 + 2]),
+                                           bf16x2(acc[a0 + 3]));
+                        } else {
+                            const int a0 = (bx * BOX_COLS + j * 4) / 2;
+                            v = make_uint4(static_cast<uint32_t>(acc[a0]),
+                                           static_cast<uint32_t>(acc[a0] >> 32),
+                                           static_cast<uint32_t>(acc[a0 + 1]),
+                                           static_cast<uint32_t>(acc[a0 + 1] >> 32));
+                        }
+                        *reinterpret_cast<uint4*>(my_cstage + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, smem_addr(my_cstage),
+                                     static_cast<int>(ncol0 + bx * BOX_COLS), static_cast<int>(wrow0));
+                        bulk_commit_group();
+                        bulk_wait_group_read0();
+                    }
+                    __syncwarp();
+                }
+            } else if (row < ti.row_end) {
+                // ragged rows: direct 16-byte stores of this thread's row
+                uint8_t* dst = static_cast<uint8_t*>(p.c) + (row * p.ldc + ncol0) * ELT;
+#pragma unroll
+                for (int j = 0; j < COLS * ELT / 16; ++j) {
+                    uint4 v;
+                    if (OUT_BF16) {
+                        v = make_uint4(bf16x2(acc[4 * j]), bf16x2(acc[4 * j + 1]),
+                                       bf16x2(acc[4 * j + 2]), bf16x2(acc[4 * j + 3]));
+                    } else {
+                        v = make_uint4(static_cast<uint32_t>(acc[2 * j]),
+                                       static_cast<uint32_t>(acc[2 * j] >> 32),
+                                       static_cast<uint32_t>(acc[2 * j + 1]),
+                                       static_cast<uint32_t>(acc[2 * j + 1] >> 32));
+                    }
+                    reinterpret_cast<uint4*>(dst)[j] = v;
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_group0();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+// -------------------------------------------------------------------- host --
+static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (fn == nullptr) {
+        void* ptr = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+    }
+    return fn;
+}
+
+// 2-D row-major tensor [outer][inner] with a 128-byte-swizzled box.
+static int make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                    uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
+    auto fn = encode_tiled();
+    if (fn == nullptr) return FP8_ERR_CUDA;
+    cuuint64_t dims[2] = {inner, outer};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {box_inner, box_outer};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
+}
+
+template <int BN, bool OUT_BF16, bool ROWSCALE, bool GROUPED>
+static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t b_rows,
+                  const GemmParams& p, int64_t tiles_upper, cudaStream_t stream) {
+    using C = Cfg<BN, ROWSCALE>;
+    auto kern = gemm_blockscaled_kernel<BN, OUT_BF16, ROWSCALE, GROUPED>;
+    int dev = 0;
+    const int sms = sm_count_current(&dev);
+    if (sms <= 0) return FP8_ERR_CUDA;
+    static bool attr_done[kMaxDevices] = {false};
+    if (!attr_done[dev]) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+            cudaSuccess)
+            return FP8_ERR_CUDA;
+        attr_done[dev] = true;
+    }
+    CUtensorMap ta, tb, tc;
+    int st;
+    if ((st = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, p.K, a_rows, p.K, BK, BM)) != FP8_OK)
+        return st;
+    if ((st = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bq, p.K, b_rows, p.K, BK, BN)) != FP8_OK)
+        return st;
+    constexpr int ELT = OUT_BF16 ? 2 : 4;
+    if ((st = make_map(&tc, OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                       p.c, p.N, p.M, p.ldc * ELT, 128 / ELT, 32)) != FP8_OK)
+        return st;
+    const int64_t grid = tiles_upper < sms ? tiles_upper : sms;
+    if (grid <= 0) return FP8_OK;
+    kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM, stream>>>(ta, tb, tc, p);
+    return launch_status();
+}
+
+template <bool GROUPED>
+static int dispatch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t b_rows,
+                    GemmParams& p, int out_type, int64_t mblk_upper, cudaStream_t stream) {
+    const bool rows = p.bmode == FP8_BSCALE_ROW1x128;
+    // 256-wide tiles halve the shared-memory operand traffic per MMA; the
+    // per-column B-scale mode keeps 128-wide tiles (its epilogue needs more
+    // registers than a 256-wide tile leaves).
+    if (p.N % 256 == 0 && !rows) {
+        const int64_t tiles = mblk_upper * (p.N / 256);
+        if (out_type == FP8_OUT_BF16)
+            return launch<256, true, false, GROUPED>(aq, a_rows, bq, b_rows, p, tiles, stream);
+        return launch<256, false, false, GROUPED>(aq, a_rows, bq, b_rows, p, tiles, stream);
+    }
+    const int64_t tiles = mblk_upper * (p.N / 128);
+    if constexpr (GROUPED) {  // grouped calls always use 128x128-block B scales
+        if (out_type == FP8_OUT_BF16)
+            return launch<128, true, false, true>(aq, a_rows, bq, b_rows, p, tiles, stream);
+        return launch<128, false, false, true>(aq, a_rows, bq, b_rows, p, tiles, stream);
+    } else {
+        if (out_type == FP8_OUT_BF16)
+            return rows ? launch<128, true, true, false>(aq, a_rows, bq, b_rows, p, tiles, stream)
+                        : launch<128, true, false, false>(aq, a_rows, bq, b_rows, p, tiles, stream);
+        return rows ? launch<128, false, true, false>(aq, a_rows, bq, b_rows, p, tiles, stream)
+                    : launch<128, false, false, false>(aq, a_rows, bq, b_rows, p, tiles, stream);
+    }
+}
+
+}  // namespace fp8fg
+
+using namespace fp8fg;
+
+extern "C" int fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, const uint8_t* bq,
+                                    const float* sb, int bmode, int64_t M, int64_t N, int64_t K,
+                                    void* c, int64_t ldc, int out_type, void* stream) {
+    if (M < 0 || N <= 0 || N % 128 != 0 || K <= 0 || K % 128 != 0 || ldc < N)
+        return FP8_ERR_SHAPE;
+    if (bmode < FP8_BSCALE_BLOCK128 || bmode > FP8_BSCALE_BLOCK128_T) return FP8_ERR_UNSUPPORTED;
+    if (out_type != FP8_OUT_F32 && out_type != FP8_OUT_BF16) return FP8_ERR_UNSUPPORTED;
+    if (M == 0) return FP8_OK;
+    if (aq == nullptr || sa == nullptr || bq == nullptr || sb == nullptr || c == nullptr)
+        return FP8_ERR_NULL;
+    const int64_t elt = out_type == FP8_OUT_BF16 ? 2 : 4;
+    if (!aligned(aq, 16) || !aligned(bq, 16) || !aligned(c, 16) || !aligned(sa, 4) ||
+        !aligned(sb, 4) || (ldc * elt) % 16 != 0)
+        return FP8_ERR_ALIGN;
+    if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL) return FP8_ERR_UNSUPPORTED;
+    GemmParams p{};
+    p.sa = sa;
+    p.lds_a = M;
+    p.sb = sb;
+    p.ld_sb = N;
+    p.sb_expert = 0;
+    p.bmode = bmode;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.c = c;
+    p.ldc = ldc;
+    p.offsets = nullptr;
+    p.E = 0;
+    return dispatch<false>(aq, M, bq, N, p, out_type, (M + BM - 1) / BM,
+                           static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8_grouped_gemm_moe(const uint8_t* aq, const float* sa, const uint8_t* bq,
+                                    const float* sb, const int32_t* offsets, int32_t E, int64_t T,
+                                    int64_t N, int64_t K, void* c, int out_type, void* stream) {
+    if (E < 1 || E > 65536 || T < 0 || N <= 0 || N % 128 != 0 || K <= 0 || K % 128 != 0)
+        return FP8_ERR_SHAPE;
+    if (out_type != FP8_OUT_F32 && out_type != FP8_OUT_BF16) return FP8_ERR_UNSUPPORTED;
+    if (T == 0) return FP8_OK;
+    if (aq == nullptr || sa == nullptr || bq == nullptr || sb == nullptr || offsets == nullptr ||
+        c == nullptr)
+        return FP8_ERR_NULL;
+    if (!aligned(aq, 16) || !aligned(bq, 16) || !aligned(c, 16) || !aligned(sa, 4) ||
+        !aligned(sb, 4) || !aligned(offsets, 4))
+        return FP8_ERR_ALIGN;
+    if (T > 0x7fffffffLL || static_cast<int64_t>(E) * N > 0x7fffffffLL || K > 0x7fffffffLL)
+        return FP8_ERR_UNSUPPORTED;
+    GemmParams p{};
+    p.sa = sa;
+    p.lds_a = T;
+    p.sb = sb;
+    p.ld_sb = 0;
+    p.sb_expert = (N / 128) * (K / 128);
+    p.bmode = FP8_BSCALE_BLOCK128;
+    p.M = T;
+    p.N = N;
+    p.K = K;
+    p.c = c;
+    p.ldc = N;
+    p.offsets = offsets;
+    p.E = E;
+    // every expert adds at most one ragged M block
+    return dispatch<true>(aq, T, bq, static_cast<int64_t>(E) * N, p, out_type,
+                          (T + BM - 1) / BM + E, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8_device_error(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return FP8_ERR_CUDA;
+    unsigned int v = 0, zero = 0;
+    if (cudaMemcpyFromSymbol(&v, g_dev_error, sizeof v) != cudaSuccess) return FP8_ERR_CUDA;
+    if (v != 0 && cudaMemcpyToSymbol(g_dev_error, &zero, sizeof zero) != cudaSuccess)
+        return FP8_ERR_CUDA;
+    if (v & 1u) return FP8_ERR_TIMEOUT;
+    if (v & 2u) return FP8_ERR_DEVICE_SHAPE;
+    return FP8_OK;
+}

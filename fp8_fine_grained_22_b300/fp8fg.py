@@ -1,0 +1,179 @@
+"""Thin ctypes binding of libfp8fg.so (include/fp8fg.h).
+
+Argument marshalling only: every step runs in the CUDA kernels of the
+library.  PyTorch supplies device memory (output tensors are allocated here
+when the caller does not pass them) and the current CUDA stream.  There is no
+fallback: if the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from .build import LIB_PATH, build as _build
+
+FP8_OK = 0
+FP8_OUT_F32 = 0
+FP8_OUT_BF16 = 1
+FP8_BSCALE_BLOCK128 = 0
+FP8_BSCALE_ROW1x128 = 1
+FP8_BSCALE_BLOCK128_T = 2
+
+# every entry point of include/fp8fg.h
+EXPORTS = ("fp8_status_str", "fp8_device_error", "fp8_quant_act_1x128", "fp8_quant_act_128x1",
+           "fp8_quant_weight_128x128", "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe")
+
+
+class Fp8Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__("%s failed: %s (status %d)" % (what, status_str(status), status))
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library; builds it in-tree first if the sources are newer."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            _build()
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libfp8fg.so is missing: build it with "
+                               "`python -m fp8_fine_grained_22_b300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I32, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int32, ctypes.c_int
+        L.fp8_status_str.restype = ctypes.c_char_p
+        L.fp8_status_str.argtypes = [I]
+        L.fp8_device_error.restype = I
+        L.fp8_device_error.argtypes = [P]
+        L.fp8_quant_act_1x128.restype = I
+        L.fp8_quant_act_1x128.argtypes = [P, I64, I64, I64, P, I64, P, P]
+        L.fp8_quant_act_128x1.restype = I
+        L.fp8_quant_act_128x1.argtypes = [P, I64, I64, I64, P, P, P]
+        L.fp8_quant_weight_128x128.restype = I
+        L.fp8_quant_weight_128x128.argtypes = [P, I64, I64, I64, P, P, P, P]
+        L.fp8_gemm_blockscaled.restype = I
+        L.fp8_gemm_blockscaled.argtypes = [P, P, P, P, I, I64, I64, I64, P, I64, I, P]
+        L.fp8_grouped_gemm_moe.restype = I
+        L.fp8_grouped_gemm_moe.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, I, P]
+        _lib = L
+    return _lib
+
+
+def status_str(status: int) -> str:
+    return lib().fp8_status_str(int(status)).decode()
+
+
+def _check(status: int, what: str):
+    if status != FP8_OK:
+        raise Fp8Error(status, what)
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _p(t):
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _cuda(t, name, dtype=None):
+    if not t.is_cuda:
+        raise ValueError("%s must be a CUDA tensor" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+
+
+def device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device-side error status."""
+    return lib().fp8_device_error(_stream(stream))
+
+
+# --------------------------------------------------------------- quantisers --
+def fp8_quant_act_1x128(x, xq=None, sx=None, stream=None):
+    """x: bf16 [M, K] (row stride x.stride(0)) -> (xq uint8 [M, K], sx f32 [K/128, M])."""
+    _cuda(x, "x", torch.bfloat16)
+    assert x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if sx is None:
+        sx = torch.empty((K // 128, M), dtype=torch.float32, device=x.device)
+    assert xq.stride(1) == 1 and sx.is_contiguous()
+    _check(lib().fp8_quant_act_1x128(_p(x), M, K, x.stride(0), _p(xq), xq.stride(0), _p(sx),
+                                     _stream(stream)), "fp8_quant_act_1x128")
+    return xq, sx
+
+
+def fp8_quant_act_128x1(x, xqT=None, sxT=None, stream=None):
+    """x: bf16 [M, K] -> (xqT uint8 [K, M], sxT f32 [M/128, K])."""
+    _cuda(x, "x", torch.bfloat16)
+    assert x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    if xqT is None:
+        xqT = torch.empty((K, M), dtype=torch.uint8, device=x.device)
+    if sxT is None:
+        sxT = torch.empty((M // 128, K), dtype=torch.float32, device=x.device)
+    assert xqT.is_contiguous() and sxT.is_contiguous()
+    _check(lib().fp8_quant_act_128x1(_p(x), M, K, x.stride(0), _p(xqT), _p(sxT),
+                                     _stream(stream)), "fp8_quant_act_128x1")
+    return xqT, sxT
+
+
+def fp8_quant_weight_128x128(w, wq=None, wqT=None, sw=None, want_wq=True, want_wqT=False,
+                             stream=None):
+    """w: bf16 [K, N] -> (wq uint8 [N, K] or None, wqT uint8 [K, N] or None, sw f32 [N/128, K/128])."""
+    _cuda(w, "w", torch.bfloat16)
+    assert w.dim() == 2 and w.stride(1) == 1
+    K, N = w.shape
+    if wq is None and want_wq:
+        wq = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    if wqT is None and want_wqT:
+        wqT = torch.empty((K, N), dtype=torch.uint8, device=w.device)
+    if sw is None:
+        sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=w.device)
+    _check(lib().fp8_quant_weight_128x128(_p(w), K, N, w.stride(0), _p(wq), _p(wqT), _p(sw),
+                                          _stream(stream)), "fp8_quant_weight_128x128")
+    return wq, wqT, sw
+
+
+# -------------------------------------------------------------------- GEMMs --
+def fp8_gemm_blockscaled(aq, sa, bq, sb, bmode=FP8_BSCALE_BLOCK128, out_dtype=torch.bfloat16,
+                         c=None, stream=None):
+    """C[M, N] of the block-scaled product; aq uint8 [M, K], bq uint8 [N, K]."""
+    for t, n in ((aq, "aq"), (sa, "sa"), (bq, "bq"), (sb, "sb")):
+        _cuda(t, n)
+    M, K = aq.shape
+    N = bq.shape[0]
+    assert aq.is_contiguous() and bq.is_contiguous() and bq.shape[1] == K
+    out_type = FP8_OUT_BF16 if out_dtype == torch.bfloat16 else FP8_OUT_F32
+    if c is None:
+        c = torch.empty((M, N), dtype=out_dtype, device=aq.device)
+    assert c.stride(1) == 1
+    _check(lib().fp8_gemm_blockscaled(_p(aq), _p(sa), _p(bq), _p(sb), int(bmode), M, N, K, _p(c),
+                                      c.stride(0), out_type, _stream(stream)),
+           "fp8_gemm_blockscaled")
+    return c
+
+
+def fp8_grouped_gemm_moe(aq, sa, bq, sb, offsets, out_dtype=torch.bfloat16, c=None,
+                         stream=None):
+    """Y[T, N] per expert; aq uint8 [T, K], bq uint8 [E, N, K], offsets int32 [E+1] (device)."""
+    for t, n in ((aq, "aq"), (sa, "sa"), (bq, "bq"), (sb, "sb"), (offsets, "offsets")):
+        _cuda(t, n)
+    assert offsets.dtype == torch.int32
+    T, K = aq.shape
+    E, N, _ = bq.shape
+    out_type = FP8_OUT_BF16 if out_dtype == torch.bfloat16 else FP8_OUT_F32
+    if c is None:
+        c = torch.empty((T, N), dtype=out_dtype, device=aq.device)
+    assert c.is_contiguous()
+    _check(lib().fp8_grouped_gemm_moe(_p(aq), _p(sa), _p(bq), _p(sb), _p(offsets), E, T, N, K,
+                                      _p(c), out_type, _stream(stream)), "fp8_grouped_gemm_moe")
+    return c

@@ -1,0 +1,169 @@
+/*
+ * fp8fg.h -- C ABI of libfp8fg.so: fine-grained FP8 quantisation and the
+ * block-scaled FP8 GEMM with per-128-K FP32 promotion, for NVIDIA B300
+ * (sm_103a).
+ *
+ * The operations are those of the FP8 mixed-precision framework of the
+ * DeepSeek-V3 Technical Report, section 3.3 (FP8 Training):
+ *   - every GEMM operand (Fprop, Dgrad, Wgrad) is E4M3 (section 3.3.1);
+ *   - activations are quantised per 1x128 tile and weights per 128x128
+ *     block, each group with its own FP32 scale amax/448 (section 3.3.2,
+ *     fine-grained quantization);
+ *   - the scales run along the GEMM inner dimension K, and each 128-wide K
+ *     interval's tensor-core partial sum is promoted to FP32 with the two
+ *     scales applied (section 3.3.2, increasing accumulation precision,
+ *     Figure 7(b));
+ *   - the Wgrad GEMM consumes activations cached in FP8, which needs the
+ *     transposed 128x1 grouping along tokens (sections 3.3.1 and 3.3.3; the
+ *     report's hardware suggestions in section 3.5.2 note that fusing the
+ *     transposition into the GEMM is awkward, so it lives in the quantiser);
+ *   - MoE experts run a grouped GEMM over variable per-expert token counts,
+ *     which is memory bound at decode batch sizes (section 3.4.2 Decoding).
+ *
+ * Conventions for every entry point:
+ *   - Pointers are DEVICE pointers into memory the caller owns.  The library
+ *     allocates nothing, frees nothing and keeps no state beyond a per-device
+ *     cache of the SM count and of kernel attributes.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous on that stream and never synchronise, except
+ *     fp8_device_error().
+ *   - Arguments are validated on the host before anything is launched; a
+ *     rejected call launches nothing and returns a status != FP8_OK.  Launch
+ *     failures come back as FP8_ERR_CUDA.  Nothing throws across the ABI.
+ *   - bfloat16 inputs are row-major with the given row stride (in elements).
+ *     E4M3 codes are the OCP FP8 E4M3 ("fn") encoding, one byte each.
+ *   - Matrix sizes are element counts; leading dimensions are in elements.
+ *   - A size of zero rows is a valid no-op.
+ */
+#ifndef FP8FG_H
+#define FP8FG_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    FP8_OK = 0,
+    FP8_ERR_NULL = 1,        /* a required pointer is NULL */
+    FP8_ERR_SHAPE = 2,       /* a size or leading dimension is invalid */
+    FP8_ERR_ALIGN = 3,       /* a pointer or stride breaks the alignment rule */
+    FP8_ERR_UNSUPPORTED = 4, /* valid request this build does not serve */
+    FP8_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
+    FP8_ERR_TIMEOUT = 6,     /* a kernel gave up waiting on a pipeline barrier */
+    FP8_ERR_DEVICE_SHAPE = 7 /* a kernel found invalid device-side data (offsets) */
+} fp8_status;
+
+/* Output element type of the GEMMs. */
+typedef enum { FP8_OUT_F32 = 0, FP8_OUT_BF16 = 1 } fp8_out_t;
+
+/* Layout of the B-operand scales of fp8_gemm_blockscaled (K = inner dim). */
+typedef enum {
+    FP8_BSCALE_BLOCK128 = 0,   /* sb[N/128][K/128]: one scale per 128x128 block (weights) */
+    FP8_BSCALE_ROW1x128 = 1,   /* sb[K/128][N]: one scale per (row n, K block), i.e. B was
+                                  quantised 1x128 along K (the Wgrad GEMM, whose B is the
+                                  128x1-quantised output gradient) */
+    FP8_BSCALE_BLOCK128_T = 2  /* sb[K/128][N/128]: the 128x128 block grid stored transposed
+                                  (the Dgrad GEMM reusing the Fprop weight scales) */
+} fp8_bscale_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char* fp8_status_str(int status);
+
+/*
+ * fp8_device_error: synchronises `stream`, then returns and clears the
+ * library's device-side error word for the current device: FP8_ERR_TIMEOUT
+ * if a GEMM kernel abandoned a barrier wait (bounded at about two seconds),
+ * FP8_ERR_DEVICE_SHAPE if a grouped GEMM found non-monotone offsets,
+ * FP8_OK otherwise.  FP8_ERR_CUDA if the synchronisation itself failed.
+ */
+int fp8_device_error(void* stream);
+
+/*
+ * fp8_quant_act_1x128 -- 1x128 activation quantisation (report section
+ * 3.3.2, fine-grained quantization; group size 1x128).
+ *   x   : bfloat16 [M][K], row stride ldx.                 (input)
+ *   xq  : E4M3 codes [M][K], row stride ldq.               (output)
+ *   sx  : float [K/128][M]: scale of row m, K group kb at sx[kb*M + m]. (output)
+ * For each row m and group kb: amax = max |x| over the 128 elements,
+ * s = fl32(amax / 448) (s = 1 when amax = 0), q = E4M3_RNE_satfinite(fl32(x / s)).
+ * Requires K % 128 == 0, ldx >= K, ldq >= K, ldx % 8 == 0, ldq % 16 == 0,
+ * x and xq 16-byte aligned, sx 4-byte aligned.  M >= 0.
+ */
+int fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx,
+                        uint8_t* xq, int64_t ldq, float* sx, void* stream);
+
+/*
+ * fp8_quant_act_128x1 -- 128x1 (token-wise transposed) activation quantisation
+ * for the Wgrad GEMM, whose inner dimension is the token dimension M (report
+ * sections 3.3.1-3.3.3; transposition moved out of the GEMM per section 3.5.2).
+ *   x   : bfloat16 [M][K], row stride ldx.                 (input)
+ *   xqT : E4M3 codes [K][M] (transposed, row stride M).    (output)
+ *   sxT : float [M/128][K]: scale of column k, token group mb at sxT[mb*K + k]. (output)
+ * Groups are 128 consecutive tokens of one column; scale and codes as above.
+ * Requires M % 128 == 0, K % 64 == 0, ldx >= K, ldx % 8 == 0, x and xqT
+ * 16-byte aligned, sxT 4-byte aligned.
+ */
+int fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx,
+                        uint8_t* xqT, float* sxT, void* stream);
+
+/*
+ * fp8_quant_weight_128x128 -- 128x128 block weight quantisation (report
+ * section 3.3.2; block size 128x128).
+ *   w   : bfloat16 [K][N] (K = inner dimension of the Fprop GEMM), row stride ldw. (input)
+ *   wq  : E4M3 codes [N][K] (K contiguous: the Fprop B operand), or NULL.  (output)
+ *   wqT : E4M3 codes [K][N] (N contiguous: the Dgrad B operand), or NULL.  (output)
+ *   sw  : float [N/128][K/128]: scale of block (nb, kb) at sw[nb*(K/128) + kb]. (output)
+ * At least one of wq, wqT must be non-NULL.  Requires K % 128 == 0,
+ * N % 128 == 0, ldw >= N, ldw % 8 == 0, w/wq/wqT 16-byte aligned.
+ */
+int fp8_quant_weight_128x128(const void* w, int64_t K, int64_t N, int64_t ldw,
+                             uint8_t* wq, uint8_t* wqT, float* sw, void* stream);
+
+/*
+ * fp8_gemm_blockscaled -- C[M][N] = sum_kb sa[m,kb] * sb(n,kb) * P_kb[m][n],
+ * P_kb[m][n] = sum over k in [128 kb, 128 kb + 128) of aq[m][k] * bq[n][k]
+ * (report section 3.3.2, Figure 7(b): tensor-core partial sums over each
+ * 128-wide K interval, promoted to FP32 with the two scales applied).
+ *   aq : E4M3 [M][K], K contiguous (row stride K).                    (input)
+ *   sa : float [K/128][M]  (layout of fp8_quant_act_1x128 / 128x1).   (input)
+ *   bq : E4M3 [N][K], K contiguous (row stride K).                    (input)
+ *   sb : float, layout per `bmode` (fp8_bscale_t).                    (input)
+ *   c  : [M][N] row stride ldc, float (FP8_OUT_F32) or bfloat16 RNE (FP8_OUT_BF16). (output)
+ * Partial sums are exact-order FP32 tensor-core accumulations of one K block;
+ * promotion and the cross-block sum are FP32 fused multiply-adds.
+ * Requires K % 128 == 0, K > 0, N % 128 == 0, ldc >= N, ldc*elt % 16 == 0,
+ * aq/bq/c 16-byte aligned, sa/sb 4-byte aligned, M >= 0.
+ */
+int fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, const uint8_t* bq,
+                         const float* sb, int bmode, int64_t M, int64_t N, int64_t K,
+                         void* c, int64_t ldc, int out_type, void* stream);
+
+/*
+ * fp8_grouped_gemm_moe -- per-expert block-scaled GEMM over rows grouped by
+ * expert (report section 3.4: MoE expert GEMMs; section 3.4.2: decode-time
+ * batches of at most a few hundred tokens per expert are memory bound).
+ *   aq      : E4M3 [T][K], rows of expert e at offsets[e] .. offsets[e+1]-1. (input)
+ *   sa      : float [K/128][T].                                            (input)
+ *   bq      : E4M3 [E][N][K] (each expert's weight, K contiguous).         (input)
+ *   sb      : float [E][N/128][K/128].                                     (input)
+ *   offsets : int32 [E+1] in DEVICE memory, offsets[0] = 0, non-decreasing,
+ *             offsets[E] <= T.  Read by the kernel (no host synchronisation);
+ *             invalid offsets make the kernel skip all work and raise
+ *             FP8_ERR_DEVICE_SHAPE in fp8_device_error().                 (input)
+ *   c       : [T][N] row stride N, float or bfloat16 per out_type.  Rows not
+ *             covered by any expert are left untouched.                    (output)
+ * Same per-expert arithmetic as fp8_gemm_blockscaled with FP8_BSCALE_BLOCK128.
+ * Requires 1 <= E <= 65536, T >= 0, K % 128 == 0, K > 0, N % 128 == 0,
+ * aq/bq/c 16-byte aligned, sa/sb/offsets 4-byte aligned.
+ */
+int fp8_grouped_gemm_moe(const uint8_t* aq, const float* sa, const uint8_t* bq,
+                         const float* sb, const int32_t* offsets, int32_t E, int64_t T,
+                         int64_t N, int64_t K, void* c, int out_type, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FP8FG_H */

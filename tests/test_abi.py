@@ -1,0 +1,84 @@
+"""The C-ABI library builds, loads and exports every entry point of
+include/fp8fg.h; host-side argument validation rejects bad calls before any
+launch (these calls touch no GPU, so they run on a CPU-only host too)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from fp8_fine_grained_22_b300 import build, fp8fg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "fp8fg.h")
+
+OK, NULL, SHAPE, ALIGN, UNSUP = 0, 1, 2, 3, 4
+
+
+def header_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(fp8_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_builds_and_exports_every_declared_symbol():
+    path = build.build()
+    assert os.path.exists(path)
+    lib = ctypes.CDLL(path)
+    declared = header_functions()
+    assert set(declared) == set(fp8fg.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    assert fp8fg.status_str(0) == "ok"
+    assert "shape" in fp8fg.status_str(SHAPE)
+    assert fp8fg.status_str(12345) == "unknown status"
+
+
+A16 = 1 << 20  # a 16-byte aligned fake address: validation never dereferences it
+
+
+@pytest.mark.parametrize("args,want", [
+    ((A16, 4, 100, 128, A16, 128, A16), SHAPE),       # K % 128
+    ((A16, -1, 128, 128, A16, 128, A16), SHAPE),      # M < 0
+    ((A16, 4, 128, 64, A16, 128, A16), SHAPE),        # ldx < K
+    ((A16, 0, 128, 128, 0, 128, 0), OK),              # M == 0: no-op, pointers unused
+    ((0, 4, 128, 128, A16, 128, A16), NULL),
+    ((A16 + 2, 4, 128, 128, A16, 128, A16), ALIGN),   # x not 16-byte aligned
+    ((A16, 4, 128, 132, A16, 128, A16), ALIGN),       # ldx % 8
+    ((A16, 4, 128, 128, A16, 136, A16), ALIGN),       # ldq % 16
+])
+def test_quant_1x128_validation(args, want):
+    assert fp8fg.lib().fp8_quant_act_1x128(*args, None) == want
+
+
+def test_other_quantiser_validation():
+    L = fp8fg.lib()
+    assert L.fp8_quant_act_128x1(A16, 100, 64, 64, A16, A16, None) == SHAPE   # M % 128
+    assert L.fp8_quant_act_128x1(A16, 128, 96, 96, A16, A16, None) == SHAPE   # K % 64
+    assert L.fp8_quant_act_128x1(A16, 128, 64, 64, 0, A16, None) == NULL
+    assert L.fp8_quant_weight_128x128(A16, 128, 100, 128, A16, 0, A16, None) == SHAPE
+    assert L.fp8_quant_weight_128x128(A16, 128, 128, 128, 0, 0, A16, None) == NULL
+    assert L.fp8_quant_weight_128x128(A16, 128, 128, 128, A16 + 8, 0, A16, None) == ALIGN
+
+
+def test_gemm_validation():
+    L = fp8fg.lib()
+    g = L.fp8_gemm_blockscaled
+    assert g(A16, A16, A16, A16, 0, 16, 100, 128, A16, 100, 1, None) == SHAPE   # N % 128
+    assert g(A16, A16, A16, A16, 0, 16, 128, 64, A16, 128, 1, None) == SHAPE    # K % 128
+    assert g(A16, A16, A16, A16, 0, 16, 128, 128, A16, 64, 1, None) == SHAPE    # ldc < N
+    assert g(A16, A16, A16, A16, 7, 16, 128, 128, A16, 128, 1, None) == UNSUP   # bmode
+    assert g(A16, A16, A16, A16, 0, 16, 128, 128, A16, 128, 9, None) == UNSUP   # out type
+    assert g(A16, A16, A16, A16, 0, 0, 128, 128, 0, 128, 1, None) == OK         # M == 0
+    assert g(A16, 0, A16, A16, 0, 16, 128, 128, A16, 128, 1, None) == NULL
+    assert g(A16 + 4, A16, A16, A16, 0, 16, 128, 128, A16, 128, 1, None) == ALIGN
+    assert g(A16, A16 + 2, A16, A16, 0, 16, 128, 128, A16, 128, 1, None) == ALIGN
+    assert g(A16, A16, A16, A16, 0, 16, 128, 128, A16, 132, 1, None) == ALIGN   # ldc*2 % 16
+    gg = L.fp8_grouped_gemm_moe
+    assert gg(A16, A16, A16, A16, A16, 0, 16, 128, 128, A16, 1, None) == SHAPE  # E < 1
+    assert gg(A16, A16, A16, A16, A16, 2, 0, 128, 128, 0, 1, None) == OK        # T == 0
+    assert gg(A16, A16, A16, A16, 0, 2, 16, 128, 128, A16, 1, None) == NULL
+    assert gg(A16, A16, A16, A16, A16 + 2, 2, 16, 128, 128, A16, 1, None) == ALIGN
