@@ -219,16 +219,17 @@ def run_ours(args, rank, world, local):
         step()
         yh.copy_(y, non_blocking=True)
 
+    e2e_steps = min(args.steps, args.e2e_steps)
     for _ in range(max(1, args.warmup)):
         e2e_step()
     torch.cuda.synchronize()
     e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e_start.record(stream)
-    for _ in range(args.steps):
+    for _ in range(e2e_steps):
         e2e_step()
     e_end.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e_start.elapsed_time(e_end) / args.steps
+    e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
     if world > 1:
         t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -265,7 +266,7 @@ def run_ours(args, rank, world, local):
                    "step": ["fp8_quant_act_1x128", "fp8_quant_weight_128x128",
                             "fp8_gemm_blockscaled"]},
         "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": h2d,
+                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * args.steps,
         "roofline": {"kernel": "fp8_gemm_blockscaled", "bound": "tensor",
@@ -355,7 +356,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")

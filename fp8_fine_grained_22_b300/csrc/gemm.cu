@@ -41,6 +41,15 @@ constexpr int kThreads = (2 + kEpiWarps) * 32;
 constexpr long long kWaitLimit = 1LL << 32;  // cycles (about 2 s at 2 GHz)
 constexpr int kSmemLimit = 232448;    // 227 KB opt-in per CTA
 
+// Output staging: each epilogue warp owns kOutSlots swizzled 4 KB boxes
+// (32 rows x 128 bytes); a TMA store is only waited on when its slot comes
+// round again, so the store of one tile overlaps the next tile's K loop.
+#ifndef FP8FG_OUT_SLOTS
+#define FP8FG_OUT_SLOTS 2
+#endif
+constexpr int kOutSlots = FP8FG_OUT_SLOTS;
+constexpr int kBoxBytes = 32 * 128;
+
 template <int BN, bool ROWSCALE>
 struct Cfg {
     static constexpr int A_BYTES = BM * BK;
@@ -48,7 +57,7 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int COLS = BN / 2;           // columns per epilogue thread
     static constexpr int TMEM_COLS = 2 * BN;      // two partial buffers
-    static constexpr int CSTAGE_BYTES = kEpiWarps * 4096;
+    static constexpr int CSTAGE_BYTES = kEpiWarps * kOutSlots * kBoxBytes;
     static constexpr int RSCALE_BYTES = ROWSCALE ? 2 * BN * 4 : 0;
     static constexpr int HEADER = 256;            // barriers, TMEM slot, flags
     static constexpr int FIXED = HEADER + 1023 + CSTAGE_BYTES + RSCALE_BYTES;
@@ -327,45 +336,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ew = warp - 2;              // 0..7
         const int q = warp & 3;               // TMEM lane quadrant of this warp
         const int cg = ew >> 2;               // column half of the tile
-        uint8_t* my_cstage = cstage + ew * 4096;
-        const int64_t NB = p.N / 128;
+        uint8_t* my_cstage = cstage + ew * kOutSlots * kBoxBytes;
+        uint32_t boxes = 0;  // TMA boxes this warp has stored so far
+        const int KBi = static_cast<int>(KB);
+        const int NB = static_cast<int>(p.N / 128);
+        const int lds_a = static_cast<int>(p.lds_a);
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + cg * COLS;
         uint32_t kbg = 0;
         bool ok = !aborted_at_start;
         for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
             Tile ti;
             if (!get_tile<BN, GROUPED>(p, t, ti)) break;
-            const int64_t row = ti.row0 + q * 32 + lane;
+            const int row = static_cast<int>(ti.row0) + q * 32 + lane;
+            const int row_end = static_cast<int>(ti.row_end);
+            const int ncol0 = static_cast<int>(ti.n0) + cg * COLS;
+            // A-row scales: sa[kb * lds_a + row]; rows past the allocation read 0
+            const float* sa_ptr = p.sa + (row < p.M ? row : 0);
             const bool row_in_alloc = row < p.M;
-            const int64_t ncol0 = ti.n0 + cg * COLS;
-            const int64_t nb = ncol0 / 128;
-            const float* sb_e = p.sb + (GROUPED ? ti.expert * p.sb_expert : 0);
-            auto b_scale_at = [&](int64_t kb) -> float {
-                return p.bmode == FP8_BSCALE_BLOCK128 ? __ldg(sb_e + nb * KB + kb)
-                                                      : __ldg(sb_e + kb * NB + nb);
-            };
-            const int rcol = ew * 32 + lane;  // ROWSCALE: column this thread stages
-            auto row_scale_at = [&](int64_t kb) -> float {
-                return rcol < BN ? __ldg(p.sb + kb * p.ld_sb + ti.n0 + rcol) : 0.0f;
-            };
-            float sa_next = row_in_alloc ? __ldg(p.sa + row) : 0.0f;
-            float sb_next = ROWSCALE ? row_scale_at(0) : b_scale_at(0);
+            // B scales: one per (128-column block, K block) for the block modes
+            const float* sb_ptr;
+            int sb_step;
+            if (ROWSCALE) {
+                const int rcol = ew * 32 + lane;  // column this thread stages
+                sb_ptr = p.sb + ti.n0 + (rcol < BN ? rcol : 0);
+                sb_step = static_cast<int>(p.ld_sb);
+            } else {
+                const float* sb_e = p.sb + (GROUPED ? ti.expert * p.sb_expert : 0);
+                const int nb = ncol0 / 128;
+                const bool blk = p.bmode == FP8_BSCALE_BLOCK128;
+                sb_ptr = sb_e + (blk ? nb * KBi : nb);
+                sb_step = blk ? 1 : NB;
+            }
+            float sa_next = row_in_alloc ? __ldg(sa_ptr) : 0.0f;
+            float sb_next = __ldg(sb_ptr);
 
             uint64_t acc[COLS / 2];
 #pragma unroll
             for (int i = 0; i < COLS / 2; ++i) acc[i] = 0;
 
-            for (int64_t kb = 0; kb < KB; ++kb, ++kbg) {
+            for (int kb = 0; kb < KBi; ++kb, ++kbg) {
                 const float sa_cur = sa_next, sb_cur = sb_next;
-                if (kb + 1 < KB) {
-                    sa_next = row_in_alloc ? __ldg(p.sa + (kb + 1) * p.lds_a + row) : 0.0f;
-                    sb_next = ROWSCALE ? row_scale_at(kb + 1) : b_scale_at(kb + 1);
+                if (kb + 1 < KBi) {
+                    sa_next = row_in_alloc ? __ldg(sa_ptr + (kb + 1) * lds_a) : 0.0f;
+                    sb_next = __ldg(sb_ptr + (kb + 1) * sb_step);
                 }
                 const uint32_t buf = kbg & 1u, tph = (kbg >> 1) & 1u;
                 if (ROWSCALE) {
                     // buffer `buf` was last read in K block kbg-2; every warp
                     // arrived on this buffer's barrier for kbg-1 only after
                     // finishing that read, so it is free to overwrite here.
-                    if (rcol < BN) rscale[buf * BN + rcol] = sb_cur;
+                    if (ew * 32 + lane < BN) rscale[buf * BN + ew * 32 + lane] = sb_cur;
                     __syncwarp();
                     if (lane == 0) mbar_arrive(rs_bar(buf));
                     if (!wait_bar_warp(rs_bar(buf), tph, abort_flag)) {
@@ -378,11 +398,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t taddr =
-                    tmem_base + (static_cast<uint32_t>(q * 32) << 16) + buf * BN + cg * COLS;
+                const uint32_t taddr = t_lane + buf * BN;
                 if (!ROWSCALE) {
                     const float sc = sa_cur * sb_cur;
                     const uint64_t sc2 = pack2(f2u(sc), f2u(sc));
+                    // 16-column loads: with 128 accumulator registers per
+                    // thread, wider loads spill under the 168-register cap
 #pragma unroll
                     for (int ch = 0; ch < COLS / 16; ++ch) {
                         uint32_t r[16];
@@ -417,11 +438,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
 
             // ---------------------------------------------------- tile store
-            const int64_t wrow0 = ti.row0 + q * 32;
-            if (wrow0 + 32 <= ti.row_end) {
+            const int wrow0 = static_cast<int>(ti.row0) + q * 32;
+            if (wrow0 + 32 <= row_end) {
                 // whole 32-row box valid: stage with the 128-byte swizzle, TMA store
 #pragma unroll
-                for (int bx = 0; bx < COLS / BOX_COLS; ++bx) {
+                for (int bx = 0; bx < COLS / BOX_COLS; ++bx, ++boxes) {
+                    uint8_t* slot = my_cstage + (boxes % kOutSlots) * kBoxBytes;
+                    // the store that last used this slot must have read it
+                    if (lane == 0 && boxes >= static_cast<uint32_t>(kOutSlots))
+                        bulk_wait_group_read<kOutSlots - 1>();
+                    __syncwarp();
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         uint4 v;
@@ -436,21 +462,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            static_cast<uint32_t>(acc[a0 + 1]),
                                            static_cast<uint32_t>(acc[a0 + 1] >> 32));
                         }
-                        *reinterpret_cast<uint4*>(my_cstage + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
+                        *reinterpret_cast<uint4*>(slot + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmC, smem_addr(my_cstage),
-                                     static_cast<int>(ncol0 + bx * BOX_COLS), static_cast<int>(wrow0));
+                        tma_store_2d(&tmC, smem_addr(slot), ncol0 + bx * BOX_COLS, wrow0);
                         bulk_commit_group();
-                        bulk_wait_group_read0();
                     }
-                    __syncwarp();
                 }
-            } else if (row < ti.row_end) {
+            } else if (row < row_end) {
                 // ragged rows: direct 16-byte stores of this thread's row
-                uint8_t* dst = static_cast<uint8_t*>(p.c) + (row * p.ldc + ncol0) * ELT;
+                uint8_t* dst = static_cast<uint8_t*>(p.c) +
+                               (static_cast<int64_t>(row) * p.ldc + ncol0) * ELT;
 #pragma unroll
                 for (int j = 0; j < COLS * ELT / 16; ++j) {
                     uint4 v;

@@ -176,7 +176,8 @@ def grouped_gemm(aq, sa, bq, sb, offsets, rows=None, nthreads=None):
 
     aq: uint8 [T, K] rows grouped by expert; sa: f32 [K/128, T];
     bq: uint8 [E, N, K]; sb: f32 [E, N/128, K/128];
-    offsets: int [E+1], rows offsets[e]..offsets[e+1]-1 belong to expert e.
+    offsets: int [E+1], rows offsets[e]..offsets[e+1]-1 belong to expert e
+    (rows at or past offsets[E] belong to no expert and may not be requested).
     Each row of Y is the dense product of that row with its expert's weight.
     """
     aq = _c(aq, np.uint8)
@@ -186,11 +187,13 @@ def grouped_gemm(aq, sa, bq, sb, offsets, rows=None, nthreads=None):
     offsets = np.asarray(offsets, dtype=np.int64)
     T, K = aq.shape
     E, N, _ = bq.shape
-    assert offsets.shape == (E + 1,) and offsets[0] == 0 and offsets[-1] == T
+    assert offsets.shape == (E + 1,) and offsets[0] == 0 and offsets[-1] <= T
+    assert np.all(np.diff(offsets) >= 0)
     if rows is None:
-        rows = np.arange(T, dtype=np.int64)
+        rows = np.arange(offsets[-1], dtype=np.int64)
     rows = np.asarray(rows, dtype=np.int64)
     out = np.empty((rows.size, N), np.float64)
+    assert rows.size == 0 or rows.max() < offsets[-1]
     expert_of = np.searchsorted(offsets, rows, side="right") - 1
     for e in range(E):
         sel = np.nonzero(expert_of == e)[0]

@@ -128,7 +128,9 @@ def _workload_parity(wl, n_rows_per_expert=4):
 
 def test_moe_prefill_workload():
     wl = inputs.moe_prefill()
-    assert wl.offsets[-1] > 8000  # skewed routing keeps roughly T*8*32/256 rows
+    counts = np.diff(wl.offsets)
+    # the biased routing is skewed: empty experts next to experts with thousands of rows
+    assert counts.min() == 0 and counts.max() > 1000
     _workload_parity(wl)
 
 
