@@ -61,9 +61,13 @@ def measured_peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
 
 
+GEMM_SOURCES = ("common.cuh", "gemm.cu", "ptx.cuh")
+
+
 def source_hash():
+    """Hash of the sources the GEMM kernel is built from."""
     h = hashlib.sha256()
-    for name in sorted(os.listdir(CSRC)):
+    for name in GEMM_SOURCES:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())

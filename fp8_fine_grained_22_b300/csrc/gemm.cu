@@ -37,7 +37,18 @@ __device__ unsigned int g_dev_error;
 constexpr int BM = 128;               // rows per tile (TMEM lanes)
 constexpr int BK = 128;               // K block = promotion interval
 constexpr int kEpiWarps = 8;          // 2 per TMEM lane quadrant
-constexpr int kThreads = (2 + kEpiWarps) * 32;
+constexpr int kEpiWarp0 = 4;          // epilogue = warpgroups 1 and 2
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;
+// Register split (setmaxnreg): the kernel is compiled for kLaunchRegs per
+// thread (the cap 384 threads leave); the control warpgroup drops to
+// kCtrlRegs and the two epilogue warpgroups rise to kEpiRegs.  The split must
+// not exceed the launch allocation, or setmaxnreg.inc would wait forever:
+// 128 * kCtrlRegs + 256 * kEpiRegs == 384 * kLaunchRegs.  The host refuses to
+// launch a build whose register count differs from kLaunchRegs.
+constexpr int kLaunchRegs = 168;
+constexpr int kCtrlRegs = 40;
+constexpr int kEpiRegs = 232;
+static_assert(128 * kCtrlRegs + 256 * kEpiRegs <= kThreads * kLaunchRegs, "register split");
 constexpr long long kWaitLimit = 1LL << 32;  // cycles (about 2 s at 2 GHz)
 constexpr int kSmemLimit = 232448;    // 227 KB opt-in per CTA
 
@@ -255,6 +266,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t KB = p.K / BK;
     const bool aborted_at_start = *abort_flag != 0;
 
+    if (warp < kEpiWarp0) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
+    }
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0 && !aborted_at_start) {
@@ -328,12 +342,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         }
-    } else {
+    } else if (warp >= kEpiWarp0) {
         // ------------------------------------------------- promotion epilogue
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
         constexpr int COLS = C::COLS;
         constexpr int ELT = OUT_BF16 ? 2 : 4;
         constexpr int BOX_COLS = 128 / ELT;  // one 128-byte swizzle row per box row
-        const int ew = warp - 2;              // 0..7
+        const int ew = warp - kEpiWarp0;      // 0..7
         const int q = warp & 3;               // TMEM lane quadrant of this warp
         const int cg = ew >> 2;               // column half of the tile
         uint8_t* my_cstage = cstage + ew * kOutSlots * kBoxBytes;
@@ -402,15 +417,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ROWSCALE) {
                     const float sc = sa_cur * sb_cur;
                     const uint64_t sc2 = pack2(f2u(sc), f2u(sc));
-                    // 16-column loads: with 128 accumulator registers per
-                    // thread, wider loads spill under the 168-register cap
+                    // 32-column TMEM loads, software-pipelined: the load of
+                    // chunk ch+1 is in flight while chunk ch is accumulated
+                    uint32_t ra[32], rb[32];
+                    tmem_ld32(taddr, ra);
+                    tmem_wait_ld(ra);
 #pragma unroll
-                    for (int ch = 0; ch < COLS / 16; ++ch) {
-                        uint32_t r[16];
-                        tmem_ld16_wait(taddr + ch * 16, r);
+                    for (int ch = 0; ch < COLS / 32; ++ch) {
+                        uint32_t (&cur)[32] = (ch & 1) ? rb : ra;
+                        uint32_t (&nxt)[32] = (ch & 1) ? ra : rb;
+                        if (ch + 1 < COLS / 32) {
+                            tmem_ld32(taddr + (ch + 1) * 32, nxt);
+                        } else {
+                            // the whole partial is in registers: hand the TMEM
+                            // buffer back before the last chunk's FMAs
+                            tc_fence_before_sync();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(tempty_bar(buf));
+                        }
 #pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            acc[ch * 8 + i] = ffma2(pack2(r[2 * i], r[2 * i + 1]), sc2, acc[ch * 8 + i]);
+                        for (int i = 0; i < 16; ++i)
+                            acc[ch * 16 + i] =
+                                ffma2(pack2(cur[2 * i], cur[2 * i + 1]), sc2, acc[ch * 16 + i]);
+                        if (ch + 1 < COLS / 32) tmem_wait_ld(nxt);
                     }
                 } else {
                     const uint64_t sa2 = pack2(f2u(sa_cur), f2u(sa_cur));
@@ -430,10 +459,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             acc[ch * 8 + 2 * i + 1] = ffma2(p1, sa2, acc[ch * 8 + 2 * i + 1]);
                         }
                     }
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty_bar(buf));
                 }
-                tc_fence_before_sync();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tempty_bar(buf));
             }
             if (!ok) break;
 
@@ -541,6 +570,10 @@ static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t 
     if (sms <= 0) return FP8_ERR_CUDA;
     static bool attr_done[kMaxDevices] = {false};
     if (!attr_done[dev]) {
+        // the setmaxnreg split is only safe for the register count it was sized for
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return FP8_ERR_CUDA;
+        if (fa.numRegs != kLaunchRegs) return FP8_ERR_UNSUPPORTED;
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
             cudaSuccess)
             return FP8_ERR_CUDA;

@@ -4,9 +4,10 @@
 // needs, sections 3.3.1-3.3.3 and 3.5.2).
 //
 // Every group: amax = max |x|; s = fl32(amax / 448) (s = 1 for amax = 0);
-// q = E4M3 RNE saturating conversion of fl32(x / s).  The divisions are
-// IEEE round-to-nearest (no fast-math, no flush-to-zero), so the codes and
-// scales are exact functions of the bf16 inputs.
+// q = E4M3 RNE saturating conversion of fl32(x / s).  The scale is an IEEE
+// division and the quotients are correctly rounded (GroupDiv below); nothing
+// is flushed to zero, so the codes and scales are exact functions of the
+// bf16 inputs.
 //
 // The kernels are HBM streams: 16-byte vector loads with the evict-first
 // hint, group amax by warp shuffles (1x128) or a shared-memory tile
@@ -25,193 +26,343 @@ __device__ __forceinline__ float group_scale(float amax) {
     return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
 }
 
-// E4M3 codes of x0 / s and x1 / s, x0 in the low byte.
-__device__ __forceinline__ uint32_t quant_pair(float x0, float x1, float s) {
-    float2 v = make_float2(__fdiv_rn(x0, s), __fdiv_rn(x1, s));
-    return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(v, __NV_SATFINITE, __NV_E4M3));
+__device__ __forceinline__ uint64_t f2x2(float lo, float hi) {
+    return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
 }
 
-// Four E4M3 codes packed little-endian.
-__device__ __forceinline__ uint32_t quant_quad(float a, float b, float c, float d, float s) {
-    return quant_pair(a, b, s) | (quant_pair(c, d, s) << 16);
-}
+// Division of every element of a group by its scale s, correctly rounded,
+// from one reciprocal per group.  Markstein's correction (P. Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. Res. Dev. 34(1), 1990): with r = RN(1/s) and
+// q0 = RN(x r), the residual e = x - q0 s is exact under a fused
+// multiply-add and RN(q0 + e r) is the correctly rounded quotient x / s.
+// Two lanes at a time with the packed FP32 instructions.  The sign of a zero
+// quotient is taken from x (s > 0).  The residual is exact only while it does
+// not underflow, i.e. for |x| >= 2^-102; with s >= 2^-91 every smaller x has
+// |x / s| < 2^-11 and encodes to a signed zero whatever the last bit of its
+// quotient, so the corrected path is used for s >= 2^-91 and groups with a
+// smaller scale take the IEEE division.  The tests compare the resulting
+// codes with IEEE division over every (x, amax) bf16 pair.
+struct GroupDiv {
+    float s;
+    uint64_t r2, ns2;
+    bool fast;
+    __device__ __forceinline__ explicit GroupDiv(float scale) : s(scale) {
+        const float r = __frcp_rn(scale);
+        r2 = f2x2(r, r);
+        ns2 = f2x2(-scale, -scale);
+        fast = scale >= 0x1p-91f;
+    }
+    // E4M3 codes of x0 / s and x1 / s, x0 in the low byte
+    __device__ __forceinline__ uint32_t pair(float x0, float x1) const {
+        float q0, q1;
+        if (fast) {
+            const uint64_t x2 = f2x2(x0, x1);
+            const uint64_t a = mul2(x2, r2);
+            const uint64_t e = fma2(a, ns2, x2);
+            const uint64_t q = fma2(e, r2, a);
+            q0 = copysignf(__uint_as_float(static_cast<uint32_t>(q)), x0);
+            q1 = copysignf(__uint_as_float(static_cast<uint32_t>(q >> 32)), x1);
+        } else {
+            q0 = __fdiv_rn(x0, s);
+            q1 = __fdiv_rn(x1, s);
+        }
+        return static_cast<uint32_t>(
+            __nv_cvt_float2_to_fp8x2(make_float2(q0, q1), __NV_SATFINITE, __NV_E4M3));
+    }
+    // four codes packed little-endian
+    __device__ __forceinline__ uint32_t quad(float a, float b, float c, float d) const {
+        return pair(a, b) | (pair(c, d) << 16);
+    }
+};
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     return __ldcs(reinterpret_cast<const uint4*>(p));
 }
 
+// All three kernels are persistent: a grid of a few CTAs per SM walks the
+// tiles with a stride of the grid size, and each thread issues the loads of
+// its next tile before it processes the current one, so HBM reads stay in
+// flight through the compute and store phases.
+constexpr int kQuantThreads = 256;
+constexpr int kQuantCtasPerSm = 4;
+
+// Largest magnitude in a word of two bf16 values, as a packed bf16 pair
+// (exact: max and abs of bf16 values do not round).
+__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
+    const __nv_bfloat162 r = __hmax2(__habs2(*reinterpret_cast<const __nv_bfloat162*>(&a)),
+                                     __habs2(*reinterpret_cast<const __nv_bfloat162*>(&b)));
+    return *reinterpret_cast<const uint32_t*>(&r);
+}
+__device__ __forceinline__ float amax_of_pair(uint32_t w) {
+    return fmaxf(bf16_lo(w), bf16_hi(w));  // both halves already non-negative
+}
+
 // ------------------------------------------------------------------ 1x128 --
-// CTA: 64 rows x one 128-wide K group.  16 lanes per group, 8 elements per
-// lane, 4 rows per thread (rows g, g+16, g+32, g+48) so that every thread has
-// four 16-byte loads in flight.
+// Tile: 64 rows x one 128-wide K group.  Four lanes per group, 32 elements
+// (four 16-byte loads) per lane, one row per thread.  Tiles are numbered
+// K-group fastest.
 constexpr int kQ1Rows = 64;
 
-__global__ void __launch_bounds__(256) quant_act_1x128_kernel(const uint16_t* __restrict__ x,
-                                                              int64_t M, int64_t ldx,
-                                                              uint8_t* __restrict__ xq,
-                                                              int64_t ldq,
-                                                              float* __restrict__ sx) {
-    const int l16 = threadIdx.x & 15;
-    const int g = threadIdx.x >> 4;
-    const int64_t kb = blockIdx.y;
-    const int64_t m0 = static_cast<int64_t>(blockIdx.x) * kQ1Rows;
+__device__ __forceinline__ void load_1x128(const uint16_t* __restrict__ x, int64_t M, int64_t ldx,
+                                           int64_t KB, int64_t t, int row, int l4, uint4 (&v)[4]) {
+    const int64_t kb = t % KB;
+    const int64_t m = (t / KB) * kQ1Rows + row;
+    const uint16_t* src = x + m * ldx + kb * 128 + l4 * 32;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = (m < M) ? ld_stream_v4(src + 8 * i) : make_uint4(0, 0, 0, 0);
+}
+
+__global__ void __launch_bounds__(kQuantThreads) quant_act_1x128_kernel(
+    const uint16_t* __restrict__ x, int64_t M, int64_t KB, int64_t ldx, uint8_t* __restrict__ xq,
+    int64_t ldq, float* __restrict__ sx, int64_t tiles) {
+    const int l4 = threadIdx.x & 3;
+    const int row = threadIdx.x >> 2;  // 0..63
+    int64_t t = blockIdx.x;
     uint4 v[4];
+    if (t < tiles) load_1x128(x, M, ldx, KB, t, row, l4, v);
+    while (t < tiles) {
+        const int64_t tn = t + gridDim.x;
+        uint4 vn[4];
+        if (tn < tiles) load_1x128(x, M, ldx, KB, tn, row, l4, vn);
+        const int64_t kb = t % KB;
+        const int64_t m = (t / KB) * kQ1Rows + row;
+        uint32_t mx = absmax_bf16x2(v[0].x, v[0].y);
+        mx = absmax_bf16x2(mx, absmax_bf16x2(v[0].z, v[0].w));
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int64_t m = m0 + g + 16 * i;
-        v[i] = (m < M) ? ld_stream_v4(x + m * ldx + kb * 128 + l16 * 8) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int64_t m = m0 + g + 16 * i;
-        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-        float f[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            f[2 * j] = bf16_lo(w[j]);
-            f[2 * j + 1] = bf16_hi(w[j]);
+        for (int i = 1; i < 4; ++i) {
+            mx = absmax_bf16x2(mx, absmax_bf16x2(v[i].x, v[i].y));
+            mx = absmax_bf16x2(mx, absmax_bf16x2(v[i].z, v[i].w));
         }
-        float amax = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(f[j]));
-#pragma unroll
-        for (int off = 8; off >= 1; off >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        float amax = amax_of_pair(mx);
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
         const float s = group_scale(amax);
+        const GroupDiv dv(s);
         if (m < M) {
-            uint2 q;
-            q.x = quant_quad(f[0], f[1], f[2], f[3], s);
-            q.y = quant_quad(f[4], f[5], f[6], f[7], s);
-            *reinterpret_cast<uint2*>(xq + m * ldq + kb * 128 + l16 * 8) = q;
-            if (l16 == 0) sx[kb * M + m] = s;
+            uint4 o[2];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t a = dv.quad(bf16_lo(v[i].x), bf16_hi(v[i].x), bf16_lo(v[i].y),
+                                           bf16_hi(v[i].y));
+                const uint32_t b = dv.quad(bf16_lo(v[i].z), bf16_hi(v[i].z), bf16_lo(v[i].w),
+                                           bf16_hi(v[i].w));
+                if (i & 1) {
+                    o[i >> 1].z = a;
+                    o[i >> 1].w = b;
+                } else {
+                    o[i >> 1].x = a;
+                    o[i >> 1].y = b;
+                }
+            }
+            uint4* dst = reinterpret_cast<uint4*>(xq + m * ldq + kb * 128 + l4 * 32);
+            dst[0] = o[0];
+            dst[1] = o[1];
+            if (l4 == 0) sx[kb * M + m] = s;
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = vn[i];
+        t = tn;
     }
 }
 
 // ------------------------------------------------------------------ 128x1 --
-// CTA: one 128-token group x 64 columns.  The bf16 tile is staged in shared
-// memory; each thread then owns one column and a quarter of the 128 rows.
-__global__ void __launch_bounds__(256) quant_act_128x1_kernel(const uint16_t* __restrict__ x,
-                                                              int64_t M, int64_t K, int64_t ldx,
-                                                              uint8_t* __restrict__ xqT,
-                                                              float* __restrict__ sxT) {
+// Tile: one 128-token group x 64 columns, staged in shared memory; each
+// thread then owns one column and a quarter of the 128 rows.  Tiles are
+// numbered column-block fastest.
+__device__ __forceinline__ void load_128x1(const uint16_t* __restrict__ x, int64_t ldx,
+                                           int64_t KC, int64_t t, int tid, uint4 (&v)[4]) {
+    const int64_t k0 = (t % KC) * 64;
+    const int64_t m0 = (t / KC) * 128;
+    const int ch = tid & 7;
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const int row = (tid >> 3) + 32 * p;
+        v[p] = ld_stream_v4(x + (m0 + row) * ldx + k0 + ch * 8);
+    }
+}
+
+__global__ void __launch_bounds__(kQuantThreads) quant_act_128x1_kernel(
+    const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t ldx, uint8_t* __restrict__ xqT,
+    float* __restrict__ sxT, int64_t tiles) {
     __shared__ __align__(16) uint16_t tile[128][64];
     __shared__ float part[4][64];
-    const int t = threadIdx.x;
-    const int64_t k0 = static_cast<int64_t>(blockIdx.x) * 64;
-    const int64_t mb = blockIdx.y;
-    const int64_t m0 = mb * 128;
-    {
-        const int ch = t & 7;
-        uint4 v[4];
+    const int t0 = threadIdx.x;
+    const int64_t KC = K / 64;
+    int64_t t = blockIdx.x;
+    uint4 v[4];
+    if (t < tiles) load_128x1(x, ldx, KC, t, t0, v);
+    while (t < tiles) {
+        const int64_t k0 = (t % KC) * 64;
+        const int64_t mb = t / KC;
+        const int64_t m0 = mb * 128;
+        {
+            const int ch = t0 & 7;
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const int row = (t >> 3) + 32 * p;
-            v[p] = ld_stream_v4(x + (m0 + row) * ldx + k0 + ch * 8);
+            for (int p = 0; p < 4; ++p) {
+                const int row = (t0 >> 3) + 32 * p;
+                *reinterpret_cast<uint4*>(&tile[row][ch * 8]) = v[p];
+            }
         }
+        const int64_t tn = t + gridDim.x;
+        if (tn < tiles) load_128x1(x, ldx, KC, tn, t0, v);  // next tile's loads in flight
+        __syncthreads();
+        const int c = t0 & 63;
+        const int qr = t0 >> 6;
+        float f[32];
+        float amax = 0.0f;
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const int row = (t >> 3) + 32 * p;
-            *reinterpret_cast<uint4*>(&tile[row][ch * 8]) = v[p];
+        for (int i = 0; i < 32; ++i) {
+            f[i] = __uint_as_float(static_cast<uint32_t>(tile[qr * 32 + i][c]) << 16);
+            amax = fmaxf(amax, fabsf(f[i]));
         }
+        part[qr][c] = amax;
+        __syncthreads();
+        amax = fmaxf(fmaxf(part[0][c], part[1][c]), fmaxf(part[2][c], part[3][c]));
+        const float s = group_scale(amax);
+        const GroupDiv dv(s);
+        if (qr == 0) sxT[mb * K + k0 + c] = s;
+        uint4 o0, o1;
+        o0.x = dv.quad(f[0], f[1], f[2], f[3]);
+        o0.y = dv.quad(f[4], f[5], f[6], f[7]);
+        o0.z = dv.quad(f[8], f[9], f[10], f[11]);
+        o0.w = dv.quad(f[12], f[13], f[14], f[15]);
+        o1.x = dv.quad(f[16], f[17], f[18], f[19]);
+        o1.y = dv.quad(f[20], f[21], f[22], f[23]);
+        o1.z = dv.quad(f[24], f[25], f[26], f[27]);
+        o1.w = dv.quad(f[28], f[29], f[30], f[31]);
+        uint8_t* dst = xqT + (k0 + c) * M + m0 + qr * 32;
+        reinterpret_cast<uint4*>(dst)[0] = o0;
+        reinterpret_cast<uint4*>(dst)[1] = o1;
+        __syncthreads();  // tile and part are rewritten by the next iteration
+        t = tn;
     }
-    __syncthreads();
-    const int c = t & 63;
-    const int qr = t >> 6;
-    float f[32];
-    float amax = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        f[i] = __uint_as_float(static_cast<uint32_t>(tile[qr * 32 + i][c]) << 16);
-        amax = fmaxf(amax, fabsf(f[i]));
-    }
-    part[qr][c] = amax;
-    __syncthreads();
-    amax = fmaxf(fmaxf(part[0][c], part[1][c]), fmaxf(part[2][c], part[3][c]));
-    const float s = group_scale(amax);
-    if (qr == 0) sxT[mb * K + k0 + c] = s;
-    uint4 o0, o1;
-    o0.x = quant_quad(f[0], f[1], f[2], f[3], s);
-    o0.y = quant_quad(f[4], f[5], f[6], f[7], s);
-    o0.z = quant_quad(f[8], f[9], f[10], f[11], s);
-    o0.w = quant_quad(f[12], f[13], f[14], f[15], s);
-    o1.x = quant_quad(f[16], f[17], f[18], f[19], s);
-    o1.y = quant_quad(f[20], f[21], f[22], f[23], s);
-    o1.z = quant_quad(f[24], f[25], f[26], f[27], s);
-    o1.w = quant_quad(f[28], f[29], f[30], f[31], s);
-    uint8_t* dst = xqT + (k0 + c) * M + m0 + qr * 32;
-    reinterpret_cast<uint4*>(dst)[0] = o0;
-    reinterpret_cast<uint4*>(dst)[1] = o1;
 }
 
 // ---------------------------------------------------------------- 128x128 --
-// CTA: one 128x128 block.  The bf16 block is held in registers (for the amax
-// and the same-orientation output) and in shared memory (for the transposed
-// output, one column per thread).
-__global__ void __launch_bounds__(256) quant_weight_128x128_kernel(
-    const uint16_t* __restrict__ w, int64_t K, int64_t N, int64_t ldw, uint8_t* __restrict__ wq,
-    uint8_t* __restrict__ wqT, float* __restrict__ sw) {
-    __shared__ __align__(16) uint16_t tile[128][128];
-    __shared__ float part[8];
-    const int t = threadIdx.x;
-    const int lane = t & 31, warp = t >> 5;
-    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 128;
-    const int64_t k0 = static_cast<int64_t>(blockIdx.y) * 128;
-    const int ch = t & 15;
-    uint4 v[8];
+// Tile: one 128x128 block, staged in shared memory (the block amax needs the
+// whole block before any code is formed).  The same-orientation output is
+// written row-wise and the transposed output one column per thread.  Blocks
+// are numbered N-block fastest.
+__device__ __forceinline__ void load_128x128(const uint16_t* __restrict__ w, int64_t ldw,
+                                             int64_t NB, int64_t t, int tid, uint4 (&v)[8]) {
+    const int64_t n0 = (t % NB) * 128;
+    const int64_t k0 = (t / NB) * 128;
+    const int ch = tid & 15;
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
-        const int row = (t >> 4) + 16 * p;
+        const int row = (tid >> 4) + 16 * p;
         v[p] = ld_stream_v4(w + (k0 + row) * ldw + n0 + ch * 8);
     }
-    float amax = 0.0f;
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        const int row = (t >> 4) + 16 * p;
-        *reinterpret_cast<uint4*>(&tile[row][ch * 8]) = v[p];
-        const uint32_t wd[4] = {v[p].x, v[p].y, v[p].z, v[p].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(wd[j])), fabsf(bf16_hi(wd[j]))));
-    }
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1)
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    if (lane == 0) part[warp] = amax;
-    __syncthreads();
-    amax = part[0];
-#pragma unroll
-    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, part[i]);
-    const float s = group_scale(amax);
-    if (t == 0) sw[blockIdx.x * (K / 128) + blockIdx.y] = s;
-    if (wqT != nullptr) {
+}
+
+__global__ void __launch_bounds__(kQuantThreads) quant_weight_128x128_kernel(
+    const uint16_t* __restrict__ w, int64_t K, int64_t N, int64_t ldw, uint8_t* __restrict__ wq,
+    uint8_t* __restrict__ wqT, float* __restrict__ sw, int64_t tiles) {
+    __shared__ __align__(16) uint16_t tile[128][128];
+    __shared__ float part[8];
+    const int t0 = threadIdx.x;
+    const int lane = t0 & 31, warp = t0 >> 5;
+    const int ch = t0 & 15;
+    const int64_t NB = N / 128, KB = K / 128;
+    int64_t t = blockIdx.x;
+    uint4 v[8];
+    if (t < tiles) load_128x128(w, ldw, NB, t, t0, v);
+    while (t < tiles) {
+        const int64_t nb = t % NB, kb = t / NB;
+        const int64_t n0 = nb * 128, k0 = kb * 128;
+        uint32_t mx = 0;
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
-            const int row = (t >> 4) + 16 * p;
-            uint2 q;
-            q.x = quant_quad(bf16_lo(v[p].x), bf16_hi(v[p].x), bf16_lo(v[p].y), bf16_hi(v[p].y), s);
-            q.y = quant_quad(bf16_lo(v[p].z), bf16_hi(v[p].z), bf16_lo(v[p].w), bf16_hi(v[p].w), s);
-            *reinterpret_cast<uint2*>(wqT + (k0 + row) * N + n0 + ch * 8) = q;
+            const int row = (t0 >> 4) + 16 * p;
+            *reinterpret_cast<uint4*>(&tile[row][ch * 8]) = v[p];
+            mx = absmax_bf16x2(mx, absmax_bf16x2(v[p].x, v[p].y));
+            mx = absmax_bf16x2(mx, absmax_bf16x2(v[p].z, v[p].w));
         }
-    }
-    if (wq != nullptr) {
-        const int n = t & 127;
-        const int h = t >> 7;
-        uint8_t* dst = wq + (n0 + n) * K + k0 + h * 64;
+        float amax = amax_of_pair(mx);
+        const int64_t tn = t + gridDim.x;
+        if (tn < tiles) load_128x128(w, ldw, NB, tn, t0, v);  // next block's loads in flight
 #pragma unroll
-        for (int c16 = 0; c16 < 4; ++c16) {
-            float f[16];
+        for (int off = 16; off >= 1; off >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+        if (lane == 0) part[warp] = amax;
+        __syncthreads();
+        amax = part[0];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                f[i] = __uint_as_float(static_cast<uint32_t>(tile[h * 64 + c16 * 16 + i][n]) << 16);
-            uint4 o;
-            o.x = quant_quad(f[0], f[1], f[2], f[3], s);
-            o.y = quant_quad(f[4], f[5], f[6], f[7], s);
-            o.z = quant_quad(f[8], f[9], f[10], f[11], s);
-            o.w = quant_quad(f[12], f[13], f[14], f[15], s);
-            reinterpret_cast<uint4*>(dst)[c16] = o;
+        for (int i = 1; i < 8; ++i) amax = fmaxf(amax, part[i]);
+        const float s = group_scale(amax);
+        const GroupDiv dv(s);
+        if (t0 == 0) sw[nb * KB + kb] = s;
+        if (wqT != nullptr) {
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                const int row = (t0 >> 4) + 16 * p;
+                const uint4 u = *reinterpret_cast<const uint4*>(&tile[row][ch * 8]);
+                uint2 q;
+                q.x = dv.quad(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+                q.y = dv.quad(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
+                *reinterpret_cast<uint2*>(wqT + (k0 + row) * N + n0 + ch * 8) = q;
+            }
         }
+        if (wq != nullptr) {
+            // columns 2cp and 2cp+1 of the block, rows rq*32 .. rq*32+31: one
+            // 32-bit shared load gives both columns of a row
+            const int cp = t0 & 63;
+            const int rq = t0 >> 6;
+            uint8_t* dst0 = wq + (n0 + 2 * cp) * K + k0 + rq * 32;
+            uint8_t* dst1 = dst0 + K;
+#pragma unroll
+            for (int c16 = 0; c16 < 2; ++c16) {
+                uint32_t wv[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    wv[i] = *reinterpret_cast<const uint32_t*>(&tile[rq * 32 + c16 * 16 + i][2 * cp]);
+                uint4 o0, o1;
+                o0.x = dv.quad(bf16_lo(wv[0]), bf16_lo(wv[1]), bf16_lo(wv[2]), bf16_lo(wv[3]));
+                o0.y = dv.quad(bf16_lo(wv[4]), bf16_lo(wv[5]), bf16_lo(wv[6]), bf16_lo(wv[7]));
+                o0.z = dv.quad(bf16_lo(wv[8]), bf16_lo(wv[9]), bf16_lo(wv[10]), bf16_lo(wv[11]));
+                o0.w = dv.quad(bf16_lo(wv[12]), bf16_lo(wv[13]), bf16_lo(wv[14]), bf16_lo(wv[15]));
+                o1.x = dv.quad(bf16_hi(wv[0]), bf16_hi(wv[1]), bf16_hi(wv[2]), bf16_hi(wv[3]));
+                o1.y = dv.quad(bf16_hi(wv[4]), bf16_hi(wv[5]), bf16_hi(wv[6]), bf16_hi(wv[7]));
+                o1.z = dv.quad(bf16_hi(wv[8]), bf16_hi(wv[9]), bf16_hi(wv[10]), bf16_hi(wv[11]));
+                o1.w = dv.quad(bf16_hi(wv[12]), bf16_hi(wv[13]), bf16_hi(wv[14]), bf16_hi(wv[15]));
+                reinterpret_cast<uint4*>(dst0)[c16] = o0;
+                reinterpret_cast<uint4*>(dst1)[c16] = o1;
+            }
+        }
+        __syncthreads();  // tile and part are rewritten by the next iteration
+        t = tn;
     }
+}
+
+// Persistent grid: as many CTAs as can be resident at once (cached per
+// kernel and device), never more than there are tiles.
+template <auto kern>
+static int64_t quant_grid(int64_t tiles) {
+    static int per_sm[kMaxDevices] = {0};
+    int dev = 0;
+    const int sms = sm_count_current(&dev);
+    if (sms <= 0) return tiles < 1024 ? tiles : 1024;
+    if (per_sm[dev] == 0) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kQuantThreads, 0) !=
+                cudaSuccess ||
+            n <= 0)
+            n = 1;
+        per_sm[dev] = n < kQuantCtasPerSm ? n : kQuantCtasPerSm;
+    }
+    const int64_t cap = static_cast<int64_t>(sms) * per_sm[dev];
+    return tiles < cap ? tiles : cap;
 }
 
 }  // namespace fp8fg
@@ -225,11 +376,10 @@ extern "C" int fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t 
     if (x == nullptr || xq == nullptr || sx == nullptr) return FP8_ERR_NULL;
     if (ldx % 8 != 0 || ldq % 16 != 0 || !aligned(x, 16) || !aligned(xq, 16) || !aligned(sx, 4))
         return FP8_ERR_ALIGN;
-    const int64_t gx = (M + kQ1Rows - 1) / kQ1Rows, gy = K / 128;
-    if (gx > 0x7fffffff || gy > 65535) return FP8_ERR_UNSUPPORTED;
-    quant_act_1x128_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0,
+    const int64_t tiles = ((M + kQ1Rows - 1) / kQ1Rows) * (K / 128);
+    quant_act_1x128_kernel<<<static_cast<unsigned>(quant_grid<quant_act_1x128_kernel>(tiles)), kQuantThreads, 0,
                              static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(x), M, ldx, xq, ldq, sx);
+        static_cast<const uint16_t*>(x), M, K / 128, ldx, xq, ldq, sx, tiles);
     return launch_status();
 }
 
@@ -240,11 +390,10 @@ extern "C" int fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t 
     if (x == nullptr || xqT == nullptr || sxT == nullptr) return FP8_ERR_NULL;
     if (ldx % 8 != 0 || !aligned(x, 16) || !aligned(xqT, 16) || !aligned(sxT, 4))
         return FP8_ERR_ALIGN;
-    const int64_t gx = K / 64, gy = M / 128;
-    if (gx > 0x7fffffff || gy > 65535) return FP8_ERR_UNSUPPORTED;
-    quant_act_128x1_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)), 256, 0,
+    const int64_t tiles = (M / 128) * (K / 64);
+    quant_act_128x1_kernel<<<static_cast<unsigned>(quant_grid<quant_act_128x1_kernel>(tiles)), kQuantThreads, 0,
                              static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(x), M, K, ldx, xqT, sxT);
+        static_cast<const uint16_t*>(x), M, K, ldx, xqT, sxT, tiles);
     return launch_status();
 }
 
@@ -256,11 +405,10 @@ extern "C" int fp8_quant_weight_128x128(const void* w, int64_t K, int64_t N, int
     if (ldw % 8 != 0 || !aligned(w, 16) || !aligned(wq, 16) || !aligned(wqT, 16) ||
         !aligned(sw, 4))
         return FP8_ERR_ALIGN;
-    const int64_t gx = N / 128, gy = K / 128;
-    if (gx > 0x7fffffff || gy > 65535) return FP8_ERR_UNSUPPORTED;
-    quant_weight_128x128_kernel<<<dim3(static_cast<unsigned>(gx), static_cast<unsigned>(gy)),
-                                  256, 0, static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(w), K, N, ldw, wq, wqT, sw);
+    const int64_t tiles = (N / 128) * (K / 128);
+    quant_weight_128x128_kernel<<<static_cast<unsigned>(quant_grid<quant_weight_128x128_kernel>(tiles)), kQuantThreads, 0,
+                                  static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t*>(w), K, N, ldw, wq, wqT, sw, tiles);
     return launch_status();
 }
 
