@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB_PATH = os.path.join(HERE, "libfp8fg.so")
 SOURCES = [os.path.join(CSRC, f) for f in ("quant.cu", "gemm.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "common.cuh")] + [
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "common.cuh", "tensormap.cuh")] + [
     os.path.join(INCLUDE, "fp8fg.h")]
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",

@@ -28,6 +28,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "tensormap.cuh"
 
 namespace fp8fg {
 
@@ -49,7 +50,6 @@ constexpr int kLaunchRegs = 168;
 constexpr int kCtrlRegs = 40;
 constexpr int kEpiRegs = 232;
 static_assert(128 * kCtrlRegs + 256 * kEpiRegs <= kThreads * kLaunchRegs, "register split");
-constexpr long long kWaitLimit = 1LL << 32;  // cycles (about 2 s at 2 GHz)
 constexpr int kSmemLimit = 232448;    // 227 KB opt-in per CTA
 
 // Output staging: each epilogue warp owns kOutSlots swizzled 4 KB boxes
@@ -67,7 +67,15 @@ struct Cfg {
     static constexpr int B_BYTES = BN * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int COLS = BN / 2;           // columns per epilogue thread
-    static constexpr int TMEM_COLS = 2 * BN;      // two partial buffers
+    // Tensor memory holds NBUF partial buffers of the whole tile (all 512
+    // columns): two for 256-wide tiles, four for 128-wide ones.  (Splitting a
+    // 256-wide tile into two 128-column sub-tiles with their own buffers was
+    // measured slower: each sub-tile MMA re-reads A from shared memory, and
+    // shared-memory bandwidth is what bounds the main loop.)
+    static constexpr int NSUB = 1;
+    static constexpr int SUBN = BN / NSUB;
+    static constexpr int NBUF = 512 / BN;
+    static constexpr int TMEM_COLS = NSUB * NBUF * SUBN;
     static constexpr int CSTAGE_BYTES = kEpiWarps * kOutSlots * kBoxBytes;
     static constexpr int RSCALE_BYTES = ROWSCALE ? 2 * BN * 4 : 0;
     static constexpr int HEADER = 256;            // barriers, TMEM slot, flags
@@ -76,8 +84,8 @@ struct Cfg {
     static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
     static constexpr int SMEM = FIXED + STAGES * STAGE_BYTES;
     static_assert(STAGES >= 2, "pipeline too shallow");
-    static_assert(2 * STAGES + 7 <= 30, "header too small for barriers");
-    static_assert(TMEM_COLS == 256 || TMEM_COLS == 512, "TMEM allocation must be a power of 2");
+    static_assert(2 * STAGES + 2 * NSUB * NBUF + 3 <= 30, "header too small for barriers");
+    static_assert(TMEM_COLS == 512, "TMEM allocation must be a power of 2");
 };
 
 struct GemmParams {
@@ -155,38 +163,14 @@ __device__ __forceinline__ uint32_t idesc_e4m3_f32() {
 }
 
 __device__ __forceinline__ void raise_error(volatile int* abort_flag, unsigned bits) {
-    *abort_flag = 1;
-    atomicOr(&g_dev_error, bits);
+    raise_device_error(abort_flag, &g_dev_error, bits);
 }
-
-// Single-thread bounded wait.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const long long t0 = clock64();
-    while (!mbar_try_wait(bar, parity)) {
-        if (*abort_flag) return false;
-        if (clock64() - t0 > kWaitLimit) {
-            raise_error(abort_flag, 1u);
-            return false;
-        }
-    }
-    return true;
+    return wait_bounded(bar, parity, abort_flag, &g_dev_error);
 }
-
-// Whole-warp bounded wait with a warp-uniform outcome.
 __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
                                               volatile int* abort_flag) {
-    const long long t0 = clock64();
-    while (true) {
-        const bool ok = mbar_try_wait(bar, parity);
-        if (__all_sync(0xffffffffu, ok)) return true;
-        const bool expired = clock64() - t0 > kWaitLimit;
-        const bool stop = (*abort_flag != 0) || expired;
-        if (__any_sync(0xffffffffu, stop)) {
-            if (expired) raise_error(abort_flag, 1u);
-            return false;
-        }
-    }
+    return wait_bounded_warp(bar, parity, abort_flag, &g_dev_error);
 }
 
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
@@ -219,22 +203,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int lane = threadIdx.x & 31;
     auto full_bar = [&](int s) { return smem_addr(&bars[s]); };
     auto empty_bar = [&](int s) { return smem_addr(&bars[S + s]); };
-    auto tfull_bar = [&](int b) { return smem_addr(&bars[2 * S + b]); };
-    auto tempty_bar = [&](int b) { return smem_addr(&bars[2 * S + 2 + b]); };
-    const uint32_t drain_bar = smem_addr(&bars[2 * S + 4]);
+    constexpr int NSUB = C::NSUB, NBUF = C::NBUF, SUBN = C::SUBN;
+    // TMEM partial buffer b of sub-tile u: full (MMA done) / empty (drained)
+    auto tfull_bar = [&](int u, int b) { return smem_addr(&bars[2 * S + u * NBUF + b]); };
+    auto tempty_bar = [&](int u, int b) {
+        return smem_addr(&bars[2 * S + NSUB * NBUF + u * NBUF + b]);
+    };
+    const uint32_t drain_bar = smem_addr(&bars[2 * S + 2 * NSUB * NBUF]);
     // ROWSCALE: the epilogue warps stage each K block's B-row scales in a
     // double buffer; this barrier pair (one per buffer) says all warps wrote.
-    auto rs_bar = [&](int b) { return smem_addr(&bars[2 * S + 5 + b]); };
+    auto rs_bar = [&](int b) { return smem_addr(&bars[2 * S + 2 * NSUB * NBUF + 1 + b]); };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), kEpiWarps);
-        }
+        for (int u = 0; u < NSUB; ++u)
+            for (int b = 0; b < NBUF; ++b) {
+                mbar_init(tfull_bar(u, b), 1);
+                mbar_init(tempty_bar(u, b), kEpiWarps / NSUB);
+            }
         mbar_init(drain_bar, 1);
         mbar_init(rs_bar(0), kEpiWarps);
         mbar_init(rs_bar(1), kEpiWarps);
@@ -259,7 +248,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (threadIdx.x == 0) bad = (__ldg(p.offsets) != 0) || (__ldg(p.offsets + p.E) > p.M);
         for (int e = threadIdx.x; e < p.E; e += kThreads)
             bad |= __ldg(p.offsets + e + 1) < __ldg(p.offsets + e);
-        if (bad) raise_error(abort_flag, 2u);
+        if (bad) raise_error(abort_flag, kErrBadOffsets);
         __syncthreads();
     }
     const uint32_t tmem_base = *tmem_slot;
@@ -306,7 +295,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
         // --------------------------------------------------------- MMA issuer
         if (lane == 0 && !aborted_at_start) {
-            const uint32_t idesc = idesc_e4m3_f32<BN>();
+            const uint32_t idesc = idesc_e4m3_f32<SUBN>();
             uint32_t it = 0, kbg = 0;
             bool ok = true, issued = false;
             for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
@@ -315,23 +304,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int64_t kb = 0; kb < KB; ++kb, ++it, ++kbg) {
                     const int s = static_cast<int>(it % S);
                     const uint32_t ph = (it / S) & 1u;
-                    const uint32_t buf = kbg & 1u, tph = (kbg >> 1) & 1u;
-                    if (!wait_bar(full_bar(s), ph, abort_flag) ||
-                        !wait_bar(tempty_bar(buf), tph ^ 1u, abort_flag)) {
+                    const uint32_t buf = kbg % NBUF, tph = (kbg / NBUF) & 1u;
+                    if (!wait_bar(full_bar(s), ph, abort_flag)) {
                         ok = false;
                         break;
                     }
-                    tc_fence_after_sync();
                     const uint32_t a_addr = smem_addr(stages + s * C::STAGE_BYTES);
                     const uint64_t adesc = smem_desc_sw128(a_addr);
-                    const uint64_t bdesc = smem_desc_sw128(a_addr + C::A_BYTES);
-                    const uint32_t d = tmem_base + buf * BN;
 #pragma unroll
-                    for (int k = 0; k < BK / 32; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
-                        mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+                    for (int u = 0; u < NSUB; ++u) {
+                        if (!wait_bar(tempty_bar(u, buf), tph ^ 1u, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after_sync();
+                        // sub-tile u reads B rows u*SUBN .. u*SUBN+SUBN-1 (128 bytes each)
+                        const uint64_t bdesc = smem_desc_sw128(a_addr + C::A_BYTES + u * SUBN * BK);
+                        const uint32_t d = tmem_base + (u * NBUF + buf) * SUBN;
+#pragma unroll
+                        for (int k = 0; k < BK / 32; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
+                            mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+                        mma_commit(tfull_bar(u, buf));
+                        issued = true;
+                    }
+                    if (!ok) break;
                     mma_commit(empty_bar(s));
-                    mma_commit(tfull_bar(buf));
-                    issued = true;
                 }
             }
             if (!ok && issued) {
@@ -356,7 +353,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int KBi = static_cast<int>(KB);
         const int NB = static_cast<int>(p.N / 128);
         const int lds_a = static_cast<int>(p.lds_a);
-        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + cg * COLS;
+        // sub-tile of this warp and its first TMEM column within the sub-tile
+        const int u = NSUB == 2 ? cg : 0;
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
+                                (NSUB == 2 ? 0 : cg * COLS) + u * NBUF * SUBN;
         uint32_t kbg = 0;
         bool ok = !aborted_at_start;
         for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
@@ -395,25 +395,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sa_next = row_in_alloc ? __ldg(sa_ptr + (kb + 1) * lds_a) : 0.0f;
                     sb_next = __ldg(sb_ptr + (kb + 1) * sb_step);
                 }
-                const uint32_t buf = kbg & 1u, tph = (kbg >> 1) & 1u;
+                const uint32_t buf = kbg % NBUF, tph = (kbg / NBUF) & 1u;
+                const uint32_t rsb = kbg & 1u;
                 if (ROWSCALE) {
-                    // buffer `buf` was last read in K block kbg-2; every warp
-                    // arrived on this buffer's barrier for kbg-1 only after
+                    // buffer `rsb` was last read in K block kbg-2; every warp
+                    // arrived on the other buffer's barrier for kbg-1 only after
                     // finishing that read, so it is free to overwrite here.
-                    if (ew * 32 + lane < BN) rscale[buf * BN + ew * 32 + lane] = sb_cur;
+                    if (ew * 32 + lane < BN) rscale[rsb * BN + ew * 32 + lane] = sb_cur;
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(rs_bar(buf));
-                    if (!wait_bar_warp(rs_bar(buf), tph, abort_flag)) {
+                    if (lane == 0) mbar_arrive(rs_bar(rsb));
+                    if (!wait_bar_warp(rs_bar(rsb), (kbg >> 1) & 1u, abort_flag)) {
                         ok = false;
                         break;
                     }
                 }
-                if (!wait_bar_warp(tfull_bar(buf), tph, abort_flag)) {
+                if (!wait_bar_warp(tfull_bar(u, buf), tph, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t taddr = t_lane + buf * BN;
+                const uint32_t taddr = t_lane + buf * SUBN;
                 if (!ROWSCALE) {
                     const float sc = sa_cur * sb_cur;
                     const uint64_t sc2 = pack2(f2u(sc), f2u(sc));
@@ -433,7 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // buffer back before the last chunk's FMAs
                             tc_fence_before_sync();
                             __syncwarp();
-                            if (lane == 0) mbar_arrive(tempty_bar(buf));
+                            if (lane == 0) mbar_arrive(tempty_bar(u, buf));
                         }
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
@@ -443,7 +444,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else {
                     const uint64_t sa2 = pack2(f2u(sa_cur), f2u(sa_cur));
-                    const float* rs = rscale + buf * BN + cg * COLS;
+                    const float* rs = rscale + rsb * BN + cg * COLS;
 #pragma unroll
                     for (int ch = 0; ch < COLS / 16; ++ch) {
                         uint32_t r[16];
@@ -461,7 +462,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     tc_fence_before_sync();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty_bar(buf));
+                    if (lane == 0) mbar_arrive(tempty_bar(u, buf));
                 }
             }
             if (!ok) break;
@@ -532,34 +533,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // -------------------------------------------------------------------- host --
-static PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (fn == nullptr) {
-        void* ptr = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                             cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
-    return fn;
-}
-
-// 2-D row-major tensor [outer][inner] with a 128-byte-swizzled box.
-static int make_map(CUtensorMap* map, CUtensorMapDataType dt, const void* base, uint64_t inner,
-                    uint64_t outer, uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer) {
-    auto fn = encode_tiled();
-    if (fn == nullptr) return FP8_ERR_CUDA;
-    cuuint64_t dims[2] = {inner, outer};
-    cuuint64_t strides[1] = {row_bytes};
-    cuuint32_t box[2] = {box_inner, box_outer};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    return r == CUDA_SUCCESS ? FP8_OK : FP8_ERR_CUDA;
-}
-
 template <int BN, bool OUT_BF16, bool ROWSCALE, bool GROUPED>
 static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t b_rows,
                   const GemmParams& p, int64_t tiles_upper, cudaStream_t stream) {
@@ -581,13 +554,16 @@ static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t 
     }
     CUtensorMap ta, tb, tc;
     int st;
-    if ((st = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, p.K, a_rows, p.K, BK, BM)) != FP8_OK)
+    if ((st = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, p.K, a_rows, p.K, BK, BM,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != FP8_OK)
         return st;
-    if ((st = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bq, p.K, b_rows, p.K, BK, BN)) != FP8_OK)
+    if ((st = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bq, p.K, b_rows, p.K, BK, BN,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != FP8_OK)
         return st;
     constexpr int ELT = OUT_BF16 ? 2 : 4;
     if ((st = make_map(&tc, OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                       p.c, p.N, p.M, p.ldc * ELT, 128 / ELT, 32)) != FP8_OK)
+                       p.c, p.N, p.M, p.ldc * ELT, 128 / ELT, 32,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != FP8_OK)
         return st;
     const int64_t grid = tiles_upper < sms ? tiles_upper : sms;
     if (grid <= 0) return FP8_OK;
@@ -700,7 +676,7 @@ extern "C" int fp8_device_error(void* stream) {
     if (cudaMemcpyFromSymbol(&v, g_dev_error, sizeof v) != cudaSuccess) return FP8_ERR_CUDA;
     if (v != 0 && cudaMemcpyToSymbol(g_dev_error, &zero, sizeof zero) != cudaSuccess)
         return FP8_ERR_CUDA;
-    if (v & 1u) return FP8_ERR_TIMEOUT;
-    if (v & 2u) return FP8_ERR_DEVICE_SHAPE;
+    if (v & kErrTimeout) return FP8_ERR_TIMEOUT;
+    if (v & kErrBadOffsets) return FP8_ERR_DEVICE_SHAPE;
     return FP8_OK;
 }

@@ -43,6 +43,52 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Bounded waits.  Every spin on a barrier gives up after kWaitLimit cycles
+// (about two seconds at 2 GHz): it then sets the CTA's abort flag and the
+// error bits in the given device error word and returns false, so the
+// caller can unwind instead of hanging.  A wait also returns false as soon
+// as another role of the CTA has set the abort flag.
+constexpr long long kWaitLimit = 1LL << 32;
+constexpr unsigned kErrTimeout = 1u;      // a barrier wait expired
+constexpr unsigned kErrBadOffsets = 2u;   // grouped GEMM offsets invalid
+
+__device__ __forceinline__ void raise_device_error(volatile int* abort_flag, unsigned* err_word,
+                                                   unsigned bits) {
+    *abort_flag = 1;
+    atomicOr(err_word, bits);
+}
+
+// single-thread wait
+__device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             unsigned* err_word) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (*abort_flag) return false;
+        if (clock64() - t0 > kWaitLimit) {
+            raise_device_error(abort_flag, err_word, kErrTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+// whole-warp wait with a warp-uniform outcome
+__device__ __forceinline__ bool wait_bounded_warp(uint32_t bar, uint32_t parity,
+                                                  volatile int* abort_flag, unsigned* err_word) {
+    const long long t0 = clock64();
+    while (true) {
+        const bool ok = mbar_try_wait(bar, parity);
+        if (__all_sync(0xffffffffu, ok)) return true;
+        const bool expired = clock64() - t0 > kWaitLimit;
+        const bool stop = (*abort_flag != 0) || expired;
+        if (__any_sync(0xffffffffu, stop)) {
+            if (expired) raise_device_error(abort_flag, err_word, kErrTimeout);
+            return false;
+        }
+    }
+}
+
 // ----------------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const void* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
