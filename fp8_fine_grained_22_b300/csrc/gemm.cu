@@ -418,29 +418,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!ROWSCALE) {
                     const float sc = sa_cur * sb_cur;
                     const uint64_t sc2 = pack2(f2u(sc), f2u(sc));
-                    // 32-column TMEM loads, software-pipelined: the load of
-                    // chunk ch+1 is in flight while chunk ch is accumulated
+                    // 32-column TMEM loads: two in flight from the start, and each
+                    // freed register chunk is refilled at once, so the whole
+                    // partial has landed after two load latencies; the TMEM
+                    // buffer goes back to the MMA before the last FMAs
+                    static_assert(COLS == 64 || COLS == 128, "column chunking");
                     uint32_t ra[32], rb[32];
                     tmem_ld32(taddr, ra);
+                    tmem_ld32(taddr + 32, rb);
                     tmem_wait_ld(ra);
-#pragma unroll
-                    for (int ch = 0; ch < COLS / 32; ++ch) {
-                        uint32_t (&cur)[32] = (ch & 1) ? rb : ra;
-                        uint32_t (&nxt)[32] = (ch & 1) ? ra : rb;
-                        if (ch + 1 < COLS / 32) {
-                            tmem_ld32(taddr + (ch + 1) * 32, nxt);
-                        } else {
-                            // the whole partial is in registers: hand the TMEM
-                            // buffer back before the last chunk's FMAs
-                            tc_fence_before_sync();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(tempty_bar(u, buf));
-                        }
+                    tmem_wait_ld(rb);
+                    auto fma_chunk = [&](uint32_t (&r)[32], int ch) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            acc[ch * 16 + i] =
-                                ffma2(pack2(cur[2 * i], cur[2 * i + 1]), sc2, acc[ch * 16 + i]);
-                        if (ch + 1 < COLS / 32) tmem_wait_ld(nxt);
+                            acc[ch * 16 + i] = ffma2(pack2(r[2 * i], r[2 * i + 1]), sc2, acc[ch * 16 + i]);
+                    };
+                    auto release = [&]() {
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tempty_bar(0, buf));
+                    };
+                    if (COLS == 128) {
+                        fma_chunk(ra, 0);
+                        tmem_ld32(taddr + 64, ra);
+                        fma_chunk(rb, 1);
+                        tmem_ld32(taddr + 96, rb);
+                        tmem_wait_ld(ra);
+                        tmem_wait_ld(rb);
+                        release();
+                        fma_chunk(ra, 2);
+                        fma_chunk(rb, 3);
+                    } else {
+                        release();
+                        fma_chunk(ra, 0);
+                        fma_chunk(rb, 1);
                     }
                 } else {
                     const uint64_t sa2 = pack2(f2u(sa_cur), f2u(sa_cur));
