@@ -145,6 +145,31 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------- multi-rank helpers --
+# One process per GPU, each running its own replica of the workload (weak
+# scaling); the only cross-rank operations are barriers around the timed
+# region and a max-reduction of the per-rank times.  No collective touches
+# the data path.
+def rank_barrier():
+    if torch.distributed.is_available() and torch.distributed.is_initialized():
+        torch.distributed.barrier()
+
+
+def reduce_max(x: float, device) -> float:
+    """Largest value of x over all ranks (x itself for a single process)."""
+    if (torch.distributed.is_available() and torch.distributed.is_initialized()
+            and torch.distributed.get_world_size() > 1):
+        t = torch.tensor([x], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        return float(t.item())
+    return x
+
+
+def whole_job_tflops(world: int, flops_per_rank: float, ms_slowest: float) -> float:
+    """Aggregate throughput: every rank's work over the slowest rank's time."""
+    return world * flops_per_rank / (ms_slowest * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- our path --
 def run_ours(args, rank, world, local):
     from fp8_fine_grained_22_b300 import fp8fg
@@ -186,8 +211,7 @@ def run_ours(args, rank, world, local):
         raise RuntimeError("device-side error during warm-up")
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
-    if world > 1:
-        torch.distributed.barrier()
+    rank_barrier()
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
         t0 = time.perf_counter()
@@ -196,17 +220,12 @@ def run_ours(args, rank, world, local):
             step(events[i])
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
-    if world > 1:
-        torch.distributed.barrier()
+    rank_barrier()
     qx = [e[0].elapsed_time(e[1]) for e in events]
     qw = [e[1].elapsed_time(e[2]) for e in events]
     gm = [e[2].elapsed_time(e[3]) for e in events]
     st = [e[0].elapsed_time(e[3]) for e in events]
-    ms_step = statistics.mean(st)
-    if world > 1:
-        t = torch.tensor([ms_step], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = reduce_max(statistics.mean(st), dev)
     gemm_ms = statistics.mean(gm)
     qx_ms, qw_ms = statistics.mean(qx), statistics.mean(qw)
 
@@ -233,11 +252,7 @@ def run_ours(args, rank, world, local):
         e2e_step()
     e_end.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e_start.elapsed_time(e_end) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = reduce_max(e_start.elapsed_time(e_end) / e2e_steps, dev)
     err = fp8fg.device_error()
     if err != 0:
         raise RuntimeError("device-side error status %d" % err)
@@ -248,7 +263,7 @@ def run_ours(args, rank, world, local):
     gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
     qx_bytes = M * K * 2 + M * K + (K // 128) * M * 4
     qw_bytes = K * N * 2 + K * N + (K // 128) * (N // 128) * 4
-    value = world * flops / (ms_step * 1e-3) / 1e12
+    value = whole_job_tflops(world, flops, ms_step)
     clocks = clk.summary()
     line = {
         "metric": METRIC,
@@ -269,7 +284,7 @@ def run_ours(args, rank, world, local):
                    "l2": "flushed between steps (%d MB write)" % (flush.numel() * 4 >> 20),
                    "step": ["fp8_quant_act_1x128", "fp8_quant_weight_128x128",
                             "fp8_gemm_blockscaled"]},
-        "e2e": {"value": round(world * flops / (e2e_ms * 1e-3) / 1e12, 3), "unit": "TFLOP/s",
+        "e2e": {"value": round(whole_job_tflops(world, flops, e2e_ms), 3), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": 3 * args.steps,
