@@ -250,98 +250,107 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_128x1_kernel(
 }
 
 // ---------------------------------------------------------------- 128x128 --
-// Tile: one 128x128 block, staged in shared memory (the block amax needs the
-// whole block before any code is formed).  The same-orientation output is
-// written row-wise and the transposed output one column per thread.  Blocks
-// are numbered N-block fastest.
-__device__ __forceinline__ void load_128x128(const uint16_t* __restrict__ w, int64_t ldw,
-                                             int64_t NB, int64_t t, int tid, uint4 (&v)[8]) {
-    const int64_t n0 = (t % NB) * 128;
-    const int64_t k0 = (t / NB) * 128;
-    const int ch = tid & 15;
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        const int row = (tid >> 4) + 16 * p;
-        v[p] = ld_stream_v4(w + (k0 + row) * ldw + n0 + ch * 8);
-    }
+// One 128-thread CTA per 128x128 block, copied global -> shared with
+// 16-byte cp.async (no register staging), so that every SM holds several
+// blocks in flight at once (32 KB of shared memory each).  The block amax
+// needs the whole block before any code is formed; the same-orientation
+// output is written row-wise and the transposed output two columns per
+// thread.
+constexpr int kWThreads = 128;
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))), "l"(gmem)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(kQuantThreads) quant_weight_128x128_kernel(
+__global__ void __launch_bounds__(kWThreads) quant_weight_128x128_kernel(
     const uint16_t* __restrict__ w, int64_t K, int64_t N, int64_t ldw, uint8_t* __restrict__ wq,
     uint8_t* __restrict__ wqT, float* __restrict__ sw, int64_t tiles) {
     __shared__ __align__(16) uint16_t tile[128][128];
-    __shared__ float part[8];
+    __shared__ __align__(16) uint8_t codes[128 * 128];  // transposed codes, [n][k] swizzled
+    // the warps' partial maxima use the first bytes of `codes` (48 KB static limit)
+    float* part = reinterpret_cast<float*>(codes);
     const int t0 = threadIdx.x;
     const int lane = t0 & 31, warp = t0 >> 5;
     const int ch = t0 & 15;
     const int64_t NB = N / 128, KB = K / 128;
-    int64_t t = blockIdx.x;
-    uint4 v[8];
-    if (t < tiles) load_128x128(w, ldw, NB, t, t0, v);
-    while (t < tiles) {
-        const int64_t nb = t % NB, kb = t / NB;
-        const int64_t n0 = nb * 128, k0 = kb * 128;
-        uint32_t mx = 0;
+    const int64_t t = blockIdx.x;
+    const int64_t nb = t % NB, kb = t / NB;
+    const int64_t n0 = nb * 128, k0 = kb * 128;
 #pragma unroll
-        for (int p = 0; p < 8; ++p) {
-            const int row = (t0 >> 4) + 16 * p;
-            *reinterpret_cast<uint4*>(&tile[row][ch * 8]) = v[p];
-            mx = absmax_bf16x2(mx, absmax_bf16x2(v[p].x, v[p].y));
-            mx = absmax_bf16x2(mx, absmax_bf16x2(v[p].z, v[p].w));
+    for (int p = 0; p < 16; ++p) {
+        const int row = (t0 >> 4) + 8 * p;
+        cp_async16(&tile[row][ch * 8], w + (k0 + row) * ldw + n0 + ch * 8);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    uint32_t mx = 0;
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+        const uint4 u = *reinterpret_cast<const uint4*>(&tile[(t0 >> 4) + 8 * p][ch * 8]);
+        mx = absmax_bf16x2(mx, absmax_bf16x2(u.x, u.y));
+        mx = absmax_bf16x2(mx, absmax_bf16x2(u.z, u.w));
+    }
+    float amax = amax_of_pair(mx);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) part[warp] = amax;
+    __syncthreads();
+    amax = fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3]));
+    __syncthreads();  // every thread has read `part` before `codes` is written
+    const float s = group_scale(amax);
+    const GroupDiv dv(s);
+    if (t0 == 0) sw[nb * KB + kb] = s;
+    if (wqT != nullptr) {
+#pragma unroll 4
+        for (int p = 0; p < 16; ++p) {
+            const int row = (t0 >> 4) + 8 * p;
+            const uint4 u = *reinterpret_cast<const uint4*>(&tile[row][ch * 8]);
+            uint2 q;
+            q.x = dv.quad(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+            q.y = dv.quad(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
+            *reinterpret_cast<uint2*>(wqT + (k0 + row) * N + n0 + ch * 8) = q;
         }
-        float amax = amax_of_pair(mx);
-        const int64_t tn = t + gridDim.x;
-        if (tn < tiles) load_128x128(w, ldw, NB, tn, t0, v);  // next block's loads in flight
+    }
+    if (wq != nullptr) {
+        // columns 2cp and 2cp+1 of the block, rows rh*64 .. rh*64+63: one
+        // 32-bit shared load gives both columns of a row.  The codes go to a
+        // shared [n][k] tile (16-byte chunks XOR-swizzled by n & 7) and are
+        // then written out as whole 128-byte rows of wq.
+        const int cp = t0 & 63;
+        const int rh = t0 >> 6;
+#pragma unroll 1
+        for (int h = 0; h < 4; ++h) {
+            uint32_t wv[16];
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-        if (lane == 0) part[warp] = amax;
+            for (int i = 0; i < 16; ++i)
+                wv[i] = *reinterpret_cast<const uint32_t*>(&tile[rh * 64 + h * 16 + i][2 * cp]);
+            uint4 o0, o1;
+            o0.x = dv.quad(bf16_lo(wv[0]), bf16_lo(wv[1]), bf16_lo(wv[2]), bf16_lo(wv[3]));
+            o0.y = dv.quad(bf16_lo(wv[4]), bf16_lo(wv[5]), bf16_lo(wv[6]), bf16_lo(wv[7]));
+            o0.z = dv.quad(bf16_lo(wv[8]), bf16_lo(wv[9]), bf16_lo(wv[10]), bf16_lo(wv[11]));
+            o0.w = dv.quad(bf16_lo(wv[12]), bf16_lo(wv[13]), bf16_lo(wv[14]), bf16_lo(wv[15]));
+            o1.x = dv.quad(bf16_hi(wv[0]), bf16_hi(wv[1]), bf16_hi(wv[2]), bf16_hi(wv[3]));
+            o1.y = dv.quad(bf16_hi(wv[4]), bf16_hi(wv[5]), bf16_hi(wv[6]), bf16_hi(wv[7]));
+            o1.z = dv.quad(bf16_hi(wv[8]), bf16_hi(wv[9]), bf16_hi(wv[10]), bf16_hi(wv[11]));
+            o1.w = dv.quad(bf16_hi(wv[12]), bf16_hi(wv[13]), bf16_hi(wv[14]), bf16_hi(wv[15]));
+            const int c = rh * 4 + h;  // 16-byte chunk of the 128-byte k row
+            const int n_a = 2 * cp, n_b = 2 * cp + 1;
+            *reinterpret_cast<uint4*>(&codes[n_a * 128 + ((c ^ (n_a & 7)) << 4)]) = o0;
+            *reinterpret_cast<uint4*>(&codes[n_b * 128 + ((c ^ (n_b & 7)) << 4)]) = o1;
+        }
         __syncthreads();
-        amax = part[0];
 #pragma unroll
-        for (int i = 1; i < 8; ++i) amax = fmaxf(amax, part[i]);
-        const float s = group_scale(amax);
-        const GroupDiv dv(s);
-        if (t0 == 0) sw[nb * KB + kb] = s;
-        if (wqT != nullptr) {
-#pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                const int row = (t0 >> 4) + 16 * p;
-                const uint4 u = *reinterpret_cast<const uint4*>(&tile[row][ch * 8]);
-                uint2 q;
-                q.x = dv.quad(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
-                q.y = dv.quad(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
-                *reinterpret_cast<uint2*>(wqT + (k0 + row) * N + n0 + ch * 8) = q;
-            }
+        for (int i = 0; i < 8; ++i) {
+            const int j = t0 + kWThreads * i;  // chunk j: row n = j / 8, chunk c = j % 8
+            const int n = j >> 3, c = j & 7;
+            const uint4 v = *reinterpret_cast<const uint4*>(&codes[n * 128 + ((c ^ (n & 7)) << 4)]);
+            *reinterpret_cast<uint4*>(wq + (n0 + n) * K + k0 + c * 16) = v;
         }
-        if (wq != nullptr) {
-            // columns 2cp and 2cp+1 of the block, rows rq*32 .. rq*32+31: one
-            // 32-bit shared load gives both columns of a row
-            const int cp = t0 & 63;
-            const int rq = t0 >> 6;
-            uint8_t* dst0 = wq + (n0 + 2 * cp) * K + k0 + rq * 32;
-            uint8_t* dst1 = dst0 + K;
-#pragma unroll
-            for (int c16 = 0; c16 < 2; ++c16) {
-                uint32_t wv[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    wv[i] = *reinterpret_cast<const uint32_t*>(&tile[rq * 32 + c16 * 16 + i][2 * cp]);
-                uint4 o0, o1;
-                o0.x = dv.quad(bf16_lo(wv[0]), bf16_lo(wv[1]), bf16_lo(wv[2]), bf16_lo(wv[3]));
-                o0.y = dv.quad(bf16_lo(wv[4]), bf16_lo(wv[5]), bf16_lo(wv[6]), bf16_lo(wv[7]));
-                o0.z = dv.quad(bf16_lo(wv[8]), bf16_lo(wv[9]), bf16_lo(wv[10]), bf16_lo(wv[11]));
-                o0.w = dv.quad(bf16_lo(wv[12]), bf16_lo(wv[13]), bf16_lo(wv[14]), bf16_lo(wv[15]));
-                o1.x = dv.quad(bf16_hi(wv[0]), bf16_hi(wv[1]), bf16_hi(wv[2]), bf16_hi(wv[3]));
-                o1.y = dv.quad(bf16_hi(wv[4]), bf16_hi(wv[5]), bf16_hi(wv[6]), bf16_hi(wv[7]));
-                o1.z = dv.quad(bf16_hi(wv[8]), bf16_hi(wv[9]), bf16_hi(wv[10]), bf16_hi(wv[11]));
-                o1.w = dv.quad(bf16_hi(wv[12]), bf16_hi(wv[13]), bf16_hi(wv[14]), bf16_hi(wv[15]));
-                reinterpret_cast<uint4*>(dst0)[c16] = o0;
-                reinterpret_cast<uint4*>(dst1)[c16] = o1;
-            }
-        }
-        __syncthreads();  // tile and part are rewritten by the next iteration
-        t = tn;
     }
 }
 
@@ -406,7 +415,8 @@ extern "C" int fp8_quant_weight_128x128(const void* w, int64_t K, int64_t N, int
         !aligned(sw, 4))
         return FP8_ERR_ALIGN;
     const int64_t tiles = (N / 128) * (K / 128);
-    quant_weight_128x128_kernel<<<static_cast<unsigned>(quant_grid<quant_weight_128x128_kernel>(tiles)), kQuantThreads, 0,
+    if (tiles > 0x7fffffffLL) return FP8_ERR_UNSUPPORTED;
+    quant_weight_128x128_kernel<<<static_cast<unsigned>(tiles), kWThreads, 0,
                                   static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t*>(w), K, N, ldw, wq, wqT, sw, tiles);
     return launch_status();
