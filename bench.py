@@ -61,7 +61,7 @@ def measured_peaks():
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
 
 
-GEMM_SOURCES = ("common.cuh", "gemm.cu", "ptx.cuh")
+GEMM_SOURCES = ("common.cuh", "gemm.cu", "ptx.cuh", "tensormap.cuh")
 
 
 def source_hash():
