@@ -72,7 +72,10 @@ struct Cfg {
     // 256-wide tile into two 128-column sub-tiles with their own buffers was
     // measured slower: each sub-tile MMA re-reads A from shared memory, and
     // shared-memory bandwidth is what bounds the main loop.)
-    static constexpr int NSUB = 1;
+#ifndef FP8FG_NSUB256
+#define FP8FG_NSUB256 1
+#endif
+    static constexpr int NSUB = (BN == 256 && !ROWSCALE) ? FP8FG_NSUB256 : 1;
     static constexpr int SUBN = BN / NSUB;
     static constexpr int NBUF = 512 / BN;
     static constexpr int TMEM_COLS = NSUB * NBUF * SUBN;
@@ -258,9 +261,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < kEpiWarp0) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
     }
+    // Dense kernels run the producer and the MMA issuer as whole warps: every
+    // lane walks the schedule and waits on the barriers, so descriptors and
+    // coordinates are warp-uniform and one elected lane issues the
+    // asynchronous operations (issued from a single divergent lane, each
+    // tcgen05.mma costs about twice the issue cycles).  The grouped kernels
+    // keep single-lane roles: their tile walk over the expert offsets does not
+    // fit the control warps' registers when run warp-wide.
+    constexpr bool kWarpRoles = !GROUPED;
+    auto role_wait = [&](uint32_t bar, uint32_t parity) {
+        return kWarpRoles ? wait_bar_warp(bar, parity, abort_flag) : wait_bar(bar, parity, abort_flag);
+    };
+    auto role_sync = [&]() {
+        if (kWarpRoles) __syncwarp();
+    };
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
-        if (lane == 0 && !aborted_at_start) {
+        if ((kWarpRoles || lane == 0) && !aborted_at_start) {
+            const bool leader = kWarpRoles ? elect_one() : true;
             uint32_t it = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
@@ -269,19 +287,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int64_t kb = 0; kb < KB; ++kb, ++it) {
                     const int s = static_cast<int>(it % S);
                     const uint32_t ph = (it / S) & 1u;
-                    if (!wait_bar(empty_bar(s), ph ^ 1u, abort_flag)) {
+                    if (!role_wait(empty_bar(s), ph ^ 1u)) {
                         ok = false;
                         break;
                     }
-                    uint8_t* st = stages + s * C::STAGE_BYTES;
-                    mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
-                    tma_load_2d(smem_addr(st), &tmA, full_bar(s), static_cast<int>(kb * BK),
-                                static_cast<int>(ti.row0));
-                    tma_load_2d(smem_addr(st + C::A_BYTES), &tmB, full_bar(s),
-                                static_cast<int>(kb * BK), static_cast<int>(ti.b_row0));
+                    if (leader) {
+                        uint8_t* st = stages + s * C::STAGE_BYTES;
+                        mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
+                        tma_load_2d(smem_addr(st), &tmA, full_bar(s), static_cast<int>(kb * BK),
+                                    static_cast<int>(ti.row0));
+                        tma_load_2d(smem_addr(st + C::A_BYTES), &tmB, full_bar(s),
+                                    static_cast<int>(kb * BK), static_cast<int>(ti.b_row0));
+                    }
+                    role_sync();
                 }
             }
-            if (!ok) {
+            if (!ok && leader) {
                 // let copies already issued land before the CTA can exit
                 const uint32_t n = it < static_cast<uint32_t>(S) ? it : static_cast<uint32_t>(S);
                 for (uint32_t i = it - n; i < it; ++i) {
@@ -291,10 +312,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            role_sync();
         }
     } else if (warp == 1) {
         // --------------------------------------------------------- MMA issuer
-        if (lane == 0 && !aborted_at_start) {
+        if ((kWarpRoles || lane == 0) && !aborted_at_start) {
+            const bool leader = kWarpRoles ? elect_one() : true;
             const uint32_t idesc = idesc_e4m3_f32<SUBN>();
             uint32_t it = 0, kbg = 0;
             bool ok = true, issued = false;
@@ -305,7 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int s = static_cast<int>(it % S);
                     const uint32_t ph = (it / S) & 1u;
                     const uint32_t buf = kbg % NBUF, tph = (kbg / NBUF) & 1u;
-                    if (!wait_bar(full_bar(s), ph, abort_flag)) {
+                    if (!role_wait(full_bar(s), ph)) {
                         ok = false;
                         break;
                     }
@@ -313,7 +336,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t adesc = smem_desc_sw128(a_addr);
 #pragma unroll
                     for (int u = 0; u < NSUB; ++u) {
-                        if (!wait_bar(tempty_bar(u, buf), tph ^ 1u, abort_flag)) {
+                        if (!role_wait(tempty_bar(u, buf), tph ^ 1u)) {
                             ok = false;
                             break;
                         }
@@ -321,23 +344,28 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // sub-tile u reads B rows u*SUBN .. u*SUBN+SUBN-1 (128 bytes each)
                         const uint64_t bdesc = smem_desc_sw128(a_addr + C::A_BYTES + u * SUBN * BK);
                         const uint32_t d = tmem_base + (u * NBUF + buf) * SUBN;
+                        if (leader) {
 #pragma unroll
-                        for (int k = 0; k < BK / 32; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
-                            mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
-                        mma_commit(tfull_bar(u, buf));
+                            for (int k = 0; k < BK / 32; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
+                                mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+                            mma_commit(tfull_bar(u, buf));
+                        }
+                        role_sync();
                         issued = true;
                     }
                     if (!ok) break;
-                    mma_commit(empty_bar(s));
+                    if (leader) mma_commit(empty_bar(s));
+                    role_sync();
                 }
             }
-            if (!ok && issued) {
+            if (!ok && issued && leader) {
                 // wait (bounded) for every MMA already issued before TMEM is freed
                 mma_commit(drain_bar);
                 const long long t0 = clock64();
                 while (!mbar_try_wait(drain_bar, 0) && clock64() - t0 < (1LL << 24)) {
                 }
             }
+            role_sync();
         }
     } else if (warp >= kEpiWarp0) {
         // ------------------------------------------------- promotion epilogue
@@ -436,7 +464,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     auto release = [&]() {
                         tc_fence_before_sync();
                         __syncwarp();
-                        if (lane == 0) mbar_arrive(tempty_bar(0, buf));
+                        if (lane == 0) mbar_arrive(tempty_bar(u, buf));
                     };
                     if (COLS == 128) {
                         fma_chunk(ra, 0);
