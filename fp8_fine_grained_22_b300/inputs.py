@@ -55,22 +55,31 @@ def bf16_bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def moe_routing(T: int, n_experts: int, topk: int, n_local: int, g: torch.Generator):
-    """Token ids per local expert (concatenated, expert-major) and offsets [n_local+1]."""
+def moe_topk(T: int, n_experts: int, topk: int, g: torch.Generator) -> torch.Tensor:
+    """Top-k expert ids [T, topk] (int64) of a sigmoid-plus-bias router."""
     logits = torch.randn(T, n_experts, generator=g, dtype=torch.float32)
     bias = torch.randn(n_experts, generator=g, dtype=torch.float32) * 0.5
     score = torch.sigmoid(logits) + bias
     # stable descending sort: among equal scores the lower expert index wins
-    order = torch.sort(score, dim=1, descending=True, stable=True).indices[:, :topk]
+    return torch.sort(score, dim=1, descending=True, stable=True).indices[:, :topk]
+
+
+def local_routing(order: torch.Tensor, n_local: int, expert_begin: int = 0):
+    """Token ids per local expert (concatenated, expert-major, ascending) and offsets."""
     tokens, counts = [], []
     for e in range(n_local):
-        tok = torch.nonzero((order == e).any(dim=1)).flatten()
+        tok = torch.nonzero((order == expert_begin + e).any(dim=1)).flatten()
         tokens.append(tok)
         counts.append(tok.numel())
     token_ids = torch.cat(tokens).to(torch.int64)
     offsets = np.zeros(n_local + 1, np.int64)
     offsets[1:] = np.cumsum(counts)
     return token_ids, offsets
+
+
+def moe_routing(T: int, n_experts: int, topk: int, n_local: int, g: torch.Generator):
+    """Token ids per local expert (concatenated, expert-major) and offsets [n_local+1]."""
+    return local_routing(moe_topk(T, n_experts, topk, g), n_local)
 
 
 def decode_counts(E: int, g: torch.Generator, lo=1, hi=256) -> np.ndarray:
@@ -145,12 +154,13 @@ def moe_prefill(seed=0, device="cpu", T=16384, K=7168, N=4096, n_experts=256, to
     """Top-8-of-256 routing of T tokens, 32 local experts with W[K, N] each."""
     g = _gen(seed)  # routing is drawn on the host
     x_tok = act(T, K, g)
-    token_ids, offsets = moe_routing(T, n_experts, topk, n_local, g)
+    order = moe_topk(T, n_experts, topk, g)
+    token_ids, offsets = local_routing(order, n_local)
     gw = _gen(seed + 1, device)
     w = torch.stack([weight(K, N, gw, device) for _ in range(n_local)])
     x = x_tok[token_ids].to(device)
     return Grouped("moe_prefill_t%d_e%d_k%d_n%d" % (T, n_local, K, N), n_local, N, K, x, w,
-                   offsets, {"token_ids": token_ids})
+                   offsets, {"token_ids": token_ids, "topk_ids": order, "x_tokens": x_tok})
 
 
 def moe_decode(seed=0, device="cpu", E=32, K=7168, N=4096, max_tokens=256) -> Grouped:

@@ -204,3 +204,38 @@ def grouped_gemm(aq, sa, bq, sb, offsets, rows=None, nthreads=None):
         out[sel] = gemm_blockscaled(aq, sa, bq[e], sb[e], BSCALE_BLOCK128,
                                     rows=rows[sel], nthreads=nthreads)
     return out
+
+
+# ------------------------------------------------------------- MoE dispatch --
+def moe_dispatch_quant(x_bf16, topk_ids, expert_begin, n_local):
+    """FP8 dispatch of token rows to the local experts.
+
+    Follows the DeepSeek-V3 Technical Report, section 3.3.3 (the activations
+    sent to the MoE experts are quantised with the fine-grained 1x128 scheme
+    and dispatched in FP8) and section 3.4 (each token goes to the experts of
+    its top-k routing).  A token is routed to global expert g when g appears
+    in its top-k row (a repeat counts once).  For every local expert
+    e = 0 .. n_local-1 (global id expert_begin + e) the routed tokens are
+    taken in ascending order; the packed rows are these token rows, expert
+    after expert, quantised 1x128.
+
+    x_bf16: uint16 [T, K] bfloat16 bits; topk_ids: int [T, topk].
+    Returns (xq uint8 [R, K], sx f32 [K/128, R], offsets int64 [n_local+1],
+    token_ids int64 [R]) with R = offsets[-1].
+    """
+    x = _c(x_bf16, np.uint16)
+    ids = np.asarray(topk_ids, dtype=np.int64)
+    ids = ids.reshape(x.shape[0], ids.shape[-1] if ids.ndim == 2 else -1)
+    T, K = x.shape
+    experts = expert_begin + np.arange(n_local, dtype=np.int64)
+    # member[t, e]: token t routed to local expert e
+    member = (ids[:, :, None] == experts[None, None, :]).any(axis=1)
+    token_lists = [np.nonzero(member[:, e])[0] for e in range(n_local)]
+    offsets = np.zeros(n_local + 1, np.int64)
+    offsets[1:] = np.cumsum([len(tl) for tl in token_lists])
+    token_ids = (np.concatenate(token_lists) if n_local else np.zeros(0)).astype(np.int64)
+    if token_ids.size == 0:
+        return (np.zeros((0, K), np.uint8), np.zeros((K // 128, 0), np.float32), offsets,
+                token_ids)
+    xq, sx = quant_act_1x128(x[token_ids])
+    return xq, sx, offsets, token_ids
