@@ -16,8 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 LIB_PATH = os.path.join(HERE, "libfp8fg.so")
-SOURCES = [os.path.join(CSRC, f) for f in ("quant.cu", "gemm.cu")]
-DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "common.cuh", "tensormap.cuh")] + [
+SOURCES = [os.path.join(CSRC, f) for f in ("quant.cu", "gemm.cu", "dispatch.cu")]
+DEPS = SOURCES + [os.path.join(CSRC, f) for f in ("ptx.cuh", "common.cuh", "tensormap.cuh", "quant_math.cuh")] + [
     os.path.join(INCLUDE, "fp8fg.h")]
 
 NVCC_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-lineinfo", "-std=c++17",

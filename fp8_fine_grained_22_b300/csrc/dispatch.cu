@@ -1,0 +1,344 @@
+// dispatch.cu -- MoE dispatch packing with fine-grained FP8 quantisation.
+//
+// Before the expert GEMMs, every token's activation row is sent to the
+// experts its router chose, in FP8 (DeepSeek-V3 Technical Report, section
+// 3.3.3, low-precision communication: the activations before the MoE
+// up-projections are quantised to FP8 with the same fine-grained scheme and
+// dispatched in that form).  On one GPU with a block of local experts this is
+// a gather: for every local expert e, the tokens routed to it, in ascending
+// token order, are written one after another as 1x128-quantised E4M3 rows, so
+// that the rows of expert e occupy offsets[e] .. offsets[e+1]-1 -- exactly
+// the A operand, A scales and offsets of fp8_grouped_gemm_moe.  1x128
+// quantisation is row-local, so quantising the gathered rows gives the same
+// bits as gathering quantised rows; a token sent to two local experts is
+// quantised once and stored twice.
+//
+// Three launches, no atomics on global memory, deterministic placement:
+//   count  one CTA per 64-token chunk: per-chunk histogram of local experts
+//          into counts[e][chunk];
+//   scan   one warp per expert: exclusive prefix of counts over the chunks
+//          (in place) and the expert's total;
+//   pack   one CTA per (chunk, K slice): the exclusive scan of the totals
+//          gives offsets; the first warp ranks the chunk's (token, expert)
+//          pairs in token order with shared-memory lane masks; all warps
+//          quantise 1x128 groups (the arithmetic of fp8_quant_act_1x128) and
+//          store each group's codes and scale at every destination row.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+#include "quant_math.cuh"
+
+namespace fp8fg {
+
+constexpr int kChunk = 64;          // tokens per chunk (ranked by one warp, 32 at a time)
+constexpr int kMaxTopk = 16;
+constexpr int kMaxLocal = 1024;     // local experts
+constexpr int kPackThreads = 256;   // 64 four-lane groups
+
+// Local expert index of slot j of a token's top-k row, or -1 when the expert
+// is not local or repeats an earlier slot of the same row.
+__device__ __forceinline__ int local_slot(const int32_t* ids, int j, int expert_begin, int E) {
+    const int64_t e = static_cast<int64_t>(ids[j]) - expert_begin;
+    if (e < 0 || e >= E) return -1;
+    for (int i = 0; i < j; ++i)
+        if (ids[i] == ids[j]) return -1;
+    return static_cast<int>(e);
+}
+
+__global__ void __launch_bounds__(kChunk) moe_count_kernel(const int32_t* __restrict__ topk_ids,
+                                                           int64_t T, int topk, int expert_begin,
+                                                           int E, int nchunks,
+                                                           int32_t* __restrict__ counts) {
+    __shared__ int hist[kMaxLocal];
+    for (int e = threadIdx.x; e < E; e += kChunk) hist[e] = 0;
+    __syncthreads();
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * kChunk + threadIdx.x;
+    if (t < T) {
+        int32_t ids[kMaxTopk];
+        for (int j = 0; j < topk; ++j) ids[j] = __ldg(topk_ids + t * topk + j);
+        for (int j = 0; j < topk; ++j) {
+            const int e = local_slot(ids, j, expert_begin, E);
+            if (e >= 0) atomicAdd(&hist[e], 1);
+        }
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kChunk)
+        counts[static_cast<int64_t>(e) * nchunks + blockIdx.x] = hist[e];
+}
+
+// counts[e][c] -> sum of counts[e][c'] over c' < c; totals[e] = sum over all c.
+__global__ void __launch_bounds__(256) moe_scan_kernel(int32_t* __restrict__ counts,
+                                                       int32_t* __restrict__ totals, int E,
+                                                       int nchunks) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * 8 + warp;
+    if (e >= E) return;  // whole warp
+    int32_t* row = counts + static_cast<int64_t>(e) * nchunks;
+    int running = 0;
+    for (int c0 = 0; c0 < nchunks; c0 += 32) {
+        const int c = c0 + lane;
+        const int v = c < nchunks ? row[c] : 0;
+        int incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += n;
+        }
+        if (c < nchunks) row[c] = running + incl - v;
+        running += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) totals[e] = running;
+}
+
+__global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
+    const uint16_t* __restrict__ x, int64_t T, int64_t KB, int64_t ldx,
+    const int32_t* __restrict__ topk_ids, int topk, int expert_begin, int E,
+    const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ totals, int nchunks,
+    int kb_per_slice, uint8_t* __restrict__ xq, float* __restrict__ sx, int64_t cap,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ token_ids) {
+    __shared__ int32_t s_ids[kChunk * kMaxTopk];
+    __shared__ int32_t s_dest[kChunk * kMaxTopk];
+    __shared__ int32_t s_base[kMaxLocal];
+    __shared__ uint32_t s_mask[kMaxLocal];
+    __shared__ int32_t s_run[kMaxLocal];
+    __shared__ int32_t s_wsum[kPackThreads / 32];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int c = blockIdx.x;
+    const int64_t t0 = static_cast<int64_t>(c) * kChunk;
+    const int n_tok = static_cast<int>(T - t0 < kChunk ? T - t0 : kChunk);
+    const bool first_cta = c == 0 && blockIdx.y == 0;
+
+    for (int i = tid; i < n_tok * topk; i += kPackThreads) s_ids[i] = __ldg(topk_ids + t0 * topk + i);
+
+    // exclusive scan of the expert totals (four experts per thread) -> offsets
+    int v[4], sum = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int e = tid * 4 + i;
+        v[i] = e < E ? __ldg(totals + e) : 0;
+        sum += v[i];
+    }
+    int incl = sum;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        int w = lane < kPackThreads / 32 ? s_wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < kPackThreads / 32; o <<= 1) {
+            const int n = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += n;
+        }
+        if (lane < kPackThreads / 32) s_wsum[lane] = w;  // inclusive warp totals
+    }
+    __syncthreads();
+    int excl = incl - sum + (warp > 0 ? s_wsum[warp - 1] : 0);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int e = tid * 4 + i;
+        if (e < E) {
+            s_base[e] = excl + __ldg(chunk_base + static_cast<int64_t>(e) * nchunks + c);
+            s_mask[e] = 0;
+            s_run[e] = 0;
+            if (first_cta) offsets[e] = excl;
+        }
+        excl += v[i];
+    }
+    if (first_cta && tid == 0) offsets[E] = s_wsum[kPackThreads / 32 - 1];
+    __syncthreads();
+
+    // rank the (token, local expert) pairs of the chunk in token order
+    if (warp == 0) {
+        for (int b = 0; b < kChunk; b += 32) {
+            const int tl = b + lane;
+            const bool valid = tl < n_tok;
+            int le[kMaxTopk];
+            for (int j = 0; j < topk; ++j) {
+                le[j] = valid ? local_slot(&s_ids[tl * topk], j, expert_begin, E) : -1;
+                if (le[j] >= 0) atomicOr(&s_mask[le[j]], 1u << lane);
+            }
+            __syncwarp();
+            for (int j = 0; j < topk; ++j) {
+                if (le[j] >= 0) {
+                    const uint32_t m = s_mask[le[j]];
+                    s_dest[tl * topk + j] =
+                        s_base[le[j]] + s_run[le[j]] + __popc(m & ((1u << lane) - 1u));
+                } else if (valid) {
+                    s_dest[tl * topk + j] = -1;
+                }
+            }
+            __syncwarp();
+            // the highest lane of each expert's mask advances its running count
+            for (int j = 0; j < topk; ++j) {
+                if (le[j] >= 0) {
+                    const uint32_t m = s_mask[le[j]];
+                    if (m != 0 && 31 - __clz(m) == lane) {
+                        s_run[le[j]] += __popc(m);
+                        s_mask[le[j]] = 0;
+                    }
+                }
+            }
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+
+    if (blockIdx.y == 0) {
+        for (int i = tid; i < n_tok * topk; i += kPackThreads) {
+            const int d = s_dest[i];
+            if (d >= 0) token_ids[d] = static_cast<int32_t>(t0 + i / topk);
+        }
+    }
+
+    // 1x128 groups (token, kb) of this K slice: four lanes per group, 32
+    // elements per lane, the arithmetic of the 1x128 quantiser
+    const int kb0 = blockIdx.y * kb_per_slice;
+    const int kb1 = static_cast<int>(KB < kb0 + kb_per_slice ? KB : kb0 + kb_per_slice);
+    const int nkb = kb1 - kb0;
+    const int items = n_tok * nkb;
+    const int l4 = tid & 3;
+    const uint32_t gmask = 0xFu << (lane & ~3);
+    const int64_t K = KB * 128;
+    for (int it = tid >> 2; it < items; it += kPackThreads / 4) {
+        const int tl = it / nkb;
+        const int kb = kb0 + it % nkb;
+        const uint16_t* src = x + (t0 + tl) * ldx + static_cast<int64_t>(kb) * 128 + l4 * 32;
+        uint4 q[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) q[i] = ld_stream_v4(src + 8 * i);
+        uint32_t mx = absmax_bf16x2(q[0].x, q[0].y);
+        mx = absmax_bf16x2(mx, absmax_bf16x2(q[0].z, q[0].w));
+#pragma unroll
+        for (int i = 1; i < 4; ++i) {
+            mx = absmax_bf16x2(mx, absmax_bf16x2(q[i].x, q[i].y));
+            mx = absmax_bf16x2(mx, absmax_bf16x2(q[i].z, q[i].w));
+        }
+        float amax = amax_of_pair(mx);
+        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
+        const float s = group_scale(amax);
+        const GroupDiv dv(s);
+        uint4 o[2];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t a = dv.quad(bf16_lo(q[i].x), bf16_hi(q[i].x), bf16_lo(q[i].y),
+                                       bf16_hi(q[i].y));
+            const uint32_t b = dv.quad(bf16_lo(q[i].z), bf16_hi(q[i].z), bf16_lo(q[i].w),
+                                       bf16_hi(q[i].w));
+            if (i & 1) {
+                o[i >> 1].z = a;
+                o[i >> 1].w = b;
+            } else {
+                o[i >> 1].x = a;
+                o[i >> 1].y = b;
+            }
+        }
+        for (int j = 0; j < topk; ++j) {
+            const int d = s_dest[tl * topk + j];
+            if (d < 0) continue;
+            uint4* dst = reinterpret_cast<uint4*>(xq + static_cast<int64_t>(d) * K +
+                                                  static_cast<int64_t>(kb) * 128 + l4 * 32);
+            dst[0] = o[0];
+            dst[1] = o[1];
+            if (l4 == 0) sx[static_cast<int64_t>(kb) * cap + d] = s;
+        }
+    }
+}
+
+struct DispatchPlan {
+    int nchunks = 0;
+    size_t count_ints = 0;  // counts[E][nchunks]
+    size_t bytes = 0;       // counts + totals, 256-byte granules
+};
+
+static DispatchPlan dispatch_plan(int64_t T, int E) {
+    DispatchPlan d;
+    d.nchunks = static_cast<int>((T + kChunk - 1) / kChunk);
+    d.count_ints = static_cast<size_t>(E) * d.nchunks;
+    const size_t ints = d.count_ints + static_cast<size_t>(E);
+    d.bytes = (ints * sizeof(int32_t) + 255) & ~static_cast<size_t>(255);
+    return d;
+}
+
+static int dispatch_checks(int64_t T, int64_t K, int64_t ldx, int32_t topk, int32_t n_local,
+                           int64_t cap) {
+    if (T < 0 || K <= 0 || K % 128 != 0 || ldx < K || topk < 1 || topk > kMaxTopk ||
+        n_local < 1 || n_local > kMaxLocal || cap < 0)
+        return FP8_ERR_SHAPE;
+    if (T > (static_cast<int64_t>(1) << 31) / kMaxTopk) return FP8_ERR_UNSUPPORTED;
+    if (cap < T * std::min<int64_t>(topk, n_local) || cap > 0x7fffffffLL) return FP8_ERR_SHAPE;
+    return FP8_OK;
+}
+
+// The three launches on a workspace of at least dispatch_plan().bytes.
+static int dispatch_launch(const void* x, int64_t T, int64_t K, int64_t ldx,
+                           const int32_t* topk_ids, int32_t topk, int32_t expert_begin,
+                           int32_t n_local, uint8_t* xq, float* sx, int64_t cap,
+                           int32_t* offsets, int32_t* token_ids, int32_t* scratch,
+                           cudaStream_t stream) {
+    const DispatchPlan d = dispatch_plan(T, n_local);
+    int32_t* counts = scratch;
+    int32_t* totals = scratch + d.count_ints;
+    moe_count_kernel<<<d.nchunks, kChunk, 0, stream>>>(topk_ids, T, topk, expert_begin, n_local,
+                                                        d.nchunks, counts);
+    moe_scan_kernel<<<(n_local + 7) / 8, 256, 0, stream>>>(counts, totals, n_local, d.nchunks);
+    const int sms = sm_count_current();
+    const int64_t KB = K / 128;
+    int64_t slices = (4LL * (sms > 0 ? sms : 148) + d.nchunks - 1) / d.nchunks;
+    slices = std::max<int64_t>(1, std::min<int64_t>(slices, KB));
+    const int kb_per_slice = static_cast<int>((KB + slices - 1) / slices);
+    slices = (KB + kb_per_slice - 1) / kb_per_slice;
+    const dim3 grid(static_cast<unsigned>(d.nchunks), static_cast<unsigned>(slices));
+    moe_pack_quant_kernel<<<grid, kPackThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(x), T, KB, ldx, topk_ids, topk, expert_begin, n_local,
+        counts, totals, d.nchunks, kb_per_slice, xq, sx, cap, offsets, token_ids);
+    return launch_status();
+}
+
+}  // namespace fp8fg
+
+using namespace fp8fg;
+
+extern "C" int fp8_moe_dispatch_workspace_size(int64_t T, int32_t n_local, size_t* bytes) {
+    if (bytes == nullptr) return FP8_ERR_NULL;
+    *bytes = 0;
+    if (T < 0 || n_local < 1 || n_local > kMaxLocal) return FP8_ERR_SHAPE;
+    if (T > (static_cast<int64_t>(1) << 31) / kMaxTopk) return FP8_ERR_UNSUPPORTED;
+    *bytes = T == 0 ? 0 : dispatch_plan(T, n_local).bytes;
+    return FP8_OK;
+}
+
+extern "C" int fp8_moe_dispatch_quant(const void* x, int64_t T, int64_t K, int64_t ldx,
+                                      const int32_t* topk_ids, int32_t topk,
+                                      int32_t expert_begin, int32_t n_local, uint8_t* xq,
+                                      float* sx, int64_t cap, int32_t* offsets,
+                                      int32_t* token_ids, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+    int st = dispatch_checks(T, K, ldx, topk, n_local, cap);
+    if (st != FP8_OK) return st;
+    if (offsets == nullptr) return FP8_ERR_NULL;
+    if (!aligned(offsets, 4)) return FP8_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        // no tokens: every expert is empty
+        if (cudaMemsetAsync(offsets, 0, (static_cast<size_t>(n_local) + 1) * sizeof(int32_t), s) !=
+            cudaSuccess)
+            return FP8_ERR_CUDA;
+        return FP8_OK;
+    }
+    if (x == nullptr || topk_ids == nullptr || xq == nullptr || sx == nullptr ||
+        token_ids == nullptr || workspace == nullptr)
+        return FP8_ERR_NULL;
+    if (ldx % 8 != 0 || !aligned(x, 16) || !aligned(xq, 16) || !aligned(sx, 4) ||
+        !aligned(topk_ids, 4) || !aligned(token_ids, 4) || !aligned(workspace, 256))
+        return FP8_ERR_ALIGN;
+    if (workspace_bytes < dispatch_plan(T, n_local).bytes) return FP8_ERR_SHAPE;
+    return dispatch_launch(x, T, K, ldx, topk_ids, topk, expert_begin, n_local, xq, sx, cap,
+                           offsets, token_ids, static_cast<int32_t*>(workspace), s);
+}

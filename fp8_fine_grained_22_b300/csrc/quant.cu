@@ -16,79 +16,9 @@
 #include <cuda_fp8.h>
 
 #include "common.cuh"
+#include "quant_math.cuh"
 
 namespace fp8fg {
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-__device__ __forceinline__ float group_scale(float amax) {
-    return amax == 0.0f ? 1.0f : __fdiv_rn(amax, 448.0f);
-}
-
-__device__ __forceinline__ uint64_t f2x2(float lo, float hi) {
-    return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
-}
-__device__ __forceinline__ uint64_t mul2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
-}
-
-// Division of every element of a group by its scale s, correctly rounded,
-// from one reciprocal per group.  Markstein's correction (P. Markstein,
-// "Computation of elementary functions on the IBM RISC System/6000
-// processor", IBM J. Res. Dev. 34(1), 1990): with r = RN(1/s) and
-// q0 = RN(x r), the residual e = x - q0 s is exact under a fused
-// multiply-add and RN(q0 + e r) is the correctly rounded quotient x / s.
-// Two lanes at a time with the packed FP32 instructions.  The sign of a zero
-// quotient is taken from x (s > 0).  The residual is exact only while it does
-// not underflow, i.e. for |x| >= 2^-102; with s >= 2^-91 every smaller x has
-// |x / s| < 2^-11 and encodes to a signed zero whatever the last bit of its
-// quotient, so the corrected path is used for s >= 2^-91 and groups with a
-// smaller scale take the IEEE division.  The tests compare the resulting
-// codes with IEEE division over every (x, amax) bf16 pair.
-struct GroupDiv {
-    float s;
-    uint64_t r2, ns2;
-    bool fast;
-    __device__ __forceinline__ explicit GroupDiv(float scale) : s(scale) {
-        const float r = __frcp_rn(scale);
-        r2 = f2x2(r, r);
-        ns2 = f2x2(-scale, -scale);
-        fast = scale >= 0x1p-91f;
-    }
-    // E4M3 codes of x0 / s and x1 / s, x0 in the low byte
-    __device__ __forceinline__ uint32_t pair(float x0, float x1) const {
-        float q0, q1;
-        if (fast) {
-            const uint64_t x2 = f2x2(x0, x1);
-            const uint64_t a = mul2(x2, r2);
-            const uint64_t e = fma2(a, ns2, x2);
-            const uint64_t q = fma2(e, r2, a);
-            q0 = copysignf(__uint_as_float(static_cast<uint32_t>(q)), x0);
-            q1 = copysignf(__uint_as_float(static_cast<uint32_t>(q >> 32)), x1);
-        } else {
-            q0 = __fdiv_rn(x0, s);
-            q1 = __fdiv_rn(x1, s);
-        }
-        return static_cast<uint32_t>(
-            __nv_cvt_float2_to_fp8x2(make_float2(q0, q1), __NV_SATFINITE, __NV_E4M3));
-    }
-    // four codes packed little-endian
-    __device__ __forceinline__ uint32_t quad(float a, float b, float c, float d) const {
-        return pair(a, b) | (pair(c, d) << 16);
-    }
-};
-
-__device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
-    return __ldcs(reinterpret_cast<const uint4*>(p));
-}
 
 // All three kernels are persistent: a grid of a few CTAs per SM walks the
 // tiles with a stride of the grid size, and each thread issues the loads of
@@ -96,17 +26,6 @@ __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
 // flight through the compute and store phases.
 constexpr int kQuantThreads = 256;
 constexpr int kQuantCtasPerSm = 4;
-
-// Largest magnitude in a word of two bf16 values, as a packed bf16 pair
-// (exact: max and abs of bf16 values do not round).
-__device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
-    const __nv_bfloat162 r = __hmax2(__habs2(*reinterpret_cast<const __nv_bfloat162*>(&a)),
-                                     __habs2(*reinterpret_cast<const __nv_bfloat162*>(&b)));
-    return *reinterpret_cast<const uint32_t*>(&r);
-}
-__device__ __forceinline__ float amax_of_pair(uint32_t w) {
-    return fmaxf(bf16_lo(w), bf16_hi(w));  // both halves already non-negative
-}
 
 // ------------------------------------------------------------------ 1x128 --
 // Tile: 64 rows x one 128-wide K group.  Four lanes per group, 32 elements

@@ -23,7 +23,8 @@ FP8_BSCALE_BLOCK128_T = 2
 
 # every entry point of include/fp8fg.h
 EXPORTS = ("fp8_status_str", "fp8_device_error", "fp8_quant_act_1x128", "fp8_quant_act_128x1",
-           "fp8_quant_weight_128x128", "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe")
+           "fp8_quant_weight_128x128", "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe",
+           "fp8_moe_dispatch_workspace_size", "fp8_moe_dispatch_quant")
 
 
 class Fp8Error(RuntimeError):
@@ -60,6 +61,11 @@ def lib() -> ctypes.CDLL:
         L.fp8_gemm_blockscaled.argtypes = [P, P, P, P, I, I64, I64, I64, P, I64, I, P]
         L.fp8_grouped_gemm_moe.restype = I
         L.fp8_grouped_gemm_moe.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, I, P]
+        L.fp8_moe_dispatch_workspace_size.restype = I
+        L.fp8_moe_dispatch_workspace_size.argtypes = [I64, I32, ctypes.POINTER(ctypes.c_size_t)]
+        L.fp8_moe_dispatch_quant.restype = I
+        L.fp8_moe_dispatch_quant.argtypes = [P, I64, I64, I64, P, I32, I32, I32, P, P, I64, P, P,
+                                             P, ctypes.c_size_t, P]
         _lib = L
     return _lib
 
@@ -177,3 +183,49 @@ def fp8_grouped_gemm_moe(aq, sa, bq, sb, offsets, out_dtype=torch.bfloat16, c=No
     _check(lib().fp8_grouped_gemm_moe(_p(aq), _p(sa), _p(bq), _p(sb), _p(offsets), E, T, N, K,
                                       _p(c), out_type, _stream(stream)), "fp8_grouped_gemm_moe")
     return c
+
+
+# ------------------------------------------------------------- MoE dispatch --
+def fp8_moe_dispatch_workspace_size(T, n_local) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().fp8_moe_dispatch_workspace_size(T, n_local, ctypes.byref(n)),
+           "fp8_moe_dispatch_workspace_size")
+    return n.value
+
+
+def moe_dispatch_workspace(T, n_local, device="cuda"):
+    """Device workspace for fp8_moe_dispatch_quant (uninitialised; None when T = 0)."""
+    n = fp8_moe_dispatch_workspace_size(T, n_local)
+    return torch.empty(n, dtype=torch.uint8, device=device) if n else None
+
+
+def fp8_moe_dispatch_quant(x, topk_ids, expert_begin, n_local, cap=None, xq=None, sx=None,
+                           offsets=None, token_ids=None, workspace=None, stream=None):
+    """x bf16 [T, K], topk_ids int32 [T, topk] -> (xq uint8 [cap, K], sx f32 [K/128, cap],
+    offsets int32 [n_local+1], token_ids int32 [cap]); rows of local expert e at
+    offsets[e]:offsets[e+1], tokens ascending."""
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(topk_ids, "topk_ids", torch.int32)
+    assert x.dim() == 2 and x.stride(1) == 1 and topk_ids.is_contiguous()
+    T, K = x.shape
+    topk = topk_ids.shape[1] if topk_ids.dim() == 2 else 1
+    assert topk_ids.shape[0] == T
+    if cap is None:
+        cap = T * min(topk, n_local)
+    dev = x.device
+    if xq is None:
+        xq = torch.empty((cap, K), dtype=torch.uint8, device=dev)
+    if sx is None:
+        sx = torch.empty((K // 128, cap), dtype=torch.float32, device=dev)
+    if offsets is None:
+        offsets = torch.empty(n_local + 1, dtype=torch.int32, device=dev)
+    if token_ids is None:
+        token_ids = torch.empty(cap, dtype=torch.int32, device=dev)
+    if workspace is None:
+        workspace = moe_dispatch_workspace(T, n_local, dev)
+    nbytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib().fp8_moe_dispatch_quant(_p(x), T, K, x.stride(0), _p(topk_ids), topk,
+                                        expert_begin, n_local, _p(xq), _p(sx), cap, _p(offsets),
+                                        _p(token_ids), _p(workspace), nbytes, _stream(stream)),
+           "fp8_moe_dispatch_quant")
+    return xq, sx, offsets, token_ids

@@ -38,6 +38,7 @@
 #ifndef FP8FG_H
 #define FP8FG_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -161,6 +162,51 @@ int fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, const uint8_t* bq,
 int fp8_grouped_gemm_moe(const uint8_t* aq, const float* sa, const uint8_t* bq,
                          const float* sb, const int32_t* offsets, int32_t E, int64_t T,
                          int64_t N, int64_t K, void* c, int out_type, void* stream);
+
+/*
+ * fp8_moe_dispatch_workspace_size -- bytes of device workspace
+ * fp8_moe_dispatch_quant needs for T tokens and n_local local experts
+ * (0 when T = 0).  *bytes is set to 0 on error.
+ */
+int fp8_moe_dispatch_workspace_size(int64_t T, int32_t n_local, size_t* bytes);
+
+/*
+ * fp8_moe_dispatch_quant -- MoE dispatch packing in FP8: the activation rows
+ * of the tokens routed to each local expert, gathered expert by expert and
+ * quantised 1x128 (report section 3.3.3: activations are dispatched to the
+ * MoE experts in FP8 with the fine-grained scheme; section 3.4: expert
+ * parallelism).  Produces the A operand, A scales and offsets of
+ * fp8_grouped_gemm_moe.
+ *   x          : bfloat16 [T][K], row stride ldx (the tokens).           (input)
+ *   topk_ids   : int32 [T][topk], the experts each token is routed to
+ *                (global ids; repeats within a row count once).          (input)
+ *   expert_begin, n_local : the local experts are global ids
+ *                expert_begin .. expert_begin + n_local - 1; local expert
+ *                e = id - expert_begin; other ids are ignored.
+ *   xq         : E4M3 [cap][K] (row stride K): rows offsets[e] ..
+ *                offsets[e+1]-1 are the tokens routed to local expert e, in
+ *                ascending token order, each quantised exactly as
+ *                fp8_quant_act_1x128 quantises it.                       (output)
+ *   sx         : float [K/128][cap]: scale of packed row r, K group kb at
+ *                sx[kb*cap + r] (pass T = cap to fp8_grouped_gemm_moe).  (output)
+ *   offsets    : int32 [n_local+1], offsets[0] = 0, offsets[n_local] = rows used. (output)
+ *   token_ids  : int32 [cap]: the source token of each packed row.       (output)
+ *   workspace  : device memory of fp8_moe_dispatch_workspace_size() bytes,
+ *                256-byte aligned; no initialisation needed (every call
+ *                overwrites what it reads).  Calls sharing a workspace must
+ *                not overlap on the GPU.
+ * Rows at or past offsets[n_local] (and their scales) are left untouched.
+ * Placement is deterministic (no atomics on global memory).
+ * Requires K % 128 == 0, K > 0, ldx >= K, ldx % 8 == 0, 1 <= topk <= 16,
+ * 1 <= n_local <= 1024, cap >= T * min(topk, n_local), cap < 2^31,
+ * T <= 2^27; x and xq 16-byte aligned, sx/topk_ids/offsets/token_ids 4-byte
+ * aligned.  T = 0 only zeroes offsets.
+ */
+int fp8_moe_dispatch_quant(const void* x, int64_t T, int64_t K, int64_t ldx,
+                           const int32_t* topk_ids, int32_t topk, int32_t expert_begin,
+                           int32_t n_local, uint8_t* xq, float* sx, int64_t cap,
+                           int32_t* offsets, int32_t* token_ids, void* workspace,
+                           size_t workspace_bytes, void* stream);
 
 #ifdef __cplusplus
 }
