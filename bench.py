@@ -10,6 +10,13 @@ The metric is the step's FP8 GEMM throughput, 2*M*N*K / step time (TFLOP/s);
 the JSON line also carries each kernel's own rate and roofline fraction.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload fprop_dense|moe_prefill]
+
+`--workload moe_prefill` times the MoE expert layer instead: FP8 dispatch
+packing of 16384 tokens routed top-8 of 256 experts to 32 local experts
+(fp8_moe_dispatch_quant) followed by the grouped GEMM against the experts'
+W[7168, 4096] (quantised once, outside the timed region); the metric is the
+grouped GEMM's FLOPs over the step time.
 
 Under torchrun each rank runs its own replica of the workload (weak scaling,
 no collective on the data path); rank 0 prints one JSON line.
@@ -38,6 +45,7 @@ sys.path.insert(0, ROOT)
 from fp8_fine_grained_22_b300 import inputs  # noqa: E402
 
 WORKLOAD = "fprop_m8192_n7168_k2048_bf16"
+MOE_WORKLOAD = "moe_prefill_t16384_top8of256_e32_k7168_n4096_bf16"
 L2_BYTES = 126 * 2 ** 20
 METRIC = "FP8 block-scaled GEMM TFLOP/s and % of B300 FP8 peak; quantizer GB/s"
 PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemm_fprop_m8192_n7168_k2048.md")
@@ -346,6 +354,211 @@ def run_ours(args, rank, world, local):
     return line
 
 
+# ------------------------------------------------------------ MoE workload --
+def run_moe(args, rank, world, local):
+    from fp8_fine_grained_22_b300 import fp8fg
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fp8fg.lib()  # fail loudly if the CUDA library is missing
+    wl = inputs.moe_prefill(seed=0, device="cpu")
+    x_tok, order = wl.extra["x_tokens"], wl.extra["topk_ids"].to(torch.int32).contiguous()
+    T, K = x_tok.shape
+    E, N = wl.E, wl.N
+    topk = order.shape[1]
+    cap = T * min(topk, E)
+    R = int(wl.offsets[-1])
+    flops = 2.0 * R * N * K
+    x = x_tok.to(dev)
+    ids = order.to(dev)
+    wq = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
+    sw = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device=dev)
+    for e in range(E):  # static weights, quantised once
+        fp8fg.fp8_quant_weight_128x128(wl.w[e].to(dev), wq=wq[e], sw=sw[e])
+    del wl
+    xq = torch.empty((cap, K), dtype=torch.uint8, device=dev)
+    sx = torch.empty((K // 128, cap), dtype=torch.float32, device=dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    tok = torch.empty(cap, dtype=torch.int32, device=dev)
+    ws = fp8fg.moe_dispatch_workspace(T, E, dev)
+    y = torch.empty((cap, N), dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def flush_l2():
+        flush.zero_()
+        torch.sum(flush, dim=0, out=flush_sink)
+
+    def dispatch():
+        fp8fg.fp8_moe_dispatch_quant(x, ids, 0, E, cap=cap, xq=xq, sx=sx, offsets=off,
+                                     token_ids=tok, workspace=ws, stream=stream)
+
+    def grouped():
+        fp8fg.fp8_grouped_gemm_moe(xq, sx, wq, sw, off, c=y, stream=stream)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        dispatch()
+        if ev is not None:
+            ev[1].record(stream)
+        grouped()
+        if ev is not None:
+            ev[2].record(stream)
+
+    def kernel_ms(fn, reps=20):
+        e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(reps)]
+        for a, b in e:
+            flush_l2()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in e)
+
+    for _ in range(args.warmup):
+        flush_l2()
+        step()
+    torch.cuda.synchronize()
+    if fp8fg.device_error() != 0:
+        raise RuntimeError("device-side error during warm-up")
+    if int(off[-1].item()) != R:
+        raise RuntimeError("dispatch produced %d rows, expected %d" % (int(off[-1].item()), R))
+    steps = min(args.steps, args.moe_steps)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    rank_barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for i in range(steps):
+            flush_l2()
+            step(events[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    rank_barrier()
+    st = [e[0].elapsed_time(e[2]) for e in events]
+    dp = [e[0].elapsed_time(e[1]) for e in events]
+    gm = [e[1].elapsed_time(e[2]) for e in events]
+    ms_step = reduce_max(statistics.mean(st), dev)
+    disp_ms, gemm_ms = statistics.mean(dp), statistics.mean(gm)
+    disp_alone = kernel_ms(dispatch)
+    gemm_alone = kernel_ms(grouped)
+
+    # end to end: tokens and routing in from pinned host memory, the R output rows out
+    xh, idh = x_tok.pin_memory(), order.pin_memory()
+    yh = torch.empty((R, N), dtype=torch.bfloat16).pin_memory()
+    offh = torch.empty(E + 1, dtype=torch.int32).pin_memory()
+
+    def e2e_step():
+        x.copy_(xh, non_blocking=True)
+        ids.copy_(idh, non_blocking=True)
+        step()
+        offh.copy_(off, non_blocking=True)
+        yh.copy_(y[:R], non_blocking=True)
+
+    e2e_steps = min(steps, args.e2e_steps)
+    e2e_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(a.elapsed_time(b) / e2e_steps, dev)
+    if fp8fg.device_error() != 0:
+        raise RuntimeError("device-side error")
+
+    peaks, peak_src = measured_peaks()
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    hbm = peaks["hbm_gbs"]
+    gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
+    # bytes the dispatch must move: the rows of tokens with a local expert
+    # (others are not read), the packed codes, scales, routing and token ids
+    n_active = int(((order >= 0) & (order < E)).any(dim=1).sum())
+    disp_bytes = n_active * K * 2 + R * K + (K // 128) * R * 4 + T * topk * 4 + R * 4
+    line = {
+        "metric": METRIC,
+        "value": round(whole_job_tflops(world, flops, ms_step), 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> f32 accumulate, bf16 out",
+        "data": "synthetic (seeded: N(0,1) tokens with 1% x100 outlier channels, sigmoid+bias "
+                "top-8 routing of 256 experts, N(0,0.006^2) expert weights)",
+        "config": {"workload": MOE_WORKLOAD, "T": T, "topk": topk, "local_experts": E,
+                   "rows": R, "N": N, "K": K, "parallelism": "replicas (dp%d, no collective)"
+                   % world,
+                   "l2": "flushed between steps (%d MB written, then read back)" % (
+                       flush.numel() * 4 >> 20),
+                   "step": ["fp8_moe_dispatch_quant", "fp8_grouped_gemm_moe"],
+                   "weights": "quantised once before timing (static)"},
+        "e2e": {"value": round(whole_job_tflops(world, flops, e2e_ms), 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+                "h2d_bytes_per_step": T * K * 2 + T * topk * 4,
+                "d2h_bytes_per_step": R * N * 2 + (E + 1) * 4},
+        "gpu_launches": 4 * steps,
+        "roofline": {"kernel": "fp8_grouped_gemm_moe", "bound": "tensor",
+                     "achieved": round(gemm_tflops, 2), "peak": round(fp8_peak, 1),
+                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
+                     "peak_source": "%s bf16 burst x 2 (nominal FP8:BF16 dense ratio)" % peak_src,
+                     "traffic": None},
+        "kernels": {
+            "fp8_moe_dispatch_quant (in step)": {"ms": round(disp_ms, 5)},
+            "fp8_moe_dispatch_quant (alone)": {
+                "ms": round(disp_alone, 5),
+                "gbs": round(disp_bytes / (disp_alone * 1e-3) / 1e9, 1),
+                "frac_hbm": round(disp_bytes / (disp_alone * 1e-3) / 1e9 / hbm, 4)},
+            "fp8_grouped_gemm_moe (in step)": {"ms": round(gemm_ms, 5),
+                                               "tflops": round(gemm_tflops, 2)},
+            "fp8_grouped_gemm_moe (alone)": {
+                "ms": round(gemm_alone, 5),
+                "tflops": round(flops / (gemm_alone * 1e-3) / 1e12, 2)},
+        },
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if args.cpu_baseline and rank == 0:
+        line["cpu_baseline"] = cpu_baseline_moe(args.ref_rows)
+    return line
+
+
+def cpu_baseline_moe(n_rows):
+    """The oracle on the host: dispatch of every token (membership, gather, 1x128
+    quantisation), quantisation of the experts the sampled rows use, and the
+    binary64 grouped GEMM of n_rows packed rows."""
+    import oracle
+
+    wl = inputs.moe_prefill(seed=0, device="cpu")
+    threads = oracle.default_threads()
+    xb = inputs.bf16_bits(wl.extra["x_tokens"])
+    order = wl.extra["topk_ids"].numpy()
+    t0 = time.perf_counter()
+    aq, sa, offsets, _ = oracle.moe_dispatch_quant(xb, order, 0, wl.E)
+    rows = np.arange(min(n_rows, aq.shape[0]))
+    experts = np.unique(np.searchsorted(offsets, rows, side="right") - 1)
+    bq = np.zeros((wl.E, wl.N, wl.K), np.uint8)
+    sb = np.ones((wl.E, wl.N // 128, wl.K // 128), np.float32)
+    for e in experts:
+        bq[e], _, sb[e] = oracle.quant_weight_128x128(inputs.bf16_bits(wl.w[e]))
+    c = oracle.grouped_gemm(aq, sa, bq, sb, offsets, rows=rows, nthreads=threads)
+    oracle.round_bf16(c)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows.size * wl.N * wl.K
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": "dispatch of all %d tokens, weights of %d experts quantised, binary64 "
+                      "grouped GEMM of the first %d of %d packed rows" % (
+                          xb.shape[0], experts.size, rows.size, aq.shape[0])}
+
+
 # ------------------------------------------------------- CPU oracle baseline --
 def cpu_baseline(n_rows, wl=None):
     """The oracle on the host cores: quantise all of W and a sample of X rows,
@@ -369,8 +582,31 @@ def cpu_baseline(n_rows, wl=None):
             "sample": "%d of %d rows of X (all of W quantised), binary64 GEMM" % (n_rows, wl.M)}
 
 
+def run_reference_moe(args):
+    times, res = [], None
+    for _ in range(args.steps):
+        res = cpu_baseline_moe(args.ref_rows)
+        times.append(res["seconds"])
+    ms = statistics.mean(times) * 1e3
+    value = res["value"]
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64 oracle (e4m3 codes, binary64 accumulate)",
+        "data": "synthetic (same seeded workload)",
+        "config": {"workload": MOE_WORKLOAD, "sample_rows": args.ref_rows},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": res["cores"],
+                         "kind": "oracle", "sample": res["sample"]},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
 def run_reference(args):
     """Reference arm: the CPU oracle, timed per step on a bounded sample."""
+    if args.workload == "moe_prefill":
+        return run_reference_moe(args)
     wl = inputs.fprop_dense(seed=0, device="cpu")
     for _ in range(args.warmup and 1):
         cpu_baseline(8, wl)
@@ -415,6 +651,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-sample-rows", type=int, default=2048)
     ap.add_argument("--ref-rows", type=int, default=512)
+    ap.add_argument("--workload", choices=["fprop_dense", "moe_prefill"], default="fprop_dense")
+    ap.add_argument("--moe-steps", type=int, default=2000,
+                    help="cap on timed steps for the MoE workload")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
@@ -427,7 +666,10 @@ def main():
         torch.distributed.init_process_group(
             backend="nccl" if torch.cuda.is_available() else "gloo")
     try:
-        line = run_ours(args, rank, world, local)
+        if args.workload == "moe_prefill":
+            line = run_moe(args, rank, world, local)
+        else:
+            line = run_ours(args, rank, world, local)
         if rank == 0:
             print(json.dumps(line), flush=True)
     finally:

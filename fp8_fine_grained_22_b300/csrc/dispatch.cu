@@ -20,9 +20,11 @@
 //          (in place) and the expert's total;
 //   pack   one CTA per (chunk, K slice): the exclusive scan of the totals
 //          gives offsets; the first warp ranks the chunk's (token, expert)
-//          pairs in token order with shared-memory lane masks; all warps
-//          quantise 1x128 groups (the arithmetic of fp8_quant_act_1x128) and
-//          store each group's codes and scale at every destination row.
+//          pairs in token order with shared-memory lane masks and lists the
+//          tokens that have a local expert; all warps quantise those tokens'
+//          1x128 groups (the arithmetic of fp8_quant_act_1x128) and store
+//          each group's codes and scale at every destination row.  Tokens
+//          routed only to other experts are not read.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -104,6 +106,8 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
     __shared__ uint32_t s_mask[kMaxLocal];
     __shared__ int32_t s_run[kMaxLocal];
     __shared__ int32_t s_wsum[kPackThreads / 32];
+    __shared__ int32_t s_active[kChunk];  // chunk tokens with a local expert, ascending
+    __shared__ int32_t s_n_active;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
     const int64_t t0 = static_cast<int64_t>(c) * kChunk;
@@ -175,8 +179,10 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
             }
             __syncwarp();
             // the highest lane of each expert's mask advances its running count
+            bool any = false;
             for (int j = 0; j < topk; ++j) {
                 if (le[j] >= 0) {
+                    any = true;
                     const uint32_t m = s_mask[le[j]];
                     if (m != 0 && 31 - __clz(m) == lane) {
                         s_run[le[j]] += __popc(m);
@@ -184,6 +190,12 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
                     }
                 }
             }
+            // tokens with no local expert are never read
+            const uint32_t act = __ballot_sync(0xffffffffu, any);
+            const int n_before = b == 0 ? 0 : s_n_active;
+            __syncwarp();
+            if (any) s_active[n_before + __popc(act & ((1u << lane) - 1u))] = tl;
+            if (lane == 0) s_n_active = n_before + __popc(act);
             __syncwarp();
         }
     }
@@ -201,12 +213,12 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
     const int kb0 = blockIdx.y * kb_per_slice;
     const int kb1 = static_cast<int>(KB < kb0 + kb_per_slice ? KB : kb0 + kb_per_slice);
     const int nkb = kb1 - kb0;
-    const int items = n_tok * nkb;
+    const int items = s_n_active * nkb;
     const int l4 = tid & 3;
     const uint32_t gmask = 0xFu << (lane & ~3);
     const int64_t K = KB * 128;
     for (int it = tid >> 2; it < items; it += kPackThreads / 4) {
-        const int tl = it / nkb;
+        const int tl = s_active[it / nkb];
         const int kb = kb0 + it % nkb;
         const uint16_t* src = x + (t0 + tl) * ldx + static_cast<int64_t>(kb) * 128 + l4 * 32;
         uint4 q[4];
