@@ -313,6 +313,29 @@ static int dispatch_launch(const void* x, int64_t T, int64_t K, int64_t ldx,
     return launch_status();
 }
 
+// Fixed device scratch for fp8_moe_dispatch_quant_noalloc: the per-chunk
+// counts and per-expert totals of one call (n_local * ceil(T / 64) + n_local
+// ints, at most 65536 = 256 KB).  One copy per device; every call overwrites
+// the entries it reads, so nothing needs to start at zero.
+constexpr size_t kDispatchScratchInts = static_cast<size_t>(1) << 16;
+static __device__ __align__(256) int32_t g_dispatch_scratch[kDispatchScratchInts];
+
+// Device address of g_dispatch_scratch on the current device, looked up once
+// per device (with that device current) and cached; nullptr on failure.
+static int32_t* dispatch_scratch() {
+    static int32_t* cached[kMaxDevices] = {nullptr};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    if (cached[dev] == nullptr) {
+        int32_t* ptr = nullptr;
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_dispatch_scratch) !=
+            cudaSuccess)
+            return nullptr;
+        cached[dev] = ptr;
+    }
+    return cached[dev];
+}
+
 }  // namespace fp8fg
 
 using namespace fp8fg;
@@ -353,4 +376,36 @@ extern "C" int fp8_moe_dispatch_quant(const void* x, int64_t T, int64_t K, int64
     if (workspace_bytes < dispatch_plan(T, n_local).bytes) return FP8_ERR_SHAPE;
     return dispatch_launch(x, T, K, ldx, topk_ids, topk, expert_begin, n_local, xq, sx, cap,
                            offsets, token_ids, static_cast<int32_t*>(workspace), s);
+}
+
+extern "C" int fp8_moe_dispatch_quant_noalloc(const void* x, int64_t T, int64_t K, int64_t ldx,
+                                              const int32_t* topk_ids, int32_t topk,
+                                              int32_t expert_begin, int32_t n_local, uint8_t* xq,
+                                              float* sx, int64_t cap, int32_t* offsets,
+                                              int32_t* token_ids, void* stream) {
+    int st = dispatch_checks(T, K, ldx, topk, n_local, cap);
+    if (st != FP8_OK) return st;
+    if (offsets == nullptr) return FP8_ERR_NULL;
+    if (!aligned(offsets, 4)) return FP8_ERR_ALIGN;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        if (cudaMemsetAsync(offsets, 0, (static_cast<size_t>(n_local) + 1) * sizeof(int32_t), s) !=
+            cudaSuccess)
+            return FP8_ERR_CUDA;
+        return FP8_OK;
+    }
+    if (x == nullptr || topk_ids == nullptr || xq == nullptr || sx == nullptr ||
+        token_ids == nullptr)
+        return FP8_ERR_NULL;
+    if (ldx % 8 != 0 || !aligned(x, 16) || !aligned(xq, 16) || !aligned(sx, 4) ||
+        !aligned(topk_ids, 4) || !aligned(token_ids, 4))
+        return FP8_ERR_ALIGN;
+    // the problem must fit the fixed scratch
+    const DispatchPlan d = dispatch_plan(T, n_local);
+    if (d.count_ints + static_cast<size_t>(n_local) > kDispatchScratchInts)
+        return FP8_ERR_UNSUPPORTED;
+    int32_t* scratch = dispatch_scratch();
+    if (scratch == nullptr) return FP8_ERR_CUDA;
+    return dispatch_launch(x, T, K, ldx, topk_ids, topk, expert_begin, n_local, xq, sx, cap,
+                           offsets, token_ids, scratch, s);
 }

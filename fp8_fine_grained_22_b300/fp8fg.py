@@ -24,7 +24,8 @@ FP8_BSCALE_BLOCK128_T = 2
 # every entry point of include/fp8fg.h
 EXPORTS = ("fp8_status_str", "fp8_device_error", "fp8_quant_act_1x128", "fp8_quant_act_128x1",
            "fp8_quant_weight_128x128", "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe",
-           "fp8_moe_dispatch_workspace_size", "fp8_moe_dispatch_quant")
+           "fp8_moe_dispatch_workspace_size", "fp8_moe_dispatch_quant",
+           "fp8_moe_dispatch_quant_noalloc")
 
 
 class Fp8Error(RuntimeError):
@@ -66,6 +67,9 @@ def lib() -> ctypes.CDLL:
         L.fp8_moe_dispatch_quant.restype = I
         L.fp8_moe_dispatch_quant.argtypes = [P, I64, I64, I64, P, I32, I32, I32, P, P, I64, P, P,
                                              P, ctypes.c_size_t, P]
+        L.fp8_moe_dispatch_quant_noalloc.restype = I
+        L.fp8_moe_dispatch_quant_noalloc.argtypes = [P, I64, I64, I64, P, I32, I32, I32, P, P,
+                                                     I64, P, P, P]
         _lib = L
     return _lib
 
@@ -228,4 +232,31 @@ def fp8_moe_dispatch_quant(x, topk_ids, expert_begin, n_local, cap=None, xq=None
                                         expert_begin, n_local, _p(xq), _p(sx), cap, _p(offsets),
                                         _p(token_ids), _p(workspace), nbytes, _stream(stream)),
            "fp8_moe_dispatch_quant")
+    return xq, sx, offsets, token_ids
+
+
+def fp8_moe_dispatch_quant_noalloc(x, topk_ids, expert_begin, n_local, cap=None, xq=None,
+                                   sx=None, offsets=None, token_ids=None, stream=None):
+    """fp8_moe_dispatch_quant on the library's fixed device scratch (no workspace)."""
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(topk_ids, "topk_ids", torch.int32)
+    assert x.dim() == 2 and x.stride(1) == 1 and topk_ids.is_contiguous()
+    T, K = x.shape
+    topk = topk_ids.shape[1] if topk_ids.dim() == 2 else 1
+    assert topk_ids.shape[0] == T
+    if cap is None:
+        cap = T * min(topk, n_local)
+    dev = x.device
+    if xq is None:
+        xq = torch.empty((cap, K), dtype=torch.uint8, device=dev)
+    if sx is None:
+        sx = torch.empty((K // 128, cap), dtype=torch.float32, device=dev)
+    if offsets is None:
+        offsets = torch.empty(n_local + 1, dtype=torch.int32, device=dev)
+    if token_ids is None:
+        token_ids = torch.empty(cap, dtype=torch.int32, device=dev)
+    _check(lib().fp8_moe_dispatch_quant_noalloc(_p(x), T, K, x.stride(0), _p(topk_ids), topk,
+                                                expert_begin, n_local, _p(xq), _p(sx), cap,
+                                                _p(offsets), _p(token_ids), _stream(stream)),
+           "fp8_moe_dispatch_quant_noalloc")
     return xq, sx, offsets, token_ids

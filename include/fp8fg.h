@@ -208,6 +208,33 @@ int fp8_moe_dispatch_quant(const void* x, int64_t T, int64_t K, int64_t ldx,
                            int32_t* offsets, int32_t* token_ids, void* workspace,
                            size_t workspace_bytes, void* stream);
 
+/*
+ * fp8_moe_dispatch_quant_noalloc -- fp8_moe_dispatch_quant without a
+ * caller-provided workspace.  The report has no counterpart: this entry point
+ * exists for callers that cannot hand the library device memory at the call
+ * site -- C callers without a device memory pool of their own, and code that
+ * must not call an allocator between its kernel launches (a device allocation
+ * can synchronise the device).  The library allocates nothing here either:
+ * the scratch is a fixed array in the library's device memory, one per
+ * device, of 65536 int32 (256 KB).
+ *   Same arguments, outputs, checks and results as fp8_moe_dispatch_quant,
+ *   minus workspace and workspace_bytes.
+ *   Limit: n_local * ceil(T / 64) + n_local <= 65536 (e.g. T <= 131008 tokens
+ *   with 32 local experts); larger problems return FP8_ERR_UNSUPPORTED and
+ *   launch nothing.
+ *   Nothing needs to start at zero: every call overwrites the scratch it
+ *   reads.
+ *   Overlapping calls on one device (on different streams, or from different
+ *   host threads without ordering) share the scratch and race; serialise them.
+ *   The first call on each device looks up the scratch's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture begins.
+ */
+int fp8_moe_dispatch_quant_noalloc(const void* x, int64_t T, int64_t K, int64_t ldx,
+                                   const int32_t* topk_ids, int32_t topk, int32_t expert_begin,
+                                   int32_t n_local, uint8_t* xq, float* sx, int64_t cap,
+                                   int32_t* offsets, int32_t* token_ids, void* stream);
+
 #ifdef __cplusplus
 }
 #endif
