@@ -171,11 +171,12 @@ def gemm_blockscaled(aq, sa, bq, sb, bmode=BSCALE_BLOCK128, rows=None, nthreads=
     return out
 
 
-def grouped_gemm(aq, sa, bq, sb, offsets, rows=None, nthreads=None):
+def grouped_gemm(aq, sa, bq, sb, offsets, rows=None, nthreads=None, bmode=BSCALE_BLOCK128):
     """binary64 Y[rows, :] of the grouped (per-expert) block-scaled product.
 
     aq: uint8 [T, K] rows grouped by expert; sa: f32 [K/128, T];
-    bq: uint8 [E, N, K]; sb: f32 [E, N/128, K/128];
+    bq: uint8 [E, N, K]; sb: f32 [E, ...] per expert in the ``bmode`` layout
+    (BLOCK128 [N/128, K/128]; BLOCK128_T [K/128, N/128] for the Dgrad GEMM);
     offsets: int [E+1], rows offsets[e]..offsets[e+1]-1 belong to expert e
     (rows at or past offsets[E] belong to no expert and may not be requested).
     Each row of Y is the dense product of that row with its expert's weight.
@@ -201,7 +202,7 @@ def grouped_gemm(aq, sa, bq, sb, offsets, rows=None, nthreads=None):
             continue
         # each row only needs its own A row and A scales; pass the whole A
         # so that the row indices stay global.
-        out[sel] = gemm_blockscaled(aq, sa, bq[e], sb[e], BSCALE_BLOCK128,
+        out[sel] = gemm_blockscaled(aq, sa, bq[e], sb[e], bmode,
                                     rows=rows[sel], nthreads=nthreads)
     return out
 

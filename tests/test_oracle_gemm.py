@@ -147,3 +147,29 @@ def test_grouped_equals_dense_per_expert():
             y[lo:hi], oracle.gemm_blockscaled(aq_e, sa_e, bq[e], sb[e]))
     rows = np.array([T - 1, 0, 3, 132])
     np.testing.assert_array_equal(oracle.grouped_gemm(aq, sa, bq, sb, offsets, rows=rows), y[rows])
+
+
+def test_grouped_dgrad_equals_dequantised_product():
+    """Dgrad of the grouped GEMM (weights' transposed codes, scales read transposed)
+    against dY_deq . W_deq^T formed from the Fprop-orientation codes and scales."""
+    g = torch.Generator().manual_seed(500)
+    K, N, E = 384, 256, 3  # Fprop W[K, N]; Dgrad contracts over N, outputs K columns
+    counts = [5, 0, 131]
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    T = int(offsets[-1])
+    dy = inputs.grad(T, N, g)
+    ws = [inputs.weight(K, N, g) for _ in range(E)]
+    q = [oracle.quant_weight_128x128(_bits(w)) for w in ws]
+    dq, sd = oracle.quant_act_1x128(_bits(dy))
+    bqT = np.stack([r[1] for r in q])  # [E][K][N]
+    sw = np.stack([r[2] for r in q])   # [E][N/128][K/128]
+    dx = oracle.grouped_gemm(dq, sd, bqT, sw, offsets, bmode=oracle.BSCALE_BLOCK128_T)
+    dy_hat = DEC[dq] * np.repeat(sd.T.astype(np.float64), 128, axis=1)
+    for e in range(E):
+        lo, hi = offsets[e], offsets[e + 1]
+        wq, _, s = q[e]
+        w_hat = DEC[wq].T * np.repeat(np.repeat(s.T.astype(np.float64), 128, axis=0), 128,
+                                      axis=1)  # [K, N]
+        ref = dy_hat[lo:hi] @ w_hat.T
+        mag = np.abs(dy_hat[lo:hi]) @ np.abs(w_hat).T
+        assert np.all(np.abs(dx[lo:hi] - ref) <= 1e-12 * mag + 1e-300)
