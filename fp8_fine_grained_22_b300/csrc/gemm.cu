@@ -674,9 +674,11 @@ extern "C" int fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, const ui
                            static_cast<cudaStream_t>(stream));
 }
 
-extern "C" int fp8_grouped_gemm_moe(const uint8_t* aq, const float* sa, const uint8_t* bq,
-                                    const float* sb, const int32_t* offsets, int32_t E, int64_t T,
-                                    int64_t N, int64_t K, void* c, int out_type, void* stream) {
+// Shared body of the grouped entry points; bmode is BLOCK128 (Fprop: per-expert
+// sb[N/128][K/128]) or BLOCK128_T (Dgrad: the Fprop weight scales read transposed).
+static int grouped_gemm(const uint8_t* aq, const float* sa, const uint8_t* bq, const float* sb,
+                        int bmode, const int32_t* offsets, int32_t E, int64_t T, int64_t N,
+                        int64_t K, void* c, int out_type, void* stream) {
     if (E < 1 || E > 65536 || T < 0 || N <= 0 || N % 128 != 0 || K <= 0 || K % 128 != 0)
         return FP8_ERR_SHAPE;
     if (out_type != FP8_OUT_F32 && out_type != FP8_OUT_BF16) return FP8_ERR_UNSUPPORTED;
@@ -695,7 +697,7 @@ extern "C" int fp8_grouped_gemm_moe(const uint8_t* aq, const float* sa, const ui
     p.sb = sb;
     p.ld_sb = 0;
     p.sb_expert = (N / 128) * (K / 128);
-    p.bmode = FP8_BSCALE_BLOCK128;
+    p.bmode = bmode;
     p.M = T;
     p.N = N;
     p.K = K;
@@ -706,6 +708,21 @@ extern "C" int fp8_grouped_gemm_moe(const uint8_t* aq, const float* sa, const ui
     // every expert adds at most one ragged M block
     return dispatch<true>(aq, T, bq, static_cast<int64_t>(E) * N, p, out_type,
                           (T + BM - 1) / BM + E, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fp8_grouped_gemm_moe(const uint8_t* aq, const float* sa, const uint8_t* bq,
+                                    const float* sb, const int32_t* offsets, int32_t E, int64_t T,
+                                    int64_t N, int64_t K, void* c, int out_type, void* stream) {
+    return grouped_gemm(aq, sa, bq, sb, FP8_BSCALE_BLOCK128, offsets, E, T, N, K, c, out_type,
+                        stream);
+}
+
+extern "C" int fp8_grouped_gemm_moe_dgrad(const uint8_t* aq, const float* sa, const uint8_t* bq,
+                                          const float* sb, const int32_t* offsets, int32_t E,
+                                          int64_t T, int64_t N, int64_t K, void* c, int out_type,
+                                          void* stream) {
+    return grouped_gemm(aq, sa, bq, sb, FP8_BSCALE_BLOCK128_T, offsets, E, T, N, K, c,
+                        out_type, stream);
 }
 
 extern "C" int fp8_device_error(void* stream) {

@@ -24,6 +24,7 @@ FP8_BSCALE_BLOCK128_T = 2
 # every entry point of include/fp8fg.h
 EXPORTS = ("fp8_status_str", "fp8_device_error", "fp8_quant_act_1x128", "fp8_quant_act_128x1",
            "fp8_quant_weight_128x128", "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe",
+           "fp8_grouped_gemm_moe_dgrad",
            "fp8_moe_dispatch_workspace_size", "fp8_moe_dispatch_quant",
            "fp8_moe_dispatch_quant_noalloc")
 
@@ -62,6 +63,8 @@ def lib() -> ctypes.CDLL:
         L.fp8_gemm_blockscaled.argtypes = [P, P, P, P, I, I64, I64, I64, P, I64, I, P]
         L.fp8_grouped_gemm_moe.restype = I
         L.fp8_grouped_gemm_moe.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, I, P]
+        L.fp8_grouped_gemm_moe_dgrad.restype = I
+        L.fp8_grouped_gemm_moe_dgrad.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, I, P]
         L.fp8_moe_dispatch_workspace_size.restype = I
         L.fp8_moe_dispatch_workspace_size.argtypes = [I64, I32, ctypes.POINTER(ctypes.c_size_t)]
         L.fp8_moe_dispatch_quant.restype = I
@@ -172,9 +175,7 @@ def fp8_gemm_blockscaled(aq, sa, bq, sb, bmode=FP8_BSCALE_BLOCK128, out_dtype=to
     return c
 
 
-def fp8_grouped_gemm_moe(aq, sa, bq, sb, offsets, out_dtype=torch.bfloat16, c=None,
-                         stream=None):
-    """Y[T, N] per expert; aq uint8 [T, K], bq uint8 [E, N, K], offsets int32 [E+1] (device)."""
+def _grouped(fn, name, aq, sa, bq, sb, offsets, out_dtype, c, stream):
     for t, n in ((aq, "aq"), (sa, "sa"), (bq, "bq"), (sb, "sb"), (offsets, "offsets")):
         _cuda(t, n)
     assert offsets.dtype == torch.int32
@@ -184,9 +185,24 @@ def fp8_grouped_gemm_moe(aq, sa, bq, sb, offsets, out_dtype=torch.bfloat16, c=No
     if c is None:
         c = torch.empty((T, N), dtype=out_dtype, device=aq.device)
     assert c.is_contiguous()
-    _check(lib().fp8_grouped_gemm_moe(_p(aq), _p(sa), _p(bq), _p(sb), _p(offsets), E, T, N, K,
-                                      _p(c), out_type, _stream(stream)), "fp8_grouped_gemm_moe")
+    _check(fn(_p(aq), _p(sa), _p(bq), _p(sb), _p(offsets), E, T, N, K, _p(c), out_type,
+              _stream(stream)), name)
     return c
+
+
+def fp8_grouped_gemm_moe(aq, sa, bq, sb, offsets, out_dtype=torch.bfloat16, c=None,
+                         stream=None):
+    """Y[T, N] per expert; aq uint8 [T, K], bq uint8 [E, N, K], offsets int32 [E+1] (device)."""
+    return _grouped(lib().fp8_grouped_gemm_moe, "fp8_grouped_gemm_moe", aq, sa, bq, sb, offsets,
+                    out_dtype, c, stream)
+
+
+def fp8_grouped_gemm_moe_dgrad(aq, sa, bqT, sw, offsets, out_dtype=torch.bfloat16, c=None,
+                               stream=None):
+    """dX[T, N] per expert from dY codes aq [T, K]; bqT uint8 [E, N, K] (each expert's wqT),
+    sw f32 [E, K/128, N/128] (each expert's Fprop weight scales)."""
+    return _grouped(lib().fp8_grouped_gemm_moe_dgrad, "fp8_grouped_gemm_moe_dgrad", aq, sa, bqT,
+                    sw, offsets, out_dtype, c, stream)
 
 
 # ------------------------------------------------------------- MoE dispatch --

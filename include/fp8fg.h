@@ -164,6 +164,26 @@ int fp8_grouped_gemm_moe(const uint8_t* aq, const float* sa, const uint8_t* bq,
                          int64_t N, int64_t K, void* c, int out_type, void* stream);
 
 /*
+ * fp8_grouped_gemm_moe_dgrad -- the Dgrad of the grouped expert GEMM: per
+ * expert e, dX_e = dY_e . W_e^T (report section 3.3.1: Dgrad in FP8 like
+ * Fprop; section 3.4: MoE experts), reusing each expert's 128x128 weight
+ * quantisation: the codes in the transposed orientation and the scales read
+ * transposed (as FP8_BSCALE_BLOCK128_T does for the dense GEMM).
+ *   aq      : E4M3 [T][K], the output gradients dY of the packed rows,
+ *             quantised 1x128 along K (K = the Fprop output width).     (input)
+ *   sa      : float [K/128][T].                                         (input)
+ *   bq      : E4M3 [E][N][K]: per expert the wqT codes of
+ *             fp8_quant_weight_128x128 (N = the Fprop inner dimension). (input)
+ *   sb      : float [E][K/128][N/128]: per expert the sw scales of
+ *             fp8_quant_weight_128x128, unchanged.                      (input)
+ *   offsets, c, out_type, E, T: as fp8_grouped_gemm_moe (c is dX [T][N]).
+ * Same checks and device-side offset validation as fp8_grouped_gemm_moe.
+ */
+int fp8_grouped_gemm_moe_dgrad(const uint8_t* aq, const float* sa, const uint8_t* bq,
+                               const float* sb, const int32_t* offsets, int32_t E, int64_t T,
+                               int64_t N, int64_t K, void* c, int out_type, void* stream);
+
+/*
  * fp8_moe_dispatch_workspace_size -- bytes of device workspace
  * fp8_moe_dispatch_quant needs for T tokens and n_local local experts
  * (0 when T = 0).  *bytes is set to 0 on error.

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from fp8_fine_grained_22_b300 import fp8fg, inputs
-from parity import bits, check_bf16, check_f32, magnitude, np_u8
+from parity import bits, check_bf16, check_f32, magnitude, np_u8, sample_rows
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -38,8 +38,8 @@ def _run(aq, sa, bq, sb, offsets, out_dtype, c=None):
     return out
 
 
-def _compare(out, aq, sa, bq, sb, offsets, rows):
-    ref = oracle.grouped_gemm(aq, sa, bq, sb, offsets, rows=rows)
+def _compare(out, aq, sa, bq, sb, offsets, rows, bmode=oracle.BSCALE_BLOCK128):
+    ref = oracle.grouped_gemm(aq, sa, bq, sb, offsets, rows=rows, bmode=bmode)
     K = aq.shape[1]
     N = bq.shape[1]
     expert_of = np.searchsorted(offsets, rows, side="right") - 1
@@ -47,7 +47,8 @@ def _compare(out, aq, sa, bq, sb, offsets, rows):
     n_fallback = 0
     for e in np.unique(expert_of):
         sel = np.nonzero(expert_of == e)[0]
-        sbm = np.repeat(sb[e], 128, axis=0)  # [N, K/128]
+        sbe = sb[e] if bmode == oracle.BSCALE_BLOCK128 else sb[e].T
+        sbm = np.repeat(sbe, 128, axis=0)  # [N, K/128]
         S = magnitude(aq, sa, bq[e], sbm, rows[sel])
         if o.dtype == torch.float32:
             got = o.numpy()[rows[sel]]
@@ -139,3 +140,48 @@ def test_moe_decode_workload():
     counts = np.diff(wl.offsets)
     assert counts.min() >= 1 and counts.max() <= 256
     _workload_parity(wl, n_rows_per_expert=6)
+
+
+def _quant_experts_T(w):
+    """Oracle 128x128 quantisation of each expert weight: (wqT [E, K, N], sw [E, N/128, K/128])."""
+    E = w.shape[0]
+    wb = [bits(w[e]) for e in range(E)]
+    with cf.ThreadPoolExecutor(8) as ex:
+        res = list(ex.map(lambda b: oracle.quant_weight_128x128(b), wb))
+    return np.stack([r[1] for r in res]), np.stack([r[2] for r in res])
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("counts", [[3, 0, 130, 1], [257, 0, 5], [0, 1]])
+def test_grouped_dgrad_small(counts, out_dtype):
+    """dX_e = dY_e . W_e^T with each expert's wqT codes and sw scales read transposed."""
+    g = torch.Generator().manual_seed(7 * sum(counts) + len(counts))
+    E, Kf, Nf = len(counts), 384, 256 if len(counts) % 2 else 512
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    T = int(offsets[-1])
+    dy = inputs.grad(max(T, 1), Nf, g)[:T]
+    w = torch.stack([inputs.weight(Kf, Nf, g) for _ in range(E)])
+    dq, sd = oracle.quant_act_1x128(bits(dy))
+    bqT, sw = _quant_experts_T(w)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    off = torch.from_numpy(offsets.astype(np.int32)).to(DEV)
+    dx = fp8fg.fp8_grouped_gemm_moe_dgrad(t(dq), t(sd), t(bqT), t(sw), off, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert fp8fg.device_error() == 0
+    _compare(dx, dq, sd, bqT, sw, offsets, np.arange(T), bmode=oracle.BSCALE_BLOCK128_T)
+
+
+def test_moe_prefill_dgrad_workload():
+    """The prefill routing's backward: dY [rows, 4096] -> dX [rows, 7168] per expert."""
+    wl = inputs.moe_prefill()
+    T = int(wl.offsets[-1])
+    dy = inputs.grad(T, wl.N, torch.Generator().manual_seed(8))
+    dq, sd = oracle.quant_act_1x128(bits(dy))
+    bqT, sw = _quant_experts_T(wl.w)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    off = torch.from_numpy(np.asarray(wl.offsets, np.int32)).to(DEV)
+    dx = fp8fg.fp8_grouped_gemm_moe_dgrad(t(dq), t(sd), t(bqT), t(sw), off)
+    torch.cuda.synchronize()
+    assert fp8fg.device_error() == 0
+    rows = sample_rows(T, 96, seed=9)
+    _compare(dx, dq, sd, bqT, sw, np.asarray(wl.offsets), rows, bmode=oracle.BSCALE_BLOCK128_T)
