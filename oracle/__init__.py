@@ -240,3 +240,64 @@ def moe_dispatch_quant(x_bf16, topk_ids, expert_begin, n_local):
                 token_ids)
     xq, sx = quant_act_1x128(x[token_ids])
     return xq, sx, offsets, token_ids
+
+
+
+# ---------------------------------------------------------------- MoE Wgrad --
+def quant_act_128x1_grouped(x_bf16, offsets):
+    """128x1 quantisation of each expert's rows along its own tokens.
+
+    DeepSeek-V3 Technical Report, sections 3.3.1-3.3.3 (Wgrad consumes the
+    activations and gradients quantised along the tokens, the GEMM's inner
+    dimension) applied per expert (section 3.4): expert e's rows
+    offsets[e] .. offsets[e+1]-1 are cut into groups of 128 consecutive
+    tokens; a short last group is completed with zero rows, which give zero
+    codes and leave the group's amax unchanged.
+
+    x_bf16: uint16 [T, K]; offsets: int [E+1].
+    Returns (xqT uint8 [K, Tp], sxT f32 [Tp/128, K], pofs int64 [E+1]) with
+    expert e in columns pofs[e] .. pofs[e+1]-1 and Tp = pofs[E].
+    """
+    x = _c(x_bf16, np.uint16)
+    offsets = np.asarray(offsets, dtype=np.int64)
+    T, K = x.shape
+    E = offsets.size - 1
+    padded = [((offsets[e + 1] - offsets[e] + 127) // 128) * 128 for e in range(E)]
+    pofs = np.zeros(E + 1, np.int64)
+    pofs[1:] = np.cumsum(padded)
+    Tp = int(pofs[-1])
+    xqT = np.zeros((K, Tp), np.uint8)
+    sxT = np.zeros((Tp // 128, K), np.float32)
+    for e in range(E):
+        if padded[e] == 0:
+            continue
+        seg = np.zeros((padded[e], K), np.uint16)  # bfloat16 +0
+        seg[:offsets[e + 1] - offsets[e]] = x[offsets[e]:offsets[e + 1]]
+        q, sc = quant_act_128x1(seg)
+        xqT[:, pofs[e]:pofs[e + 1]] = q
+        sxT[pofs[e] // 128:pofs[e + 1] // 128] = sc
+    return xqT, sxT, pofs
+
+
+def grouped_wgrad(aqT, sa, bqT, sb, pofs, rows=None, nthreads=None):
+    """binary64 dW[e][rows, :] for every expert: the per-expert product of the
+    transposed operands over the expert's padded token columns, promoted per
+    128-token block with the per-row A scale and the per-column B scale
+    (section 3.3.2).  aqT uint8 [M, Tp], sa f32 [Tp/128, M], bqT uint8 [N, Tp],
+    sb f32 [Tp/128, N], pofs int [E+1].  Returns [E, len(rows), N]."""
+    aqT = _c(aqT, np.uint8)
+    bqT = _c(bqT, np.uint8)
+    pofs = np.asarray(pofs, dtype=np.int64)
+    M = aqT.shape[0]
+    N = bqT.shape[0]
+    E = pofs.size - 1
+    rows = np.arange(M) if rows is None else np.asarray(rows, dtype=np.int64)
+    out = np.zeros((E, rows.size, N))
+    for e in range(E):
+        lo, hi = int(pofs[e]), int(pofs[e + 1])
+        if hi == lo:
+            continue
+        out[e] = gemm_blockscaled(aqT[:, lo:hi], sa[lo // 128:hi // 128], bqT[:, lo:hi],
+                                  sb[lo // 128:hi // 128], BSCALE_ROW1x128, rows=rows,
+                                  nthreads=nthreads)
+    return out

@@ -173,3 +173,71 @@ def test_grouped_dgrad_equals_dequantised_product():
         ref = dy_hat[lo:hi] @ w_hat.T
         mag = np.abs(dy_hat[lo:hi]) @ np.abs(w_hat).T
         assert np.all(np.abs(dx[lo:hi] - ref) <= 1e-12 * mag + 1e-300)
+
+
+def test_grouped_128x1_single_expert_is_the_dense_quantiser():
+    g = torch.Generator().manual_seed(600)
+    x = inputs.act(256, 192, g)
+    xqT, sxT, pofs = oracle.quant_act_128x1_grouped(_bits(x), [0, 256])
+    q, s = oracle.quant_act_128x1(_bits(x))
+    assert pofs.tolist() == [0, 256]
+    np.testing.assert_array_equal(xqT, q)
+    np.testing.assert_array_equal(sxT, s)
+
+
+def test_grouped_128x1_short_groups():
+    """Short groups: zero codes in the padding, amax element at +-448, codes within the
+    E4M3 rounding bound of x / s."""
+    g = torch.Generator().manual_seed(601)
+    counts = [5, 0, 130, 128]
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    T, K = int(offsets[-1]), 128
+    x = inputs.act(T, K, g)
+    xqT, sxT, pofs = oracle.quant_act_128x1_grouped(_bits(x), offsets)
+    assert pofs.tolist() == [0, 128, 128, 384, 512]
+    xf = x.double().numpy()
+    for e in range(len(counts)):
+        t_e = counts[e]
+        for grp in range((t_e + 127) // 128):
+            col0 = int(pofs[e]) + 128 * grp
+            n = min(128, t_e - 128 * grp)
+            seg = xf[offsets[e] + 128 * grp:offsets[e] + 128 * grp + n]  # [n, K]
+            codes = xqT[:, col0:col0 + 128]                                # [K, 128]
+            assert np.all(codes[:, n:] == 0)
+            s = sxT[col0 // 128].astype(np.float64)                        # [K]
+            deq = DEC[codes[:, :n]].T * s[None, :]
+            r = np.abs(seg / s[None, :])
+            ulp = np.exp2(np.floor(np.log2(np.maximum(r, 2.0 ** -6))) - 3)
+            assert np.all(np.abs(deq - seg) <= (0.5 * ulp + r * 2.0 ** -23) * s[None, :])
+            amax_rows = np.abs(seg).argmax(axis=0)
+            top = codes[np.arange(K), amax_rows] & 0x7F
+            assert np.all((top == 0x7E) | (np.abs(seg).max(axis=0) == 0))
+
+
+def test_grouped_wgrad_equals_dequantised_product():
+    g = torch.Generator().manual_seed(602)
+    counts = [3, 0, 200, 128]
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    T, M, N = int(offsets[-1]), 256, 384  # M: Fprop inner dim, N: Fprop output dim
+    x = inputs.act(T, M, g)
+    dy = inputs.grad(T, N, g)
+    xqT, sxT, pofs = oracle.quant_act_128x1_grouped(_bits(x), offsets)
+    dqT, sdT, pofs2 = oracle.quant_act_128x1_grouped(_bits(dy), offsets)
+    assert np.array_equal(pofs, pofs2)
+    dw = oracle.grouped_wgrad(xqT, sxT, dqT, sdT, pofs)
+    for e in range(len(counts)):
+        lo, hi = int(pofs[e]), int(pofs[e + 1])
+        if hi == lo:
+            assert np.all(dw[e] == 0)
+            continue
+        a_hat = DEC[xqT[:, lo:hi]] * np.repeat(sxT[lo // 128:hi // 128].T.astype(np.float64), 128,
+                                                 axis=1)
+        b_hat = DEC[dqT[:, lo:hi]] * np.repeat(sdT[lo // 128:hi // 128].T.astype(np.float64), 128,
+                                                 axis=1)
+        ref = a_hat @ b_hat.T
+        mag = np.abs(a_hat) @ np.abs(b_hat).T
+        assert np.all(np.abs(dw[e] - ref) <= 1e-12 * mag + 1e-300)
+        # and it approximates the unquantised X_e^T dY_e
+        exact = x.double().numpy()[offsets[e]:offsets[e + 1]].T @ \
+            dy.double().numpy()[offsets[e]:offsets[e + 1]]
+        assert np.linalg.norm(dw[e] - exact) < 0.1 * np.linalg.norm(exact)
