@@ -112,6 +112,10 @@ struct Tile {
     int64_t b_row0;   // first row of B (expert-major for grouped)
     int64_t n0;       // first output column
     int expert;
+    // grouped-K (per-expert contraction) tiles only:
+    int64_t c_row0;   // first row of C (expert-major)
+    int kb_begin;     // first K block of the expert
+    int kb_count;     // K blocks of the expert (0: the tile is written as zeros)
 };
 
 template <int BN, bool GROUPED>
@@ -146,6 +150,37 @@ __device__ __forceinline__ bool get_tile(const GemmParams& p, int64_t t, Tile& t
         }
         return false;
     }
+}
+
+// Grouped-K tiles (the per-expert Wgrad GEMM): every expert has the same
+// (M/128) x (N/BN) output tiles; its contraction covers the padded token
+// columns pofs[e] .. pofs[e+1]-1 of both operands (p.offsets = pofs).
+template <int BN>
+__device__ __forceinline__ bool get_tile_gk(const GemmParams& p, int64_t t, Tile& ti) {
+    const int64_t nblk = p.N / BN;
+    const int64_t per_expert = (p.M / BM) * nblk;
+    if (t >= per_expert * p.E) return false;
+    const int64_t e = t / per_expert, local = t % per_expert;
+    const int64_t mb = local / nblk, nb = local % nblk;
+    ti.row0 = mb * BM;
+    ti.row_end = p.M;
+    ti.n0 = nb * BN;
+    ti.b_row0 = ti.n0;
+    ti.expert = static_cast<int>(e);
+    ti.c_row0 = e * p.M + mb * BM;
+    const int32_t lo = __ldg(p.offsets + e), hi = __ldg(p.offsets + e + 1);
+    ti.kb_begin = lo / BK;
+    ti.kb_count = (hi - lo) / BK;
+    return true;
+}
+
+// GM: 0 dense, 1 grouped over rows (MoE Fprop/Dgrad), 2 grouped over K (MoE Wgrad)
+template <int BN, int GM>
+__device__ __forceinline__ bool get_tile_gm(const GemmParams& p, int64_t t, Tile& ti) {
+    if constexpr (GM == 2)
+        return get_tile_gk<BN>(p, t, ti);
+    else
+        return get_tile<BN, GM == 1>(p, t, ti);
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile whose rows are
@@ -185,11 +220,13 @@ __device__ __forceinline__ uint32_t bf16x2(uint64_t pair) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-template <int BN, bool OUT_BF16, bool ROWSCALE, bool GROUPED>
+template <int BN, bool OUT_BF16, bool ROWSCALE, int GM>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+    constexpr bool GROUPED = GM == 1;  // tiles walk the expert row offsets
+    constexpr bool GK = GM == 2;       // every expert contracts over its own K range
     using C = Cfg<BN, ROWSCALE>;
     constexpr int S = C::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -254,6 +291,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (bad) raise_error(abort_flag, kErrBadOffsets);
         __syncthreads();
     }
+    if (GK) {
+        // padded K offsets: pofs[0] == 0, non-decreasing multiples of 128, pofs[E] <= K
+        bool bad = false;
+        if (threadIdx.x == 0) bad = (__ldg(p.offsets) != 0) || (__ldg(p.offsets + p.E) > p.K);
+        for (int e = threadIdx.x; e < p.E; e += kThreads) {
+            const int32_t lo = __ldg(p.offsets + e), hi = __ldg(p.offsets + e + 1);
+            bad |= hi < lo || (hi % BK) != 0;
+        }
+        if (bad) raise_error(abort_flag, kErrBadOffsets);
+        __syncthreads();
+    }
     const uint32_t tmem_base = *tmem_slot;
     const int64_t KB = p.K / BK;
     const bool aborted_at_start = *abort_flag != 0;
@@ -268,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tcgen05.mma costs about twice the issue cycles).  The grouped kernels
     // keep single-lane roles: their tile walk over the expert offsets does not
     // fit the control warps' registers when run warp-wide.
-    constexpr bool kWarpRoles = !GROUPED;
+    constexpr bool kWarpRoles = !GROUPED;  // dense and grouped-K tiles are cheap to walk
     auto role_wait = [&](uint32_t bar, uint32_t parity) {
         return kWarpRoles ? wait_bar_warp(bar, parity, abort_flag) : wait_bar(bar, parity, abort_flag);
     };
@@ -283,8 +331,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
                 Tile ti;
-                if (!get_tile<BN, GROUPED>(p, t, ti)) break;
-                for (int64_t kb = 0; kb < KB; ++kb, ++it) {
+                if (!get_tile_gm<BN, GM>(p, t, ti)) break;
+                const int64_t nkb = GK ? ti.kb_count : KB;
+                const int64_t kbo = GK ? ti.kb_begin : 0;
+                for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
                     const int s = static_cast<int>(it % S);
                     const uint32_t ph = (it / S) & 1u;
                     if (!role_wait(empty_bar(s), ph ^ 1u)) {
@@ -294,10 +344,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (leader) {
                         uint8_t* st = stages + s * C::STAGE_BYTES;
                         mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
-                        tma_load_2d(smem_addr(st), &tmA, full_bar(s), static_cast<int>(kb * BK),
-                                    static_cast<int>(ti.row0));
+                        tma_load_2d(smem_addr(st), &tmA, full_bar(s),
+                                    static_cast<int>((kb + kbo) * BK), static_cast<int>(ti.row0));
                         tma_load_2d(smem_addr(st + C::A_BYTES), &tmB, full_bar(s),
-                                    static_cast<int>(kb * BK), static_cast<int>(ti.b_row0));
+                                    static_cast<int>((kb + kbo) * BK),
+                                    static_cast<int>(ti.b_row0));
                     }
                     role_sync();
                 }
@@ -323,8 +374,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true, issued = false;
             for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
                 Tile ti;
-                if (!get_tile<BN, GROUPED>(p, t, ti)) break;
-                for (int64_t kb = 0; kb < KB; ++kb, ++it, ++kbg) {
+                if (!get_tile_gm<BN, GM>(p, t, ti)) break;
+                const int64_t nkb = GK ? ti.kb_count : KB;
+                for (int64_t kb = 0; kb < nkb; ++kb, ++it, ++kbg) {
                     const int s = static_cast<int>(it % S);
                     const uint32_t ph = (it / S) & 1u;
                     const uint32_t buf = kbg % NBUF, tph = (kbg / NBUF) & 1u;
@@ -389,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         bool ok = !aborted_at_start;
         for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
             Tile ti;
-            if (!get_tile<BN, GROUPED>(p, t, ti)) break;
+            if (!get_tile_gm<BN, GM>(p, t, ti)) break;
             const int row = static_cast<int>(ti.row0) + q * 32 + lane;
             const int row_end = static_cast<int>(ti.row_end);
             const int ncol0 = static_cast<int>(ti.n0) + cg * COLS;
@@ -410,16 +462,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sb_ptr = sb_e + (blk ? nb * KBi : nb);
                 sb_step = blk ? 1 : NB;
             }
-            float sa_next = row_in_alloc ? __ldg(sa_ptr) : 0.0f;
-            float sb_next = __ldg(sb_ptr);
+            int nkb = KBi;
+            if constexpr (GK) {
+                // this expert's K blocks: its scale rows start at kb_begin
+                nkb = ti.kb_count;
+                sa_ptr += static_cast<int64_t>(ti.kb_begin) * lds_a;
+                sb_ptr += static_cast<int64_t>(ti.kb_begin) * sb_step;
+            }
+            float sa_next = 0.0f, sb_next = 0.0f;
+            if (!GK || nkb > 0) {
+                sa_next = row_in_alloc ? __ldg(sa_ptr) : 0.0f;
+                sb_next = __ldg(sb_ptr);
+            }
 
             uint64_t acc[COLS / 2];
 #pragma unroll
             for (int i = 0; i < COLS / 2; ++i) acc[i] = 0;
 
-            for (int kb = 0; kb < KBi; ++kb, ++kbg) {
+            for (int kb = 0; kb < nkb; ++kb, ++kbg) {
                 const float sa_cur = sa_next, sb_cur = sb_next;
-                if (kb + 1 < KBi) {
+                if (kb + 1 < nkb) {
                     sa_next = row_in_alloc ? __ldg(sa_ptr + (kb + 1) * lds_a) : 0.0f;
                     sb_next = __ldg(sb_ptr + (kb + 1) * sb_step);
                 }
@@ -507,8 +569,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!ok) break;
 
             // ---------------------------------------------------- tile store
-            const int wrow0 = static_cast<int>(ti.row0) + q * 32;
-            if (wrow0 + 32 <= row_end) {
+            // grouped-K: C is [E][M][N], the tile's rows start at c_row0 and are all valid
+            const int wrow0 = static_cast<int>(GK ? ti.c_row0 : ti.row0) + q * 32;
+            if (GK || wrow0 + 32 <= row_end) {
                 // whole 32-row box valid: stage with the 128-byte swizzle, TMA store
 #pragma unroll
                 for (int bx = 0; bx < COLS / BOX_COLS; ++bx, ++boxes) {
@@ -572,11 +635,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // -------------------------------------------------------------------- host --
-template <int BN, bool OUT_BF16, bool ROWSCALE, bool GROUPED>
+template <int BN, bool OUT_BF16, bool ROWSCALE, int GM>
 static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t b_rows,
                   const GemmParams& p, int64_t tiles_upper, cudaStream_t stream) {
     using C = Cfg<BN, ROWSCALE>;
-    auto kern = gemm_blockscaled_kernel<BN, OUT_BF16, ROWSCALE, GROUPED>;
+    auto kern = gemm_blockscaled_kernel<BN, OUT_BF16, ROWSCALE, GM>;
     int dev = 0;
     const int sms = sm_count_current(&dev);
     if (sms <= 0) return FP8_ERR_CUDA;
@@ -600,8 +663,9 @@ static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t 
                        CU_TENSOR_MAP_SWIZZLE_128B)) != FP8_OK)
         return st;
     constexpr int ELT = OUT_BF16 ? 2 : 4;
+    const int64_t c_rows = GM == 2 ? p.M * p.E : p.M;  // grouped-K: one [M][N] per expert
     if ((st = make_map(&tc, OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
-                       p.c, p.N, p.M, p.ldc * ELT, 128 / ELT, 32,
+                       p.c, p.N, c_rows, p.ldc * ELT, 128 / ELT, 32,
                        CU_TENSOR_MAP_SWIZZLE_128B)) != FP8_OK)
         return st;
     const int64_t grid = tiles_upper < sms ? tiles_upper : sms;
@@ -610,30 +674,39 @@ static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t 
     return launch_status();
 }
 
-template <bool GROUPED>
+template <int GM>
 static int dispatch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t b_rows,
                     GemmParams& p, int out_type, int64_t mblk_upper, cudaStream_t stream) {
-    const bool rows = p.bmode == FP8_BSCALE_ROW1x128;
-    // 256-wide tiles halve the shared-memory operand traffic per MMA; the
-    // per-column B-scale mode keeps 128-wide tiles (its epilogue needs more
-    // registers than a 256-wide tile leaves).
-    if (p.N % 256 == 0 && !rows) {
-        const int64_t tiles = mblk_upper * (p.N / 256);
-        if (out_type == FP8_OUT_BF16)
-            return launch<256, true, false, GROUPED>(aq, a_rows, bq, b_rows, p, tiles, stream);
-        return launch<256, false, false, GROUPED>(aq, a_rows, bq, b_rows, p, tiles, stream);
-    }
-    const int64_t tiles = mblk_upper * (p.N / 128);
-    if constexpr (GROUPED) {  // grouped calls always use 128x128-block B scales
-        if (out_type == FP8_OUT_BF16)
-            return launch<128, true, false, true>(aq, a_rows, bq, b_rows, p, tiles, stream);
-        return launch<128, false, false, true>(aq, a_rows, bq, b_rows, p, tiles, stream);
+    constexpr bool GROUPED = GM == 1;
+    if constexpr (GM == 2) {
+        // the per-expert Wgrad GEMM: per-column B scales, 128-wide tiles, FP32 out
+        (void)out_type;
+        (void)mblk_upper;
+        const int64_t tiles = static_cast<int64_t>(p.E) * (p.M / BM) * (p.N / 128);
+        return launch<128, false, true, 2>(aq, a_rows, bq, b_rows, p, tiles, stream);
     } else {
-        if (out_type == FP8_OUT_BF16)
-            return rows ? launch<128, true, true, false>(aq, a_rows, bq, b_rows, p, tiles, stream)
-                        : launch<128, true, false, false>(aq, a_rows, bq, b_rows, p, tiles, stream);
-        return rows ? launch<128, false, true, false>(aq, a_rows, bq, b_rows, p, tiles, stream)
-                    : launch<128, false, false, false>(aq, a_rows, bq, b_rows, p, tiles, stream);
+        const bool rows = p.bmode == FP8_BSCALE_ROW1x128;
+        // 256-wide tiles halve the shared-memory operand traffic per MMA; the
+        // per-column B-scale mode keeps 128-wide tiles (its epilogue needs more
+        // registers than a 256-wide tile leaves).
+        if (p.N % 256 == 0 && !rows) {
+            const int64_t tiles = mblk_upper * (p.N / 256);
+            if (out_type == FP8_OUT_BF16)
+                return launch<256, true, false, GM>(aq, a_rows, bq, b_rows, p, tiles, stream);
+            return launch<256, false, false, GM>(aq, a_rows, bq, b_rows, p, tiles, stream);
+        }
+        const int64_t tiles = mblk_upper * (p.N / 128);
+        if constexpr (GROUPED) {  // grouped-row calls use 128x128-block B scales
+            if (out_type == FP8_OUT_BF16)
+                return launch<128, true, false, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
+            return launch<128, false, false, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
+        } else {
+            if (out_type == FP8_OUT_BF16)
+                return rows ? launch<128, true, true, 0>(aq, a_rows, bq, b_rows, p, tiles, stream)
+                            : launch<128, true, false, 0>(aq, a_rows, bq, b_rows, p, tiles, stream);
+            return rows ? launch<128, false, true, 0>(aq, a_rows, bq, b_rows, p, tiles, stream)
+                        : launch<128, false, false, 0>(aq, a_rows, bq, b_rows, p, tiles, stream);
+        }
     }
 }
 
@@ -670,7 +743,7 @@ extern "C" int fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, const ui
     p.ldc = ldc;
     p.offsets = nullptr;
     p.E = 0;
-    return dispatch<false>(aq, M, bq, N, p, out_type, (M + BM - 1) / BM,
+    return dispatch<0>(aq, M, bq, N, p, out_type, (M + BM - 1) / BM,
                            static_cast<cudaStream_t>(stream));
 }
 
@@ -706,7 +779,7 @@ static int grouped_gemm(const uint8_t* aq, const float* sa, const uint8_t* bq, c
     p.offsets = offsets;
     p.E = E;
     // every expert adds at most one ragged M block
-    return dispatch<true>(aq, T, bq, static_cast<int64_t>(E) * N, p, out_type,
+    return dispatch<1>(aq, T, bq, static_cast<int64_t>(E) * N, p, out_type,
                           (T + BM - 1) / BM + E, static_cast<cudaStream_t>(stream));
 }
 
@@ -723,6 +796,38 @@ extern "C" int fp8_grouped_gemm_moe_dgrad(const uint8_t* aq, const float* sa, co
                                           void* stream) {
     return grouped_gemm(aq, sa, bq, sb, FP8_BSCALE_BLOCK128_T, offsets, E, T, N, K, c,
                         out_type, stream);
+}
+
+extern "C" int fp8_grouped_gemm_moe_wgrad(const uint8_t* aqT, const float* sa,
+                                          const uint8_t* bqT, const float* sb,
+                                          const int32_t* pofs, int32_t E, int64_t Tp, int64_t M,
+                                          int64_t N, float* c, void* stream) {
+    if (E < 1 || E > 65536 || Tp < 0 || Tp % 128 != 0 || M <= 0 || M % 128 != 0 || N <= 0 ||
+        N % 128 != 0)
+        return FP8_ERR_SHAPE;
+    if (aqT == nullptr || sa == nullptr || bqT == nullptr || sb == nullptr || pofs == nullptr ||
+        c == nullptr)
+        return FP8_ERR_NULL;
+    if (!aligned(aqT, 16) || !aligned(bqT, 16) || !aligned(c, 16) || !aligned(sa, 4) ||
+        !aligned(sb, 4) || !aligned(pofs, 4))
+        return FP8_ERR_ALIGN;
+    if (Tp > 0x7fffffffLL || static_cast<int64_t>(E) * M > 0x7fffffffLL || N > 0x7fffffffLL)
+        return FP8_ERR_UNSUPPORTED;
+    if (Tp == 0) Tp = 128;  // every expert empty: no operand is read, outputs are zero
+    GemmParams p{};
+    p.sa = sa;
+    p.lds_a = M;
+    p.sb = sb;
+    p.ld_sb = N;
+    p.bmode = FP8_BSCALE_ROW1x128;
+    p.M = M;
+    p.N = N;
+    p.K = Tp;
+    p.c = c;
+    p.ldc = N;
+    p.offsets = pofs;
+    p.E = E;
+    return dispatch<2>(aqT, M, bqT, N, p, FP8_OUT_F32, 0, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fp8_device_error(void* stream) {

@@ -168,6 +168,101 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_128x1_kernel(
     }
 }
 
+// ---------------------------------------------------- 128x1, per expert --
+// The 128x1 grouping for a grouped Wgrad GEMM, whose contraction runs over
+// each expert's own tokens: expert e's rows offsets[e] .. offsets[e+1]-1 of
+// x form ceil(t_e / 128) groups of 128 tokens (the last one short).  The
+// transposed codes of expert e start at the padded column pofs[e] (the sum of
+// the previous experts' group counts x 128); a short group's missing tokens
+// get code 0, which adds nothing to the product, and do not enter its amax.
+// One CTA per (group, 64-column block) tile, tiles walked expert-major;
+// CTAs past the last tile exit.
+__global__ void __launch_bounds__(kQuantThreads) quant_act_128x1_grouped_kernel(
+    const uint16_t* __restrict__ x, int64_t T, int64_t K, int64_t ldx,
+    const int32_t* __restrict__ offsets, int E, uint8_t* __restrict__ xqT,
+    float* __restrict__ sxT, int64_t Tp, int32_t* __restrict__ pofs) {
+    __shared__ __align__(16) uint16_t tile[128][64];
+    __shared__ float part[4][64];
+    __shared__ int64_t s_m0, s_p0;
+    __shared__ int s_rows;
+    const int t0 = threadIdx.x;
+    const int64_t KC = K / 64;
+    if (t0 == 0) {
+        // locate this CTA's tile; CTA 0 also writes the padded offsets.  Expert
+        // ranges outside [0, T] or decreasing count as empty (memory safety;
+        // the results of such offsets are unspecified).
+        int64_t t = blockIdx.x, padded = 0, lo = 0;
+        int rows = 0;
+        int64_t m0 = 0, p0 = 0;
+        for (int e = 0; e < E; ++e) {
+            if (blockIdx.x == 0) pofs[e] = static_cast<int32_t>(padded);
+            int64_t hi = __ldg(offsets + e + 1);
+            if (hi < lo || hi > T) hi = lo;
+            const int64_t g = (hi - lo + 127) / 128;
+            if (rows == 0 && t >= 0 && t < g * KC) {
+                const int64_t grp = t / KC;
+                m0 = lo + grp * 128;
+                p0 = padded + grp * 128;
+                rows = static_cast<int>(hi - m0 < 128 ? hi - m0 : 128);
+                t = -(t % KC) - 1;  // remember the column block, stop matching
+            } else if (rows == 0) {
+                t -= g * KC;
+            }
+            padded += g * 128;
+            lo = hi;
+        }
+        if (blockIdx.x == 0) pofs[E] = static_cast<int32_t>(padded);
+        if (rows > 0 && p0 + 128 > Tp) rows = 0;  // capacity guard
+        s_rows = rows;
+        s_m0 = m0;
+        s_p0 = rows > 0 ? p0 * KC + (-t - 1) : 0;  // padded column, column block
+    }
+    __syncthreads();
+    const int rows = s_rows;
+    if (rows == 0) return;
+    const int64_t m0 = s_m0;
+    const int64_t p0 = s_p0 / KC;
+    const int64_t k0 = (s_p0 % KC) * 64;
+    {
+        const int ch = t0 & 7;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int row = (t0 >> 3) + 32 * p;
+            const uint4 v = row < rows ? ld_stream_v4(x + (m0 + row) * ldx + k0 + ch * 8)
+                                       : make_uint4(0, 0, 0, 0);
+            *reinterpret_cast<uint4*>(&tile[row][ch * 8]) = v;
+        }
+    }
+    __syncthreads();
+    const int c = t0 & 63;
+    const int qr = t0 >> 6;
+    float f[32];
+    float amax = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+        f[i] = __uint_as_float(static_cast<uint32_t>(tile[qr * 32 + i][c]) << 16);
+        amax = fmaxf(amax, fabsf(f[i]));
+    }
+    part[qr][c] = amax;
+    __syncthreads();
+    amax = fmaxf(fmaxf(part[0][c], part[1][c]), fmaxf(part[2][c], part[3][c]));
+    const float s = group_scale(amax);
+    const GroupDiv dv(s);
+    if (qr == 0) sxT[(p0 / 128) * K + k0 + c] = s;
+    uint4 o0, o1;
+    o0.x = dv.quad(f[0], f[1], f[2], f[3]);
+    o0.y = dv.quad(f[4], f[5], f[6], f[7]);
+    o0.z = dv.quad(f[8], f[9], f[10], f[11]);
+    o0.w = dv.quad(f[12], f[13], f[14], f[15]);
+    o1.x = dv.quad(f[16], f[17], f[18], f[19]);
+    o1.y = dv.quad(f[20], f[21], f[22], f[23]);
+    o1.z = dv.quad(f[24], f[25], f[26], f[27]);
+    o1.w = dv.quad(f[28], f[29], f[30], f[31]);
+    uint8_t* dst = xqT + (k0 + c) * Tp + p0 + qr * 32;
+    reinterpret_cast<uint4*>(dst)[0] = o0;
+    reinterpret_cast<uint4*>(dst)[1] = o1;
+}
+
 // ---------------------------------------------------------------- 128x128 --
 // One 128-thread CTA per 128x128 block, copied global -> shared with
 // 16-byte cp.async (no register staging), so that every SM holds several
@@ -322,6 +417,30 @@ extern "C" int fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t 
     quant_act_128x1_kernel<<<static_cast<unsigned>(quant_grid<quant_act_128x1_kernel>(tiles)), kQuantThreads, 0,
                              static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t*>(x), M, K, ldx, xqT, sxT, tiles);
+    return launch_status();
+}
+
+extern "C" int fp8_quant_act_128x1_grouped(const void* x, int64_t T, int64_t K, int64_t ldx,
+                                           const int32_t* offsets, int32_t E, uint8_t* xqT,
+                                           float* sxT, int64_t Tp, int32_t* pofs,
+                                           void* stream) {
+    if (T < 0 || K <= 0 || K % 64 != 0 || ldx < K || E < 1 || E > 65536 || Tp < 0 ||
+        Tp % 128 != 0)
+        return FP8_ERR_SHAPE;
+    // every expert pads at most 127 tokens
+    if (Tp < ((T + 127 * static_cast<int64_t>(E) + 127) / 128) * 128) return FP8_ERR_SHAPE;
+    if (Tp > 0x7fffffffLL) return FP8_ERR_UNSUPPORTED;
+    if (offsets == nullptr || pofs == nullptr) return FP8_ERR_NULL;
+    if (T > 0 && (x == nullptr || xqT == nullptr || sxT == nullptr)) return FP8_ERR_NULL;
+    if (ldx % 8 != 0 || !aligned(x, 16) || !aligned(xqT, 16) || !aligned(sxT, 4) ||
+        !aligned(offsets, 4) || !aligned(pofs, 4))
+        return FP8_ERR_ALIGN;
+    // upper bound of the tiles: sum over experts of ceil(t_e / 128) groups x K/64
+    const int64_t tiles = ((T + 127 * static_cast<int64_t>(E)) / 128 + 1) * (K / 64);
+    if (tiles > 0x7fffffffLL) return FP8_ERR_UNSUPPORTED;
+    quant_act_128x1_grouped_kernel<<<static_cast<unsigned>(tiles), kQuantThreads, 0,
+                                     static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t*>(x), T, K, ldx, offsets, E, xqT, sxT, Tp, pofs);
     return launch_status();
 }
 

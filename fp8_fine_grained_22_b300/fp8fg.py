@@ -24,7 +24,8 @@ FP8_BSCALE_BLOCK128_T = 2
 # every entry point of include/fp8fg.h
 EXPORTS = ("fp8_status_str", "fp8_device_error", "fp8_quant_act_1x128", "fp8_quant_act_128x1",
            "fp8_quant_weight_128x128", "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe",
-           "fp8_grouped_gemm_moe_dgrad",
+           "fp8_grouped_gemm_moe_dgrad", "fp8_quant_act_128x1_grouped",
+           "fp8_grouped_gemm_moe_wgrad",
            "fp8_moe_dispatch_workspace_size", "fp8_moe_dispatch_quant",
            "fp8_moe_dispatch_quant_noalloc")
 
@@ -63,6 +64,10 @@ def lib() -> ctypes.CDLL:
         L.fp8_gemm_blockscaled.argtypes = [P, P, P, P, I, I64, I64, I64, P, I64, I, P]
         L.fp8_grouped_gemm_moe.restype = I
         L.fp8_grouped_gemm_moe.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, I, P]
+        L.fp8_quant_act_128x1_grouped.restype = I
+        L.fp8_quant_act_128x1_grouped.argtypes = [P, I64, I64, I64, P, I32, P, P, I64, P, P]
+        L.fp8_grouped_gemm_moe_wgrad.restype = I
+        L.fp8_grouped_gemm_moe_wgrad.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, P]
         L.fp8_grouped_gemm_moe_dgrad.restype = I
         L.fp8_grouped_gemm_moe_dgrad.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, I, P]
         L.fp8_moe_dispatch_workspace_size.restype = I
@@ -276,3 +281,48 @@ def fp8_moe_dispatch_quant_noalloc(x, topk_ids, expert_begin, n_local, cap=None,
                                                 _p(offsets), _p(token_ids), _stream(stream)),
            "fp8_moe_dispatch_quant_noalloc")
     return xq, sx, offsets, token_ids
+
+
+# ---------------------------------------------------------- MoE Wgrad path --
+def padded_tokens(T, E):
+    """Column capacity Tp that fp8_quant_act_128x1_grouped needs for T rows over E experts."""
+    return ((T + 127 * E + 127) // 128) * 128
+
+
+def fp8_quant_act_128x1_grouped(x, offsets, E, Tp=None, xqT=None, sxT=None, pofs=None,
+                                stream=None):
+    """x bf16 [T, K], offsets int32 [E+1] (device) -> (xqT uint8 [K, Tp], sxT f32 [Tp/128, K],
+    pofs int32 [E+1]): per-expert 128-token groups, short groups zero-padded."""
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(offsets, "offsets", torch.int32)
+    assert x.dim() == 2 and x.stride(1) == 1
+    T, K = x.shape
+    if Tp is None:
+        Tp = padded_tokens(T, E)
+    if xqT is None:
+        xqT = torch.empty((K, Tp), dtype=torch.uint8, device=x.device)
+    if sxT is None:
+        sxT = torch.empty((Tp // 128, K), dtype=torch.float32, device=x.device)
+    if pofs is None:
+        pofs = torch.empty(E + 1, dtype=torch.int32, device=x.device)
+    _check(lib().fp8_quant_act_128x1_grouped(_p(x), T, K, x.stride(0), _p(offsets), E, _p(xqT),
+                                             _p(sxT), Tp, _p(pofs), _stream(stream)),
+           "fp8_quant_act_128x1_grouped")
+    return xqT, sxT, pofs
+
+
+def fp8_grouped_gemm_moe_wgrad(aqT, sa, bqT, sb, pofs, c=None, stream=None):
+    """dW [E, M, N] FP32 from aqT uint8 [M, Tp], sa [Tp/128, M], bqT uint8 [N, Tp],
+    sb [Tp/128, N], pofs int32 [E+1] (device)."""
+    for t, n in ((aqT, "aqT"), (sa, "sa"), (bqT, "bqT"), (sb, "sb"), (pofs, "pofs")):
+        _cuda(t, n)
+    M, Tp = aqT.shape
+    N = bqT.shape[0]
+    E = pofs.numel() - 1
+    if c is None:
+        c = torch.empty((E, M, N), dtype=torch.float32, device=aqT.device)
+    assert c.is_contiguous() and c.dtype == torch.float32
+    _check(lib().fp8_grouped_gemm_moe_wgrad(_p(aqT), _p(sa), _p(bqT), _p(sb), _p(pofs), E, Tp, M,
+                                            N, _p(c), _stream(stream)),
+           "fp8_grouped_gemm_moe_wgrad")
+    return c

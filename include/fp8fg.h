@@ -184,6 +184,56 @@ int fp8_grouped_gemm_moe_dgrad(const uint8_t* aq, const float* sa, const uint8_t
                                int64_t N, int64_t K, void* c, int out_type, void* stream);
 
 /*
+ * fp8_quant_act_128x1_grouped -- the 128x1 (token-wise, transposed)
+ * quantisation of expert-grouped rows for the MoE Wgrad GEMM, whose
+ * contraction runs over each expert's own tokens (report sections 3.3.1-3.3.3:
+ * Wgrad in FP8 on 128x1 groups along the tokens; section 3.4: MoE experts).
+ * Expert e's rows offsets[e] .. offsets[e+1]-1 form ceil(t_e/128) groups of
+ * 128 consecutive tokens; the last group of an expert is short and is read as
+ * if padded with zero rows (zero codes, no effect on its amax or the product).
+ *   x       : bfloat16 [T][K], row stride ldx.                          (input)
+ *   offsets : int32 [E+1] in DEVICE memory (offsets[0] = 0, non-decreasing,
+ *             offsets[E] <= T; other values give unspecified results but
+ *             no access outside x, xqT, sxT).                           (input)
+ *   xqT     : E4M3 [K][Tp]: expert e's codes in columns pofs[e] .. pofs[e+1]-1,
+ *             padding columns 0.  Columns >= pofs[E] are untouched.     (output)
+ *   sxT     : float [Tp/128][K]: scale of group g (padded column 128 g), column k
+ *             at sxT[g*K + k].                                          (output)
+ *   pofs    : int32 [E+1] in device memory: pofs[e] = sum over e' < e of
+ *             128 ceil(t_e'/128).                                       (output)
+ * Requires K % 64 == 0, ldx >= K, ldx % 8 == 0, 1 <= E <= 65536,
+ * Tp % 128 == 0 and Tp >= T + 127 E rounded up to 128; x, xqT 16-byte aligned,
+ * sxT, offsets, pofs 4-byte aligned.
+ */
+int fp8_quant_act_128x1_grouped(const void* x, int64_t T, int64_t K, int64_t ldx,
+                                const int32_t* offsets, int32_t E, uint8_t* xqT, float* sxT,
+                                int64_t Tp, int32_t* pofs, void* stream);
+
+/*
+ * fp8_grouped_gemm_moe_wgrad -- the Wgrad of the grouped expert GEMM: per
+ * expert e, dW_e[M][N] = X_e^T . dY_e, the contraction running over the
+ * expert's padded token columns pofs[e] .. pofs[e+1]-1 in 128-token blocks,
+ * each block's partial promoted to FP32 with the per-row A scale and the
+ * per-column B scale (report section 3.3.2, Figure 7(b); section 3.3.1,
+ * Wgrad in FP8).  Operands as fp8_quant_act_128x1_grouped produces them.
+ *   aqT  : E4M3 [M][Tp]: the activations' transposed codes (M = the Fprop
+ *          inner dimension).                                            (input)
+ *   sa   : float [Tp/128][M].                                           (input)
+ *   bqT  : E4M3 [N][Tp]: the output gradients' transposed codes.        (input)
+ *   sb   : float [Tp/128][N].                                           (input)
+ *   pofs : int32 [E+1] in device memory: multiples of 128, pofs[0] = 0,
+ *          non-decreasing, pofs[E] <= Tp; invalid values make the kernel skip
+ *          all work and raise FP8_ERR_DEVICE_SHAPE in fp8_device_error(). (input)
+ *   c    : float [E][M][N] (FP32, the weight gradients); an expert with no
+ *          tokens gets zeros.                                           (output)
+ * Requires M % 128 == 0, N % 128 == 0, Tp % 128 == 0, 1 <= E <= 65536;
+ * aqT, bqT, c 16-byte aligned, sa, sb, pofs 4-byte aligned.
+ */
+int fp8_grouped_gemm_moe_wgrad(const uint8_t* aqT, const float* sa, const uint8_t* bqT,
+                               const float* sb, const int32_t* pofs, int32_t E, int64_t Tp,
+                               int64_t M, int64_t N, float* c, void* stream);
+
+/*
  * fp8_moe_dispatch_workspace_size -- bytes of device workspace
  * fp8_moe_dispatch_quant needs for T tokens and n_local local experts
  * (0 when T = 0).  *bytes is set to 0 on error.
