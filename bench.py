@@ -12,6 +12,9 @@ the JSON line also carries each kernel's own rate and roofline fraction.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload fprop_dense|moe_prefill]
 
+`--workload moe_backward` times that layer's backward (dY quantisation, grouped
+Dgrad, per-expert 128x1 quantisation of X and dY, grouped Wgrad into FP32 dW).
+
 `--workload moe_prefill` times the MoE expert layer instead: FP8 dispatch
 packing of 16384 tokens routed top-8 of 256 experts to 32 local experts
 (fp8_moe_dispatch_quant) followed by the grouped GEMM against the experts'
@@ -530,6 +533,223 @@ def run_moe(args, rank, world, local):
     return line
 
 
+def run_moe_backward(args, rank, world, local):
+    """The expert layer's backward on the prefill routing: 1x128 quantisation of dY,
+    grouped Dgrad, per-expert 128x1 quantisation of X and dY, grouped Wgrad."""
+    from fp8_fine_grained_22_b300 import fp8fg
+
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    fp8fg.lib()
+    wl = inputs.moe_prefill(seed=0, device="cpu")
+    E, N, K = wl.E, wl.N, wl.K
+    R = int(wl.offsets[-1])
+    x = wl.x.to(dev)  # packed rows [R, K] (the Fprop inputs)
+    dy = inputs.grad(R, N, torch.Generator().manual_seed(1)).to(dev)
+    off = torch.from_numpy(np.asarray(wl.offsets, np.int32)).to(dev)
+    wqT = torch.empty((E, K, N), dtype=torch.uint8, device=dev)
+    sw = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device=dev)
+    for e in range(E):  # static weights: the transposed codes Dgrad reads
+        fp8fg.fp8_quant_weight_128x128(wl.w[e].to(dev), want_wq=False, wqT=wqT[e], sw=sw[e])
+    del wl
+    Tp = fp8fg.padded_tokens(R, E)
+    dq = torch.empty((R, N), dtype=torch.uint8, device=dev)
+    sd = torch.empty((N // 128, R), dtype=torch.float32, device=dev)
+    dx = torch.empty((R, K), dtype=torch.bfloat16, device=dev)
+    xqT = torch.empty((K, Tp), dtype=torch.uint8, device=dev)
+    sxT = torch.empty((Tp // 128, K), dtype=torch.float32, device=dev)
+    dqT = torch.empty((N, Tp), dtype=torch.uint8, device=dev)
+    sdT = torch.empty((Tp // 128, N), dtype=torch.float32, device=dev)
+    pofs = torch.empty(E + 1, dtype=torch.int32, device=dev)
+    dw = torch.empty((E, K, N), dtype=torch.float32, device=dev)
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def flush_l2():
+        flush.zero_()
+        torch.sum(flush, dim=0, out=flush_sink)
+
+    def dgrad():
+        fp8fg.fp8_quant_act_1x128(dy, dq, sd, stream=stream)
+        fp8fg.fp8_grouped_gemm_moe_dgrad(dq, sd, wqT, sw, off, c=dx, stream=stream)
+
+    def wgrad():
+        fp8fg.fp8_quant_act_128x1_grouped(x, off, E, Tp=Tp, xqT=xqT, sxT=sxT, pofs=pofs,
+                                          stream=stream)
+        fp8fg.fp8_quant_act_128x1_grouped(dy, off, E, Tp=Tp, xqT=dqT, sxT=sdT, pofs=pofs,
+                                          stream=stream)
+        fp8fg.fp8_grouped_gemm_moe_wgrad(xqT, sxT, dqT, sdT, pofs, c=dw, stream=stream)
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        dgrad()
+        if ev is not None:
+            ev[1].record(stream)
+        wgrad()
+        if ev is not None:
+            ev[2].record(stream)
+
+    def kernel_ms(fn, reps=10):
+        e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(reps)]
+        for a, b in e:
+            flush_l2()
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(a.elapsed_time(b) for a, b in e)
+
+    for _ in range(args.warmup):
+        flush_l2()
+        step()
+    torch.cuda.synchronize()
+    if fp8fg.device_error() != 0:
+        raise RuntimeError("device-side error during warm-up")
+    steps = min(args.steps, args.moe_steps // 4)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    rank_barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for i in range(steps):
+            flush_l2()
+            step(events[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    rank_barrier()
+    ms_step = reduce_max(statistics.mean(e[0].elapsed_time(e[2]) for e in events), dev)
+    dgrad_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
+    wgrad_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
+    wg_gemm_ms = kernel_ms(lambda: fp8fg.fp8_grouped_gemm_moe_wgrad(xqT, sxT, dqT, sdT, pofs,
+                                                                     c=dw, stream=stream))
+    dg_gemm_ms = kernel_ms(lambda: fp8fg.fp8_grouped_gemm_moe_dgrad(dq, sd, wqT, sw, off, c=dx,
+                                                                     stream=stream))
+    P = int(pofs[-1].item())
+
+    # end to end: dY in from pinned host memory, dX and dW out
+    dyh = dy.cpu().pin_memory()
+    dxh = torch.empty((R, K), dtype=torch.bfloat16).pin_memory()
+    dwh = torch.empty((E, K, N), dtype=torch.float32).pin_memory()
+
+    def e2e_step():
+        dy.copy_(dyh, non_blocking=True)
+        step()
+        dxh.copy_(dx, non_blocking=True)
+        dwh.copy_(dw, non_blocking=True)
+
+    e2e_steps = min(steps, max(1, args.e2e_steps // 10))
+    e2e_step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = reduce_max(a.elapsed_time(b) / e2e_steps, dev)
+    if fp8fg.device_error() != 0:
+        raise RuntimeError("device-side error")
+
+    peaks, peak_src = measured_peaks()
+    hbm = peaks["hbm_gbs"]
+    fp8_peak = 2.0 * peaks["bf16_tflops"]
+    flops = 2.0 * R * N * K * 2  # Dgrad + Wgrad over the real tokens
+    wg_flops_padded = 2.0 * K * N * P
+    wg_bytes = E * K * N * 4 + (K + N) * P + (P // 128) * (K + N) * 4
+    wg_gbs = wg_bytes / (wg_gemm_ms * 1e-3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": round(whole_job_tflops(world, flops, ms_step), 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3 x e4m3 -> f32 accumulate; dX bf16, dW f32",
+        "data": "synthetic (seeded: the prefill routing's packed rows, N(0,1e-3^2) output "
+                "gradients, N(0,0.006^2) expert weights)",
+        "config": {"workload": MOE_WORKLOAD + "_backward", "rows": R, "padded_rows": P,
+                   "local_experts": E, "N": N, "K": K,
+                   "parallelism": "replicas (dp%d, no collective)" % world,
+                   "l2": "flushed between steps (%d MB written, then read back)" % (
+                       flush.numel() * 4 >> 20),
+                   "step": ["fp8_quant_act_1x128 (dY)", "fp8_grouped_gemm_moe_dgrad",
+                            "fp8_quant_act_128x1_grouped (X, dY)", "fp8_grouped_gemm_moe_wgrad"],
+                   "weights": "quantised once before timing (static)"},
+        "e2e": {"value": round(whole_job_tflops(world, flops, e2e_ms), 3), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+                "h2d_bytes_per_step": R * N * 2,
+                "d2h_bytes_per_step": R * K * 2 + E * K * N * 4},
+        "gpu_launches": 5 * steps,
+        "roofline": {"kernel": "fp8_grouped_gemm_moe_wgrad", "bound": "hbm",
+                     "achieved": round(wg_gbs, 1), "peak": round(hbm, 1), "unit": "GB/s",
+                     "frac": round(wg_gbs / hbm, 4),
+                     "peak_source": "%s copy bandwidth" % peak_src, "traffic": None,
+                     "note": "dW is E x %d x %d FP32 (%.2f GB): writing it dominates the "
+                             "kernel's %.3f TFLOP" % (K, N, E * K * N * 4 / 1e9,
+                                                       wg_flops_padded / 1e12)},
+        "kernels": {
+            "dgrad phase (quant dY + grouped Dgrad)": {"ms": round(dgrad_ms, 5)},
+            "wgrad phase (2 grouped 128x1 quants + grouped Wgrad)": {"ms": round(wgrad_ms, 5)},
+            "fp8_grouped_gemm_moe_dgrad (alone)": {
+                "ms": round(dg_gemm_ms, 5),
+                "tflops": round(2.0 * R * N * K / (dg_gemm_ms * 1e-3) / 1e12, 2),
+                "frac_fp8_peak": round(2.0 * R * N * K / (dg_gemm_ms * 1e-3) / 1e12 / fp8_peak,
+                                       4)},
+            "fp8_grouped_gemm_moe_wgrad (alone)": {
+                "ms": round(wg_gemm_ms, 5), "gbs": round(wg_gbs, 1),
+                "tflops_padded": round(wg_flops_padded / (wg_gemm_ms * 1e-3) / 1e12, 2)},
+        },
+        "clocks": clk.summary(),
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if args.cpu_baseline and rank == 0:
+        line["cpu_baseline"] = cpu_baseline_moe_backward(args.ref_rows)
+    return line
+
+
+def cpu_baseline_moe_backward(n_rows):
+    """The oracle on the host for the expert backward: 1x128 quantisation of dY and the
+    binary64 grouped Dgrad of the first n_rows packed rows (their experts' weights
+    quantised), per-expert 128x1 quantisation of X and dY and the binary64 grouped Wgrad of
+    8 rows of every expert's dW."""
+    import oracle
+
+    wl = inputs.moe_prefill(seed=0, device="cpu")
+    threads = oracle.default_threads()
+    R = int(wl.offsets[-1])
+    dy = inputs.bf16_bits(inputs.grad(R, wl.N, torch.Generator().manual_seed(1)))
+    xb = inputs.bf16_bits(wl.x)
+    t0 = time.perf_counter()
+    dq, sd = oracle.quant_act_1x128(dy)
+    rows = np.arange(min(n_rows, R))
+    experts = np.unique(np.searchsorted(wl.offsets, rows, side="right") - 1)
+    bqT = np.zeros((wl.E, wl.K, wl.N), np.uint8)
+    sw = np.ones((wl.E, wl.N // 128, wl.K // 128), np.float32)
+    for e in experts:
+        _, bqT[e], sw[e] = oracle.quant_weight_128x128(inputs.bf16_bits(wl.w[e]))
+    dx = oracle.grouped_gemm(dq, sd, bqT, sw, wl.offsets, rows=rows, nthreads=threads,
+                             bmode=oracle.BSCALE_BLOCK128_T)
+    oracle.round_bf16(dx)
+    xqT, sxT, pofs = oracle.quant_act_128x1_grouped(xb, wl.offsets)
+    dqT, sdT, _ = oracle.quant_act_128x1_grouped(dy, wl.offsets)
+    wrows = np.arange(8)
+    oracle.grouped_wgrad(xqT, sxT, dqT, sdT, pofs, rows=wrows, nthreads=threads)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows.size * wl.N * wl.K + 2.0 * wrows.size * wl.E * wl.N * int(pofs[-1]) / wl.E
+    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
+            "kind": "oracle", "seconds": round(dt, 2),
+            "sample": "quantisation of all of dY, X; grouped Dgrad of the first %d of %d rows; "
+                      "grouped Wgrad of %d rows of each of %d experts' dW" % (
+                          rows.size, R, wrows.size, wl.E)}
+
+
 def cpu_baseline_moe(n_rows):
     """The oracle on the host: dispatch of every token (membership, gather, 1x128
     quantisation), quantisation of the experts the sampled rows use, and the
@@ -584,8 +804,9 @@ def cpu_baseline(n_rows, wl=None):
 
 def run_reference_moe(args):
     times, res = [], None
+    base = cpu_baseline_moe_backward if args.workload == "moe_backward" else cpu_baseline_moe
     for _ in range(args.steps):
-        res = cpu_baseline_moe(args.ref_rows)
+        res = base(args.ref_rows)
         times.append(res["seconds"])
     ms = statistics.mean(times) * 1e3
     value = res["value"]
@@ -595,7 +816,8 @@ def run_reference_moe(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64 oracle (e4m3 codes, binary64 accumulate)",
         "data": "synthetic (same seeded workload)",
-        "config": {"workload": MOE_WORKLOAD, "sample_rows": args.ref_rows},
+        "config": {"workload": MOE_WORKLOAD + ("_backward" if args.workload == "moe_backward"
+                                                else ""), "sample_rows": args.ref_rows},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": res["cores"],
                          "kind": "oracle", "sample": res["sample"]},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -605,7 +827,7 @@ def run_reference_moe(args):
 
 def run_reference(args):
     """Reference arm: the CPU oracle, timed per step on a bounded sample."""
-    if args.workload == "moe_prefill":
+    if args.workload in ("moe_prefill", "moe_backward"):
         return run_reference_moe(args)
     wl = inputs.fprop_dense(seed=0, device="cpu")
     for _ in range(args.warmup and 1):
@@ -651,7 +873,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
     ap.add_argument("--cpu-sample-rows", type=int, default=2048)
     ap.add_argument("--ref-rows", type=int, default=512)
-    ap.add_argument("--workload", choices=["fprop_dense", "moe_prefill"], default="fprop_dense")
+    ap.add_argument("--workload", choices=["fprop_dense", "moe_prefill", "moe_backward"],
+                    default="fprop_dense")
     ap.add_argument("--moe-steps", type=int, default=2000,
                     help="cap on timed steps for the MoE workload")
     args = ap.parse_args()
@@ -668,6 +891,8 @@ def main():
     try:
         if args.workload == "moe_prefill":
             line = run_moe(args, rank, world, local)
+        elif args.workload == "moe_backward":
+            line = run_moe_backward(args, rank, world, local)
         else:
             line = run_ours(args, rank, world, local)
         if rank == 0:
