@@ -106,3 +106,19 @@ def test_moe_prefill_wgrad_workload():
     assert fp8fg.device_error() == 0
     rows = np.array([0, 1, 127, 128, 3000, 7167])
     _compare_wgrad(dw, rq, rs, rdq, rds, rpofs, rows)
+
+
+def test_full_width_two_experts():
+    """dW [2, 7168, 4096] from 700 + 300 tokens (ragged groups in both experts)."""
+    g = torch.Generator().manual_seed(11)
+    counts = [700, 300]
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    T, M, N, E = int(offsets[-1]), 7168, 4096, 2
+    x = inputs.act(T, M, g)
+    dy = inputs.grad(T, N, g)
+    xqT, sxT, pofs, rq, rs, rpofs = _check_quant(x, offsets, E)
+    dqT, sdT, _, rdq, rds, _ = _check_quant(dy, offsets, E)
+    dw = fp8fg.fp8_grouped_gemm_moe_wgrad(xqT, sxT, dqT, sdT, pofs)
+    torch.cuda.synchronize()
+    assert fp8fg.device_error() == 0
+    _compare_wgrad(dw, rq, rs, rdq, rds, rpofs, np.array([0, 5, 127, 128, 4000, 7167]))
