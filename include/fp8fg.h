@@ -50,7 +50,7 @@ typedef enum {
     FP8_ERR_NULL = 1,        /* a required pointer is NULL */
     FP8_ERR_SHAPE = 2,       /* a size or leading dimension is invalid */
     FP8_ERR_ALIGN = 3,       /* a pointer or stride breaks the alignment rule */
-    FP8_ERR_UNSUPPORTED = 4, /* valid request this build does not serve */
+    FP8_ERR_UNSUPPORTED = 4, /* valid request the library does not serve */
     FP8_ERR_CUDA = 5,        /* a CUDA runtime/driver call failed */
     FP8_ERR_TIMEOUT = 6,     /* a kernel gave up waiting on a pipeline barrier */
     FP8_ERR_DEVICE_SHAPE = 7 /* a kernel found invalid device-side data (offsets) */
