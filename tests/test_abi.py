@@ -82,3 +82,49 @@ def test_gemm_validation():
     assert gg(A16, A16, A16, A16, A16, 2, 0, 128, 128, 0, 1, None) == OK        # T == 0
     assert gg(A16, A16, A16, A16, 0, 2, 16, 128, 128, A16, 1, None) == NULL
     assert gg(A16, A16, A16, A16, A16 + 2, 2, 16, 128, 128, A16, 1, None) == ALIGN
+
+
+def test_moe_backward_validation():
+    L = fp8fg.lib()
+    dg = L.fp8_grouped_gemm_moe_dgrad
+    assert dg(A16, A16, A16, A16, A16, 0, 16, 128, 128, A16, 1, None) == SHAPE  # E < 1
+    assert dg(A16, A16, A16, A16, A16, 2, 0, 128, 128, 0, 1, None) == OK        # T == 0
+    assert dg(A16, A16, 0, A16, A16, 2, 16, 128, 128, A16, 1, None) == NULL
+    assert dg(A16, A16, A16 + 8, A16, A16, 2, 16, 128, 128, A16, 1, None) == ALIGN
+    q = L.fp8_quant_act_128x1_grouped
+    # T=300 rows, K=128, E=2: Tp must be a multiple of 128 and >= ceil((300 + 2*127)/128)*128 = 640
+    assert q(A16, 300, 96, 96, A16, 2, A16, A16, 640, A16, None) == SHAPE     # K % 64
+    assert q(A16, 300, 128, 128, A16, 2, A16, A16, 600, A16, None) == SHAPE   # Tp % 128
+    assert q(A16, 300, 128, 128, A16, 2, A16, A16, 512, A16, None) == SHAPE   # Tp too small
+    assert q(A16, 300, 128, 128, 0, 2, A16, A16, 640, A16, None) == NULL      # offsets
+    assert q(A16, 300, 128, 128, A16, 2, A16, A16, 640, A16 + 2, None) == ALIGN
+    wg = L.fp8_grouped_gemm_moe_wgrad
+    assert wg(A16, A16, A16, A16, A16, 2, 256, 100, 128, A16, None) == SHAPE  # M % 128
+    assert wg(A16, A16, A16, A16, A16, 2, 200, 128, 128, A16, None) == SHAPE  # Tp % 128
+    assert wg(A16, A16, A16, A16, 0, 2, 256, 128, 128, A16, None) == NULL
+    assert wg(A16, A16, A16 + 4, A16, A16, 2, 256, 128, 128, A16, None) == ALIGN
+
+
+def test_dispatch_validation_and_workspace_size():
+    L = fp8fg.lib()
+    n = ctypes.c_size_t(99)
+    assert L.fp8_moe_dispatch_workspace_size(0, 8, ctypes.byref(n)) == OK and n.value == 0
+    assert L.fp8_moe_dispatch_workspace_size(1000, 0, ctypes.byref(n)) == SHAPE
+    assert L.fp8_moe_dispatch_workspace_size(1 << 40, 8, ctypes.byref(n)) == UNSUP
+    # 1000 tokens -> 16 chunks of 64; counts [8][16] + totals [8] ints, 256-byte granules
+    assert L.fp8_moe_dispatch_workspace_size(1000, 8, ctypes.byref(n)) == OK
+    assert n.value == ((8 * 16 + 8) * 4 + 255) // 256 * 256
+    d = L.fp8_moe_dispatch_quant
+    args = lambda **k: [k.get("x", A16), 1000, 256, 256, k.get("ids", A16), k.get("topk", 2), 0,
+                        8, k.get("xq", A16), A16, k.get("cap", 2000), A16, A16,
+                        k.get("ws", A16), 4096, None]
+    assert d(*args(topk=0)) == SHAPE
+    assert d(*args(topk=17)) == SHAPE
+    assert d(*args(cap=1999)) == SHAPE          # cap < T * min(topk, n_local)
+    assert d(*args(ids=0)) == NULL
+    assert d(*args(x=A16 + 2)) == ALIGN
+    assert d(*args(ws=A16 + 16)) == ALIGN       # workspace must be 256-byte aligned
+    na = L.fp8_moe_dispatch_quant_noalloc
+    # 32 local experts: n_local * ceil(T/64) + n_local must stay <= 65536
+    assert na(A16, 131072, 256, 256, A16, 1, 0, 32, A16, A16, 131072, A16, A16, None) == UNSUP
+    assert na(A16, 1000, 256, 256, 0, 2, 0, 8, A16, A16, 2000, A16, A16, None) == NULL
