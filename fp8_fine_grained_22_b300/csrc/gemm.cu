@@ -686,11 +686,17 @@ static int dispatch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_
         return launch<128, false, true, 2>(aq, a_rows, bq, b_rows, p, tiles, stream);
     } else {
         const bool rows = p.bmode == FP8_BSCALE_ROW1x128;
-        // 256-wide tiles halve the shared-memory operand traffic per MMA; the
-        // per-column B-scale mode keeps 128-wide tiles (its epilogue needs more
-        // registers than a 256-wide tile leaves).
-        if (p.N % 256 == 0 && !rows) {
+        // 256-wide tiles halve the shared-memory operand traffic per MMA and
+        // run the tensor core at its full rate; 128-wide ones serve N % 256 != 0.
+        if (p.N % 256 == 0) {
             const int64_t tiles = mblk_upper * (p.N / 256);
+            if constexpr (!GROUPED) {
+                if (rows) {
+                    if (out_type == FP8_OUT_BF16)
+                        return launch<256, true, true, GM>(aq, a_rows, bq, b_rows, p, tiles, stream);
+                    return launch<256, false, true, GM>(aq, a_rows, bq, b_rows, p, tiles, stream);
+                }
+            }
             if (out_type == FP8_OUT_BF16)
                 return launch<256, true, false, GM>(aq, a_rows, bq, b_rows, p, tiles, stream);
             return launch<256, false, false, GM>(aq, a_rows, bq, b_rows, p, tiles, stream);
