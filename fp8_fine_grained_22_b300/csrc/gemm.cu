@@ -679,9 +679,13 @@ static int dispatch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_
                     GemmParams& p, int out_type, int64_t mblk_upper, cudaStream_t stream) {
     constexpr bool GROUPED = GM == 1;
     if constexpr (GM == 2) {
-        // the per-expert Wgrad GEMM: per-column B scales, 128-wide tiles, FP32 out
+        // the per-expert Wgrad GEMM: per-column B scales, FP32 out
         (void)out_type;
         (void)mblk_upper;
+        if (p.N % 256 == 0) {
+            const int64_t tiles = static_cast<int64_t>(p.E) * (p.M / BM) * (p.N / 256);
+            return launch<256, false, true, 2>(aq, a_rows, bq, b_rows, p, tiles, stream);
+        }
         const int64_t tiles = static_cast<int64_t>(p.E) * (p.M / BM) * (p.N / 128);
         return launch<128, false, true, 2>(aq, a_rows, bq, b_rows, p, tiles, stream);
     } else {
