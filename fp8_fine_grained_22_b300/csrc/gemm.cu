@@ -546,10 +546,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     const uint64_t sa2 = pack2(f2u(sa_cur), f2u(sa_cur));
                     const float* rs = rscale + rsb * BN + cg * COLS;
-#pragma unroll
-                    for (int ch = 0; ch < COLS / 16; ++ch) {
-                        uint32_t r[16];
-                        tmem_ld16_wait(taddr + ch * 16, r);
+                    // 16 columns: P * sb[col] (packed), then * sa + acc
+                    auto fma16 = [&](uint32_t (&r)[16], int ch) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             const float4 b4 = *reinterpret_cast<const float4*>(rs + ch * 16 + 4 * i);
@@ -560,10 +558,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                             acc[ch * 8 + 2 * i] = ffma2(p0, sa2, acc[ch * 8 + 2 * i]);
                             acc[ch * 8 + 2 * i + 1] = ffma2(p1, sa2, acc[ch * 8 + 2 * i + 1]);
                         }
+                    };
+                    // two 16-column loads in flight; the TMEM buffer goes back to
+                    // the MMA once the last pair has landed
+                    uint32_t r0[16], r1[16];
+                    tmem_ld16(taddr, r0);
+                    tmem_ld16(taddr + 16, r1);
+#pragma unroll
+                    for (int ch = 0; ch < COLS / 16; ch += 2) {
+                        tmem_wait_ld16(r0);
+                        tmem_wait_ld16(r1);
+                        if (ch + 2 < COLS / 16) {
+                            fma16(r0, ch);
+                            tmem_ld16(taddr + (ch + 2) * 16, r0);
+                            fma16(r1, ch + 1);
+                            tmem_ld16(taddr + (ch + 3) * 16, r1);
+                        } else {
+                            tc_fence_before_sync();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(tempty_bar(u, buf));
+                            fma16(r0, ch);
+                            fma16(r1, ch + 1);
+                        }
                     }
-                    tc_fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(tempty_bar(u, buf));
                 }
             }
             if (!ok) break;
