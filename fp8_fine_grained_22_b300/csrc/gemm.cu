@@ -857,6 +857,27 @@ extern "C" int fp8_grouped_gemm_moe_wgrad(const uint8_t* aqT, const float* sa,
     return dispatch<2>(aqT, M, bqT, N, p, FP8_OUT_F32, 0, static_cast<cudaStream_t>(stream));
 }
 
+// Self-test of the failure path: one thread waits, through the same bounded
+// wait as the GEMM roles, on a barrier nothing ever arrives on.  The wait gives
+// up after its limit (about two seconds), records FP8_ERR_TIMEOUT in the
+// device error word and the kernel returns.
+__global__ void selftest_wait_kernel() {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ volatile int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_addr(&bar), 1);
+        abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) (void)wait_bar(smem_addr(&bar), 0, &abort_flag);
+}
+
+extern "C" int fp8_selftest_wait_timeout(void* stream) {
+    selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
+    return launch_status();
+}
+
 extern "C" int fp8_device_error(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return FP8_ERR_CUDA;

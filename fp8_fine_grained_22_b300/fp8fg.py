@@ -22,10 +22,10 @@ FP8_BSCALE_ROW1x128 = 1
 FP8_BSCALE_BLOCK128_T = 2
 
 # every entry point of include/fp8fg.h
-EXPORTS = ("fp8_status_str", "fp8_device_error", "fp8_quant_act_1x128", "fp8_quant_act_128x1",
-           "fp8_quant_weight_128x128", "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe",
-           "fp8_grouped_gemm_moe_dgrad", "fp8_quant_act_128x1_grouped",
-           "fp8_grouped_gemm_moe_wgrad",
+EXPORTS = ("fp8_status_str", "fp8_device_error", "fp8_selftest_wait_timeout",
+           "fp8_quant_act_1x128", "fp8_quant_act_128x1", "fp8_quant_weight_128x128",
+           "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe", "fp8_grouped_gemm_moe_dgrad",
+           "fp8_quant_act_128x1_grouped", "fp8_grouped_gemm_moe_wgrad",
            "fp8_moe_dispatch_workspace_size", "fp8_moe_dispatch_quant",
            "fp8_moe_dispatch_quant_noalloc")
 
@@ -54,6 +54,8 @@ def lib() -> ctypes.CDLL:
         L.fp8_status_str.argtypes = [I]
         L.fp8_device_error.restype = I
         L.fp8_device_error.argtypes = [P]
+        L.fp8_selftest_wait_timeout.restype = I
+        L.fp8_selftest_wait_timeout.argtypes = [P]
         L.fp8_quant_act_1x128.restype = I
         L.fp8_quant_act_1x128.argtypes = [P, I64, I64, I64, P, I64, P, P]
         L.fp8_quant_act_128x1.restype = I
@@ -106,6 +108,12 @@ def _cuda(t, name, dtype=None):
         raise ValueError("%s must be a CUDA tensor" % name)
     if dtype is not None and t.dtype != dtype:
         raise TypeError("%s must be %s, got %s" % (name, dtype, t.dtype))
+
+
+def selftest_wait_timeout(stream=None):
+    """Launch the bounded-wait self-test (a wait nothing completes); device_error() then
+    reports FP8_ERR_TIMEOUT (6)."""
+    _check(lib().fp8_selftest_wait_timeout(_stream(stream)), "fp8_selftest_wait_timeout")
 
 
 def device_error(stream=None) -> int:

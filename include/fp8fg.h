@@ -82,6 +82,16 @@ const char* fp8_status_str(int status);
 int fp8_device_error(void* stream);
 
 /*
+ * fp8_selftest_wait_timeout: launches one thread that waits, with the same
+ * bounded barrier wait the GEMM kernels use, on a barrier that nothing ever
+ * completes; after the wait limit (about two seconds) it records
+ * FP8_ERR_TIMEOUT for fp8_device_error() and returns, leaving the context
+ * usable.  A check of the failure-detection path; the report has no
+ * counterpart.  Asynchronous on `stream`.
+ */
+int fp8_selftest_wait_timeout(void* stream);
+
+/*
  * fp8_quant_act_1x128 -- 1x128 activation quantisation (report section
  * 3.3.2, fine-grained quantization; group size 1x128).
  *   x   : bfloat16 [M][K], row stride ldx.                 (input)
