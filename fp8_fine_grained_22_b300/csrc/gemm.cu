@@ -7,18 +7,26 @@
 // interval, and accumulated in FP32 outside the tensor core.
 //
 // Blackwell mapping (the report's H800 design copied WGMMA register partials
-// to CUDA-core registers; here the partials live in tensor memory):
+// to CUDA-core registers; here the partials live in tensor memory), 384
+// threads in three warpgroups:
 //   warp 0      TMA producer: A tile 128x128 and B tile BNx128 (E4M3, 128-byte
 //               swizzle) per K block into a STAGES-deep shared-memory ring.
-//   warp 1      MMA issuer: four tcgen05.mma kind::f8f6f4 (K = 32 each) per K
-//               block into one of two TMEM partial buffers (BN FP32 columns
-//               each), then tcgen05.commit to release the smem stage and to
-//               signal the epilogue.
-//   warps 2..9  promotion epilogue: tcgen05.ld the partial of K block kb,
-//               acc += partial * (sa[m,kb] * sb[kb]) with packed FP32 FMAs
-//               in registers, release the TMEM buffer; after the last K block,
-//               convert and store the tile through a swizzled shared-memory
-//               staging buffer and TMA bulk stores.
+//   warp 1      TMEM allocator and MMA issuer: four tcgen05.mma kind::f8f6f4
+//               (K = 32 each) per K block into one of the TMEM partial buffers
+//               (two of 256 FP32 columns, or four of 128), then tcgen05.commit
+//               to release the smem stage and to signal the epilogue.  In the
+//               dense kernels both roles run as whole warps with one elected
+//               lane issuing; the grouped-row kernels use one lane.
+//   warps 2, 3  idle (they complete the control warpgroup for setmaxnreg).
+//   warps 4..11 promotion epilogue, two per TMEM lane quadrant: tcgen05.ld the
+//               partial of K block kb, acc += partial * (sa[m,kb] * sb[kb])
+//               (or * sb[n,kb] per column in the Wgrad mode) with packed FP32
+//               FMAs in registers, release the TMEM buffer; after the last K
+//               block, convert and store the tile through a swizzled
+//               shared-memory staging buffer and TMA bulk stores.
+// Group modes: dense; grouped over rows (MoE Fprop and Dgrad: tiles walk the
+// expert row offsets); grouped over K (MoE Wgrad: every expert has the same
+// output tiles and contracts over its own padded token range).
 // The kernel is persistent: one CTA per SM walks a static tile schedule.
 // Every barrier wait is bounded; on expiry the kernel records
 // FP8_ERR_TIMEOUT in a device error word, unwinds and frees its TMEM.
@@ -55,10 +63,7 @@ constexpr int kSmemLimit = 232448;    // 227 KB opt-in per CTA
 // Output staging: each epilogue warp owns kOutSlots swizzled 4 KB boxes
 // (32 rows x 128 bytes); a TMA store is only waited on when its slot comes
 // round again, so the store of one tile overlaps the next tile's K loop.
-#ifndef FP8FG_OUT_SLOTS
-#define FP8FG_OUT_SLOTS 2
-#endif
-constexpr int kOutSlots = FP8FG_OUT_SLOTS;
+constexpr int kOutSlots = 2;
 constexpr int kBoxBytes = 32 * 128;
 
 template <int BN, bool ROWSCALE>
@@ -72,10 +77,7 @@ struct Cfg {
     // 256-wide tile into two 128-column sub-tiles with their own buffers was
     // measured slower: each sub-tile MMA re-reads A from shared memory, and
     // shared-memory bandwidth is what bounds the main loop.)
-#ifndef FP8FG_NSUB256
-#define FP8FG_NSUB256 1
-#endif
-    static constexpr int NSUB = (BN == 256 && !ROWSCALE) ? FP8FG_NSUB256 : 1;
+    static constexpr int NSUB = 1;  // N sub-tiles with their own TMEM buffers (one)
     static constexpr int SUBN = BN / NSUB;
     static constexpr int NBUF = 512 / BN;
     static constexpr int TMEM_COLS = NSUB * NBUF * SUBN;
