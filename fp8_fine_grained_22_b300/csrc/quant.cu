@@ -42,6 +42,48 @@ __device__ __forceinline__ void load_1x128(const uint16_t* __restrict__ x, int64
     for (int i = 0; i < 4; ++i) v[i] = (m < M) ? ld_stream_v4(src + 8 * i) : make_uint4(0, 0, 0, 0);
 }
 
+// Quantises the 1x128 tile whose bf16 values this thread holds in v (row
+// `row` of the tile, lanes l4 = 0..3 of its four-lane group).
+__device__ __forceinline__ void quant_1x128_tile(int64_t M, int64_t KB, uint8_t* __restrict__ xq,
+                                                 int64_t ldq, float* __restrict__ sx, int64_t t,
+                                                 int row, int l4, const uint4 (&v)[4]) {
+    const int64_t kb = t % KB;
+    const int64_t m = (t / KB) * kQ1Rows + row;
+    uint32_t mx = absmax_bf16x2(v[0].x, v[0].y);
+    mx = absmax_bf16x2(mx, absmax_bf16x2(v[0].z, v[0].w));
+#pragma unroll
+    for (int i = 1; i < 4; ++i) {
+        mx = absmax_bf16x2(mx, absmax_bf16x2(v[i].x, v[i].y));
+        mx = absmax_bf16x2(mx, absmax_bf16x2(v[i].z, v[i].w));
+    }
+    float amax = amax_of_pair(mx);
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float s = group_scale(amax);
+    const GroupDiv dv(s);
+    if (m < M) {
+        uint4 o[2];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t a = dv.quad(bf16_lo(v[i].x), bf16_hi(v[i].x), bf16_lo(v[i].y),
+                                       bf16_hi(v[i].y));
+            const uint32_t b = dv.quad(bf16_lo(v[i].z), bf16_hi(v[i].z), bf16_lo(v[i].w),
+                                       bf16_hi(v[i].w));
+            if (i & 1) {
+                o[i >> 1].z = a;
+                o[i >> 1].w = b;
+            } else {
+                o[i >> 1].x = a;
+                o[i >> 1].y = b;
+            }
+        }
+        uint4* dst = reinterpret_cast<uint4*>(xq + m * ldq + kb * 128 + l4 * 32);
+        dst[0] = o[0];
+        dst[1] = o[1];
+        if (l4 == 0) sx[kb * M + m] = s;
+    }
+}
+
 __global__ void __launch_bounds__(kQuantThreads) quant_act_1x128_kernel(
     const uint16_t* __restrict__ x, int64_t M, int64_t KB, int64_t ldx, uint8_t* __restrict__ xq,
     int64_t ldq, float* __restrict__ sx, int64_t tiles) {
@@ -54,41 +96,7 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_1x128_kernel(
         const int64_t tn = t + gridDim.x;
         uint4 vn[4];
         if (tn < tiles) load_1x128(x, M, ldx, KB, tn, row, l4, vn);
-        const int64_t kb = t % KB;
-        const int64_t m = (t / KB) * kQ1Rows + row;
-        uint32_t mx = absmax_bf16x2(v[0].x, v[0].y);
-        mx = absmax_bf16x2(mx, absmax_bf16x2(v[0].z, v[0].w));
-#pragma unroll
-        for (int i = 1; i < 4; ++i) {
-            mx = absmax_bf16x2(mx, absmax_bf16x2(v[i].x, v[i].y));
-            mx = absmax_bf16x2(mx, absmax_bf16x2(v[i].z, v[i].w));
-        }
-        float amax = amax_of_pair(mx);
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        const float s = group_scale(amax);
-        const GroupDiv dv(s);
-        if (m < M) {
-            uint4 o[2];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint32_t a = dv.quad(bf16_lo(v[i].x), bf16_hi(v[i].x), bf16_lo(v[i].y),
-                                           bf16_hi(v[i].y));
-                const uint32_t b = dv.quad(bf16_lo(v[i].z), bf16_hi(v[i].z), bf16_lo(v[i].w),
-                                           bf16_hi(v[i].w));
-                if (i & 1) {
-                    o[i >> 1].z = a;
-                    o[i >> 1].w = b;
-                } else {
-                    o[i >> 1].x = a;
-                    o[i >> 1].y = b;
-                }
-            }
-            uint4* dst = reinterpret_cast<uint4*>(xq + m * ldq + kb * 128 + l4 * 32);
-            dst[0] = o[0];
-            dst[1] = o[1];
-            if (l4 == 0) sx[kb * M + m] = s;
-        }
+        quant_1x128_tile(M, KB, xq, ldq, sx, t, row, l4, v);
 #pragma unroll
         for (int i = 0; i < 4; ++i) v[i] = vn[i];
         t = tn;
@@ -368,6 +376,201 @@ __global__ void __launch_bounds__(kWThreads) quant_weight_128x128_kernel(
     }
 }
 
+// ------------------------------------------------- both Fprop operands --
+// One persistent launch quantises the activation (1x128) and the weight
+// (128x128) of one GEMM.  Run as two kernels, the operands serialise: each
+// kernel fills the SMs on its own, and neither is large enough to reach the
+// HBM rate alone.  Here one grid walks a single list of items, weight blocks
+// spread evenly among the activation tiles, with a stride of the grid size,
+// prefetching the next item while it converts the current one: a weight
+// block by cp.async into the other of two 32 KB shared buffers, an
+// activation tile into registers.  The per-group arithmetic is the same code
+// as the single-operand kernels.
+constexpr int kPairThreads = 256;
+constexpr int kPairCtasPerSm = 3;
+constexpr int kPairSmem = 2 * 128 * 128 * 2;  // two bf16 blocks
+
+struct PairArgs {
+    const uint16_t* x;
+    int64_t M, ldx, ldq, act_tiles;
+    uint8_t* xq;
+    float* sx;
+    const uint16_t* w;
+    int64_t N, ldw, w_tiles;
+    uint8_t* wq;
+    uint8_t* wqT;
+    float* sw;
+    int64_t KB;  // K / 128, shared by both operands
+};
+
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_prev() {  // all groups but the newest
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
+// Item i of the list is a weight block when the count of weight blocks
+// among items 0..i, floor((i + 1) W / total), steps up at i; *idx is then
+// the block's index, else the activation tile's.
+__device__ __forceinline__ bool pair_item(const PairArgs& p, int64_t i, int64_t* idx) {
+    const int64_t total = p.w_tiles + p.act_tiles;
+    const int64_t w_upto = ((i + 1) * p.w_tiles) / total;
+    const bool is_w = w_upto > (i * p.w_tiles) / total;
+    *idx = is_w ? w_upto - 1 : i - w_upto;
+    return is_w;
+}
+
+// Starts the loads of item t: weight block t into `tile`, or activation
+// tile t into v.
+__device__ __forceinline__ void pair_issue(const PairArgs& p, bool is_w, int64_t t,
+                                           uint16_t (*tile)[128], int row, int l4,
+                                           uint4 (&v)[4]) {
+    if (is_w) {
+        const int64_t NB = p.N / 128;
+        const int64_t n0 = (t % NB) * 128, k0 = (t / NB) * 128;
+        const int ch = threadIdx.x & 15;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int r = (threadIdx.x >> 4) + 16 * q;
+            cp_async16(&tile[r][ch * 8], p.w + (k0 + r) * p.ldw + n0 + ch * 8);
+        }
+    } else {
+        load_1x128(p.x, p.M, p.ldx, p.KB, t, row, l4, v);
+    }
+}
+
+// Converts the weight block t staged in `tile` (all 256 threads).  The
+// transposed codes are staged in the first 16 KB of `tile` once every
+// thread has read its values.  Ends with a barrier, after which `tile` and
+// `part` may be reused.
+__device__ __forceinline__ void pair_weight_block(const PairArgs& p, int64_t t,
+                                                  uint16_t (*tile)[128], float* part) {
+    const int t0 = threadIdx.x;
+    const int lane = t0 & 31, warp = t0 >> 5;
+    const int ch = t0 & 15;
+    const int64_t NB = p.N / 128, K = p.KB * 128;
+    const int64_t nb = t % NB, kb = t / NB;
+    const int64_t n0 = nb * 128, k0 = kb * 128;
+    uint32_t mx = 0;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const uint4 u = *reinterpret_cast<const uint4*>(&tile[(t0 >> 4) + 16 * q][ch * 8]);
+        mx = absmax_bf16x2(mx, absmax_bf16x2(u.x, u.y));
+        mx = absmax_bf16x2(mx, absmax_bf16x2(u.z, u.w));
+    }
+    float amax = amax_of_pair(mx);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1)
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) part[warp] = amax;
+    __syncthreads();
+    amax = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
+                 fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
+    const float s = group_scale(amax);
+    const GroupDiv dv(s);
+    if (t0 == 0) p.sw[nb * p.KB + kb] = s;
+    if (p.wqT != nullptr) {
+#pragma unroll 4
+        for (int q = 0; q < 8; ++q) {
+            const int r = (t0 >> 4) + 16 * q;
+            const uint4 u = *reinterpret_cast<const uint4*>(&tile[r][ch * 8]);
+            uint2 o;
+            o.x = dv.quad(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+            o.y = dv.quad(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
+            *reinterpret_cast<uint2*>(p.wqT + (k0 + r) * p.N + n0 + ch * 8) = o;
+        }
+    }
+    if (p.wq != nullptr) {
+        // columns 2cp, 2cp+1; rows rq*32 .. rq*32+31 in two chunks of 16
+        // k values; codes staged as [n][k] rows with 16-byte chunks
+        // XOR-swizzled by n & 7, then written out as 128-byte rows of wq.
+        const int cp = t0 & 63;
+        const int rq = t0 >> 6;
+        uint4 oc[2][2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            uint32_t wv[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                wv[i] = *reinterpret_cast<const uint32_t*>(&tile[rq * 32 + h * 16 + i][2 * cp]);
+            uint4 o0, o1;
+            o0.x = dv.quad(bf16_lo(wv[0]), bf16_lo(wv[1]), bf16_lo(wv[2]), bf16_lo(wv[3]));
+            o0.y = dv.quad(bf16_lo(wv[4]), bf16_lo(wv[5]), bf16_lo(wv[6]), bf16_lo(wv[7]));
+            o0.z = dv.quad(bf16_lo(wv[8]), bf16_lo(wv[9]), bf16_lo(wv[10]), bf16_lo(wv[11]));
+            o0.w = dv.quad(bf16_lo(wv[12]), bf16_lo(wv[13]), bf16_lo(wv[14]), bf16_lo(wv[15]));
+            o1.x = dv.quad(bf16_hi(wv[0]), bf16_hi(wv[1]), bf16_hi(wv[2]), bf16_hi(wv[3]));
+            o1.y = dv.quad(bf16_hi(wv[4]), bf16_hi(wv[5]), bf16_hi(wv[6]), bf16_hi(wv[7]));
+            o1.z = dv.quad(bf16_hi(wv[8]), bf16_hi(wv[9]), bf16_hi(wv[10]), bf16_hi(wv[11]));
+            o1.w = dv.quad(bf16_hi(wv[12]), bf16_hi(wv[13]), bf16_hi(wv[14]), bf16_hi(wv[15]));
+            oc[h][0] = o0;
+            oc[h][1] = o1;
+        }
+        __syncthreads();  // every value of the block has been read
+        uint8_t* codes = reinterpret_cast<uint8_t*>(tile);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = rq * 2 + h;  // 16-byte chunk of the 128-byte k row
+            const int n_a = 2 * cp, n_b = 2 * cp + 1;
+            *reinterpret_cast<uint4*>(&codes[n_a * 128 + ((c ^ (n_a & 7)) << 4)]) = oc[h][0];
+            *reinterpret_cast<uint4*>(&codes[n_b * 128 + ((c ^ (n_b & 7)) << 4)]) = oc[h][1];
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int j = t0 + kPairThreads * i;  // chunk j: row n = j / 8, chunk c = j % 8
+            const int n = j >> 3, c = j & 7;
+            const uint4 v = *reinterpret_cast<const uint4*>(&codes[n * 128 + ((c ^ (n & 7)) << 4)]);
+            *reinterpret_cast<uint4*>(p.wq + (n0 + n) * K + k0 + c * 16) = v;
+        }
+    }
+    __syncthreads();
+}
+
+__global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm) quant_fprop_pair_kernel(const PairArgs p) {
+    extern __shared__ __align__(128) uint8_t pair_smem[];
+    __shared__ float part[kPairThreads / 32];
+    uint16_t (*tiles)[128][128] = reinterpret_cast<uint16_t (*)[128][128]>(pair_smem);
+    const int l4 = threadIdx.x & 3;
+    const int row = threadIdx.x >> 2;  // 0..63
+    const int64_t total = p.w_tiles + p.act_tiles;
+    int64_t i = blockIdx.x;  // item; the same in every thread of the CTA
+    int buf = 0;
+    uint4 v[4];
+    int64_t idx = 0;
+    bool is_w = false;
+    if (i < total) {
+        is_w = pair_item(p, i, &idx);
+        pair_issue(p, is_w, idx, tiles[0], row, l4, v);
+    }
+    cp_async_commit();
+    while (i < total) {
+        const int64_t in = i + gridDim.x;
+        uint4 vn[4];
+        int64_t idx_n = 0;
+        bool is_w_n = false;
+        if (in < total) {
+            is_w_n = pair_item(p, in, &idx_n);
+            pair_issue(p, is_w_n, idx_n, tiles[buf ^ 1], row, l4, vn);
+        }
+        cp_async_commit();  // possibly empty: one group per item keeps the count
+        if (is_w) {
+            cp_async_wait_prev();
+            __syncthreads();
+            pair_weight_block(p, idx, tiles[buf], part);
+        } else {
+            quant_1x128_tile(p.M, p.KB, p.xq, p.ldq, p.sx, idx, row, l4, v);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) v[k] = vn[k];
+        buf ^= 1;
+        i = in;
+        idx = idx_n;
+        is_w = is_w_n;
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
 // Persistent grid: as many CTAs as can be resident at once (cached per
 // kernel and device), never more than there are tiles.
 template <auto kern>
@@ -457,6 +660,65 @@ extern "C" int fp8_quant_weight_128x128(const void* w, int64_t K, int64_t N, int
     quant_weight_128x128_kernel<<<static_cast<unsigned>(tiles), kWThreads, 0,
                                   static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t*>(w), K, N, ldw, wq, wqT, sw, tiles);
+    return launch_status();
+}
+
+extern "C" int fp8_quant_fprop_operands(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                        uint8_t* xq, int64_t ldq, float* sx, const void* w,
+                                        int64_t N, int64_t ldw, uint8_t* wq, uint8_t* wqT,
+                                        float* sw, void* stream) {
+    if (M < 0 || K < 0 || K % 128 != 0 || N < 0 || N % 128 != 0) return FP8_ERR_SHAPE;
+    const bool act = M > 0 && K > 0, wgt = N > 0 && K > 0;
+    if (act && (ldx < K || ldq < K)) return FP8_ERR_SHAPE;
+    if (wgt && ldw < N) return FP8_ERR_SHAPE;
+    if (!act && !wgt) return FP8_OK;
+    if (act && (x == nullptr || xq == nullptr || sx == nullptr)) return FP8_ERR_NULL;
+    if (wgt && (w == nullptr || sw == nullptr || (wq == nullptr && wqT == nullptr)))
+        return FP8_ERR_NULL;
+    if (act && (ldx % 8 != 0 || ldq % 16 != 0 || !aligned(x, 16) || !aligned(xq, 16) ||
+                !aligned(sx, 4)))
+        return FP8_ERR_ALIGN;
+    if (wgt && (ldw % 8 != 0 || !aligned(w, 16) || !aligned(wq, 16) || !aligned(wqT, 16) ||
+                !aligned(sw, 4)))
+        return FP8_ERR_ALIGN;
+    PairArgs p;
+    p.x = static_cast<const uint16_t*>(x);
+    p.M = act ? M : 0;
+    p.ldx = ldx;
+    p.ldq = ldq;
+    p.xq = xq;
+    p.sx = sx;
+    p.act_tiles = act ? ((M + kQ1Rows - 1) / kQ1Rows) * (K / 128) : 0;
+    p.w = static_cast<const uint16_t*>(w);
+    p.N = wgt ? N : 128;
+    p.ldw = ldw;
+    p.wq = wq;
+    p.wqT = wqT;
+    p.sw = sw;
+    p.w_tiles = wgt ? (N / 128) * (K / 128) : 0;
+    p.KB = K / 128;
+    const int64_t total = p.act_tiles + p.w_tiles;
+    static int per_sm[kMaxDevices] = {0};
+    int dev = 0;
+    const int sms = sm_count_current(&dev);
+    if (sms <= 0) return FP8_ERR_CUDA;
+    if (per_sm[dev] == 0) {
+        if (cudaFuncSetAttribute(quant_fprop_pair_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem) !=
+            cudaSuccess)
+            return FP8_ERR_CUDA;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_fprop_pair_kernel,
+                                                          kPairThreads, kPairSmem) !=
+                cudaSuccess ||
+            n <= 0)
+            return FP8_ERR_CUDA;
+        per_sm[dev] = n < kPairCtasPerSm ? n : kPairCtasPerSm;
+    }
+    const int64_t cap = static_cast<int64_t>(sms) * per_sm[dev];
+    const int64_t grid = total < cap ? total : cap;
+    quant_fprop_pair_kernel<<<static_cast<unsigned>(grid), kPairThreads, kPairSmem,
+                              static_cast<cudaStream_t>(stream)>>>(p);
     return launch_status();
 }
 

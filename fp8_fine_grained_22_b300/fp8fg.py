@@ -24,6 +24,7 @@ FP8_BSCALE_BLOCK128_T = 2
 # every entry point of include/fp8fg.h
 EXPORTS = ("fp8_status_str", "fp8_device_error", "fp8_selftest_wait_timeout",
            "fp8_quant_act_1x128", "fp8_quant_act_128x1", "fp8_quant_weight_128x128",
+           "fp8_quant_fprop_operands",
            "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe", "fp8_grouped_gemm_moe_dgrad",
            "fp8_quant_act_128x1_grouped", "fp8_grouped_gemm_moe_wgrad",
            "fp8_moe_dispatch_workspace_size", "fp8_moe_dispatch_quant",
@@ -62,6 +63,9 @@ def lib() -> ctypes.CDLL:
         L.fp8_quant_act_128x1.argtypes = [P, I64, I64, I64, P, P, P]
         L.fp8_quant_weight_128x128.restype = I
         L.fp8_quant_weight_128x128.argtypes = [P, I64, I64, I64, P, P, P, P]
+        L.fp8_quant_fprop_operands.restype = I
+        L.fp8_quant_fprop_operands.argtypes = [P, I64, I64, I64, P, I64, P, P, I64, I64, P, P,
+                                               P, P]
         L.fp8_gemm_blockscaled.restype = I
         L.fp8_gemm_blockscaled.argtypes = [P, P, P, P, I, I64, I64, I64, P, I64, I, P]
         L.fp8_grouped_gemm_moe.restype = I
@@ -167,6 +171,38 @@ def fp8_quant_weight_128x128(w, wq=None, wqT=None, sw=None, want_wq=True, want_w
     _check(lib().fp8_quant_weight_128x128(_p(w), K, N, w.stride(0), _p(wq), _p(wqT), _p(sw),
                                           _stream(stream)), "fp8_quant_weight_128x128")
     return wq, wqT, sw
+
+
+def fp8_quant_fprop_operands(x, w, xq=None, sx=None, wq=None, wqT=None, sw=None, want_wq=True,
+                             want_wqT=False, stream=None):
+    """x: bf16 [M, K], w: bf16 [K, N] in one launch ->
+    (xq uint8 [M, K], sx f32 [K/128, M], wq [N, K] or None, wqT [K, N] or None,
+    sw f32 [N/128, K/128]); the same bits as fp8_quant_act_1x128 and
+    fp8_quant_weight_128x128."""
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(w, "w", torch.bfloat16)
+    assert x.dim() == 2 and x.stride(1) == 1 and w.dim() == 2 and w.stride(1) == 1
+    M, K = x.shape
+    K2, N = w.shape
+    if K != K2:
+        raise ValueError("x and w disagree on K: %d vs %d" % (K, K2))
+    dev = x.device
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
+    if sx is None:
+        sx = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
+    if wq is None and want_wq:
+        wq = torch.empty((N, K), dtype=torch.uint8, device=dev)
+    if wqT is None and want_wqT:
+        wqT = torch.empty((K, N), dtype=torch.uint8, device=dev)
+    if sw is None:
+        sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
+    assert xq.stride(1) == 1 and sx.is_contiguous() and sw.is_contiguous()
+    assert (wq is None or wq.is_contiguous()) and (wqT is None or wqT.is_contiguous())
+    _check(lib().fp8_quant_fprop_operands(_p(x), M, K, x.stride(0), _p(xq), xq.stride(0), _p(sx),
+                                          _p(w), N, w.stride(0), _p(wq), _p(wqT), _p(sw),
+                                          _stream(stream)), "fp8_quant_fprop_operands")
+    return xq, sx, wq, wqT, sw
 
 
 # -------------------------------------------------------------------- GEMMs --

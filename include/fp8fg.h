@@ -133,6 +133,24 @@ int fp8_quant_weight_128x128(const void* w, int64_t K, int64_t N, int64_t ldw,
                              uint8_t* wq, uint8_t* wqT, float* sw, void* stream);
 
 /*
+ * fp8_quant_fprop_operands -- both operands of one Fprop GEMM in a single
+ * launch: the activation quantised 1x128 exactly as fp8_quant_act_1x128 and
+ * the weight quantised 128x128 exactly as fp8_quant_weight_128x128 (report
+ * section 3.3.2, fine-grained quantization; the two groupings of one GEMM).
+ *   x, M, ldx, xq, ldq, sx : as fp8_quant_act_1x128 (x bfloat16 [M][K]).
+ *   w, N, ldw, wq, wqT, sw : as fp8_quant_weight_128x128 (w bfloat16 [K][N]).
+ *   K : the shared inner dimension, K % 128 == 0.
+ * Codes and scales are bit-identical to the two single-operand calls.  M == 0
+ * skips the activation (its pointers may be NULL), N == 0 the weight, and
+ * K == 0 returns FP8_OK without launching.  Every other requirement is the
+ * union of the two calls' requirements, checked before anything is launched.
+ */
+int fp8_quant_fprop_operands(const void* x, int64_t M, int64_t K, int64_t ldx,
+                             uint8_t* xq, int64_t ldq, float* sx,
+                             const void* w, int64_t N, int64_t ldw,
+                             uint8_t* wq, uint8_t* wqT, float* sw, void* stream);
+
+/*
  * fp8_gemm_blockscaled -- C[M][N] = sum_kb sa[m,kb] * sb(n,kb) * P_kb[m][n],
  * P_kb[m][n] = sum over k in [128 kb, 128 kb + 128) of aq[m][k] * bq[n][k]
  * (report section 3.3.2, Figure 7(b): tensor-core partial sums over each

@@ -64,6 +64,30 @@ def test_other_quantiser_validation():
     assert L.fp8_quant_weight_128x128(A16, 128, 128, 128, A16 + 8, 0, A16, None) == ALIGN
 
 
+
+def test_fprop_operands_validation():
+    L = fp8fg.lib()
+    q = L.fp8_quant_fprop_operands
+    # x, M, K, ldx, xq, ldq, sx, w, N, ldw, wq, wqT, sw, stream
+    assert q(A16, 4, 100, 128, A16, 128, A16, A16, 128, 128, A16, 0, A16, None) == SHAPE  # K % 128
+    assert q(A16, 4, 128, 128, A16, 128, A16, A16, 100, 128, A16, 0, A16, None) == SHAPE  # N % 128
+    assert q(A16, -1, 128, 128, A16, 128, A16, A16, 128, 128, A16, 0, A16, None) == SHAPE
+    assert q(A16, 4, 128, 64, A16, 128, A16, A16, 128, 128, A16, 0, A16, None) == SHAPE   # ldx < K
+    assert q(A16, 4, 128, 128, A16, 128, A16, A16, 128, 64, A16, 0, A16, None) == SHAPE   # ldw < N
+    assert q(0, 4, 128, 128, A16, 128, A16, A16, 128, 128, A16, 0, A16, None) == NULL
+    assert q(A16, 4, 128, 128, A16, 128, A16, A16, 128, 128, 0, 0, A16, None) == NULL     # no wq/wqT
+    assert q(A16, 4, 128, 128, A16, 128, A16, A16, 128, 128, A16, 0, 0, None) == NULL     # sw
+    assert q(A16 + 2, 4, 128, 128, A16, 128, A16, A16, 128, 128, A16, 0, A16, None) == ALIGN
+    assert q(A16, 4, 128, 128, A16, 136, A16, A16, 128, 128, A16, 0, A16, None) == ALIGN  # ldq % 16
+    assert q(A16, 4, 128, 128, A16, 128, A16, A16, 128, 128, A16 + 8, 0, A16, None) == ALIGN
+    assert q(A16, 4, 128, 128, A16, 128, A16, A16, 128, 132, A16, 0, A16, None) == ALIGN  # ldw % 8
+    # nothing to do: K == 0, or M == 0 and N == 0 (pointers unused)
+    assert q(0, 4, 0, 0, 0, 0, 0, 0, 128, 0, 0, 0, 0, None) == OK
+    assert q(0, 0, 128, 0, 0, 0, 0, 0, 0, 0, 0, 0, 0, None) == OK
+    # M == 0 still validates the weight half, N == 0 the activation half
+    assert q(0, 0, 128, 0, 0, 0, 0, 0, 128, 128, A16, 0, A16, None) == NULL
+    assert q(0, 4, 128, 128, A16, 128, A16, 0, 0, 0, 0, 0, 0, None) == NULL
+
 def test_gemm_validation():
     L = fp8fg.lib()
     g = L.fp8_gemm_blockscaled
