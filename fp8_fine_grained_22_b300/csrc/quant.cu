@@ -274,11 +274,13 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_128x1_grouped_kernel(
 // ---------------------------------------------------------------- 128x128 --
 // One 128-thread CTA per 128x128 block, copied global -> shared with
 // 16-byte cp.async (no register staging), so that every SM holds several
-// blocks in flight at once (32 KB of shared memory each).  The block amax
-// needs the whole block before any code is formed; the same-orientation
-// output is written row-wise and the transposed output two columns per
-// thread.
+// blocks in flight at once (32 KB of shared memory each, seven CTAs per SM:
+// the transposed codes are staged in the block's own buffer once every value
+// has been read).  The block amax needs the whole block before any code is
+// formed; the same-orientation output is written row-wise and the transposed
+// output two columns per thread.
 constexpr int kWThreads = 128;
+constexpr int kWCtasPerSm = 7;
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))), "l"(gmem)
@@ -288,13 +290,11 @@ __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
 }
 
-__global__ void __launch_bounds__(kWThreads) quant_weight_128x128_kernel(
+__global__ void __launch_bounds__(kWThreads, kWCtasPerSm) quant_weight_128x128_kernel(
     const uint16_t* __restrict__ w, int64_t K, int64_t N, int64_t ldw, uint8_t* __restrict__ wq,
     uint8_t* __restrict__ wqT, float* __restrict__ sw, int64_t tiles) {
     __shared__ __align__(16) uint16_t tile[128][128];
-    __shared__ __align__(16) uint8_t codes[128 * 128];  // transposed codes, [n][k] swizzled
-    // the warps' partial maxima use the first bytes of `codes` (48 KB static limit)
-    float* part = reinterpret_cast<float*>(codes);
+    __shared__ float part[kWThreads / 32];
     const int t0 = threadIdx.x;
     const int lane = t0 & 31, warp = t0 >> 5;
     const int ch = t0 & 15;
@@ -323,7 +323,6 @@ __global__ void __launch_bounds__(kWThreads) quant_weight_128x128_kernel(
     if (lane == 0) part[warp] = amax;
     __syncthreads();
     amax = fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3]));
-    __syncthreads();  // every thread has read `part` before `codes` is written
     const float s = group_scale(amax);
     const GroupDiv dv(s);
     if (t0 == 0) sw[nb * KB + kb] = s;
@@ -345,7 +344,8 @@ __global__ void __launch_bounds__(kWThreads) quant_weight_128x128_kernel(
         // then written out as whole 128-byte rows of wq.
         const int cp = t0 & 63;
         const int rh = t0 >> 6;
-#pragma unroll 1
+        uint4 oc[4][2];
+#pragma unroll
         for (int h = 0; h < 4; ++h) {
             uint32_t wv[16];
 #pragma unroll
@@ -360,10 +360,17 @@ __global__ void __launch_bounds__(kWThreads) quant_weight_128x128_kernel(
             o1.y = dv.quad(bf16_hi(wv[4]), bf16_hi(wv[5]), bf16_hi(wv[6]), bf16_hi(wv[7]));
             o1.z = dv.quad(bf16_hi(wv[8]), bf16_hi(wv[9]), bf16_hi(wv[10]), bf16_hi(wv[11]));
             o1.w = dv.quad(bf16_hi(wv[12]), bf16_hi(wv[13]), bf16_hi(wv[14]), bf16_hi(wv[15]));
+            oc[h][0] = o0;
+            oc[h][1] = o1;
+        }
+        __syncthreads();  // every value of the block has been read
+        uint8_t* codes = reinterpret_cast<uint8_t*>(tile);
+#pragma unroll
+        for (int h = 0; h < 4; ++h) {
             const int c = rh * 4 + h;  // 16-byte chunk of the 128-byte k row
             const int n_a = 2 * cp, n_b = 2 * cp + 1;
-            *reinterpret_cast<uint4*>(&codes[n_a * 128 + ((c ^ (n_a & 7)) << 4)]) = o0;
-            *reinterpret_cast<uint4*>(&codes[n_b * 128 + ((c ^ (n_b & 7)) << 4)]) = o1;
+            *reinterpret_cast<uint4*>(&codes[n_a * 128 + ((c ^ (n_a & 7)) << 4)]) = oc[h][0];
+            *reinterpret_cast<uint4*>(&codes[n_b * 128 + ((c ^ (n_b & 7)) << 4)]) = oc[h][1];
         }
         __syncthreads();
 #pragma unroll
