@@ -476,28 +476,58 @@ def run_moe(args, rank, world, local):
     disp_alone = kernel_ms(dispatch)
     gemm_alone = kernel_ms(grouped)
 
-    # end to end: tokens and routing in from pinned host memory, the R output rows out
+    # end to end: tokens and routing in from pinned host memory, the offsets
+    # and the R output rows out, every step; the copies of neighbouring steps
+    # overlap on two copy streams as in the dense bench (two buffer sets).
+    depth = 2
     xh, idh = x_tok.pin_memory(), order.pin_memory()
-    yh = torch.empty((R, N), dtype=torch.bfloat16).pin_memory()
-    offh = torch.empty(E + 1, dtype=torch.int32).pin_memory()
+    yh = [torch.empty((R, N), dtype=torch.bfloat16).pin_memory() for _ in range(depth)]
+    offh = [torch.empty(E + 1, dtype=torch.int32).pin_memory() for _ in range(depth)]
+    xs = [x] + [torch.empty_like(x) for _ in range(depth - 1)]
+    idss = [ids] + [torch.empty_like(ids) for _ in range(depth - 1)]
+    ys = [y] + [torch.empty_like(y) for _ in range(depth - 1)]
+    offs = [off] + [torch.empty_like(off) for _ in range(depth - 1)]
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(depth)]
+    ev_comp = [torch.cuda.Event() for _ in range(depth)]
+    ev_out = [torch.cuda.Event() for _ in range(depth)]
 
-    def e2e_step():
-        x.copy_(xh, non_blocking=True)
-        ids.copy_(idh, non_blocking=True)
-        step()
-        offh.copy_(off, non_blocking=True)
-        yh.copy_(y[:R], non_blocking=True)
+    def e2e_step(i):
+        sl = i % depth
+        up.wait_event(ev_comp[sl])
+        with torch.cuda.stream(up):
+            xs[sl].copy_(xh, non_blocking=True)
+            idss[sl].copy_(idh, non_blocking=True)
+        ev_in[sl].record(up)
+        stream.wait_event(ev_in[sl])
+        stream.wait_event(ev_out[sl])
+        fp8fg.fp8_moe_dispatch_quant(xs[sl], idss[sl], 0, E, cap=cap, xq=xq, sx=sx,
+                                     offsets=offs[sl], token_ids=tok, workspace=ws,
+                                     stream=stream)
+        fp8fg.fp8_grouped_gemm_moe(xq, sx, wq, sw, offs[sl], c=ys[sl], stream=stream)
+        ev_comp[sl].record(stream)
+        down.wait_event(ev_comp[sl])
+        with torch.cuda.stream(down):
+            offh[sl].copy_(offs[sl], non_blocking=True)
+            yh[sl].copy_(ys[sl][:R], non_blocking=True)
+        ev_out[sl].record(down)
 
     e2e_steps = min(steps, args.e2e_steps)
-    e2e_step()
+    for i in range(depth):
+        e2e_step(i)
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    b.record(stream)
+    a.record(up)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    b.record(down)
     torch.cuda.synchronize()
     e2e_ms = reduce_max(a.elapsed_time(b) / e2e_steps, dev)
+    last = (e2e_steps - 1) % depth
+    step()
+    torch.cuda.synchronize()
+    if not (torch.equal(offh[last], off.cpu()) and torch.equal(yh[last], y[:R].cpu())):
+        raise RuntimeError("end-to-end result differs from the device-resident step")
     if fp8fg.device_error() != 0:
         raise RuntimeError("device-side error")
 
