@@ -30,6 +30,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "ptx.cuh"
 #include "quant_math.cuh"
 
 namespace fp8fg {
@@ -100,6 +101,7 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
     const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ totals, int nchunks,
     int kb_per_slice, uint8_t* __restrict__ xq, float* __restrict__ sx, int64_t cap,
     int32_t* __restrict__ offsets, int32_t* __restrict__ token_ids) {
+    griddep_launch_dependents();  // the grouped GEMM that follows may set up meanwhile
     __shared__ int32_t s_ids[kChunk * kMaxTopk];
     __shared__ int32_t s_dest[kChunk * kMaxTopk];
     __shared__ int32_t s_base[kMaxLocal];

@@ -284,6 +284,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // Nothing above reads global memory.  The operands, scales and offsets
+    // may come from the kernel launched just before this one (the launch
+    // allows a programmatic dependency), so wait for it here.
+    griddep_wait();
     if (GROUPED) {
         // offsets[0] == 0, non-decreasing, offsets[E] <= T; checked by all threads
         bool bad = false;
@@ -689,7 +693,23 @@ static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t 
         return st;
     const int64_t grid = tiles_upper < sms ? tiles_upper : sms;
     if (grid <= 0) return FP8_OK;
-    kern<<<static_cast<unsigned>(grid), kThreads, C::SMEM, stream>>>(ta, tb, tc, p);
+    // Programmatic stream serialisation: the CTAs may be scheduled while the
+    // previous kernel on the stream finishes (once it allows it); they set
+    // up barriers and tensor memory, then wait for it in griddep_wait.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return FP8_ERR_CUDA;
+    }
     return launch_status();
 }
 

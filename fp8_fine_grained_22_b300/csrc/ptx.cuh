@@ -22,6 +22,21 @@ __device__ __forceinline__ bool elect_one() {
     return pred != 0;
 }
 
+// ---------------------------------------------- programmatic dependent launch
+// Blocks until the grid this one was launched to follow (programmatic stream
+// serialisation) has completed and its memory is visible; returns at once
+// for a grid launched without that attribute.
+__device__ __forceinline__ void griddep_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Allows the grid launched after this one with programmatic stream
+// serialisation to be scheduled once every CTA of this grid has executed
+// this instruction or exited.  It says nothing about memory: the dependent
+// grid still waits in griddep_wait for this grid to complete.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------ mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");

@@ -16,6 +16,7 @@
 #include <cuda_fp8.h>
 
 #include "common.cuh"
+#include "ptx.cuh"
 #include "quant_math.cuh"
 
 namespace fp8fg {
@@ -87,6 +88,7 @@ __device__ __forceinline__ void quant_1x128_tile(int64_t M, int64_t KB, uint8_t*
 __global__ void __launch_bounds__(kQuantThreads) quant_act_1x128_kernel(
     const uint16_t* __restrict__ x, int64_t M, int64_t KB, int64_t ldx, uint8_t* __restrict__ xq,
     int64_t ldq, float* __restrict__ sx, int64_t tiles) {
+    griddep_launch_dependents();  // the GEMM that follows may set up meanwhile
     const int l4 = threadIdx.x & 3;
     const int row = threadIdx.x >> 2;  // 0..63
     int64_t t = blockIdx.x;
@@ -122,6 +124,7 @@ __device__ __forceinline__ void load_128x1(const uint16_t* __restrict__ x, int64
 __global__ void __launch_bounds__(kQuantThreads) quant_act_128x1_kernel(
     const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t ldx, uint8_t* __restrict__ xqT,
     float* __restrict__ sxT, int64_t tiles) {
+    griddep_launch_dependents();  // the GEMM that follows may set up meanwhile
     __shared__ __align__(16) uint16_t tile[128][64];
     __shared__ float part[4][64];
     const int t0 = threadIdx.x;
@@ -189,6 +192,7 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_128x1_grouped_kernel(
     const uint16_t* __restrict__ x, int64_t T, int64_t K, int64_t ldx,
     const int32_t* __restrict__ offsets, int E, uint8_t* __restrict__ xqT,
     float* __restrict__ sxT, int64_t Tp, int32_t* __restrict__ pofs) {
+    griddep_launch_dependents();  // the GEMM that follows may set up meanwhile
     __shared__ __align__(16) uint16_t tile[128][64];
     __shared__ float part[4][64];
     __shared__ int64_t s_m0, s_p0;
@@ -293,6 +297,7 @@ __device__ __forceinline__ void cp_async_wait_all() {
 __global__ void __launch_bounds__(kWThreads, kWCtasPerSm) quant_weight_128x128_kernel(
     const uint16_t* __restrict__ w, int64_t K, int64_t N, int64_t ldw, uint8_t* __restrict__ wq,
     uint8_t* __restrict__ wqT, float* __restrict__ sw, int64_t tiles) {
+    griddep_launch_dependents();  // the GEMM that follows may set up meanwhile
     __shared__ __align__(16) uint16_t tile[128][128];
     __shared__ float part[kWThreads / 32];
     const int t0 = threadIdx.x;
@@ -535,6 +540,7 @@ __device__ __forceinline__ void pair_weight_block(const PairArgs& p, int64_t t,
 }
 
 __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm) quant_fprop_pair_kernel(const PairArgs p) {
+    griddep_launch_dependents();  // the GEMM that follows may set up meanwhile
     extern __shared__ __align__(128) uint8_t pair_smem[];
     __shared__ float part[kPairThreads / 32];
     uint16_t (*tiles)[128][128] = reinterpret_cast<uint16_t (*)[128][128]>(pair_smem);
