@@ -241,10 +241,8 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
         uint4 o[2];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t a = dv.quad(bf16_lo(q[i].x), bf16_hi(q[i].x), bf16_lo(q[i].y),
-                                       bf16_hi(q[i].y));
-            const uint32_t b = dv.quad(bf16_lo(q[i].z), bf16_hi(q[i].z), bf16_lo(q[i].w),
-                                       bf16_hi(q[i].w));
+            const uint32_t a = dv.quad_words(q[i].x, q[i].y);
+            const uint32_t b = dv.quad_words(q[i].z, q[i].w);
             if (i & 1) {
                 o[i >> 1].z = a;
                 o[i >> 1].w = b;

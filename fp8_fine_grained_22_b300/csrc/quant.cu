@@ -66,10 +66,8 @@ __device__ __forceinline__ void quant_1x128_tile(int64_t M, int64_t KB, uint8_t*
         uint4 o[2];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t a = dv.quad(bf16_lo(v[i].x), bf16_hi(v[i].x), bf16_lo(v[i].y),
-                                       bf16_hi(v[i].y));
-            const uint32_t b = dv.quad(bf16_lo(v[i].z), bf16_hi(v[i].z), bf16_lo(v[i].w),
-                                       bf16_hi(v[i].w));
+            const uint32_t a = dv.quad_words(v[i].x, v[i].y);
+            const uint32_t b = dv.quad_words(v[i].z, v[i].w);
             if (i & 1) {
                 o[i >> 1].z = a;
                 o[i >> 1].w = b;
@@ -337,8 +335,8 @@ __global__ void __launch_bounds__(kWThreads, kWCtasPerSm) quant_weight_128x128_k
             const int row = (t0 >> 4) + 8 * p;
             const uint4 u = *reinterpret_cast<const uint4*>(&tile[row][ch * 8]);
             uint2 q;
-            q.x = dv.quad(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
-            q.y = dv.quad(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
+            q.x = dv.quad_words(u.x, u.y);
+            q.y = dv.quad_words(u.z, u.w);
             *reinterpret_cast<uint2*>(wqT + (k0 + row) * N + n0 + ch * 8) = q;
         }
     }
@@ -357,14 +355,10 @@ __global__ void __launch_bounds__(kWThreads, kWCtasPerSm) quant_weight_128x128_k
             for (int i = 0; i < 16; ++i)
                 wv[i] = *reinterpret_cast<const uint32_t*>(&tile[rh * 64 + h * 16 + i][2 * cp]);
             uint4 o0, o1;
-            o0.x = dv.quad(bf16_lo(wv[0]), bf16_lo(wv[1]), bf16_lo(wv[2]), bf16_lo(wv[3]));
-            o0.y = dv.quad(bf16_lo(wv[4]), bf16_lo(wv[5]), bf16_lo(wv[6]), bf16_lo(wv[7]));
-            o0.z = dv.quad(bf16_lo(wv[8]), bf16_lo(wv[9]), bf16_lo(wv[10]), bf16_lo(wv[11]));
-            o0.w = dv.quad(bf16_lo(wv[12]), bf16_lo(wv[13]), bf16_lo(wv[14]), bf16_lo(wv[15]));
-            o1.x = dv.quad(bf16_hi(wv[0]), bf16_hi(wv[1]), bf16_hi(wv[2]), bf16_hi(wv[3]));
-            o1.y = dv.quad(bf16_hi(wv[4]), bf16_hi(wv[5]), bf16_hi(wv[6]), bf16_hi(wv[7]));
-            o1.z = dv.quad(bf16_hi(wv[8]), bf16_hi(wv[9]), bf16_hi(wv[10]), bf16_hi(wv[11]));
-            o1.w = dv.quad(bf16_hi(wv[12]), bf16_hi(wv[13]), bf16_hi(wv[14]), bf16_hi(wv[15]));
+            dv.quad_halves(wv[0], wv[1], wv[2], wv[3], o0.x, o1.x);
+            dv.quad_halves(wv[4], wv[5], wv[6], wv[7], o0.y, o1.y);
+            dv.quad_halves(wv[8], wv[9], wv[10], wv[11], o0.z, o1.z);
+            dv.quad_halves(wv[12], wv[13], wv[14], wv[15], o0.w, o1.w);
             oc[h][0] = o0;
             oc[h][1] = o1;
         }
@@ -488,8 +482,8 @@ __device__ __forceinline__ void pair_weight_block(const PairArgs& p, int64_t t,
             const int r = (t0 >> 4) + 16 * q;
             const uint4 u = *reinterpret_cast<const uint4*>(&tile[r][ch * 8]);
             uint2 o;
-            o.x = dv.quad(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
-            o.y = dv.quad(bf16_lo(u.z), bf16_hi(u.z), bf16_lo(u.w), bf16_hi(u.w));
+            o.x = dv.quad_words(u.x, u.y);
+            o.y = dv.quad_words(u.z, u.w);
             *reinterpret_cast<uint2*>(p.wqT + (k0 + r) * p.N + n0 + ch * 8) = o;
         }
     }
@@ -507,14 +501,10 @@ __device__ __forceinline__ void pair_weight_block(const PairArgs& p, int64_t t,
             for (int i = 0; i < 16; ++i)
                 wv[i] = *reinterpret_cast<const uint32_t*>(&tile[rq * 32 + h * 16 + i][2 * cp]);
             uint4 o0, o1;
-            o0.x = dv.quad(bf16_lo(wv[0]), bf16_lo(wv[1]), bf16_lo(wv[2]), bf16_lo(wv[3]));
-            o0.y = dv.quad(bf16_lo(wv[4]), bf16_lo(wv[5]), bf16_lo(wv[6]), bf16_lo(wv[7]));
-            o0.z = dv.quad(bf16_lo(wv[8]), bf16_lo(wv[9]), bf16_lo(wv[10]), bf16_lo(wv[11]));
-            o0.w = dv.quad(bf16_lo(wv[12]), bf16_lo(wv[13]), bf16_lo(wv[14]), bf16_lo(wv[15]));
-            o1.x = dv.quad(bf16_hi(wv[0]), bf16_hi(wv[1]), bf16_hi(wv[2]), bf16_hi(wv[3]));
-            o1.y = dv.quad(bf16_hi(wv[4]), bf16_hi(wv[5]), bf16_hi(wv[6]), bf16_hi(wv[7]));
-            o1.z = dv.quad(bf16_hi(wv[8]), bf16_hi(wv[9]), bf16_hi(wv[10]), bf16_hi(wv[11]));
-            o1.w = dv.quad(bf16_hi(wv[12]), bf16_hi(wv[13]), bf16_hi(wv[14]), bf16_hi(wv[15]));
+            dv.quad_halves(wv[0], wv[1], wv[2], wv[3], o0.x, o1.x);
+            dv.quad_halves(wv[4], wv[5], wv[6], wv[7], o0.y, o1.y);
+            dv.quad_halves(wv[8], wv[9], wv[10], wv[11], o0.z, o1.z);
+            dv.quad_halves(wv[12], wv[13], wv[14], wv[15], o0.w, o1.w);
             oc[h][0] = o0;
             oc[h][1] = o1;
         }

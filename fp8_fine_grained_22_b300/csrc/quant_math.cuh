@@ -78,6 +78,54 @@ struct GroupDiv {
     __device__ __forceinline__ uint32_t quad(float a, float b, float c, float d) const {
         return pair(a, b) | (pair(c, d) << 16);
     }
+
+    // As pair(), but a zero quotient may carry the wrong sign: the callers
+    // below set every code's sign bit from its input instead, one permute
+    // for four inputs (for a nonzero quotient that bit is already right).
+    __device__ __forceinline__ uint32_t pair_unsigned(float x0, float x1) const {
+        float q0, q1;
+        if (fast) {
+            const uint64_t x2 = f2x2(x0, x1);
+            const uint64_t a = mul2(x2, r2);
+            const uint64_t e = fma2(a, ns2, x2);
+            const uint64_t q = fma2(e, r2, a);
+            q0 = __uint_as_float(static_cast<uint32_t>(q));
+            q1 = __uint_as_float(static_cast<uint32_t>(q >> 32));
+        } else {
+            q0 = __fdiv_rn(x0, s);
+            q1 = __fdiv_rn(x1, s);
+        }
+        return static_cast<uint32_t>(
+            __nv_cvt_float2_to_fp8x2(make_float2(q0, q1), __NV_SATFINITE, __NV_E4M3));
+    }
+    // Codes of the four bf16 values of words w0, w1 in memory order
+    // (lo w0, hi w0, lo w1, hi w1), packed little-endian.
+    __device__ __forceinline__ uint32_t quad_words(uint32_t w0, uint32_t w1) const {
+        const uint32_t c = pair_unsigned(bf16_lo(w0), bf16_hi(w0)) |
+                           (pair_unsigned(bf16_lo(w1), bf16_hi(w1)) << 16);
+        return c | (sign_bytes(w0, w1) & 0x80808080u);
+    }
+    // Codes of the low halves (lo) and of the high halves (hi) of four words.
+    __device__ __forceinline__ void quad_halves(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
+                                                uint32_t& lo, uint32_t& hi) const {
+        const uint32_t s01 = sign_bytes(w0, w1), s23 = sign_bytes(w2, w3);
+        lo = pair_unsigned(bf16_lo(w0), bf16_lo(w1)) | (pair_unsigned(bf16_lo(w2), bf16_lo(w3)) << 16);
+        hi = pair_unsigned(bf16_hi(w0), bf16_hi(w1)) | (pair_unsigned(bf16_hi(w2), bf16_hi(w3)) << 16);
+        lo |= byte_perm(s01, s23, 0x6420) & 0x80808080u;
+        hi |= byte_perm(s01, s23, 0x7531) & 0x80808080u;
+    }
+
+  private:
+    __device__ __forceinline__ static uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
+        uint32_t d;
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+        return d;
+    }
+    // 0xFF or 0x00 per byte: the signs of (lo w0, hi w0, lo w1, hi w1), each
+    // the top bit of a bf16's high byte (bytes 1, 3, 5, 7) replicated.
+    __device__ __forceinline__ static uint32_t sign_bytes(uint32_t w0, uint32_t w1) {
+        return byte_perm(w0, w1, 0xFDB9);
+    }
 };
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
