@@ -274,117 +274,21 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_128x1_grouped_kernel(
 }
 
 // ---------------------------------------------------------------- 128x128 --
-// One 128-thread CTA per 128x128 block, copied global -> shared with
-// 16-byte cp.async (no register staging), so that every SM holds several
-// blocks in flight at once (32 KB of shared memory each, seven CTAs per SM:
-// the transposed codes are staged in the block's own buffer once every value
-// has been read).  The block amax needs the whole block before any code is
-// formed; the same-orientation output is written row-wise and the transposed
-// output two columns per thread.
-constexpr int kWThreads = 128;
-constexpr int kWCtasPerSm = 7;
+// The weight quantiser is the persistent kernel below run on weight blocks
+// alone: one grid walks the blocks with a stride of the grid size, each CTA
+// converting one 128x128 block from shared memory while the cp.async copy
+// of its next block lands in a second buffer.  (One 128-thread CTA per
+// block, without that overlap, was 7-15 % slower at every measured shape:
+// the grid ran in whole waves of load, reduce, convert and store.)
 
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(static_cast<uint32_t>(__cvta_generic_to_shared(smem))), "l"(gmem)
                  : "memory");
 }
-__device__ __forceinline__ void cp_async_wait_all() {
-    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
-}
-
-__global__ void __launch_bounds__(kWThreads, kWCtasPerSm) quant_weight_128x128_kernel(
-    const uint16_t* __restrict__ w, int64_t K, int64_t N, int64_t ldw, uint8_t* __restrict__ wq,
-    uint8_t* __restrict__ wqT, float* __restrict__ sw, int64_t tiles) {
-    griddep_launch_dependents();  // the GEMM that follows may set up meanwhile
-    __shared__ __align__(16) uint16_t tile[128][128];
-    __shared__ float part[kWThreads / 32];
-    const int t0 = threadIdx.x;
-    const int lane = t0 & 31, warp = t0 >> 5;
-    const int ch = t0 & 15;
-    const int64_t NB = N / 128, KB = K / 128;
-    const int64_t t = blockIdx.x;
-    const int64_t nb = t % NB, kb = t / NB;
-    const int64_t n0 = nb * 128, k0 = kb * 128;
-#pragma unroll
-    for (int p = 0; p < 16; ++p) {
-        const int row = (t0 >> 4) + 8 * p;
-        cp_async16(&tile[row][ch * 8], w + (k0 + row) * ldw + n0 + ch * 8);
-    }
-    cp_async_wait_all();
-    __syncthreads();
-    uint32_t mx = 0;
-#pragma unroll
-    for (int p = 0; p < 16; ++p) {
-        const uint4 u = *reinterpret_cast<const uint4*>(&tile[(t0 >> 4) + 8 * p][ch * 8]);
-        mx = absmax_bf16x2(mx, absmax_bf16x2(u.x, u.y));
-        mx = absmax_bf16x2(mx, absmax_bf16x2(u.z, u.w));
-    }
-    float amax = amax_of_pair(mx);
-#pragma unroll
-    for (int off = 16; off >= 1; off >>= 1)
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    if (lane == 0) part[warp] = amax;
-    __syncthreads();
-    amax = fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3]));
-    const float s = group_scale(amax);
-    const GroupDiv dv(s);
-    if (t0 == 0) sw[nb * KB + kb] = s;
-    if (wqT != nullptr) {
-#pragma unroll 4
-        for (int p = 0; p < 16; ++p) {
-            const int row = (t0 >> 4) + 8 * p;
-            const uint4 u = *reinterpret_cast<const uint4*>(&tile[row][ch * 8]);
-            uint2 q;
-            q.x = dv.quad_words(u.x, u.y);
-            q.y = dv.quad_words(u.z, u.w);
-            *reinterpret_cast<uint2*>(wqT + (k0 + row) * N + n0 + ch * 8) = q;
-        }
-    }
-    if (wq != nullptr) {
-        // columns 2cp and 2cp+1 of the block, rows rh*64 .. rh*64+63: one
-        // 32-bit shared load gives both columns of a row.  The codes go to a
-        // shared [n][k] tile (16-byte chunks XOR-swizzled by n & 7) and are
-        // then written out as whole 128-byte rows of wq.
-        const int cp = t0 & 63;
-        const int rh = t0 >> 6;
-        uint4 oc[4][2];
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            uint32_t wv[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                wv[i] = *reinterpret_cast<const uint32_t*>(&tile[rh * 64 + h * 16 + i][2 * cp]);
-            uint4 o0, o1;
-            dv.quad_halves(wv[0], wv[1], wv[2], wv[3], o0.x, o1.x);
-            dv.quad_halves(wv[4], wv[5], wv[6], wv[7], o0.y, o1.y);
-            dv.quad_halves(wv[8], wv[9], wv[10], wv[11], o0.z, o1.z);
-            dv.quad_halves(wv[12], wv[13], wv[14], wv[15], o0.w, o1.w);
-            oc[h][0] = o0;
-            oc[h][1] = o1;
-        }
-        __syncthreads();  // every value of the block has been read
-        uint8_t* codes = reinterpret_cast<uint8_t*>(tile);
-#pragma unroll
-        for (int h = 0; h < 4; ++h) {
-            const int c = rh * 4 + h;  // 16-byte chunk of the 128-byte k row
-            const int n_a = 2 * cp, n_b = 2 * cp + 1;
-            *reinterpret_cast<uint4*>(&codes[n_a * 128 + ((c ^ (n_a & 7)) << 4)]) = oc[h][0];
-            *reinterpret_cast<uint4*>(&codes[n_b * 128 + ((c ^ (n_b & 7)) << 4)]) = oc[h][1];
-        }
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int j = t0 + kWThreads * i;  // chunk j: row n = j / 8, chunk c = j % 8
-            const int n = j >> 3, c = j & 7;
-            const uint4 v = *reinterpret_cast<const uint4*>(&codes[n * 128 + ((c ^ (n & 7)) << 4)]);
-            *reinterpret_cast<uint4*>(wq + (n0 + n) * K + k0 + c * 16) = v;
-        }
-    }
-}
 
 // ------------------------------------------------- both Fprop operands --
 // One persistent launch quantises the activation (1x128) and the weight
-// (128x128) of one GEMM.  Run as two kernels, the operands serialise: each
+// (128x128) of one GEMM, or the weight alone.  Run as two kernels, the operands serialise: each
 // kernel fills the SMs on its own, and neither is large enough to reach the
 // HBM rate alone.  Here one grid walks a single list of items, weight blocks
 // spread evenly among the activation tiles, with a stride of the grid size,
@@ -650,6 +554,34 @@ extern "C" int fp8_quant_act_128x1_grouped(const void* x, int64_t T, int64_t K, 
     return launch_status();
 }
 
+// Persistent grid of the operand kernel: as many CTAs as are resident (at
+// most kPairCtasPerSm per SM), never more than there are items.
+static int launch_pair(const PairArgs& p, cudaStream_t stream) {
+    const int64_t total = p.act_tiles + p.w_tiles;
+    if (total == 0) return FP8_OK;
+    static int per_sm[kMaxDevices] = {0};
+    int dev = 0;
+    const int sms = sm_count_current(&dev);
+    if (sms <= 0) return FP8_ERR_CUDA;
+    if (per_sm[dev] == 0) {
+        if (cudaFuncSetAttribute(quant_fprop_pair_kernel,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem) !=
+            cudaSuccess)
+            return FP8_ERR_CUDA;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_fprop_pair_kernel,
+                                                          kPairThreads, kPairSmem) !=
+                cudaSuccess ||
+            n <= 0)
+            return FP8_ERR_CUDA;
+        per_sm[dev] = n < kPairCtasPerSm ? n : kPairCtasPerSm;
+    }
+    const int64_t cap = static_cast<int64_t>(sms) * per_sm[dev];
+    const int64_t grid = total < cap ? total : cap;
+    quant_fprop_pair_kernel<<<static_cast<unsigned>(grid), kPairThreads, kPairSmem, stream>>>(p);
+    return launch_status();
+}
+
 extern "C" int fp8_quant_weight_128x128(const void* w, int64_t K, int64_t N, int64_t ldw,
                                         uint8_t* wq, uint8_t* wqT, float* sw, void* stream) {
     if (K < 0 || K % 128 != 0 || N < 0 || N % 128 != 0 || ldw < N) return FP8_ERR_SHAPE;
@@ -658,12 +590,16 @@ extern "C" int fp8_quant_weight_128x128(const void* w, int64_t K, int64_t N, int
     if (ldw % 8 != 0 || !aligned(w, 16) || !aligned(wq, 16) || !aligned(wqT, 16) ||
         !aligned(sw, 4))
         return FP8_ERR_ALIGN;
-    const int64_t tiles = (N / 128) * (K / 128);
-    if (tiles > 0x7fffffffLL) return FP8_ERR_UNSUPPORTED;
-    quant_weight_128x128_kernel<<<static_cast<unsigned>(tiles), kWThreads, 0,
-                                  static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(w), K, N, ldw, wq, wqT, sw, tiles);
-    return launch_status();
+    PairArgs p = {};
+    p.w = static_cast<const uint16_t*>(w);
+    p.N = N;
+    p.ldw = ldw;
+    p.wq = wq;
+    p.wqT = wqT;
+    p.sw = sw;
+    p.w_tiles = (N / 128) * (K / 128);
+    p.KB = K / 128;
+    return launch_pair(p, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fp8_quant_fprop_operands(const void* x, int64_t M, int64_t K, int64_t ldx,
@@ -700,29 +636,7 @@ extern "C" int fp8_quant_fprop_operands(const void* x, int64_t M, int64_t K, int
     p.sw = sw;
     p.w_tiles = wgt ? (N / 128) * (K / 128) : 0;
     p.KB = K / 128;
-    const int64_t total = p.act_tiles + p.w_tiles;
-    static int per_sm[kMaxDevices] = {0};
-    int dev = 0;
-    const int sms = sm_count_current(&dev);
-    if (sms <= 0) return FP8_ERR_CUDA;
-    if (per_sm[dev] == 0) {
-        if (cudaFuncSetAttribute(quant_fprop_pair_kernel,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem) !=
-            cudaSuccess)
-            return FP8_ERR_CUDA;
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_fprop_pair_kernel,
-                                                          kPairThreads, kPairSmem) !=
-                cudaSuccess ||
-            n <= 0)
-            return FP8_ERR_CUDA;
-        per_sm[dev] = n < kPairCtasPerSm ? n : kPairCtasPerSm;
-    }
-    const int64_t cap = static_cast<int64_t>(sms) * per_sm[dev];
-    const int64_t grid = total < cap ? total : cap;
-    quant_fprop_pair_kernel<<<static_cast<unsigned>(grid), kPairThreads, kPairSmem,
-                              static_cast<cudaStream_t>(stream)>>>(p);
-    return launch_status();
+    return launch_pair(p, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" const char* fp8_status_str(int status) {
