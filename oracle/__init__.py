@@ -11,6 +11,10 @@ numpy arrays into it.
 
 Conventions: bfloat16 tensors are passed as ``uint16`` numpy arrays holding
 the raw bfloat16 bit patterns; E4M3 codes are ``uint8`` arrays.
+
+When the environment variable ``FP8FG_ORACLE_LIB`` names a library, that
+library is loaded instead of the built ``liboracle.so``: the mutant tests use
+it to run the oracle's pins against deliberately broken builds.
 """
 from __future__ import annotations
 
@@ -31,9 +35,12 @@ BSCALE_BLOCK128_T = 2  # sb[K/128][N/128]
 def _load():
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            _build()
-        lib = ctypes.CDLL(LIB_PATH)
+        path = os.environ.get("FP8FG_ORACLE_LIB")
+        if not path:
+            path = LIB_PATH
+            if not os.path.exists(path):
+                _build()
+        lib = ctypes.CDLL(path)
         P = ctypes.c_void_p
         I64 = ctypes.c_int64
         lib.fo_e4m3_encode.restype = ctypes.c_uint8
