@@ -27,6 +27,11 @@
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  *     are asynchronous on that stream and never synchronise, except
  *     fp8_device_error().
+ *   - The GEMM entry points launch with programmatic stream serialisation:
+ *     their CTAs may start setting up (barriers, tensor memory) while the
+ *     kernel before them on the stream finishes, and read nothing from
+ *     global memory until that kernel has completed.  Stream order, as the
+ *     caller sees it, is unchanged.
  *   - Arguments are validated on the host before anything is launched; a
  *     rejected call launches nothing and returns a status != FP8_OK.  Launch
  *     failures come back as FP8_ERR_CUDA.  Nothing throws across the ABI.
