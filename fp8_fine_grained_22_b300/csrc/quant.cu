@@ -21,10 +21,11 @@
 
 namespace fp8fg {
 
-// All three kernels are persistent: a grid of a few CTAs per SM walks the
-// tiles with a stride of the grid size, and each thread issues the loads of
-// its next tile before it processes the current one, so HBM reads stay in
-// flight through the compute and store phases.
+// The 1x128, 128x1 and operand (128x128) kernels are persistent: a grid of a
+// few CTAs per SM walks the tiles with a stride of the grid size, and each
+// thread issues the loads of its next tile before it processes the current
+// one, so HBM reads stay in flight through the compute and store phases.
+// The per-expert 128x1 kernel runs one CTA per (token group, column block).
 constexpr int kQuantThreads = 256;
 constexpr int kQuantCtasPerSm = 4;
 
