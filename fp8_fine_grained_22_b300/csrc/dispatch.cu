@@ -320,27 +320,31 @@ static int dispatch_launch(const void* x, int64_t T, int64_t K, int64_t ldx,
 constexpr size_t kDispatchScratchInts = static_cast<size_t>(1) << 16;
 static __device__ __align__(256) int32_t g_dispatch_scratch[kDispatchScratchInts];
 
-// Device address of g_dispatch_scratch on the current device, looked up once
-// per device (with that device current) and cached; nullptr on failure.
+// Device address of g_dispatch_scratch in the CUDA context current on this
+// thread, or nullptr.  Host code cannot use the array's name as a device
+// address; the runtime's cudaGetSymbolAddress gives it, for the module as
+// loaded into the current context.  It is looked up once per (device,
+// context) -- with that context current -- and cached together with the
+// context's id, so a call made in another context of the same device (a
+// driver-API context of the caller's, or the primary context re-created
+// after cudaDeviceReset) looks it up again instead of reusing an address
+// that is not valid there.
 static int32_t* dispatch_scratch() {
-    static int32_t* cached[kMaxDevices] = {nullptr};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-    if (cached[dev] == nullptr) {
-        int32_t* ptr = nullptr;
-        if (cudaGetSymbolAddress(reinterpret_cast<void**>(&ptr), g_dispatch_scratch) !=
-            cudaSuccess)
-            return nullptr;
-        cached[dev] = ptr;
-    }
-    return cached[dev];
+    static ContextCache<int32_t*> cache;
+    int32_t* ptr = nullptr;
+    const int st = cache.get(&ptr, [](int32_t** v) {
+        if (cudaGetSymbolAddress(reinterpret_cast<void**>(v), g_dispatch_scratch) != cudaSuccess)
+            return static_cast<int>(FP8_ERR_CUDA);
+        return static_cast<int>(FP8_OK);
+    });
+    return st == FP8_OK ? ptr : nullptr;
 }
 
 }  // namespace fp8fg
 
 using namespace fp8fg;
 
-extern "C" int fp8_moe_dispatch_workspace_size(int64_t T, int32_t n_local, size_t* bytes) {
+extern "C" fp8_status fp8_moe_dispatch_workspace_size(int64_t T, int32_t n_local, size_t* bytes) {
     if (bytes == nullptr) return FP8_ERR_NULL;
     *bytes = 0;
     if (T < 0 || n_local < 1 || n_local > kMaxLocal) return FP8_ERR_SHAPE;
@@ -349,14 +353,14 @@ extern "C" int fp8_moe_dispatch_workspace_size(int64_t T, int32_t n_local, size_
     return FP8_OK;
 }
 
-extern "C" int fp8_moe_dispatch_quant(const void* x, int64_t T, int64_t K, int64_t ldx,
+extern "C" fp8_status fp8_moe_dispatch_quant(const void* x, int64_t T, int64_t K, int64_t ldx,
                                       const int32_t* topk_ids, int32_t topk,
                                       int32_t expert_begin, int32_t n_local, uint8_t* xq,
                                       float* sx, int64_t cap, int32_t* offsets,
                                       int32_t* token_ids, void* workspace,
                                       size_t workspace_bytes, void* stream) {
     int st = dispatch_checks(T, K, ldx, topk, n_local, cap);
-    if (st != FP8_OK) return st;
+    if (st != FP8_OK) return to_status(st);
     if (offsets == nullptr) return FP8_ERR_NULL;
     if (!aligned(offsets, 4)) return FP8_ERR_ALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -374,17 +378,17 @@ extern "C" int fp8_moe_dispatch_quant(const void* x, int64_t T, int64_t K, int64
         !aligned(topk_ids, 4) || !aligned(token_ids, 4) || !aligned(workspace, 256))
         return FP8_ERR_ALIGN;
     if (workspace_bytes < dispatch_plan(T, n_local).bytes) return FP8_ERR_SHAPE;
-    return dispatch_launch(x, T, K, ldx, topk_ids, topk, expert_begin, n_local, xq, sx, cap,
-                           offsets, token_ids, static_cast<int32_t*>(workspace), s);
+    return to_status(dispatch_launch(x, T, K, ldx, topk_ids, topk, expert_begin, n_local, xq, sx, cap,
+                           offsets, token_ids, static_cast<int32_t*>(workspace), s));
 }
 
-extern "C" int fp8_moe_dispatch_quant_noalloc(const void* x, int64_t T, int64_t K, int64_t ldx,
+extern "C" fp8_status fp8_moe_dispatch_quant_noalloc(const void* x, int64_t T, int64_t K, int64_t ldx,
                                               const int32_t* topk_ids, int32_t topk,
                                               int32_t expert_begin, int32_t n_local, uint8_t* xq,
                                               float* sx, int64_t cap, int32_t* offsets,
                                               int32_t* token_ids, void* stream) {
     int st = dispatch_checks(T, K, ldx, topk, n_local, cap);
-    if (st != FP8_OK) return st;
+    if (st != FP8_OK) return to_status(st);
     if (offsets == nullptr) return FP8_ERR_NULL;
     if (!aligned(offsets, 4)) return FP8_ERR_ALIGN;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -406,6 +410,6 @@ extern "C" int fp8_moe_dispatch_quant_noalloc(const void* x, int64_t T, int64_t 
         return FP8_ERR_UNSUPPORTED;
     int32_t* scratch = dispatch_scratch();
     if (scratch == nullptr) return FP8_ERR_CUDA;
-    return dispatch_launch(x, T, K, ldx, topk_ids, topk, expert_begin, n_local, xq, sx, cap,
-                           offsets, token_ids, scratch, s);
+    return to_status(dispatch_launch(x, T, K, ldx, topk_ids, topk, expert_begin, n_local, xq, sx, cap,
+                           offsets, token_ids, scratch, s));
 }

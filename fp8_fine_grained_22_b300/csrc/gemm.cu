@@ -663,20 +663,24 @@ static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t 
                   const GemmParams& p, int64_t tiles_upper, cudaStream_t stream) {
     using C = Cfg<BN, ROWSCALE>;
     auto kern = gemm_blockscaled_kernel<BN, OUT_BF16, ROWSCALE, GM>;
-    int dev = 0;
-    const int sms = sm_count_current(&dev);
+    const int sms = sm_count_current();
     if (sms <= 0) return FP8_ERR_CUDA;
-    static bool attr_done[kMaxDevices] = {false};
-    if (!attr_done[dev]) {
+    // Per context: the register check and the shared-memory opt-in (a kernel
+    // attribute belongs to the context it was set in).
+    static ContextCache<int> attr_cache;
+    int ok = 0;
+    const int ast = attr_cache.get(&ok, [&](int* v) {
         // the setmaxnreg split is only safe for the register count it was sized for
         cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return FP8_ERR_CUDA;
-        if (fa.numRegs != kLaunchRegs) return FP8_ERR_UNSUPPORTED;
+        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return static_cast<int>(FP8_ERR_CUDA);
+        if (fa.numRegs != kLaunchRegs) return static_cast<int>(FP8_ERR_UNSUPPORTED);
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
             cudaSuccess)
-            return FP8_ERR_CUDA;
-        attr_done[dev] = true;
-    }
+            return static_cast<int>(FP8_ERR_CUDA);
+        *v = 1;
+        return static_cast<int>(FP8_OK);
+    });
+    if (ast != FP8_OK) return ast;
     CUtensorMap ta, tb, tc;
     int st;
     if ((st = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, p.K, a_rows, p.K, BK, BM,
@@ -763,9 +767,9 @@ static int dispatch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_
 
 using namespace fp8fg;
 
-extern "C" int fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, const uint8_t* bq,
-                                    const float* sb, int bmode, int64_t M, int64_t N, int64_t K,
-                                    void* c, int64_t ldc, int out_type, void* stream) {
+extern "C" fp8_status fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, const uint8_t* bq,
+                                    const float* sb, fp8_bscale_t bmode, int64_t M, int64_t N, int64_t K,
+                                    void* c, int64_t ldc, fp8_out_t out_type, void* stream) {
     if (M < 0 || N <= 0 || N % 128 != 0 || K <= 0 || K % 128 != 0 || ldc < N)
         return FP8_ERR_SHAPE;
     if (bmode < FP8_BSCALE_BLOCK128 || bmode > FP8_BSCALE_BLOCK128_T) return FP8_ERR_UNSUPPORTED;
@@ -792,8 +796,8 @@ extern "C" int fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, const ui
     p.ldc = ldc;
     p.offsets = nullptr;
     p.E = 0;
-    return dispatch<0>(aq, M, bq, N, p, out_type, (M + BM - 1) / BM,
-                           static_cast<cudaStream_t>(stream));
+    return to_status(dispatch<0>(aq, M, bq, N, p, out_type, (M + BM - 1) / BM,
+                           static_cast<cudaStream_t>(stream)));
 }
 
 // Shared body of the grouped entry points; bmode is BLOCK128 (Fprop: per-expert
@@ -832,22 +836,22 @@ static int grouped_gemm(const uint8_t* aq, const float* sa, const uint8_t* bq, c
                           (T + BM - 1) / BM + E, static_cast<cudaStream_t>(stream));
 }
 
-extern "C" int fp8_grouped_gemm_moe(const uint8_t* aq, const float* sa, const uint8_t* bq,
+extern "C" fp8_status fp8_grouped_gemm_moe(const uint8_t* aq, const float* sa, const uint8_t* bq,
                                     const float* sb, const int32_t* offsets, int32_t E, int64_t T,
-                                    int64_t N, int64_t K, void* c, int out_type, void* stream) {
-    return grouped_gemm(aq, sa, bq, sb, FP8_BSCALE_BLOCK128, offsets, E, T, N, K, c, out_type,
-                        stream);
+                                    int64_t N, int64_t K, void* c, fp8_out_t out_type, void* stream) {
+    return to_status(grouped_gemm(aq, sa, bq, sb, FP8_BSCALE_BLOCK128, offsets, E, T, N, K, c, out_type,
+                        stream));
 }
 
-extern "C" int fp8_grouped_gemm_moe_dgrad(const uint8_t* aq, const float* sa, const uint8_t* bq,
+extern "C" fp8_status fp8_grouped_gemm_moe_dgrad(const uint8_t* aq, const float* sa, const uint8_t* bq,
                                           const float* sb, const int32_t* offsets, int32_t E,
-                                          int64_t T, int64_t N, int64_t K, void* c, int out_type,
+                                          int64_t T, int64_t N, int64_t K, void* c, fp8_out_t out_type,
                                           void* stream) {
-    return grouped_gemm(aq, sa, bq, sb, FP8_BSCALE_BLOCK128_T, offsets, E, T, N, K, c,
-                        out_type, stream);
+    return to_status(grouped_gemm(aq, sa, bq, sb, FP8_BSCALE_BLOCK128_T, offsets, E, T, N, K, c,
+                        out_type, stream));
 }
 
-extern "C" int fp8_grouped_gemm_moe_wgrad(const uint8_t* aqT, const float* sa,
+extern "C" fp8_status fp8_grouped_gemm_moe_wgrad(const uint8_t* aqT, const float* sa,
                                           const uint8_t* bqT, const float* sb,
                                           const int32_t* pofs, int32_t E, int64_t Tp, int64_t M,
                                           int64_t N, float* c, void* stream) {
@@ -876,7 +880,7 @@ extern "C" int fp8_grouped_gemm_moe_wgrad(const uint8_t* aqT, const float* sa,
     p.ldc = N;
     p.offsets = pofs;
     p.E = E;
-    return dispatch<2>(aqT, M, bqT, N, p, FP8_OUT_F32, 0, static_cast<cudaStream_t>(stream));
+    return to_status(dispatch<2>(aqT, M, bqT, N, p, FP8_OUT_F32, 0, static_cast<cudaStream_t>(stream)));
 }
 
 // Self-test of the failure path: one thread waits, through the same bounded
@@ -895,12 +899,12 @@ __global__ void selftest_wait_kernel() {
     if (threadIdx.x == 0) (void)wait_bar(smem_addr(&bar), 0, &abort_flag);
 }
 
-extern "C" int fp8_selftest_wait_timeout(void* stream) {
+extern "C" fp8_status fp8_selftest_wait_timeout(void* stream) {
     selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>();
-    return launch_status();
+    return to_status(launch_status());
 }
 
-extern "C" int fp8_device_error(void* stream) {
+extern "C" fp8_status fp8_device_error(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return FP8_ERR_CUDA;
     unsigned int v = 0, zero = 0;

@@ -483,19 +483,20 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm) quant_fprop_pair
 // kernel and device), never more than there are tiles.
 template <auto kern>
 static int64_t quant_grid(int64_t tiles) {
-    static int per_sm[kMaxDevices] = {0};
-    int dev = 0;
-    const int sms = sm_count_current(&dev);
-    if (sms <= 0) return tiles < 1024 ? tiles : 1024;
-    if (per_sm[dev] == 0) {
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kQuantThreads, 0) !=
-                cudaSuccess ||
-            n <= 0)
-            n = 1;
-        per_sm[dev] = n < kQuantCtasPerSm ? n : kQuantCtasPerSm;
-    }
-    const int64_t cap = static_cast<int64_t>(sms) * per_sm[dev];
+    static ContextCache<int> per_sm;
+    const int sms = sm_count_current();
+    int n = 0;
+    if (sms <= 0 || per_sm.get(&n, [](int* v) {
+            int b = 0;
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, kQuantThreads, 0) !=
+                    cudaSuccess ||
+                b <= 0)
+                b = 1;
+            *v = b < kQuantCtasPerSm ? b : kQuantCtasPerSm;
+            return static_cast<int>(FP8_OK);
+        }) != FP8_OK)
+        return tiles < 1024 ? tiles : 1024;
+    const int64_t cap = static_cast<int64_t>(sms) * n;
     return tiles < cap ? tiles : cap;
 }
 
@@ -503,7 +504,7 @@ static int64_t quant_grid(int64_t tiles) {
 
 using namespace fp8fg;
 
-extern "C" int fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
+extern "C" fp8_status fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
                                    int64_t ldq, float* sx, void* stream) {
     if (M < 0 || K <= 0 || K % 128 != 0 || ldx < K || ldq < K) return FP8_ERR_SHAPE;
     if (M == 0) return FP8_OK;
@@ -514,10 +515,10 @@ extern "C" int fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t 
     quant_act_1x128_kernel<<<static_cast<unsigned>(quant_grid<quant_act_1x128_kernel>(tiles)), kQuantThreads, 0,
                              static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t*>(x), M, K / 128, ldx, xq, ldq, sx, tiles);
-    return launch_status();
+    return to_status(launch_status());
 }
 
-extern "C" int fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx,
+extern "C" fp8_status fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx,
                                    uint8_t* xqT, float* sxT, void* stream) {
     if (M < 0 || M % 128 != 0 || K <= 0 || K % 64 != 0 || ldx < K) return FP8_ERR_SHAPE;
     if (M == 0) return FP8_OK;
@@ -528,10 +529,10 @@ extern "C" int fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t 
     quant_act_128x1_kernel<<<static_cast<unsigned>(quant_grid<quant_act_128x1_kernel>(tiles)), kQuantThreads, 0,
                              static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t*>(x), M, K, ldx, xqT, sxT, tiles);
-    return launch_status();
+    return to_status(launch_status());
 }
 
-extern "C" int fp8_quant_act_128x1_grouped(const void* x, int64_t T, int64_t K, int64_t ldx,
+extern "C" fp8_status fp8_quant_act_128x1_grouped(const void* x, int64_t T, int64_t K, int64_t ldx,
                                            const int32_t* offsets, int32_t E, uint8_t* xqT,
                                            float* sxT, int64_t Tp, int32_t* pofs,
                                            void* stream) {
@@ -552,7 +553,7 @@ extern "C" int fp8_quant_act_128x1_grouped(const void* x, int64_t T, int64_t K, 
     quant_act_128x1_grouped_kernel<<<static_cast<unsigned>(tiles), kQuantThreads, 0,
                                      static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t*>(x), T, K, ldx, offsets, E, xqT, sxT, Tp, pofs);
-    return launch_status();
+    return to_status(launch_status());
 }
 
 // Persistent grid of the operand kernel: as many CTAs as are resident (at
@@ -560,30 +561,32 @@ extern "C" int fp8_quant_act_128x1_grouped(const void* x, int64_t T, int64_t K, 
 static int launch_pair(const PairArgs& p, cudaStream_t stream) {
     const int64_t total = p.act_tiles + p.w_tiles;
     if (total == 0) return FP8_OK;
-    static int per_sm[kMaxDevices] = {0};
-    int dev = 0;
-    const int sms = sm_count_current(&dev);
+    static ContextCache<int> per_sm;
+    const int sms = sm_count_current();
     if (sms <= 0) return FP8_ERR_CUDA;
-    if (per_sm[dev] == 0) {
+    int n = 0;
+    const int st = per_sm.get(&n, [](int* v) {
         if (cudaFuncSetAttribute(quant_fprop_pair_kernel,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, kPairSmem) !=
             cudaSuccess)
-            return FP8_ERR_CUDA;
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, quant_fprop_pair_kernel,
+            return static_cast<int>(FP8_ERR_CUDA);
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, quant_fprop_pair_kernel,
                                                           kPairThreads, kPairSmem) !=
                 cudaSuccess ||
-            n <= 0)
-            return FP8_ERR_CUDA;
-        per_sm[dev] = n < kPairCtasPerSm ? n : kPairCtasPerSm;
-    }
-    const int64_t cap = static_cast<int64_t>(sms) * per_sm[dev];
+            b <= 0)
+            return static_cast<int>(FP8_ERR_CUDA);
+        *v = b < kPairCtasPerSm ? b : kPairCtasPerSm;
+        return static_cast<int>(FP8_OK);
+    });
+    if (st != FP8_OK) return st;
+    const int64_t cap = static_cast<int64_t>(sms) * n;
     const int64_t grid = total < cap ? total : cap;
     quant_fprop_pair_kernel<<<static_cast<unsigned>(grid), kPairThreads, kPairSmem, stream>>>(p);
     return launch_status();
 }
 
-extern "C" int fp8_quant_weight_128x128(const void* w, int64_t K, int64_t N, int64_t ldw,
+extern "C" fp8_status fp8_quant_weight_128x128(const void* w, int64_t K, int64_t N, int64_t ldw,
                                         uint8_t* wq, uint8_t* wqT, float* sw, void* stream) {
     if (K < 0 || K % 128 != 0 || N < 0 || N % 128 != 0 || ldw < N) return FP8_ERR_SHAPE;
     if (K == 0 || N == 0) return FP8_OK;
@@ -600,10 +603,10 @@ extern "C" int fp8_quant_weight_128x128(const void* w, int64_t K, int64_t N, int
     p.sw = sw;
     p.w_tiles = (N / 128) * (K / 128);
     p.KB = K / 128;
-    return launch_pair(p, static_cast<cudaStream_t>(stream));
+    return to_status(launch_pair(p, static_cast<cudaStream_t>(stream)));
 }
 
-extern "C" int fp8_quant_fprop_operands(const void* x, int64_t M, int64_t K, int64_t ldx,
+extern "C" fp8_status fp8_quant_fprop_operands(const void* x, int64_t M, int64_t K, int64_t ldx,
                                         uint8_t* xq, int64_t ldq, float* sx, const void* w,
                                         int64_t N, int64_t ldw, uint8_t* wq, uint8_t* wqT,
                                         float* sw, void* stream) {
@@ -637,10 +640,10 @@ extern "C" int fp8_quant_fprop_operands(const void* x, int64_t M, int64_t K, int
     p.sw = sw;
     p.w_tiles = wgt ? (N / 128) * (K / 128) : 0;
     p.KB = K / 128;
-    return launch_pair(p, static_cast<cudaStream_t>(stream));
+    return to_status(launch_pair(p, static_cast<cudaStream_t>(stream)));
 }
 
-extern "C" const char* fp8_status_str(int status) {
+extern "C" const char* fp8_status_str(fp8_status status) {
     switch (status) {
         case FP8_OK: return "ok";
         case FP8_ERR_NULL: return "null pointer";

@@ -11,15 +11,18 @@
 namespace fp8fg {
 
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_tiled() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (fn == nullptr) {
+    // initialised once (thread-safe static initialisation)
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void* ptr = nullptr;
         cudaDriverEntryPointQueryResult q;
+        PFN_cuTensorMapEncodeTiled_v12000 f = nullptr;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
                                              cudaEnableDefault, &q) == cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
-    }
+            f = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+        (void)cudaGetLastError();
+        return f;
+    }();
     return fn;
 }
 

@@ -23,7 +23,11 @@
  * Conventions for every entry point:
  *   - Pointers are DEVICE pointers into memory the caller owns.  The library
  *     allocates nothing, frees nothing and keeps no state beyond a per-device
- *     cache of the SM count and of kernel attributes.
+ *     cache of the SM count and per-context caches of kernel attributes and
+ *     of the device address of its scratch array (each entry is tagged with
+ *     the id of the CUDA context it was made in and is remade when another
+ *     context of that device is current).  The caches are guarded by a mutex:
+ *     concurrent first calls from several host threads are safe.
  *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  *     are asynchronous on that stream and never synchronise, except
  *     fp8_device_error().
@@ -75,7 +79,7 @@ typedef enum {
 } fp8_bscale_t;
 
 /* Human-readable name of a status code (static string, never NULL). */
-const char* fp8_status_str(int status);
+const char* fp8_status_str(fp8_status status);
 
 /*
  * fp8_device_error: synchronises `stream`, then returns and clears the
@@ -84,7 +88,7 @@ const char* fp8_status_str(int status);
  * FP8_ERR_DEVICE_SHAPE if a grouped GEMM found non-monotone offsets,
  * FP8_OK otherwise.  FP8_ERR_CUDA if the synchronisation itself failed.
  */
-int fp8_device_error(void* stream);
+fp8_status fp8_device_error(void* stream);
 
 /*
  * fp8_selftest_wait_timeout: launches one thread that waits, with the same
@@ -94,7 +98,7 @@ int fp8_device_error(void* stream);
  * usable.  A check of the failure-detection path; the report has no
  * counterpart.  Asynchronous on `stream`.
  */
-int fp8_selftest_wait_timeout(void* stream);
+fp8_status fp8_selftest_wait_timeout(void* stream);
 
 /*
  * fp8_quant_act_1x128 -- 1x128 activation quantisation (report section
@@ -107,7 +111,7 @@ int fp8_selftest_wait_timeout(void* stream);
  * Requires K % 128 == 0, ldx >= K, ldq >= K, ldx % 8 == 0, ldq % 16 == 0,
  * x and xq 16-byte aligned, sx 4-byte aligned.  M >= 0.
  */
-int fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx,
+fp8_status fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx,
                         uint8_t* xq, int64_t ldq, float* sx, void* stream);
 
 /*
@@ -121,7 +125,7 @@ int fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx,
  * Requires M % 128 == 0, K % 64 == 0, ldx >= K, ldx % 8 == 0, x and xqT
  * 16-byte aligned, sxT 4-byte aligned.
  */
-int fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx,
+fp8_status fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx,
                         uint8_t* xqT, float* sxT, void* stream);
 
 /*
@@ -134,7 +138,7 @@ int fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx,
  * At least one of wq, wqT must be non-NULL.  Requires K % 128 == 0,
  * N % 128 == 0, ldw >= N, ldw % 8 == 0, w/wq/wqT 16-byte aligned.
  */
-int fp8_quant_weight_128x128(const void* w, int64_t K, int64_t N, int64_t ldw,
+fp8_status fp8_quant_weight_128x128(const void* w, int64_t K, int64_t N, int64_t ldw,
                              uint8_t* wq, uint8_t* wqT, float* sw, void* stream);
 
 /*
@@ -150,7 +154,7 @@ int fp8_quant_weight_128x128(const void* w, int64_t K, int64_t N, int64_t ldw,
  * K == 0 returns FP8_OK without launching.  Every other requirement is the
  * union of the two calls' requirements, checked before anything is launched.
  */
-int fp8_quant_fprop_operands(const void* x, int64_t M, int64_t K, int64_t ldx,
+fp8_status fp8_quant_fprop_operands(const void* x, int64_t M, int64_t K, int64_t ldx,
                              uint8_t* xq, int64_t ldq, float* sx,
                              const void* w, int64_t N, int64_t ldw,
                              uint8_t* wq, uint8_t* wqT, float* sw, void* stream);
@@ -170,9 +174,9 @@ int fp8_quant_fprop_operands(const void* x, int64_t M, int64_t K, int64_t ldx,
  * Requires K % 128 == 0, K > 0, N % 128 == 0, ldc >= N, ldc*elt % 16 == 0,
  * aq/bq/c 16-byte aligned, sa/sb 4-byte aligned, M >= 0.
  */
-int fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, const uint8_t* bq,
-                         const float* sb, int bmode, int64_t M, int64_t N, int64_t K,
-                         void* c, int64_t ldc, int out_type, void* stream);
+fp8_status fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, const uint8_t* bq,
+                         const float* sb, fp8_bscale_t bmode, int64_t M, int64_t N, int64_t K,
+                         void* c, int64_t ldc, fp8_out_t out_type, void* stream);
 
 /*
  * fp8_grouped_gemm_moe -- per-expert block-scaled GEMM over rows grouped by
@@ -192,9 +196,9 @@ int fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, const uint8_t* bq,
  * Requires 1 <= E <= 65536, T >= 0, K % 128 == 0, K > 0, N % 128 == 0,
  * aq/bq/c 16-byte aligned, sa/sb/offsets 4-byte aligned.
  */
-int fp8_grouped_gemm_moe(const uint8_t* aq, const float* sa, const uint8_t* bq,
+fp8_status fp8_grouped_gemm_moe(const uint8_t* aq, const float* sa, const uint8_t* bq,
                          const float* sb, const int32_t* offsets, int32_t E, int64_t T,
-                         int64_t N, int64_t K, void* c, int out_type, void* stream);
+                         int64_t N, int64_t K, void* c, fp8_out_t out_type, void* stream);
 
 /*
  * fp8_grouped_gemm_moe_dgrad -- the Dgrad of the grouped expert GEMM: per
@@ -212,9 +216,9 @@ int fp8_grouped_gemm_moe(const uint8_t* aq, const float* sa, const uint8_t* bq,
  *   offsets, c, out_type, E, T: as fp8_grouped_gemm_moe (c is dX [T][N]).
  * Same checks and device-side offset validation as fp8_grouped_gemm_moe.
  */
-int fp8_grouped_gemm_moe_dgrad(const uint8_t* aq, const float* sa, const uint8_t* bq,
+fp8_status fp8_grouped_gemm_moe_dgrad(const uint8_t* aq, const float* sa, const uint8_t* bq,
                                const float* sb, const int32_t* offsets, int32_t E, int64_t T,
-                               int64_t N, int64_t K, void* c, int out_type, void* stream);
+                               int64_t N, int64_t K, void* c, fp8_out_t out_type, void* stream);
 
 /*
  * fp8_quant_act_128x1_grouped -- the 128x1 (token-wise, transposed)
@@ -238,7 +242,7 @@ int fp8_grouped_gemm_moe_dgrad(const uint8_t* aq, const float* sa, const uint8_t
  * Tp % 128 == 0 and Tp >= T + 127 E rounded up to 128; x, xqT 16-byte aligned,
  * sxT, offsets, pofs 4-byte aligned.
  */
-int fp8_quant_act_128x1_grouped(const void* x, int64_t T, int64_t K, int64_t ldx,
+fp8_status fp8_quant_act_128x1_grouped(const void* x, int64_t T, int64_t K, int64_t ldx,
                                 const int32_t* offsets, int32_t E, uint8_t* xqT, float* sxT,
                                 int64_t Tp, int32_t* pofs, void* stream);
 
@@ -262,7 +266,7 @@ int fp8_quant_act_128x1_grouped(const void* x, int64_t T, int64_t K, int64_t ldx
  * Requires M % 128 == 0, N % 128 == 0, Tp % 128 == 0, 1 <= E <= 65536;
  * aqT, bqT, c 16-byte aligned, sa, sb, pofs 4-byte aligned.
  */
-int fp8_grouped_gemm_moe_wgrad(const uint8_t* aqT, const float* sa, const uint8_t* bqT,
+fp8_status fp8_grouped_gemm_moe_wgrad(const uint8_t* aqT, const float* sa, const uint8_t* bqT,
                                const float* sb, const int32_t* pofs, int32_t E, int64_t Tp,
                                int64_t M, int64_t N, float* c, void* stream);
 
@@ -271,7 +275,7 @@ int fp8_grouped_gemm_moe_wgrad(const uint8_t* aqT, const float* sa, const uint8_
  * fp8_moe_dispatch_quant needs for T tokens and n_local local experts
  * (0 when T = 0).  *bytes is set to 0 on error.
  */
-int fp8_moe_dispatch_workspace_size(int64_t T, int32_t n_local, size_t* bytes);
+fp8_status fp8_moe_dispatch_workspace_size(int64_t T, int32_t n_local, size_t* bytes);
 
 /*
  * fp8_moe_dispatch_quant -- MoE dispatch packing in FP8: the activation rows
@@ -305,7 +309,7 @@ int fp8_moe_dispatch_workspace_size(int64_t T, int32_t n_local, size_t* bytes);
  * T <= 2^27; x and xq 16-byte aligned, sx/topk_ids/offsets/token_ids 4-byte
  * aligned.  T = 0 only zeroes offsets.
  */
-int fp8_moe_dispatch_quant(const void* x, int64_t T, int64_t K, int64_t ldx,
+fp8_status fp8_moe_dispatch_quant(const void* x, int64_t T, int64_t K, int64_t ldx,
                            const int32_t* topk_ids, int32_t topk, int32_t expert_begin,
                            int32_t n_local, uint8_t* xq, float* sx, int64_t cap,
                            int32_t* offsets, int32_t* token_ids, void* workspace,
@@ -329,11 +333,14 @@ int fp8_moe_dispatch_quant(const void* x, int64_t T, int64_t K, int64_t ldx,
  *   reads.
  *   Overlapping calls on one device (on different streams, or from different
  *   host threads without ordering) share the scratch and race; serialise them.
- *   The first call on each device looks up the scratch's device address
- *   (cudaGetSymbolAddress) with that device current; make that first call
- *   before any stream capture begins.
+ *   The first call in each CUDA context looks up the scratch's device
+ *   address (cudaGetSymbolAddress) with that context current and caches it,
+ *   tagged with the context's id; a later call in another context of the
+ *   same device (one the caller made with the driver API, or the primary
+ *   context re-created after cudaDeviceReset) looks it up again.  Make the
+ *   first call in a context before any stream capture begins.
  */
-int fp8_moe_dispatch_quant_noalloc(const void* x, int64_t T, int64_t K, int64_t ldx,
+fp8_status fp8_moe_dispatch_quant_noalloc(const void* x, int64_t T, int64_t K, int64_t ldx,
                                    const int32_t* topk_ids, int32_t topk, int32_t expert_begin,
                                    int32_t n_local, uint8_t* xq, float* sx, int64_t cap,
                                    int32_t* offsets, int32_t* token_ids, void* stream);
