@@ -2,7 +2,8 @@
 
 Bit-exact: offsets, source token ids, E4M3 codes and scales of every packed
 row; rows past the last used one stay untouched.  Then the packed operands
-feed the grouped GEMM, compared with the oracle on sampled rows.
+feed the grouped GEMM, compared with the oracle on 1024 rows that include
+the first and last row of every expert and of every 128-row tile.
 """
 import numpy as np
 import pytest
@@ -10,8 +11,8 @@ import torch
 
 import oracle
 from fp8_fine_grained_22_b300 import fp8fg, inputs
-from parity import bits, sample_rows
-from test_grouped_parity import _compare
+from parity import bits, group_rows
+from test_grouped_parity import _compare, _quant_experts as _oracle_weights
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -128,9 +129,10 @@ def test_prefill_workload_dispatch_then_grouped_gemm():
     y = fp8fg.fp8_grouped_gemm_moe(xq, sx, wq, sw, off)
     torch.cuda.synchronize()
     assert fp8fg.device_error() == 0
-    rows = sample_rows(R, 64, seed=5)
     rxq, rsx, roff, _ = oracle.moe_dispatch_quant(bits(x_tok), order.numpy(), 0, wl.E)
-    # the oracle's A rows with the GPU weights' codes and scales (the weight
-    # quantiser has its own parity tests)
-    _compare(y, rxq, rsx, wq.cpu().numpy(), sw.cpu().numpy(), roff, rows)
+    rows = group_rows(roff, 1024, seed=5)
+    # every operand of the oracle product comes from the oracle: the packed A
+    # rows of its dispatch and its own 128x128 quantisation of each weight
+    bq, sb = _oracle_weights(wl.w)
+    _compare(y, rxq, rsx, bq, sb, roff, rows)
     assert cap >= R

@@ -13,7 +13,8 @@ import torch
 
 import oracle
 from fp8_fine_grained_22_b300 import fp8fg, inputs
-from parity import bits, check_bf16, check_f32, magnitude, np_u8, sample_rows
+from parity import (bits, check_bf16, check_f32, check_f32_elementwise, group_rows, magnitude,
+                    np_u8)
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -39,9 +40,9 @@ def _run(aq, sa, bq, sb, offsets, out_dtype, c=None):
 
 
 def _compare(out, aq, sa, bq, sb, offsets, rows, bmode=oracle.BSCALE_BLOCK128):
+    """The requested rows, elementwise, each against its expert's oracle product."""
     ref = oracle.grouped_gemm(aq, sa, bq, sb, offsets, rows=rows, bmode=bmode)
     K = aq.shape[1]
-    N = bq.shape[1]
     expert_of = np.searchsorted(offsets, rows, side="right") - 1
     o = out.cpu()
     n_fallback = 0
@@ -49,11 +50,11 @@ def _compare(out, aq, sa, bq, sb, offsets, rows, bmode=oracle.BSCALE_BLOCK128):
         sel = np.nonzero(expert_of == e)[0]
         sbe = sb[e] if bmode == oracle.BSCALE_BLOCK128 else sb[e].T
         sbm = np.repeat(sbe, 128, axis=0)  # [N, K/128]
-        S = magnitude(aq, sa, bq[e], sbm, rows[sel])
+        S = lambda idx, e=e, sel=sel, sbm=sbm: magnitude(aq, sa, bq[e], sbm, rows[sel][idx])
         if o.dtype == torch.float32:
             got = o.numpy()[rows[sel]]
             check_f32(got, ref[sel])
-            assert np.all(np.abs(got - ref[sel]) <= 2.0 ** -24 * (K // 128 + 128) * S + 1e-300)
+            check_f32_elementwise(got, ref[sel], K, S)
         else:
             n_fallback += check_bf16(o.view(torch.int16).numpy().view(np.uint16)[rows[sel]],
                                      ref[sel], S=S, K=K)
@@ -110,36 +111,34 @@ def test_bad_offsets_reported_on_device():
     assert fp8fg.device_error() == 0  # cleared
 
 
-def _workload_parity(wl, n_rows_per_expert=4):
+def _workload_parity(wl, n_rows):
+    """Grouped GEMM of a routing workload; rows: the first and last row of
+    every expert and of every 128-row tile inside it, plus random rows up to
+    n_rows (all rows when n_rows >= the row count)."""
     xb = bits(wl.x)
     aq, sa = oracle.quant_act_1x128(xb)
     bq, sb = _quant_experts(wl.w)
     out = _run(aq, sa, bq, sb, wl.offsets, torch.bfloat16)
     assert fp8fg.device_error() == 0
-    # every expert: first and last row, plus a few random rows
-    rng = np.random.default_rng(0)
-    rows = []
-    for e in range(wl.E):
-        lo, hi = int(wl.offsets[e]), int(wl.offsets[e + 1])
-        if hi > lo:
-            rows += [lo, hi - 1] + list(rng.integers(lo, hi, n_rows_per_expert))
-    rows = np.unique(np.array(rows, np.int64))
+    rows = group_rows(wl.offsets, n_rows, seed=0)
     return _compare(out, aq, sa, bq, sb, wl.offsets, rows)
 
 
 def test_moe_prefill_workload():
+    """Top-8 of 256 routing, 32 local experts: 1024 rows covering every expert and tile edge."""
     wl = inputs.moe_prefill()
     counts = np.diff(wl.offsets)
     # the biased routing is skewed: empty experts next to experts with thousands of rows
     assert counts.min() == 0 and counts.max() > 1000
-    _workload_parity(wl)
+    _workload_parity(wl, 1024)
 
 
 def test_moe_decode_workload():
+    """1-256 tokens per expert, 32 experts: every row against the oracle."""
     wl = inputs.moe_decode()
     counts = np.diff(wl.offsets)
     assert counts.min() >= 1 and counts.max() <= 256
-    _workload_parity(wl, n_rows_per_expert=6)
+    _workload_parity(wl, int(wl.offsets[-1]))
 
 
 def _quant_experts_T(w):
@@ -183,5 +182,5 @@ def test_moe_prefill_dgrad_workload():
     dx = fp8fg.fp8_grouped_gemm_moe_dgrad(t(dq), t(sd), t(bqT), t(sw), off)
     torch.cuda.synchronize()
     assert fp8fg.device_error() == 0
-    rows = sample_rows(T, 96, seed=9)
+    rows = group_rows(wl.offsets, 1024, seed=9)
     _compare(dx, dq, sd, bqT, sw, np.asarray(wl.offsets), rows, bmode=oracle.BSCALE_BLOCK128_T)

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from fp8_fine_grained_22_b300 import fp8fg, inputs
-from parity import b_scale_matrix, bits, check_f32, magnitude
+from parity import b_scale_matrix, bits, check_f32, check_f32_elementwise, magnitude, sample_rows
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -50,10 +50,9 @@ def _compare_wgrad(dw, rq, rs, rdq, rds, pofs, rows):
         check_f32(got[e], ref[e])
         a, sa = rq[:, lo:hi], rs[lo // 128:hi // 128]
         b, sb = rdq[:, lo:hi], rds[lo // 128:hi // 128]
-        S = magnitude(a, sa, b, b_scale_matrix(sb, oracle.BSCALE_ROW1x128, b.shape[0], hi - lo),
-                      rows)
-        K = hi - lo
-        assert np.all(np.abs(got[e] - ref[e]) <= 2.0 ** -24 * (K // 128 + 128) * S + 1e-300)
+        sbm = b_scale_matrix(sb, oracle.BSCALE_ROW1x128, b.shape[0], hi - lo)
+        S = lambda idx, a=a, sa=sa, b=b, sbm=sbm: magnitude(a, sa, b, sbm, rows[idx])
+        check_f32_elementwise(got[e], ref[e], hi - lo, S)
 
 
 @pytest.mark.parametrize("counts", [[3, 0, 130, 1], [128, 256], [0, 0, 1], [257, 5, 0, 300]])
@@ -104,8 +103,8 @@ def test_moe_prefill_wgrad_workload():
     dw = fp8fg.fp8_grouped_gemm_moe_wgrad(xqT, sxT, dqT, sdT, pofs)
     torch.cuda.synchronize()
     assert fp8fg.device_error() == 0
-    rows = np.array([0, 1, 127, 128, 3000, 7167])
-    _compare_wgrad(dw, rq, rs, rdq, rds, rpofs, rows)
+    # 1024 rows of every expert's dW, including the first and last row of every 128-row M tile
+    _compare_wgrad(dw, rq, rs, rdq, rds, rpofs, sample_rows(wl.K, 1024, seed=12))
 
 
 def test_full_width_two_experts():
@@ -121,4 +120,4 @@ def test_full_width_two_experts():
     dw = fp8fg.fp8_grouped_gemm_moe_wgrad(xqT, sxT, dqT, sdT, pofs)
     torch.cuda.synchronize()
     assert fp8fg.device_error() == 0
-    _compare_wgrad(dw, rq, rs, rdq, rds, rpofs, np.array([0, 5, 127, 128, 4000, 7167]))
+    _compare_wgrad(dw, rq, rs, rdq, rds, rpofs, sample_rows(M, 1024, seed=13))

@@ -7,7 +7,7 @@ host synchronisation, alternating two different inputs, so that every GEMM
 follows a producer that is overwriting the very buffers it reads.  Each
 result must be bitwise equal to the same pair run with a synchronisation in
 between (the kernels are deterministic), and those reference results are
-checked against the oracle on sampled rows.
+checked against the oracle on rows that include every tile and expert edge.
 """
 import numpy as np
 import pytest
@@ -15,8 +15,8 @@ import torch
 
 import oracle
 from fp8_fine_grained_22_b300 import fp8fg, inputs
-from parity import b_scale_matrix, bits, check_bf16, magnitude, sample_rows
-from test_grouped_parity import _compare
+from parity import b_scale_matrix, bits, check_bf16, group_rows, magnitude, sample_rows
+from test_grouped_parity import _compare, _quant_experts as _oracle_weights
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda"
@@ -47,11 +47,11 @@ def test_operand_quantiser_then_gemm_back_to_back():
         # the synchronised result against the oracle on sampled rows
         aq, sa = oracle.quant_act_1x128(bits(xs[j].cpu()))
         bq, _, sb = oracle.quant_weight_128x128(bits(ws[j].cpu()))
-        rows = sample_rows(M, 24, seed=j)
+        rows = sample_rows(M, 256, seed=j)
         want = oracle.gemm_blockscaled(aq, sa, bq, sb, rows=rows)
         got = ref[j].cpu().view(torch.int16).numpy().view(np.uint16)[rows]
-        S = magnitude(aq, sa, bq, b_scale_matrix(sb, oracle.BSCALE_BLOCK128, N, K), rows)
-        check_bf16(got, want, S=S, K=K)
+        sbm = b_scale_matrix(sb, oracle.BSCALE_BLOCK128, N, K)
+        check_bf16(got, want, S=lambda idx: magnitude(aq, sa, bq, sbm, rows[idx]), K=K)
 
     outs = [torch.empty((M, N), dtype=torch.bfloat16, device=DEV) for _ in range(16)]
     for i, y in enumerate(outs):
@@ -85,6 +85,7 @@ def test_dispatch_then_grouped_gemm_back_to_back():
                                      token_ids=tok, workspace=ws)
         fp8fg.fp8_grouped_gemm_moe(xq, sx, wq, sw, off, c=y)
 
+    bq_ref, sb_ref = _oracle_weights(torch.stack(w_host))  # the oracle's own weight codes
     ref, rows_used = [], []
     for j in range(2):
         y = torch.zeros((cap, N), dtype=torch.bfloat16, device=DEV)
@@ -99,7 +100,7 @@ def test_dispatch_then_grouped_gemm_back_to_back():
         rxq, rsx, roff, _ = oracle.moe_dispatch_quant(bits(xs[j].cpu()), ids[j].cpu().numpy(),
                                                       0, E)
         assert int(roff[-1]) == R
-        _compare(y, rxq, rsx, wq.cpu().numpy(), sw.cpu().numpy(), roff, sample_rows(R, 24, seed=j))
+        _compare(y, rxq, rsx, bq_ref, sb_ref, roff, group_rows(roff, 256, seed=j))
     assert rows_used[0] != rows_used[1]  # the two routings pack different row counts
 
     outs = [torch.zeros((cap, N), dtype=torch.bfloat16, device=DEV) for _ in range(12)]
