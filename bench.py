@@ -1,30 +1,32 @@
 #!/usr/bin/env python3
 """Benchmark of the fine-grained FP8 hot path on one (or N independent) B300s.
 
-One step = one pass of the path over one batch of the dense Fprop workload
-X[8192, 2048] (BF16, outlier channels) . W[2048, 7168] (BF16) -> Y (BF16):
-  1. 1x128 activation quantisation of X and 128x128 weight quantisation of W,
-     one launch for both operands             (fp8_quant_fprop_operands)
-  2. block-scaled FP8 GEMM with per-128-K FP32 promotion (fp8_gemm_blockscaled)
-The metric is the step's FP8 GEMM throughput, 2*M*N*K / step time (TFLOP/s);
-the JSON line also carries each kernel's own rate and roofline fraction.
+One step = one pass of the path over the training trio of an expert MLP
+(hidden 7168, intermediate 4096, 8192 tokens; BF16 inputs drawn seeded):
+  1. X [8192, 7168] 1x128 and W [7168, 4096] 128x128 (both orientations),
+     one launch                                   (fp8_quant_fprop_operands)
+  2. dY [8192, 4096] 1x128                        (fp8_quant_act_1x128)
+  3. X and dY 128x1, transposed, for the Wgrad    (fp8_quant_act_128x1, twice)
+  4. Fprop  Y  = X . W          -> BF16 [8192, 4096]   (fp8_gemm_blockscaled)
+  5. Dgrad  dX = dY . W^T       -> BF16 [8192, 7168]   (transposed block scales)
+  6. Wgrad  dW = X^T . dY       -> FP32 [7168, 4096]   (per-row B scales)
+The metric is the step's FP8 GEMM throughput: 3 * 2 * 8192 * 7168 * 4096
+FLOP / step time (TFLOP/s).  The JSON line also carries each kernel's time in
+the step, the roofline of the kernel that takes the most time, an end-to-end
+figure through the same API with host buffers, the oracle on the host cores,
+and a `configs` object with device-timed results for the other workloads
+(the 128x256x512 GEMM's latency, the dense Fprop step, the MoE prefill
+dispatch + grouped GEMM, the decode grouped GEMM against HBM, and every
+quantiser at the trio and prefill sizes).
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload fprop_dense|moe_prefill]
-
-`--workload moe_backward` times that layer's backward (dY quantisation, grouped
-Dgrad, per-expert 128x1 quantisation of X and dY, grouped Wgrad into FP32 dW).
-
-`--workload moe_prefill` times the MoE expert layer instead: FP8 dispatch
-packing of 16384 tokens routed top-8 of 256 experts to 32 local experts
-(fp8_moe_dispatch_quant) followed by the grouped GEMM against the experts'
-W[7168, 4096] (quantised once, outside the timed region); the metric is the
-grouped GEMM's FLOPs over the step time.
+                    [--workload trio|fprop_dense|moe_prefill|moe_backward|moe_decode]
+                    [--no-configs] [--no-cpu-baseline]
 
 Under torchrun each rank runs its own replica of the workload (weak scaling,
-no collective on the data path); rank 0 prints one JSON line.
-`--impl reference` times the CPU oracle on a bounded sample of the same
-workload instead (on rank 0 only).
+no collective on the data path); rank 0 prints one JSON line.  `--impl
+reference` times the CPU oracle on a bounded sample of the same workload
+instead (on rank 0 only).
 """
 from __future__ import annotations
 
@@ -32,9 +34,7 @@ import argparse
 import hashlib
 import json
 import os
-import re
 import statistics
-import subprocess
 import sys
 import threading
 import time
@@ -47,12 +47,13 @@ sys.path.insert(0, ROOT)
 
 from fp8_fine_grained_22_b300 import inputs  # noqa: E402
 
-WORKLOAD = "fprop_m8192_n7168_k2048_bf16"
-MOE_WORKLOAD = "moe_prefill_t16384_top8of256_e32_k7168_n4096_bf16"
-L2_BYTES = 126 * 2 ** 20
 METRIC = "FP8 block-scaled GEMM TFLOP/s and % of B300 FP8 peak; quantizer GB/s"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "gemm_fprop_m8192_n7168_k2048.md")
+L2_BYTES = 126 * 2 ** 20
+FP8_DATASHEET_TFLOPS = 4500.0  # B300 dense FP8, nominal
+HBM_NOMINAL_GBS = 7700.0
 CSRC = os.path.join(ROOT, "fp8_fine_grained_22_b300", "csrc")
+TRAFFIC_JSON = os.path.join(ROOT, "profiles", "traffic.json")
+TRIO = dict(M=8192, K=7168, N=4096)
 
 
 # ------------------------------------------------------------------ helpers --
@@ -67,93 +68,128 @@ def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
         with open(path) as f:
-            d = json.load(f)
-        return d, "measured"
+            return json.load(f), "measured"
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}, "fallback"
 
 
-GEMM_SOURCES = ("common.cuh", "gemm.cu", "ptx.cuh", "tensormap.cuh")
-
-
-def source_hash():
-    """Hash of the sources the GEMM kernel is built from."""
+def source_hash(names):
+    """Hash of the kernel sources a traffic figure was captured from."""
     h = hashlib.sha256()
-    for name in GEMM_SOURCES:
+    for name in names:
         with open(os.path.join(CSRC, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per GEMM launch from the committed ncu summary, if the
-    kernel sources are unchanged since it was taken; else None."""
-    if not os.path.exists(PROFILE_SUMMARY):
+def profiled_traffic(key):
+    """DRAM bytes per launch (dram__bytes_read.sum + dram__bytes_write.sum) for
+    `key` from profiles/traffic.json, if the kernel's sources are unchanged
+    since the capture; else None."""
+    if not os.path.exists(TRAFFIC_JSON):
         return None
-    txt = open(PROFILE_SUMMARY).read()
-    m_b = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)", txt)
-    m_h = re.search(r"source_sha256:\s*([0-9a-f]+)", txt)
-    if not (m_b and m_h) or m_h.group(1) != source_hash():
+    with open(TRAFFIC_JSON) as f:
+        d = json.load(f).get(key)
+    if not d:
         return None
-    return float(m_b.group(1))
+    if source_hash(d["sources"]) != d["source_sha256_16"]:
+        return None
+    return float(d["bytes_per_launch"])
 
 
 class ClockSampler:
-    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+    """Read-only NVML samples of the SM clock, power and clock-event reasons,
+    taken every `period` seconds by a background thread for as long as the
+    sampler is open."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
+               ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
+               ("sw_thermal_slowdown", "nvmlClocksEventReasonSwThermalSlowdown"),
+               ("sw_power_cap", "nvmlClocksEventReasonSwPowerCap"),
+               ("hw_power_brake", "nvmlClocksEventReasonHwPowerBrakeSlowdown"))
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
+    def __init__(self, device, period=0.01):
+        self.period = period
+        self.samples = []  # (t, sm_mhz, power_w, reasons_mask), taken while busy
+        self.busy = 0      # > 0 while a GPU measurement runs
+        self.max_mhz = None
+        self.err = None
+        self._stop = threading.Event()
+        self._thread = None
+        try:
+            import pynvml as nv
+            nv.nvmlInit()
+            p = torch.cuda.get_device_properties(device)
+            bus = "%08x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+            self.h = nv.nvmlDeviceGetHandleByPciBusId(bus)
+            self.nv = nv
+            self.max_mhz = nv.nvmlDeviceGetMaxClockInfo(self.h, nv.NVML_CLOCK_SM)
+            self.masks = {name: getattr(nv, attr, 0) for name, attr in self.REASONS}
+        except Exception as e:  # no NVML: the line says so
+            self.nv = None
+            self.err = repr(e)
+
+    def _run(self):
+        nv = self.nv
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons",
+                              getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons", None))
+        while not self._stop.is_set():
+            if self.busy <= 0:
+                self._stop.wait(self.period)
+                continue
+            try:
+                sm = nv.nvmlDeviceGetClockInfo(self.h, nv.NVML_CLOCK_SM)
+                pw = nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0
+                rs = get_reasons(self.h) if get_reasons else 0
+                self.samples.append((time.perf_counter(), sm, pw, rs))
+            except Exception as e:
+                self.err = repr(e)
+            self._stop.wait(self.period)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
-        except (OSError, FileNotFoundError):
-            self.proc = None
+        if self.nv is not None:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    class _Busy:
+        def __init__(self, clk):
+            self.clk = clk
+
+        def __enter__(self):
+            self.clk.busy += 1
+
+        def __exit__(self, *exc):
+            self.clk.busy -= 1
+
+    def measuring(self):
+        """Context manager: sample while a GPU measurement runs (idle host-side
+        set-up between measurements is not sampled)."""
+        return ClockSampler._Busy(self)
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
-            self.thread.join(timeout=5)
+        self._stop.set()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
 
-    def summary(self):
-        sm, mx, reasons = [], [], set()
-        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
+    def summary(self, t0=None, t1=None):
+        s = [x for x in self.samples if (t0 is None or x[0] >= t0) and (t1 is None or x[0] <= t1)]
+        out = {"source": "NVML, read-only, every %.0f ms while a GPU measurement runs"
+                         % (self.period * 1e3),
+               "samples": len(s), "sm_max_mhz": self.max_mhz}
+        if not s:
+            out.update({"sm_mhz": None, "reasons": [], "error": self.err})
+            return out
+        reasons = set()
+        for _, _, _, r in s:
+            for name, m in self.masks.items():
+                if m and (r & m):
                     reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "reasons": sorted(reasons), "samples": len(sm)}
+        out.update({"sm_mhz": statistics.median(x[1] for x in s),
+                    "sm_mhz_min": min(x[1] for x in s),
+                    "power_w_max": round(max(x[2] for x in s), 1),
+                    "reasons": sorted(reasons)})
+        return out
 
 
 # ------------------------------------------------------- multi-rank helpers --
@@ -181,158 +217,283 @@ def whole_job_tflops(world: int, flops_per_rank: float, ms_slowest: float) -> fl
     return world * flops_per_rank / (ms_slowest * 1e-3) / 1e12
 
 
-# ---------------------------------------------------------------- our path --
-def run_ours(args, rank, world, local):
+# ----------------------------------------------------------- device timing --
+class Dev:
+    """Device, stream and the L2 flush shared by the measurements."""
+
+    def __init__(self, local, clk=None):
+        self.clk = clk
+        self.dev = torch.device("cuda", local)
+        torch.cuda.set_device(self.dev)
+        self.stream = torch.cuda.current_stream(self.dev)
+        self._flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=self.dev)
+        self._sink = torch.empty((), dtype=torch.float32, device=self.dev)
+
+    def flush_l2(self):
+        """Evict the previous work's data from L2: write a buffer twice the L2
+        size, then read it back so that the dirty lines are written back to
+        HBM here rather than inside the next timed launch.  It also keeps the
+        device busy while the host issues the launch that follows."""
+        self._flush.zero_()
+        torch.sum(self._flush, dim=0, out=self._sink)
+
+    def kernel_ms(self, fn, reps=20, flush=True):
+        """Mean device time of fn's launches (CUDA events on the launching
+        stream), with L2 flushed before each repetition."""
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(reps)]
+        fn()  # warm-up (first-call attribute setup stays out of the timing)
+        with self.busy():
+            self._reps(fn, ev, flush)
+        return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+    def busy(self):
+        return self.clk.measuring() if self.clk is not None else _Null()
+
+    def _reps(self, fn, ev, flush):
+        for a, b in ev:
+            if flush:
+                self.flush_l2()
+            else:
+                torch.cuda._sleep(200_000)  # the device is busy while the host issues fn
+            a.record(self.stream)
+            fn()
+            b.record(self.stream)
+        torch.cuda.synchronize()
+
+
+class _Null:
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        return False
+
+
+def gbs(nbytes, ms):
+    return nbytes / (ms * 1e-3) / 1e9
+
+
+def tflops(flops, ms):
+    return flops / (ms * 1e-3) / 1e12
+
+
+def cublas_fp8_peak(dev):
+    """Best of a cuBLAS FP8 (E4M3, per-tensor scales) 8192^3 GEMM through
+    torch._scaled_mm: the measured FP8 denominator beside the 2 x BF16 one.
+    Timed only (a library reference point, not part of the path)."""
+    try:
+        n = 8192
+        a = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn)
+        b = torch.randn(n, n, device=dev).to(torch.float8_e4m3fn).t()
+        one = torch.ones((), device=dev)
+        for _ in range(3):
+            torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+        torch.cuda.synchronize()
+        best = None
+        for _ in range(10):
+            s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            s.record()
+            for _ in range(5):
+                torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+            e.record()
+            torch.cuda.synchronize()
+            ms = s.elapsed_time(e) / 5
+            best = ms if best is None else min(best, ms)
+        del a, b
+        return round(tflops(2.0 * n ** 3, best), 1)
+    except Exception as e:  # reported, never fatal
+        return "unavailable: %r" % (e,)
+
+
+def fp8_peaks(dev):
+    peaks, src = measured_peaks()
+    p = {"fp8_from_bf16": round(2.0 * peaks["bf16_tflops"], 1),
+         "fp8_from_bf16_source": "%s bf16 burst x 2 (nominal FP8:BF16 dense ratio)" % src,
+         "fp8_cublas_measured": cublas_fp8_peak(dev),
+         "fp8_datasheet": FP8_DATASHEET_TFLOPS,
+         "hbm": peaks["hbm_gbs"], "hbm_source": "%s copy bandwidth" % src,
+         "hbm_nominal": HBM_NOMINAL_GBS}
+    return p
+
+
+def frac_set(tf, peaks):
+    """A GEMM's TFLOP/s as a fraction of each FP8 denominator."""
+    out = {"of_2x_bf16_measured": round(tf / peaks["fp8_from_bf16"], 4),
+           "of_datasheet": round(tf / peaks["fp8_datasheet"], 4)}
+    if isinstance(peaks["fp8_cublas_measured"], float):
+        out["of_cublas_fp8_measured"] = round(tf / peaks["fp8_cublas_measured"], 4)
+    return out
+
+
+# ----------------------------------------------------- byte/FLOP accounting --
+def q1x128_bytes(M, K):
+    return M * K * 3 + (K // 128) * M * 4
+
+
+def q128x1_bytes(M, K):
+    return M * K * 3 + (M // 128) * K * 4
+
+
+def q128x128_bytes(K, N, both):
+    return K * N * (2 + (2 if both else 1)) + (K // 128) * (N // 128) * 4
+
+
+def gemm_bytes(M, N, K, out_elt, a_scales, b_scales):
+    return M * K + N * K + M * N * out_elt + 4 * (a_scales + b_scales)
+
+
+# -------------------------------------------------------------- the trio --
+class Trio:
+    """Device buffers of the training trio and its seven launches."""
+
+    def __init__(self, d: Dev, wl):
+        from fp8_fine_grained_22_b300 import fp8fg
+        self.fp8fg = fp8fg
+        self.d = d
+        dev = d.dev
+        M, K, N = wl.M, wl.K, wl.N
+        self.M, self.K, self.N = M, K, N
+        self.x, self.w, self.dy = wl.x.to(dev), wl.w.to(dev), wl.dy.to(dev)
+        u8, f32 = torch.uint8, torch.float32
+        e = lambda shape, dt: torch.empty(shape, dtype=dt, device=dev)
+        self.xq, self.sx = e((M, K), u8), e((K // 128, M), f32)
+        self.wq, self.wqT, self.sw = e((N, K), u8), e((K, N), u8), e((N // 128, K // 128), f32)
+        self.dyq, self.sdy = e((M, N), u8), e((N // 128, M), f32)
+        self.xqT, self.sxT = e((K, M), u8), e((M // 128, K), f32)
+        self.dyqT, self.sdyT = e((N, M), u8), e((M // 128, N), f32)
+        self.y = e((M, N), torch.bfloat16)
+        self.dx = e((M, K), torch.bfloat16)
+        self.dw = e((K, N), f32)
+        self.gemm_flops = 2.0 * M * N * K
+
+    NAMES = ("fp8_quant_fprop_operands (X 1x128 + W 128x128, wq and wqT)",
+             "fp8_quant_act_1x128 (dY)", "fp8_quant_act_128x1 (X)", "fp8_quant_act_128x1 (dY)",
+             "fp8_gemm_blockscaled Fprop", "fp8_gemm_blockscaled Dgrad",
+             "fp8_gemm_blockscaled Wgrad")
+
+    def launches(self, x=None, w=None, dy=None, y=None, dx=None, dw=None):
+        f, s = self.fp8fg, self.d.stream
+        x = self.x if x is None else x
+        w = self.w if w is None else w
+        dy = self.dy if dy is None else dy
+        y = self.y if y is None else y
+        dx = self.dx if dx is None else dx
+        dw = self.dw if dw is None else dw
+        return [
+            lambda: f.fp8_quant_fprop_operands(x, w, xq=self.xq, sx=self.sx, wq=self.wq,
+                                               wqT=self.wqT, sw=self.sw, stream=s),
+            lambda: f.fp8_quant_act_1x128(dy, self.dyq, self.sdy, stream=s),
+            lambda: f.fp8_quant_act_128x1(x, self.xqT, self.sxT, stream=s),
+            lambda: f.fp8_quant_act_128x1(dy, self.dyqT, self.sdyT, stream=s),
+            lambda: f.fp8_gemm_blockscaled(self.xq, self.sx, self.wq, self.sw,
+                                           bmode=f.FP8_BSCALE_BLOCK128,
+                                           out_dtype=torch.bfloat16, c=y, stream=s),
+            lambda: f.fp8_gemm_blockscaled(self.dyq, self.sdy, self.wqT, self.sw,
+                                           bmode=f.FP8_BSCALE_BLOCK128_T,
+                                           out_dtype=torch.bfloat16, c=dx, stream=s),
+            lambda: f.fp8_gemm_blockscaled(self.xqT, self.sxT, self.dyqT, self.sdyT,
+                                           bmode=f.FP8_BSCALE_ROW1x128,
+                                           out_dtype=torch.float32, c=dw, stream=s),
+        ]
+
+    def step(self, ev=None, **bufs):
+        for i, fn in enumerate(self.launches(**bufs)):
+            if ev is not None:
+                ev[i].record(self.d.stream)
+            fn()
+        if ev is not None:
+            ev[-1].record(self.d.stream)
+
+    def kernel_info(self, i, ms, peaks):
+        """Algorithmic work of launch i of the step, its rate and roofline fraction."""
+        M, K, N = self.M, self.K, self.N
+        if i < 4:
+            nbytes = [q1x128_bytes(M, K) + q128x128_bytes(K, N, True), q1x128_bytes(M, N),
+                      q128x1_bytes(M, K), q128x1_bytes(M, N)][i]
+            g = gbs(nbytes, ms)
+            return {"ms": round(ms, 5), "bound": "hbm", "algorithmic_bytes": nbytes,
+                    "gbs": round(g, 1), "frac_hbm": round(g / peaks["hbm"], 4)}
+        tf = tflops(self.gemm_flops, ms)
+        return {"ms": round(ms, 5), "bound": "tensor", "flops": self.gemm_flops,
+                "tflops": round(tf, 2), "frac": frac_set(tf, peaks)}
+
+
+def run_trio(args, rank, world, local):
     from fp8_fine_grained_22_b300 import fp8fg
 
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
+    torch.cuda.set_device(local)
+    clk = ClockSampler(torch.device("cuda", local)).__enter__()
+    d = Dev(local, clk)
     fp8fg.lib()  # fail loudly if the CUDA library is missing
-    wl = inputs.fprop_dense(seed=0, device="cpu")
-    M, N, K = wl.M, wl.N, wl.K
-    flops = 2.0 * M * N * K
-    x = wl.x.to(dev)
-    w = wl.w.to(dev)
-    xq = torch.empty((M, K), dtype=torch.uint8, device=dev)
-    sx = torch.empty((K // 128, M), dtype=torch.float32, device=dev)
-    wq = torch.empty((N, K), dtype=torch.uint8, device=dev)
-    sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=dev)
-    y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def flush_l2():
-        """Evict the step's data from L2: write a buffer twice the L2 size,
-        then read it back so that the dirty lines are written back to HBM
-        here rather than inside the next timed step."""
-        flush.zero_()
-        torch.sum(flush, dim=0, out=flush_sink)
-
-
-    # Both operands are quantised by one launch: run as two kernels they
-    # serialise (each fills the SMs) and neither reaches the HBM rate alone.
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        fp8fg.fp8_quant_fprop_operands(x, w, xq=xq, sx=sx, wq=wq, sw=sw, stream=stream)
-        if ev is not None:
-            ev[1].record(stream)
-        fp8fg.fp8_gemm_blockscaled(xq, sx, wq, sw, out_dtype=torch.bfloat16, c=y, stream=stream)
-        if ev is not None:
-            ev[2].record(stream)
-
-    def kernel_ms(fn, reps=50):
-        """Mean device time of one kernel launched alone (L2 flushed before each)."""
-        e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(reps)]
-        for a, b in e:
-            flush_l2()
-            a.record(stream)
-            fn()
-            b.record(stream)
+    wl = inputs.training_trio(seed=0, device="cpu")
+    tr = Trio(d, wl)
+    flops = 3 * tr.gemm_flops
+    with d.busy():
+        for _ in range(args.warmup):
+            d.flush_l2()
+            tr.step()
         torch.cuda.synchronize()
-        return statistics.mean(a.elapsed_time(b) for a, b in e)
-
-    for _ in range(args.warmup):
-        flush_l2()
-        step()
-    torch.cuda.synchronize()
     if fp8fg.device_error() != 0:
         raise RuntimeError("device-side error during warm-up")
 
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    nk = len(Trio.NAMES)
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
+              for _ in range(args.steps)]
     rank_barrier()
     torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t0 = time.perf_counter()
+    with d.busy():
+        t_start = time.perf_counter()
         for i in range(args.steps):
-            flush_l2()  # between steps, outside the step's events
-            step(events[i])
+            d.flush_l2()  # between steps, outside the step's events
+            tr.step(events[i])
         torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
+        t_end = time.perf_counter()
     rank_barrier()
-    qp = [e[0].elapsed_time(e[1]) for e in events]
-    gm = [e[1].elapsed_time(e[2]) for e in events]
-    st = [e[0].elapsed_time(e[2]) for e in events]
-    ms_step = reduce_max(statistics.mean(st), dev)
-    gemm_ms = statistics.mean(gm)
-    quant_phase_ms = statistics.mean(qp)
-    # the operand quantiser alone, and the single-operand quantisers for comparison
-    qp_ms = kernel_ms(lambda: fp8fg.fp8_quant_fprop_operands(x, w, xq=xq, sx=sx, wq=wq, sw=sw,
-                                                              stream=stream))
-    qx_ms = kernel_ms(lambda: fp8fg.fp8_quant_act_1x128(x, xq, sx, stream=stream))
-    qw_ms = kernel_ms(lambda: fp8fg.fp8_quant_weight_128x128(w, wq=wq, sw=sw, stream=stream))
+    per = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in events) for j in range(nk)]
+    step_ms = statistics.mean(e[0].elapsed_time(e[nk]) for e in events)
+    ms_step = reduce_max(step_ms, d.dev)
+    if fp8fg.device_error() != 0:
+        raise RuntimeError("device-side error in the timed steps")
 
-    # ----- end to end through the public API: pinned host in, host out -----
-    # Every step copies its own X and W up from pinned host memory and its
-    # own Y down.  The copies of neighbouring steps overlap: step i's inputs
-    # go up on one copy stream while step i-1 computes and step i-2's result
-    # comes down on another (two device buffer sets rotate; events order the
-    # reuse of each set).
-    xh = wl.x.pin_memory()
-    wh = wl.w.pin_memory()
-    depth = 2
-    yh = [torch.empty((M, N), dtype=torch.bfloat16).pin_memory() for _ in range(depth)]
-    xs = [x] + [torch.empty_like(x) for _ in range(depth - 1)]
-    ws = [w] + [torch.empty_like(w) for _ in range(depth - 1)]
-    ys = [y] + [torch.empty_like(y) for _ in range(depth - 1)]
-    h2d = xh.numel() * 2 + wh.numel() * 2
-    d2h = yh[0].numel() * 2
-    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(depth)]
-    ev_comp = [torch.cuda.Event() for _ in range(depth)]
-    ev_out = [torch.cuda.Event() for _ in range(depth)]
+    peaks = fp8_peaks(d.dev)
+    kernels = {Trio.NAMES[j]: tr.kernel_info(j, per[j], peaks) for j in range(nk)}
+    dom = max(range(nk), key=lambda j: per[j])
+    dk = kernels[Trio.NAMES[dom]]
+    if dk["bound"] == "tensor":
+        achieved, peak, unit = dk["tflops"], peaks["fp8_from_bf16"], "TFLOP/s"
+        traffic_key = ["", "", "", "", "gemm_fprop_m8192_n4096_k7168", "gemm_dgrad_m8192_n7168_k4096",
+                       "gemm_wgrad_m7168_n4096_k8192"][dom]
+    else:
+        achieved, peak, unit = dk["gbs"], peaks["hbm"], "GB/s"
+        traffic_key = ["quant_fprop_operands_m8192_k7168_n4096", "quant_act_1x128_m8192_k4096",
+                       "quant_act_128x1_m8192_k7168", "quant_act_128x1_m8192_k4096"][dom]
+    roofline = {"kernel": Trio.NAMES[dom], "bound": dk["bound"], "achieved": achieved,
+                "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
+                "peak_source": peaks["fp8_from_bf16_source"] if unit == "TFLOP/s"
+                else peaks["hbm_source"],
+                "traffic": profiled_traffic(traffic_key), "traffic_key": traffic_key,
+                "share_of_step": round(per[dom] / step_ms, 4)}
+    if unit == "TFLOP/s":
+        roofline["frac_other_peaks"] = frac_set(achieved, peaks)
+        M, K, N = tr.M, tr.K, tr.N
+        roofline["algorithmic_bytes"] = [
+            gemm_bytes(M, N, K, 2, M * K // 128, N * K // 16384),   # Fprop
+            gemm_bytes(M, K, N, 2, M * N // 128, N * K // 16384),   # Dgrad
+            gemm_bytes(K, N, M, 4, K * M // 128, N * M // 128)][dom - 4]  # Wgrad
+    else:
+        roofline["algorithmic_bytes"] = dk["algorithmic_bytes"]
 
-    def e2e_step(i):
-        sl = i % depth
-        up.wait_event(ev_comp[sl])            # the set's previous compute has read it
-        with torch.cuda.stream(up):
-            xs[sl].copy_(xh, non_blocking=True)
-            ws[sl].copy_(wh, non_blocking=True)
-        ev_in[sl].record(up)
-        stream.wait_event(ev_in[sl])
-        stream.wait_event(ev_out[sl])         # the set's previous result is down
-        fp8fg.fp8_quant_fprop_operands(xs[sl], ws[sl], xq=xq, sx=sx, wq=wq, sw=sw, stream=stream)
-        fp8fg.fp8_gemm_blockscaled(xq, sx, wq, sw, out_dtype=torch.bfloat16, c=ys[sl],
-                                   stream=stream)
-        ev_comp[sl].record(stream)
-        down.wait_event(ev_comp[sl])
-        with torch.cuda.stream(down):
-            yh[sl].copy_(ys[sl], non_blocking=True)
-        ev_out[sl].record(down)
-
-    e2e_steps = min(args.steps, args.e2e_steps)
-    for i in range(max(depth, args.warmup)):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e_start.record(up)
-    for i in range(e2e_steps):
-        e2e_step(i)
-    e_end.record(down)                        # after the last result is down
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max(e_start.elapsed_time(e_end) / e2e_steps, dev)
-    # the pipelined path gives the same Y as the device-resident step
-    step()
-    torch.cuda.synchronize()
-    if not torch.equal(yh[(e2e_steps - 1) % depth], y.cpu()):
-        raise RuntimeError("end-to-end result differs from the device-resident step")
-    err = fp8fg.device_error()
-    if err != 0:
-        raise RuntimeError("device-side error status %d" % err)
-
-    peaks, peak_src = measured_peaks()
-    fp8_peak = 2.0 * peaks["bf16_tflops"]  # FP8 dense = 2 x BF16 dense (nominal ratio)
-    hbm = peaks["hbm_gbs"]
-    gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
-    qx_bytes = M * K * 2 + M * K + (K // 128) * M * 4
-    qw_bytes = K * N * 2 + K * N + (K // 128) * (N // 128) * 4
-    value = whole_job_tflops(world, flops, ms_step)
-    clocks = clk.summary()
+    with d.busy():
+        e2e = trio_e2e(args, tr, d, flops, world)
+    configs = {}
+    if args.configs:
+        configs = measure_configs(args, d, peaks, tr)
+    t_all = time.perf_counter()
+    clk.__exit__()
     line = {
         "metric": METRIC,
-        "value": round(value, 2),
+        "value": round(whole_job_tflops(world, flops, ms_step), 2),
         "unit": "TFLOP/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -341,578 +502,466 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "e4m3 x e4m3 -> f32 accumulate, bf16 out",
+        "dtype": "e4m3 x e4m3 -> f32 accumulate; Y and dX bf16, dW f32",
         "data": "synthetic (seeded: N(0,1) activations with 1% x100 outlier channels, "
-                "N(0,0.006^2) weights)",
-        "config": {"workload": WORKLOAD, "M": M, "N": N, "K": K, "global_batch": M * world,
+                "N(0,0.006^2) weights, N(0,1e-3^2) output gradients)",
+        "config": {"workload": wl.name + "_training_trio", "M_tokens": tr.M, "hidden": tr.K,
+                   "intermediate": tr.N, "gemm_flops_per_step": flops,
+                   "global_batch": tr.M * world,
                    "parallelism": "replicas (dp%d, no collective)" % world,
-                   "l2": "flushed between steps (%d MB written, then read back)" % (
-                       flush.numel() * 4 >> 20),
-                   "step": ["fp8_quant_fprop_operands (X 1x128 + W 128x128, one launch)",
-                            "fp8_gemm_blockscaled"]},
-        "e2e": {"value": round(whole_job_tflops(world, flops, e2e_ms), 3), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
-        "gpu_launches": 2 * args.steps,
-        "roofline": {"kernel": "fp8_gemm_blockscaled", "bound": "tensor",
-                     "achieved": round(gemm_tflops, 2), "peak": round(fp8_peak, 1),
-                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
-                     "peak_source": "%s bf16 burst x 2 (nominal FP8:BF16 dense ratio)" % peak_src,
-                     "traffic": profiled_traffic(),
-                     "algorithmic_bytes": M * K + N * K + M * N * 2 + (K // 128) * (M + N // 128) * 4},
-        "quant_phase_ms": round(quant_phase_ms, 5),
-        "kernels": {
-            "fp8_gemm_blockscaled": {"ms": round(gemm_ms, 5), "tflops": round(gemm_tflops, 2),
-                                     "frac_fp8_peak": round(gemm_tflops / fp8_peak, 4)},
-            "fp8_quant_fprop_operands": {
-                "ms": round(qp_ms, 5),
-                "gbs": round((qx_bytes + qw_bytes) / (qp_ms * 1e-3) / 1e9, 1),
-                "frac_hbm": round((qx_bytes + qw_bytes) / (qp_ms * 1e-3) / 1e9 / hbm, 4)},
-            "fp8_quant_act_1x128": {"ms": round(qx_ms, 5),
-                                    "gbs": round(qx_bytes / (qx_ms * 1e-3) / 1e9, 1),
-                                    "frac_hbm": round(qx_bytes / (qx_ms * 1e-3) / 1e9 / hbm, 4)},
-            "fp8_quant_weight_128x128": {"ms": round(qw_ms, 5),
-                                         "gbs": round(qw_bytes / (qw_ms * 1e-3) / 1e9, 1),
-                                         "frac_hbm": round(qw_bytes / (qw_ms * 1e-3) / 1e9 / hbm,
-                                                           4)},
-        },
-        "clocks": clocks,
-        "wall_s_timed_region": round(wall, 3),
+                   "l2": "flushed between steps (%d MB written, then read back); the step's "
+                         "operands (~0.8 GB) are larger than L2" % (2 * L2_BYTES >> 20),
+                   "step": list(Trio.NAMES)},
+        "e2e": e2e,
+        "gpu_launches": nk * args.steps,
+        "roofline": roofline,
+        "kernels": kernels,
+        "peaks": peaks,
+        "configs": configs,
+        "clocks": clk.summary(),
+        "clocks_timed_region": clk.summary(t_start, t_end),
+        "wall_s_timed_region": round(t_end - t_start, 4),
+        "wall_s_measurement": round(t_all - t_start, 2),
     }
     if args.cpu_baseline and rank == 0:
-        line["cpu_baseline"] = cpu_baseline(args.cpu_sample_rows)
+        line["cpu_baseline"] = cpu_baseline_trio(args.cpu_tokens, wl)
     return line
 
 
-# ------------------------------------------------------------ MoE workload --
-def run_moe(args, rank, world, local):
-    from fp8_fine_grained_22_b300 import fp8fg
+def trio_e2e(args, tr, d, flops, world):
+    """The trio through the public API with host buffers: every step copies its
+    X, W and dY up from pinned host memory and its Y, dX and dW down.  The
+    copies of neighbouring steps overlap: step i's inputs go up on one copy
+    stream while step i-1 computes and step i-2's results come down on
+    another (two device buffer sets rotate; events order the reuse of each
+    set).  The last result that came down must equal the device-resident
+    step's."""
+    dev = d.dev
+    depth = 2
+    host_in = [t.cpu().pin_memory() for t in (tr.x, tr.w, tr.dy)]
+    dev_in = [[tr.x, tr.w, tr.dy]] + [[torch.empty_like(t) for t in (tr.x, tr.w, tr.dy)]
+                                      for _ in range(depth - 1)]
+    dev_out = [[tr.y, tr.dx, tr.dw]] + [[torch.empty_like(t) for t in (tr.y, tr.dx, tr.dw)]
+                                        for _ in range(depth - 1)]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (tr.y, tr.dx, tr.dw)]
+                for _ in range(depth)]
+    h2d = sum(t.numel() * t.element_size() for t in host_in)
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(depth)]
+    ev_comp = [torch.cuda.Event() for _ in range(depth)]
+    ev_out = [torch.cuda.Event() for _ in range(depth)]
+    s = d.stream
 
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
-    fp8fg.lib()  # fail loudly if the CUDA library is missing
-    wl = inputs.moe_prefill(seed=0, device="cpu")
+    def e2e_step(i):
+        sl = i % depth
+        up.wait_event(ev_comp[sl])            # the set's previous compute has read it
+        with torch.cuda.stream(up):
+            for dst, src in zip(dev_in[sl], host_in):
+                dst.copy_(src, non_blocking=True)
+        ev_in[sl].record(up)
+        s.wait_event(ev_in[sl])
+        s.wait_event(ev_out[sl])              # the set's previous results are down
+        x, w, dy = dev_in[sl]
+        y, dx, dw = dev_out[sl]
+        tr.step(x=x, w=w, dy=dy, y=y, dx=dx, dw=dw)
+        ev_comp[sl].record(s)
+        down.wait_event(ev_comp[sl])
+        with torch.cuda.stream(down):
+            for dst, src in zip(host_out[sl], dev_out[sl]):
+                dst.copy_(src, non_blocking=True)
+        ev_out[sl].record(down)
+
+    n = max(1, min(args.steps, args.e2e_steps))
+    for i in range(depth):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(up)
+    for i in range(n):
+        e2e_step(i)
+    b.record(down)                            # after the last results are down
+    torch.cuda.synchronize()
+    ms = reduce_max(a.elapsed_time(b) / n, dev)
+    last = host_out[(n - 1) % depth]
+    tr.step()
+    torch.cuda.synchronize()
+    for h, t in zip(last, (tr.y, tr.dx, tr.dw)):
+        if not torch.equal(h, t.cpu()):
+            raise RuntimeError("end-to-end result differs from the device-resident step")
+    return {"value": round(whole_job_tflops(world, flops, ms), 3), "unit": "TFLOP/s",
+            "ms_per_step": round(ms, 4), "steps": n, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h,
+            "how": "pinned host X, W, dY up and Y, dX, dW down every step; copies of "
+                   "neighbouring steps overlap on two copy streams"}
+
+
+# ------------------------------------------------- the other configurations --
+def measure_configs(args, d, peaks, tr):
+    out = {}
+    out["cfg1_gemm_m128_n256_k512_f32"] = cfg1(d, peaks)
+    out["cfg2_fprop_m8192_n7168_k2048_bf16"] = cfg2(d, peaks)
+    out["cfg3_training_trio"] = "the headline step above (kernels, roofline, e2e)"
+    moe = cfg4(d, peaks)
+    out["cfg4_moe_prefill_t16384_top8of256_e32"] = moe.pop("result")
+    out["cfg5_moe_decode_e32_t1to256"] = cfg5(d, peaks, moe)
+    out["quantisers"] = quantisers(d, peaks, tr, moe)
+    return out
+
+
+def cfg1(d, peaks):
+    """M=128, N=256, K=512, FP32 out: latency of the path and of the GEMM alone
+    (device time, the device kept busy while the host issues the launches)."""
+    from fp8_fine_grained_22_b300 import fp8fg
+    wl = inputs.small_dense(seed=0)
+    x, w = wl.x.to(d.dev), wl.w.to(d.dev)
+    xq, sx = fp8fg.fp8_quant_act_1x128(x)
+    wq, _, sw = fp8fg.fp8_quant_weight_128x128(w)
+    y = torch.empty((wl.M, wl.N), dtype=torch.float32, device=d.dev)
+    s = d.stream
+    gemm = lambda: fp8fg.fp8_gemm_blockscaled(xq, sx, wq, sw, out_dtype=torch.float32, c=y,
+                                              stream=s)
+
+    def path():
+        fp8fg.fp8_quant_fprop_operands(x, w, xq=xq, sx=sx, wq=wq, sw=sw, stream=s)
+        gemm()
+
+    g_ms = d.kernel_ms(gemm, reps=200, flush=False)
+    p_ms = d.kernel_ms(path, reps=200, flush=False)
+    f = 2.0 * wl.M * wl.N * wl.K
+    return {"gemm_us": round(g_ms * 1e3, 2), "path_us": round(p_ms * 1e3, 2),
+            "path": "fp8_quant_fprop_operands + fp8_gemm_blockscaled (2 launches)",
+            "gemm_tflops": round(tflops(f, g_ms), 3), "bound": "latency (report us)",
+            "l2": "hot (latency case)"}
+
+
+def cfg2(d, peaks):
+    """X[8192, 2048] . W[2048, 7168] -> BF16: operand quantiser + GEMM."""
+    from fp8_fine_grained_22_b300 import fp8fg
+    wl = inputs.fprop_dense(seed=0)
+    M, N, K = wl.M, wl.N, wl.K
+    x, w = wl.x.to(d.dev), wl.w.to(d.dev)
+    xq = torch.empty((M, K), dtype=torch.uint8, device=d.dev)
+    sx = torch.empty((K // 128, M), dtype=torch.float32, device=d.dev)
+    wq = torch.empty((N, K), dtype=torch.uint8, device=d.dev)
+    sw = torch.empty((N // 128, K // 128), dtype=torch.float32, device=d.dev)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=d.dev)
+    s = d.stream
+    quant = lambda: fp8fg.fp8_quant_fprop_operands(x, w, xq=xq, sx=sx, wq=wq, sw=sw, stream=s)
+    gemm = lambda: fp8fg.fp8_gemm_blockscaled(xq, sx, wq, sw, out_dtype=torch.bfloat16, c=y,
+                                              stream=s)
+
+    def step():
+        quant()
+        gemm()
+
+    st = d.kernel_ms(step, reps=50)
+    g = d.kernel_ms(gemm, reps=50)
+    q = d.kernel_ms(quant, reps=50)
+    qx = d.kernel_ms(lambda: fp8fg.fp8_quant_act_1x128(x, xq, sx, stream=s), reps=50)
+    qw = d.kernel_ms(lambda: fp8fg.fp8_quant_weight_128x128(w, wq=wq, sw=sw, stream=s), reps=50)
+    f = 2.0 * M * N * K
+    qb = q1x128_bytes(M, K) + q128x128_bytes(K, N, False)
+    tf = tflops(f, g)
+    return {"step_ms": round(st, 5), "step_tflops": round(tflops(f, st), 2),
+            "gemm_ms": round(g, 5), "gemm_tflops": round(tf, 2), "gemm_frac": frac_set(tf, peaks),
+            "gemm_traffic": profiled_traffic("gemm_fprop_m8192_n7168_k2048"),
+            "quant_operands_ms": round(q, 5), "quant_operands_gbs": round(gbs(qb, q), 1),
+            "quant_operands_frac_hbm": round(gbs(qb, q) / peaks["hbm"], 4),
+            "quant_1x128_x_ms": round(qx, 5),
+            "quant_1x128_x_frac_hbm": round(gbs(q1x128_bytes(M, K), qx) / peaks["hbm"], 4),
+            "quant_128x128_w_ms": round(qw, 5),
+            "quant_128x128_w_frac_hbm": round(gbs(q128x128_bytes(K, N, False), qw) / peaks["hbm"],
+                                              4),
+            "l2": "flushed before each repetition"}
+
+
+def cfg4(d, peaks):
+    """MoE prefill: FP8 dispatch of 16384 tokens (top-8 of 256, 32 local
+    experts) + grouped GEMM against W[7168, 4096] per expert.  The weights are
+    static (quantised once); their quantisation is timed separately."""
+    from fp8_fine_grained_22_b300 import fp8fg
+    wl = inputs.moe_prefill(seed=0, device=d.dev)
     x_tok, order = wl.extra["x_tokens"], wl.extra["topk_ids"].to(torch.int32).contiguous()
     T, K = x_tok.shape
     E, N = wl.E, wl.N
     topk = order.shape[1]
     cap = T * min(topk, E)
     R = int(wl.offsets[-1])
-    flops = 2.0 * R * N * K
-    x = x_tok.to(dev)
-    ids = order.to(dev)
-    wq = torch.empty((E, N, K), dtype=torch.uint8, device=dev)
-    sw = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device=dev)
-    for e in range(E):  # static weights, quantised once
-        fp8fg.fp8_quant_weight_128x128(wl.w[e].to(dev), wq=wq[e], sw=sw[e])
-    del wl
-    xq = torch.empty((cap, K), dtype=torch.uint8, device=dev)
-    sx = torch.empty((K // 128, cap), dtype=torch.float32, device=dev)
-    off = torch.empty(E + 1, dtype=torch.int32, device=dev)
-    tok = torch.empty(cap, dtype=torch.int32, device=dev)
-    ws = fp8fg.moe_dispatch_workspace(T, E, dev)
-    y = torch.empty((cap, N), dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    x = x_tok.to(d.dev)
+    ids = order.to(d.dev)
+    s = d.stream
+    wq = torch.empty((E, N, K), dtype=torch.uint8, device=d.dev)
+    sw = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device=d.dev)
 
-    def flush_l2():
-        flush.zero_()
-        torch.sum(flush, dim=0, out=flush_sink)
+    def quant_weights():
+        for e in range(E):
+            fp8fg.fp8_quant_weight_128x128(wl.w[e], wq=wq[e], sw=sw[e], stream=s)
 
-    def dispatch():
-        fp8fg.fp8_moe_dispatch_quant(x, ids, 0, E, cap=cap, xq=xq, sx=sx, offsets=off,
-                                     token_ids=tok, workspace=ws, stream=stream)
+    wq_ms = d.kernel_ms(quant_weights, reps=5)
+    xq = torch.empty((cap, K), dtype=torch.uint8, device=d.dev)
+    sx = torch.empty((K // 128, cap), dtype=torch.float32, device=d.dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=d.dev)
+    tok = torch.empty(cap, dtype=torch.int32, device=d.dev)
+    ws = fp8fg.moe_dispatch_workspace(T, E, d.dev)
+    y = torch.empty((cap, N), dtype=torch.bfloat16, device=d.dev)
+    dispatch = lambda: fp8fg.fp8_moe_dispatch_quant(x, ids, 0, E, cap=cap, xq=xq, sx=sx,
+                                                    offsets=off, token_ids=tok, workspace=ws,
+                                                    stream=s)
+    grouped = lambda: fp8fg.fp8_grouped_gemm_moe(xq, sx, wq, sw, off, c=y, stream=s)
 
-    def grouped():
-        fp8fg.fp8_grouped_gemm_moe(xq, sx, wq, sw, off, c=y, stream=stream)
-
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+    def step():
         dispatch()
-        if ev is not None:
-            ev[1].record(stream)
         grouped()
-        if ev is not None:
-            ev[2].record(stream)
 
-    def kernel_ms(fn, reps=20):
-        e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(reps)]
-        for a, b in e:
-            flush_l2()
-            a.record(stream)
-            fn()
-            b.record(stream)
-        torch.cuda.synchronize()
-        return statistics.mean(a.elapsed_time(b) for a, b in e)
-
-    for _ in range(args.warmup):
-        flush_l2()
-        step()
-    torch.cuda.synchronize()
-    if fp8fg.device_error() != 0:
-        raise RuntimeError("device-side error during warm-up")
+    st = d.kernel_ms(step, reps=20)
     if int(off[-1].item()) != R:
         raise RuntimeError("dispatch produced %d rows, expected %d" % (int(off[-1].item()), R))
-    steps = min(args.steps, args.moe_steps)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-    rank_barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t0 = time.perf_counter()
-        for i in range(steps):
-            flush_l2()
-            step(events[i])
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
-    rank_barrier()
-    st = [e[0].elapsed_time(e[2]) for e in events]
-    dp = [e[0].elapsed_time(e[1]) for e in events]
-    gm = [e[1].elapsed_time(e[2]) for e in events]
-    ms_step = reduce_max(statistics.mean(st), dev)
-    disp_ms, gemm_ms = statistics.mean(dp), statistics.mean(gm)
-    disp_alone = kernel_ms(dispatch)
-    gemm_alone = kernel_ms(grouped)
-
-    # end to end: tokens and routing in from pinned host memory, the offsets
-    # and the R output rows out, every step; the copies of neighbouring steps
-    # overlap on two copy streams as in the dense bench (two buffer sets).
-    depth = 2
-    xh, idh = x_tok.pin_memory(), order.pin_memory()
-    yh = [torch.empty((R, N), dtype=torch.bfloat16).pin_memory() for _ in range(depth)]
-    offh = [torch.empty(E + 1, dtype=torch.int32).pin_memory() for _ in range(depth)]
-    xs = [x] + [torch.empty_like(x) for _ in range(depth - 1)]
-    idss = [ids] + [torch.empty_like(ids) for _ in range(depth - 1)]
-    ys = [y] + [torch.empty_like(y) for _ in range(depth - 1)]
-    offs = [off] + [torch.empty_like(off) for _ in range(depth - 1)]
-    up, down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(depth)]
-    ev_comp = [torch.cuda.Event() for _ in range(depth)]
-    ev_out = [torch.cuda.Event() for _ in range(depth)]
-
-    def e2e_step(i):
-        sl = i % depth
-        up.wait_event(ev_comp[sl])
-        with torch.cuda.stream(up):
-            xs[sl].copy_(xh, non_blocking=True)
-            idss[sl].copy_(idh, non_blocking=True)
-        ev_in[sl].record(up)
-        stream.wait_event(ev_in[sl])
-        stream.wait_event(ev_out[sl])
-        fp8fg.fp8_moe_dispatch_quant(xs[sl], idss[sl], 0, E, cap=cap, xq=xq, sx=sx,
-                                     offsets=offs[sl], token_ids=tok, workspace=ws,
-                                     stream=stream)
-        fp8fg.fp8_grouped_gemm_moe(xq, sx, wq, sw, offs[sl], c=ys[sl], stream=stream)
-        ev_comp[sl].record(stream)
-        down.wait_event(ev_comp[sl])
-        with torch.cuda.stream(down):
-            offh[sl].copy_(offs[sl], non_blocking=True)
-            yh[sl].copy_(ys[sl][:R], non_blocking=True)
-        ev_out[sl].record(down)
-
-    e2e_steps = min(steps, args.e2e_steps)
-    for i in range(depth):
-        e2e_step(i)
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(up)
-    for i in range(e2e_steps):
-        e2e_step(i)
-    b.record(down)
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max(a.elapsed_time(b) / e2e_steps, dev)
-    last = (e2e_steps - 1) % depth
-    step()
-    torch.cuda.synchronize()
-    if not (torch.equal(offh[last], off.cpu()) and torch.equal(yh[last], y[:R].cpu())):
-        raise RuntimeError("end-to-end result differs from the device-resident step")
-    if fp8fg.device_error() != 0:
-        raise RuntimeError("device-side error")
-
-    peaks, peak_src = measured_peaks()
-    fp8_peak = 2.0 * peaks["bf16_tflops"]
-    hbm = peaks["hbm_gbs"]
-    gemm_tflops = flops / (gemm_ms * 1e-3) / 1e12
-    # bytes the dispatch must move: the rows of tokens with a local expert
-    # (others are not read), the packed codes, scales, routing and token ids
+    dp = d.kernel_ms(dispatch, reps=20)
+    gm = d.kernel_ms(grouped, reps=20)
+    f = 2.0 * R * N * K
     n_active = int(((order >= 0) & (order < E)).any(dim=1).sum())
     disp_bytes = n_active * K * 2 + R * K + (K // 128) * R * 4 + T * topk * 4 + R * 4
-    line = {
-        "metric": METRIC,
-        "value": round(whole_job_tflops(world, flops, ms_step), 2),
-        "unit": "TFLOP/s",
-        "n_gpus": world,
-        "steps": steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "e4m3 x e4m3 -> f32 accumulate, bf16 out",
-        "data": "synthetic (seeded: N(0,1) tokens with 1% x100 outlier channels, sigmoid+bias "
-                "top-8 routing of 256 experts, N(0,0.006^2) expert weights)",
-        "config": {"workload": MOE_WORKLOAD, "T": T, "topk": topk, "local_experts": E,
-                   "rows": R, "N": N, "K": K, "parallelism": "replicas (dp%d, no collective)"
-                   % world,
-                   "l2": "flushed between steps (%d MB written, then read back)" % (
-                       flush.numel() * 4 >> 20),
-                   "step": ["fp8_moe_dispatch_quant", "fp8_grouped_gemm_moe"],
-                   "weights": "quantised once before timing (static)"},
-        "e2e": {"value": round(whole_job_tflops(world, flops, e2e_ms), 3), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
-                "h2d_bytes_per_step": T * K * 2 + T * topk * 4,
-                "d2h_bytes_per_step": R * N * 2 + (E + 1) * 4},
-        "gpu_launches": 4 * steps,
-        "roofline": {"kernel": "fp8_grouped_gemm_moe", "bound": "tensor",
-                     "achieved": round(gemm_tflops, 2), "peak": round(fp8_peak, 1),
-                     "unit": "TFLOP/s", "frac": round(gemm_tflops / fp8_peak, 4),
-                     "peak_source": "%s bf16 burst x 2 (nominal FP8:BF16 dense ratio)" % peak_src,
-                     "traffic": None},
-        "kernels": {
-            "fp8_moe_dispatch_quant (in step)": {"ms": round(disp_ms, 5)},
-            "fp8_moe_dispatch_quant (alone)": {
-                "ms": round(disp_alone, 5),
-                "gbs": round(disp_bytes / (disp_alone * 1e-3) / 1e9, 1),
-                "frac_hbm": round(disp_bytes / (disp_alone * 1e-3) / 1e9 / hbm, 4)},
-            "fp8_grouped_gemm_moe (in step)": {"ms": round(gemm_ms, 5),
-                                               "tflops": round(gemm_tflops, 2)},
-            "fp8_grouped_gemm_moe (alone)": {
-                "ms": round(gemm_alone, 5),
-                "tflops": round(flops / (gemm_alone * 1e-3) / 1e12, 2)},
-        },
-        "clocks": clk.summary(),
-        "wall_s_timed_region": round(wall, 3),
-    }
-    if args.cpu_baseline and rank == 0:
-        line["cpu_baseline"] = cpu_baseline_moe(args.ref_rows)
-    return line
+    wbytes = E * q128x128_bytes(K, N, False)
+    tf = tflops(f, gm)
+    res = {"rows": R, "tokens": T, "experts": E, "gemm_flops": f,
+           "step_ms": round(st, 5), "step_tflops": round(tflops(f, st), 2),
+           "dispatch_ms": round(dp, 5), "dispatch_gbs": round(gbs(disp_bytes, dp), 1),
+           "dispatch_frac_hbm": round(gbs(disp_bytes, dp) / peaks["hbm"], 4),
+           "grouped_gemm_ms": round(gm, 5), "grouped_gemm_tflops": round(tf, 2),
+           "grouped_gemm_frac": frac_set(tf, peaks),
+           "weight_quant_ms (32 experts, static, outside the step)": round(wq_ms, 5),
+           "weight_quant_gbs": round(gbs(wbytes, wq_ms), 1),
+           "weight_quant_frac_hbm": round(gbs(wbytes, wq_ms) / peaks["hbm"], 4),
+           "reading": "routing as drawn (sigmoid + N(0,0.5) bias, top-8 of 256); the local "
+                      "experts receive %d of the 16384 x 8 assignments" % R,
+           "l2": "flushed before each repetition"}
+    return {"result": res, "wq": wq, "sw": sw, "x": x, "R": R}
 
 
-def run_moe_backward(args, rank, world, local):
-    """The expert layer's backward on the prefill routing: 1x128 quantisation of dY,
-    grouped Dgrad, per-expert 128x1 quantisation of X and dY, grouped Wgrad."""
+def cfg5(d, peaks, moe):
+    """Decode-shaped grouped GEMM: 32 experts with t_e ~ U[1, 256] tokens each,
+    X pre-quantised 1x128, W FP8 [7168, 4096] pre-quantised (the prefill
+    workload's expert weights, the same distribution), BF16 out; against HBM."""
     from fp8_fine_grained_22_b300 import fp8fg
+    wl = inputs.moe_decode(seed=0, device="cpu")
+    E, K, N = wl.E, wl.K, wl.N
+    T = int(wl.offsets[-1])
+    s = d.stream
+    xq, sx = fp8fg.fp8_quant_act_1x128(wl.x.to(d.dev))
+    off = torch.from_numpy(np.asarray(wl.offsets, np.int32)).to(d.dev)
+    y = torch.empty((T, N), dtype=torch.bfloat16, device=d.dev)
+    wq, sw = moe["wq"], moe["sw"]
+    gm = d.kernel_ms(lambda: fp8fg.fp8_grouped_gemm_moe(xq, sx, wq, sw, off, c=y, stream=s),
+                     reps=20)
+    nbytes = E * N * K + E * (N // 128) * (K // 128) * 4 + T * K + (K // 128) * T * 4 + T * N * 2
+    g = gbs(nbytes, gm)
+    f = 2.0 * T * N * K
+    return {"rows": T, "experts": E, "grouped_gemm_ms": round(gm, 5),
+            "algorithmic_bytes": nbytes, "gbs": round(g, 1),
+            "frac_hbm": round(g / peaks["hbm"], 4),
+            "frac_hbm_nominal": round(g / peaks["hbm_nominal"], 4),
+            "tflops": round(tflops(f, gm), 2),
+            "traffic": profiled_traffic("gemm_moe_decode_e32"),
+            "bound": "hbm (the weights: %.1f MB of the %.1f MB)" % (E * N * K / 1e6, nbytes / 1e6),
+            "l2": "flushed before each repetition"}
 
-    dev = torch.device("cuda", local)
-    torch.cuda.set_device(dev)
+
+def quantisers(d, peaks, tr, moe):
+    """Every quantiser alone at the trio and prefill sizes (L2 flushed)."""
+    from fp8_fine_grained_22_b300 import fp8fg
+    s = d.stream
+    M, K, N = tr.M, tr.K, tr.N
+    hbm = peaks["hbm"]
+    res = {}
+
+    def add(name, fn, nbytes):
+        ms = d.kernel_ms(fn, reps=20)
+        g = gbs(nbytes, ms)
+        res[name] = {"ms": round(ms, 5), "algorithmic_bytes": nbytes, "gbs": round(g, 1),
+                     "frac_hbm": round(g / hbm, 4)}
+
+    add("1x128 X[8192,7168]", lambda: fp8fg.fp8_quant_act_1x128(tr.x, tr.xq, tr.sx, stream=s),
+        q1x128_bytes(M, K))
+    add("1x128 dY[8192,4096]", lambda: fp8fg.fp8_quant_act_1x128(tr.dy, tr.dyq, tr.sdy, stream=s),
+        q1x128_bytes(M, N))
+    add("128x1 X[8192,7168]", lambda: fp8fg.fp8_quant_act_128x1(tr.x, tr.xqT, tr.sxT, stream=s),
+        q128x1_bytes(M, K))
+    add("128x1 dY[8192,4096]",
+        lambda: fp8fg.fp8_quant_act_128x1(tr.dy, tr.dyqT, tr.sdyT, stream=s), q128x1_bytes(M, N))
+    add("128x128 W[7168,4096] wq",
+        lambda: fp8fg.fp8_quant_weight_128x128(tr.w, wq=tr.wq, sw=tr.sw, stream=s),
+        q128x128_bytes(K, N, False))
+    add("128x128 W[7168,4096] wq+wqT",
+        lambda: fp8fg.fp8_quant_weight_128x128(tr.w, wq=tr.wq, wqT=tr.wqT, sw=tr.sw, stream=s),
+        q128x128_bytes(K, N, True))
+    add("operands X 1x128 + W 128x128 wq+wqT (trio)",
+        lambda: fp8fg.fp8_quant_fprop_operands(tr.x, tr.w, xq=tr.xq, sx=tr.sx, wq=tr.wq,
+                                               wqT=tr.wqT, sw=tr.sw, stream=s),
+        q1x128_bytes(M, K) + q128x128_bytes(K, N, True))
+    xp = moe["x"]
+    T = xp.shape[0]
+    xq = torch.empty((T, K), dtype=torch.uint8, device=d.dev)
+    sx = torch.empty((K // 128, T), dtype=torch.float32, device=d.dev)
+    add("1x128 X[16384,7168] (prefill tokens)",
+        lambda: fp8fg.fp8_quant_act_1x128(xp, xq, sx, stream=s), q1x128_bytes(T, K))
+    return res
+
+
+# ------------------------------------------------- single-workload lines --
+def run_single(args, rank, world, local):
+    """--workload fprop_dense | moe_prefill | moe_decode | moe_backward: one
+    workload's line on its own (its step timed as the headline)."""
+    from fp8_fine_grained_22_b300 import fp8fg
+    torch.cuda.set_device(local)
+    clk = ClockSampler(torch.device("cuda", local)).__enter__()
+    d = Dev(local, clk)
     fp8fg.lib()
-    wl = inputs.moe_prefill(seed=0, device="cpu")
+    peaks = fp8_peaks(d.dev)
+    t0 = time.perf_counter()
+    if args.workload == "fprop_dense":
+        r = cfg2(d, peaks)
+        flops, ms, name = 2.0 * 8192 * 7168 * 2048, r["step_ms"], "fprop_m8192_n7168_k2048_bf16"
+        rl = {"kernel": "fp8_gemm_blockscaled", "bound": "tensor", "achieved": r["gemm_tflops"],
+              "peak": peaks["fp8_from_bf16"], "unit": "TFLOP/s",
+              "frac": r["gemm_frac"]["of_2x_bf16_measured"], "traffic": r["gemm_traffic"]}
+    elif args.workload == "moe_prefill":
+        r = cfg4(d, peaks)["result"]
+        flops, ms, name = r["gemm_flops"], r["step_ms"], "moe_prefill_t16384_top8of256_e32"
+        rl = {"kernel": "fp8_grouped_gemm_moe", "bound": "tensor",
+              "achieved": r["grouped_gemm_tflops"], "peak": peaks["fp8_from_bf16"],
+              "unit": "TFLOP/s", "frac": r["grouped_gemm_frac"]["of_2x_bf16_measured"],
+              "traffic": None}
+    elif args.workload == "moe_decode":
+        moe = cfg4(d, peaks)
+        r = cfg5(d, peaks, moe)
+        flops, ms, name = 2.0 * r["rows"] * 4096 * 7168, r["grouped_gemm_ms"], "moe_decode_e32"
+        rl = {"kernel": "fp8_grouped_gemm_moe", "bound": "hbm", "achieved": r["gbs"],
+              "peak": peaks["hbm"], "unit": "GB/s", "frac": r["frac_hbm"],
+              "traffic": r["traffic"]}
+    else:
+        r = moe_backward(d, peaks)
+        flops, ms, name = r["flops"], r["step_ms"], "moe_prefill_backward_e32"
+        rl = r.pop("roofline")
+    t1 = time.perf_counter()
+    clk.__exit__()
+    return {"metric": METRIC, "value": round(whole_job_tflops(world, flops, ms), 2),
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "e4m3 x e4m3 -> f32 accumulate",
+            "data": "synthetic (seeded)", "config": {"workload": name},
+            "roofline": rl, "detail": r, "peaks": peaks, "clocks": clk.summary(t0, t1)}
+
+
+def moe_backward(d, peaks):
+    """The prefill expert layer's backward: 1x128 quantisation of dY, grouped
+    Dgrad, per-expert 128x1 quantisation of X and dY, grouped Wgrad (FP32 dW)."""
+    from fp8_fine_grained_22_b300 import fp8fg
+    wl = inputs.moe_prefill(seed=0, device=d.dev)
     E, N, K = wl.E, wl.N, wl.K
     R = int(wl.offsets[-1])
-    x = wl.x.to(dev)  # packed rows [R, K] (the Fprop inputs)
-    dy = inputs.grad(R, N, torch.Generator().manual_seed(1)).to(dev)
-    off = torch.from_numpy(np.asarray(wl.offsets, np.int32)).to(dev)
-    wqT = torch.empty((E, K, N), dtype=torch.uint8, device=dev)
-    sw = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device=dev)
-    for e in range(E):  # static weights: the transposed codes Dgrad reads
-        fp8fg.fp8_quant_weight_128x128(wl.w[e].to(dev), want_wq=False, wqT=wqT[e], sw=sw[e])
-    del wl
+    s = d.stream
+    x = wl.x.to(d.dev)
+    dy = inputs.grad(R, N, torch.Generator().manual_seed(1)).to(d.dev)
+    off = torch.from_numpy(np.asarray(wl.offsets, np.int32)).to(d.dev)
+    wqT = torch.empty((E, K, N), dtype=torch.uint8, device=d.dev)
+    sw = torch.empty((E, N // 128, K // 128), dtype=torch.float32, device=d.dev)
+    for e in range(E):
+        fp8fg.fp8_quant_weight_128x128(wl.w[e], want_wq=False, wqT=wqT[e], sw=sw[e])
     Tp = fp8fg.padded_tokens(R, E)
-    dq = torch.empty((R, N), dtype=torch.uint8, device=dev)
-    sd = torch.empty((N // 128, R), dtype=torch.float32, device=dev)
-    dx = torch.empty((R, K), dtype=torch.bfloat16, device=dev)
-    xqT = torch.empty((K, Tp), dtype=torch.uint8, device=dev)
-    sxT = torch.empty((Tp // 128, K), dtype=torch.float32, device=dev)
-    dqT = torch.empty((N, Tp), dtype=torch.uint8, device=dev)
-    sdT = torch.empty((Tp // 128, N), dtype=torch.float32, device=dev)
-    pofs = torch.empty(E + 1, dtype=torch.int32, device=dev)
-    dw = torch.empty((E, K, N), dtype=torch.float32, device=dev)
-    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
-    flush_sink = torch.empty((), dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    e_ = lambda shape, dt: torch.empty(shape, dtype=dt, device=d.dev)
+    dq, sd = e_((R, N), torch.uint8), e_((N // 128, R), torch.float32)
+    dx = e_((R, K), torch.bfloat16)
+    xqT, sxT = e_((K, Tp), torch.uint8), e_((Tp // 128, K), torch.float32)
+    dqT, sdT = e_((N, Tp), torch.uint8), e_((Tp // 128, N), torch.float32)
+    pofs = e_(E + 1, torch.int32)
+    dw = e_((E, K, N), torch.float32)
 
-    def flush_l2():
-        flush.zero_()
-        torch.sum(flush, dim=0, out=flush_sink)
-
-    def dgrad():
-        fp8fg.fp8_quant_act_1x128(dy, dq, sd, stream=stream)
-        fp8fg.fp8_grouped_gemm_moe_dgrad(dq, sd, wqT, sw, off, c=dx, stream=stream)
-
-    def wgrad():
+    def step():
+        fp8fg.fp8_quant_act_1x128(dy, dq, sd, stream=s)
+        fp8fg.fp8_grouped_gemm_moe_dgrad(dq, sd, wqT, sw, off, c=dx, stream=s)
         fp8fg.fp8_quant_act_128x1_grouped(x, off, E, Tp=Tp, xqT=xqT, sxT=sxT, pofs=pofs,
-                                          stream=stream)
+                                          stream=s)
         fp8fg.fp8_quant_act_128x1_grouped(dy, off, E, Tp=Tp, xqT=dqT, sxT=sdT, pofs=pofs,
-                                          stream=stream)
-        fp8fg.fp8_grouped_gemm_moe_wgrad(xqT, sxT, dqT, sdT, pofs, c=dw, stream=stream)
+                                          stream=s)
+        fp8fg.fp8_grouped_gemm_moe_wgrad(xqT, sxT, dqT, sdT, pofs, c=dw, stream=s)
 
-    def step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
-        dgrad()
-        if ev is not None:
-            ev[1].record(stream)
-        wgrad()
-        if ev is not None:
-            ev[2].record(stream)
-
-    def kernel_ms(fn, reps=10):
-        e = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-             for _ in range(reps)]
-        for a, b in e:
-            flush_l2()
-            a.record(stream)
-            fn()
-            b.record(stream)
-        torch.cuda.synchronize()
-        return statistics.mean(a.elapsed_time(b) for a, b in e)
-
-    for _ in range(args.warmup):
-        flush_l2()
-        step()
-    torch.cuda.synchronize()
-    if fp8fg.device_error() != 0:
-        raise RuntimeError("device-side error during warm-up")
-    steps = min(args.steps, args.moe_steps // 4)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
-    rank_barrier()
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        t0 = time.perf_counter()
-        for i in range(steps):
-            flush_l2()
-            step(events[i])
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - t0
-    rank_barrier()
-    ms_step = reduce_max(statistics.mean(e[0].elapsed_time(e[2]) for e in events), dev)
-    dgrad_ms = statistics.mean(e[0].elapsed_time(e[1]) for e in events)
-    wgrad_ms = statistics.mean(e[1].elapsed_time(e[2]) for e in events)
-    wg_gemm_ms = kernel_ms(lambda: fp8fg.fp8_grouped_gemm_moe_wgrad(xqT, sxT, dqT, sdT, pofs,
-                                                                     c=dw, stream=stream))
-    dg_gemm_ms = kernel_ms(lambda: fp8fg.fp8_grouped_gemm_moe_dgrad(dq, sd, wqT, sw, off, c=dx,
-                                                                     stream=stream))
+    st = d.kernel_ms(step, reps=10)
+    wg = d.kernel_ms(lambda: fp8fg.fp8_grouped_gemm_moe_wgrad(xqT, sxT, dqT, sdT, pofs, c=dw,
+                                                              stream=s), reps=10)
+    dg = d.kernel_ms(lambda: fp8fg.fp8_grouped_gemm_moe_dgrad(dq, sd, wqT, sw, off, c=dx,
+                                                              stream=s), reps=10)
     P = int(pofs[-1].item())
-
-    # end to end: dY in from pinned host memory, dX and dW out
-    dyh = dy.cpu().pin_memory()
-    dxh = torch.empty((R, K), dtype=torch.bfloat16).pin_memory()
-    dwh = torch.empty((E, K, N), dtype=torch.float32).pin_memory()
-
-    def e2e_step():
-        dy.copy_(dyh, non_blocking=True)
-        step()
-        dxh.copy_(dx, non_blocking=True)
-        dwh.copy_(dw, non_blocking=True)
-
-    e2e_steps = min(steps, max(1, args.e2e_steps // 10))
-    e2e_step()
-    torch.cuda.synchronize()
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    b.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = reduce_max(a.elapsed_time(b) / e2e_steps, dev)
-    if fp8fg.device_error() != 0:
-        raise RuntimeError("device-side error")
-
-    peaks, peak_src = measured_peaks()
-    hbm = peaks["hbm_gbs"]
-    fp8_peak = 2.0 * peaks["bf16_tflops"]
-    flops = 2.0 * R * N * K * 2  # Dgrad + Wgrad over the real tokens
-    wg_flops_padded = 2.0 * K * N * P
+    flops = 2.0 * R * N * K * 2
     wg_bytes = E * K * N * 4 + (K + N) * P + (P // 128) * (K + N) * 4
-    wg_gbs = wg_bytes / (wg_gemm_ms * 1e-3) / 1e9
-    line = {
-        "metric": METRIC,
-        "value": round(whole_job_tflops(world, flops, ms_step), 2),
-        "unit": "TFLOP/s",
-        "n_gpus": world,
-        "steps": steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "e4m3 x e4m3 -> f32 accumulate; dX bf16, dW f32",
-        "data": "synthetic (seeded: the prefill routing's packed rows, N(0,1e-3^2) output "
-                "gradients, N(0,0.006^2) expert weights)",
-        "config": {"workload": MOE_WORKLOAD + "_backward", "rows": R, "padded_rows": P,
-                   "local_experts": E, "N": N, "K": K,
-                   "parallelism": "replicas (dp%d, no collective)" % world,
-                   "l2": "flushed between steps (%d MB written, then read back)" % (
-                       flush.numel() * 4 >> 20),
-                   "step": ["fp8_quant_act_1x128 (dY)", "fp8_grouped_gemm_moe_dgrad",
-                            "fp8_quant_act_128x1_grouped (X, dY)", "fp8_grouped_gemm_moe_wgrad"],
-                   "weights": "quantised once before timing (static)"},
-        "e2e": {"value": round(whole_job_tflops(world, flops, e2e_ms), 3), "unit": "TFLOP/s",
-                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
-                "h2d_bytes_per_step": R * N * 2,
-                "d2h_bytes_per_step": R * K * 2 + E * K * N * 4},
-        "gpu_launches": 5 * steps,
-        "roofline": {"kernel": "fp8_grouped_gemm_moe_wgrad", "bound": "hbm",
-                     "achieved": round(wg_gbs, 1), "peak": round(hbm, 1), "unit": "GB/s",
-                     "frac": round(wg_gbs / hbm, 4),
-                     "peak_source": "%s copy bandwidth" % peak_src, "traffic": None,
-                     "note": "dW is E x %d x %d FP32 (%.2f GB): writing it dominates the "
-                             "kernel's %.3f TFLOP" % (K, N, E * K * N * 4 / 1e9,
-                                                       wg_flops_padded / 1e12)},
-        "kernels": {
-            "dgrad phase (quant dY + grouped Dgrad)": {"ms": round(dgrad_ms, 5)},
-            "wgrad phase (2 grouped 128x1 quants + grouped Wgrad)": {"ms": round(wgrad_ms, 5)},
-            "fp8_grouped_gemm_moe_dgrad (alone)": {
-                "ms": round(dg_gemm_ms, 5),
-                "tflops": round(2.0 * R * N * K / (dg_gemm_ms * 1e-3) / 1e12, 2),
-                "frac_fp8_peak": round(2.0 * R * N * K / (dg_gemm_ms * 1e-3) / 1e12 / fp8_peak,
-                                       4)},
-            "fp8_grouped_gemm_moe_wgrad (alone)": {
-                "ms": round(wg_gemm_ms, 5), "gbs": round(wg_gbs, 1),
-                "tflops_padded": round(wg_flops_padded / (wg_gemm_ms * 1e-3) / 1e12, 2)},
-        },
-        "clocks": clk.summary(),
-        "wall_s_timed_region": round(wall, 3),
-    }
-    if args.cpu_baseline and rank == 0:
-        line["cpu_baseline"] = cpu_baseline_moe_backward(args.ref_rows)
-    return line
-
-
-def cpu_baseline_moe_backward(n_rows):
-    """The oracle on the host for the expert backward: 1x128 quantisation of dY and the
-    binary64 grouped Dgrad of the first n_rows packed rows (their experts' weights
-    quantised), per-expert 128x1 quantisation of X and dY and the binary64 grouped Wgrad of
-    8 rows of every expert's dW."""
-    import oracle
-
-    wl = inputs.moe_prefill(seed=0, device="cpu")
-    threads = oracle.default_threads()
-    R = int(wl.offsets[-1])
-    dy = inputs.bf16_bits(inputs.grad(R, wl.N, torch.Generator().manual_seed(1)))
-    xb = inputs.bf16_bits(wl.x)
-    t0 = time.perf_counter()
-    dq, sd = oracle.quant_act_1x128(dy)
-    rows = np.arange(min(n_rows, R))
-    experts = np.unique(np.searchsorted(wl.offsets, rows, side="right") - 1)
-    bqT = np.zeros((wl.E, wl.K, wl.N), np.uint8)
-    sw = np.ones((wl.E, wl.N // 128, wl.K // 128), np.float32)
-    for e in experts:
-        _, bqT[e], sw[e] = oracle.quant_weight_128x128(inputs.bf16_bits(wl.w[e]))
-    dx = oracle.grouped_gemm(dq, sd, bqT, sw, wl.offsets, rows=rows, nthreads=threads,
-                             bmode=oracle.BSCALE_BLOCK128_T)
-    oracle.round_bf16(dx)
-    xqT, sxT, pofs = oracle.quant_act_128x1_grouped(xb, wl.offsets)
-    dqT, sdT, _ = oracle.quant_act_128x1_grouped(dy, wl.offsets)
-    wrows = np.arange(8)
-    oracle.grouped_wgrad(xqT, sxT, dqT, sdT, pofs, rows=wrows, nthreads=threads)
-    dt = time.perf_counter() - t0
-    flops = 2.0 * rows.size * wl.N * wl.K + 2.0 * wrows.size * wl.E * wl.N * int(pofs[-1]) / wl.E
-    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
-            "kind": "oracle", "seconds": round(dt, 2),
-            "sample": "quantisation of all of dY, X; grouped Dgrad of the first %d of %d rows; "
-                      "grouped Wgrad of %d rows of each of %d experts' dW" % (
-                          rows.size, R, wrows.size, wl.E)}
-
-
-def cpu_baseline_moe(n_rows):
-    """The oracle on the host: dispatch of every token (membership, gather, 1x128
-    quantisation), quantisation of the experts the sampled rows use, and the
-    binary64 grouped GEMM of n_rows packed rows."""
-    import oracle
-
-    wl = inputs.moe_prefill(seed=0, device="cpu")
-    threads = oracle.default_threads()
-    xb = inputs.bf16_bits(wl.extra["x_tokens"])
-    order = wl.extra["topk_ids"].numpy()
-    t0 = time.perf_counter()
-    aq, sa, offsets, _ = oracle.moe_dispatch_quant(xb, order, 0, wl.E)
-    rows = np.arange(min(n_rows, aq.shape[0]))
-    experts = np.unique(np.searchsorted(offsets, rows, side="right") - 1)
-    bq = np.zeros((wl.E, wl.N, wl.K), np.uint8)
-    sb = np.ones((wl.E, wl.N // 128, wl.K // 128), np.float32)
-    for e in experts:
-        bq[e], _, sb[e] = oracle.quant_weight_128x128(inputs.bf16_bits(wl.w[e]))
-    c = oracle.grouped_gemm(aq, sa, bq, sb, offsets, rows=rows, nthreads=threads)
-    oracle.round_bf16(c)
-    dt = time.perf_counter() - t0
-    flops = 2.0 * rows.size * wl.N * wl.K
-    return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
-            "kind": "oracle", "seconds": round(dt, 2),
-            "sample": "dispatch of all %d tokens, weights of %d experts quantised, binary64 "
-                      "grouped GEMM of the first %d of %d packed rows" % (
-                          xb.shape[0], experts.size, rows.size, aq.shape[0])}
+    return {"flops": flops, "step_ms": round(st, 5), "rows": R, "padded_rows": P,
+            "dgrad_ms": round(dg, 5), "dgrad_tflops": round(tflops(2.0 * R * N * K, dg), 2),
+            "wgrad_ms": round(wg, 5), "wgrad_gbs": round(gbs(wg_bytes, wg), 1),
+            "roofline": {"kernel": "fp8_grouped_gemm_moe_wgrad", "bound": "hbm",
+                         "achieved": round(gbs(wg_bytes, wg), 1), "peak": peaks["hbm"],
+                         "unit": "GB/s", "frac": round(gbs(wg_bytes, wg) / peaks["hbm"], 4),
+                         "traffic": None}}
 
 
 # ------------------------------------------------------- CPU oracle baseline --
-def cpu_baseline(n_rows, wl=None):
-    """The oracle on the host cores: quantise all of W and a sample of X rows,
-    then the binary64 block-scaled GEMM of those rows."""
+def cpu_baseline_trio(n_tokens, wl=None, slice_index=0):
+    """The oracle on the host cores: the whole trio on a slice of n_tokens
+    consecutive tokens (a multiple of 128): 1x128 and 128x1 quantisation of
+    the slice's X and dY, 128x128 quantisation of all of W, then the binary64
+    Fprop and Dgrad of the slice's rows and the Wgrad contracted over the
+    slice's tokens.  Its FLOPs are exactly n_tokens / 8192 of the step's."""
     import oracle
 
     if wl is None:
-        wl = inputs.fprop_dense(seed=0, device="cpu")
+        wl = inputs.training_trio(seed=0, device="cpu")
     threads = oracle.default_threads()
-    xb = inputs.bf16_bits(wl.x[:n_rows])
+    lo = (slice_index * n_tokens) % wl.M
+    xb = inputs.bf16_bits(wl.x[lo:lo + n_tokens])
+    dyb = inputs.bf16_bits(wl.dy[lo:lo + n_tokens])
     wb = inputs.bf16_bits(wl.w)
     t0 = time.perf_counter()
     aq, sa = oracle.quant_act_1x128(xb)
-    bq, _, sw = oracle.quant_weight_128x128(wb)
-    c = oracle.gemm_blockscaled(aq, sa, bq, sw, nthreads=threads)
-    oracle.round_bf16(c)
+    wq, wqT, sw = oracle.quant_weight_128x128(wb)
+    y = oracle.gemm_blockscaled(aq, sa, wq, sw, nthreads=threads)
+    oracle.round_bf16(y)
+    dq, sd = oracle.quant_act_1x128(dyb)
+    # sw [N/128][K/128] is the transposed-block layout of the Dgrad GEMM (K' = N, N' = K)
+    dx = oracle.gemm_blockscaled(dq, sd, wqT, sw, oracle.BSCALE_BLOCK128_T, nthreads=threads)
+    oracle.round_bf16(dx)
+    xqT, sxT = oracle.quant_act_128x1(xb)
+    dqT, sdT = oracle.quant_act_128x1(dyb)
+    oracle.gemm_blockscaled(xqT, sxT, dqT, sdT, oracle.BSCALE_ROW1x128, nthreads=threads)
     dt = time.perf_counter() - t0
-    flops = 2.0 * n_rows * wl.N * wl.K
+    flops = 3 * 2.0 * n_tokens * wl.K * wl.N
     return {"value": round(flops / dt / 1e12, 6), "unit": "TFLOP/s", "cores": threads,
             "kind": "oracle", "seconds": round(dt, 2),
-            "sample": "%d of %d rows of X (all of W quantised), binary64 GEMM" % (n_rows, wl.M)}
-
-
-def run_reference_moe(args):
-    times, res = [], None
-    base = cpu_baseline_moe_backward if args.workload == "moe_backward" else cpu_baseline_moe
-    for _ in range(args.steps):
-        res = base(args.ref_rows)
-        times.append(res["seconds"])
-    ms = statistics.mean(times) * 1e3
-    value = res["value"]
-    return {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f64 oracle (e4m3 codes, binary64 accumulate)",
-        "data": "synthetic (same seeded workload)",
-        "config": {"workload": MOE_WORKLOAD + ("_backward" if args.workload == "moe_backward"
-                                                else ""), "sample_rows": args.ref_rows},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": res["cores"],
-                         "kind": "oracle", "sample": res["sample"]},
-        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
-                "d2h_bytes_per_step": 0},
-    }
+            "sample": "the whole trio on tokens %d..%d of %d (1x128/128x1 quantisation of that "
+                      "slice of X and dY, 128x128 of all of W, binary64 Fprop, Dgrad and Wgrad "
+                      "of the slice): %d/%d of the step's FLOPs" % (
+                          lo, lo + n_tokens - 1, wl.M, n_tokens, wl.M)}
 
 
 def run_reference(args):
-    """Reference arm: the CPU oracle, timed per step on a bounded sample."""
-    if args.workload in ("moe_prefill", "moe_backward"):
-        return run_reference_moe(args)
-    wl = inputs.fprop_dense(seed=0, device="cpu")
-    for _ in range(args.warmup and 1):
-        cpu_baseline(8, wl)
-    times = []
-    res = None
-    for _ in range(args.steps):
-        res = cpu_baseline(args.ref_rows, wl)
+    """Reference arm: the CPU oracle (as it stands) on the host cores, each step
+    the trio on a bounded slice of the tokens (the slices rotate)."""
+    wl = inputs.training_trio(seed=0, device="cpu")
+    for _ in range(min(args.warmup, 1)):
+        cpu_baseline_trio(128, wl)
+    times, res = [], None
+    for i in range(args.steps):
+        res = cpu_baseline_trio(args.ref_tokens, wl, slice_index=i)
         times.append(res["seconds"])
-    flops = 2.0 * args.ref_rows * wl.N * wl.K
+    flops = 3 * 2.0 * args.ref_tokens * wl.K * wl.N
     ms = statistics.mean(times) * 1e3
     value = flops / (ms * 1e-3) / 1e12
     return {
-        "impl": "reference",
-        "metric": METRIC,
-        "value": round(value, 6),
-        "unit": "TFLOP/s",
-        "n_gpus": 1,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(ms, 1),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f64 oracle (e4m3 codes, binary64 accumulate)",
-        "data": "synthetic (same seeded workload)",
-        "config": {"workload": WORKLOAD, "M": wl.M, "N": wl.N, "K": wl.K,
-                   "sample_rows": args.ref_rows},
+        "data": "synthetic (the same seeded workload)",
+        "config": {"workload": wl.name + "_training_trio", "M_tokens": wl.M, "hidden": wl.K,
+                   "intermediate": wl.N, "sample_tokens_per_step": args.ref_tokens},
         "cpu_baseline": {"value": round(value, 6), "unit": "TFLOP/s", "cores": res["cores"],
                          "kind": "oracle", "sample": res["sample"]},
         "e2e": {"value": round(value, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
@@ -923,18 +972,21 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=4000)
-    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", dest="cpu_baseline", action="store_false")
-    ap.add_argument("--cpu-sample-rows", type=int, default=2048)
-    ap.add_argument("--ref-rows", type=int, default=512)
-    ap.add_argument("--workload", choices=["fprop_dense", "moe_prefill", "moe_backward"],
-                    default="fprop_dense")
-    ap.add_argument("--moe-steps", type=int, default=2000,
-                    help="cap on timed steps for the MoE workload")
+    ap.add_argument("--no-configs", dest="configs", action="store_false")
+    ap.add_argument("--ref-tokens", type=int, default=512,
+                    help="tokens of the trio the oracle runs per reference step (multiple of 128)")
+    ap.add_argument("--cpu-tokens", type=int, default=1024,
+                    help="tokens of the trio the cpu_baseline oracle run covers (multiple of 128)")
+    ap.add_argument("--workload", default="trio",
+                    choices=["trio", "fprop_dense", "moe_prefill", "moe_decode", "moe_backward"])
     args = ap.parse_args()
+    if args.ref_tokens % 128 or args.cpu_tokens % 128:
+        ap.error("--ref-tokens and --cpu-tokens must be multiples of 128")
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     rank, world, local = dist_env()
@@ -946,12 +998,10 @@ def main():
         torch.distributed.init_process_group(
             backend="nccl" if torch.cuda.is_available() else "gloo")
     try:
-        if args.workload == "moe_prefill":
-            line = run_moe(args, rank, world, local)
-        elif args.workload == "moe_backward":
-            line = run_moe_backward(args, rank, world, local)
+        if args.workload == "trio":
+            line = run_trio(args, rank, world, local)
         else:
-            line = run_ours(args, rank, world, local)
+            line = run_single(args, rank, world, local)
         if rank == 0:
             print(json.dumps(line), flush=True)
     finally:
