@@ -66,6 +66,14 @@ constexpr int kSmemLimit = 232448;    // 227 KB opt-in per CTA
 constexpr int kOutSlots = 2;
 constexpr int kBoxBytes = 32 * 128;
 
+// Scale ring: warp 2 copies each K block's scales into shared memory ahead of
+// the epilogue (cp.async, completion on an mbarrier): the A scales of the
+// tile's 128 rows, then the B scales of its columns (one per 128-column
+// block, or one per column in the per-row B-scale mode).  The epilogue reads
+// them there and frees the slot, so no global load sits on its path and no
+// barrier couples its warps.
+constexpr int kScaleSlots = 8;
+
 template <int BN, bool ROWSCALE>
 struct Cfg {
     static constexpr int A_BYTES = BM * BK;
@@ -73,23 +81,23 @@ struct Cfg {
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int COLS = BN / 2;           // columns per epilogue thread
     // Tensor memory holds NBUF partial buffers of the whole tile (all 512
-    // columns): two for 256-wide tiles, four for 128-wide ones.  (Splitting a
-    // 256-wide tile into two 128-column sub-tiles with their own buffers was
-    // measured slower: each sub-tile MMA re-reads A from shared memory, and
-    // shared-memory bandwidth is what bounds the main loop.)
-    static constexpr int NSUB = 1;  // N sub-tiles with their own TMEM buffers (one)
-    static constexpr int SUBN = BN / NSUB;
+    // columns): two for 256-wide tiles, four for 128-wide ones.  With four,
+    // an epilogue thread's 64 columns fit in registers next to its
+    // accumulators, so it hands the buffer back before any arithmetic.
     static constexpr int NBUF = 512 / BN;
-    static constexpr int TMEM_COLS = NSUB * NBUF * SUBN;
+    static constexpr int TMEM_COLS = NBUF * BN;
+    static constexpr int SB_FLOATS = ROWSCALE ? BN : 4;   // B scales in a slot (padded)
+    static constexpr int SLOT_FLOATS = BM + SB_FLOATS;
+    static constexpr int RING_BYTES = ROWSCALE ? kScaleSlots * SLOT_FLOATS * 4 : 0;
     static constexpr int CSTAGE_BYTES = kEpiWarps * kOutSlots * kBoxBytes;
-    static constexpr int RSCALE_BYTES = ROWSCALE ? 2 * BN * 4 : 0;
-    static constexpr int HEADER = 256;            // barriers, TMEM slot, flags
-    static constexpr int FIXED = HEADER + 1023 + CSTAGE_BYTES + RSCALE_BYTES;
+    static constexpr int HEADER = 512;            // barriers, TMEM slot, flags
+    static constexpr int FIXED = HEADER + 1023 + CSTAGE_BYTES + RING_BYTES;
     static constexpr int STAGES_FIT = (kSmemLimit - FIXED) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
     static constexpr int SMEM = FIXED + STAGES * STAGE_BYTES;
+    static constexpr int NBARS = 2 * STAGES + 2 * NBUF + 1 + 2 * kScaleSlots;
     static_assert(STAGES >= 2, "pipeline too shallow");
-    static_assert(2 * STAGES + 2 * NSUB * NBUF + 3 <= 30, "header too small for barriers");
+    static_assert(NBARS * 8 <= HEADER - 16, "header too small for barriers");
     static_assert(TMEM_COLS == 512, "TMEM allocation must be a power of 2");
 };
 
@@ -231,44 +239,56 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr bool GK = GM == 2;       // every expert contracts over its own K range
     using C = Cfg<BN, ROWSCALE>;
     constexpr int S = C::STAGES;
+    constexpr int NBUF = C::NBUF;
+    constexpr int SR = kScaleSlots;
     extern __shared__ uint8_t smem_raw[];
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + 240);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + 244);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + C::HEADER - 16);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + C::HEADER - 12);
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + C::HEADER + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* stages = base;
     uint8_t* cstage = base + S * C::STAGE_BYTES;
-    float* rscale = reinterpret_cast<float*>(cstage + C::CSTAGE_BYTES);
+    float* ring = reinterpret_cast<float*>(cstage + C::CSTAGE_BYTES);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    auto full_bar = [&](int s) { return smem_addr(&bars[s]); };
-    auto empty_bar = [&](int s) { return smem_addr(&bars[S + s]); };
-    constexpr int NSUB = C::NSUB, NBUF = C::NBUF, SUBN = C::SUBN;
-    // TMEM partial buffer b of sub-tile u: full (MMA done) / empty (drained)
-    auto tfull_bar = [&](int u, int b) { return smem_addr(&bars[2 * S + u * NBUF + b]); };
-    auto tempty_bar = [&](int u, int b) {
-        return smem_addr(&bars[2 * S + NSUB * NBUF + u * NBUF + b]);
-    };
-    const uint32_t drain_bar = smem_addr(&bars[2 * S + 2 * NSUB * NBUF]);
-    // ROWSCALE: the epilogue warps stage each K block's B-row scales in a
-    // double buffer; this barrier pair (one per buffer) says all warps wrote.
-    auto rs_bar = [&](int b) { return smem_addr(&bars[2 * S + 2 * NSUB * NBUF + 1 + b]); };
+    // barriers: operand stages full / empty, TMEM partial buffers full
+    // (MMA done) / empty (drained), the MMA drain on abort, scale slots
+    // full (copies landed) / empty (read by every epilogue warp)
+    // (32-bit shared-window addresses: one register each)
+    const uint32_t bars_s = smem_addr(bars);
+    auto bar_at = [bars_s](int i) { return bars_s + 8u * static_cast<uint32_t>(i); };
+    auto full_bar = [&](int s) { return bar_at(s); };
+    auto empty_bar = [&](int s) { return bar_at(S + s); };
+    auto tfull_bar = [&](int b) { return bar_at(2 * S + b); };
+    auto tempty_bar = [&](int b) { return bar_at(2 * S + NBUF + b); };
+    const uint32_t drain_bar = bar_at(2 * S + 2 * NBUF);
+    auto sfull_bar = [&](int r) { return bar_at(2 * S + 2 * NBUF + 1 + r); };
+    auto sempty_bar = [&](int r) { return bar_at(2 * S + 2 * NBUF + 1 + SR + r); };
+    // The scale loader runs as a whole warp in the dense and grouped-K
+    // kernels and as one lane in the grouped-row kernels (whose tile walk
+    // over the expert offsets is kept to single lanes).
+    constexpr int kLoaderLanes = GROUPED ? 1 : 32;
+    // The ring carries the per-column B scales of the Wgrad mode.  In the
+    // block modes the epilogue needs two scalars per K block and prefetches
+    // them from global memory one K block ahead instead.
+    constexpr bool kRing = ROWSCALE;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
             mbar_init(empty_bar(s), 1);
         }
-        for (int u = 0; u < NSUB; ++u)
-            for (int b = 0; b < NBUF; ++b) {
-                mbar_init(tfull_bar(u, b), 1);
-                mbar_init(tempty_bar(u, b), kEpiWarps / NSUB);
-            }
+        for (int b = 0; b < NBUF; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), kEpiWarps);
+        }
         mbar_init(drain_bar, 1);
-        mbar_init(rs_bar(0), kEpiWarps);
-        mbar_init(rs_bar(1), kEpiWarps);
+        for (int r = 0; r < SR; ++r) {
+            mbar_init(sfull_bar(r), kLoaderLanes);
+            mbar_init(sempty_bar(r), kEpiWarps);
+        }
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -375,7 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // --------------------------------------------------------- MMA issuer
         if ((kWarpRoles || lane == 0) && !aborted_at_start) {
             const bool leader = kWarpRoles ? elect_one() : true;
-            const uint32_t idesc = idesc_e4m3_f32<SUBN>();
+            const uint32_t idesc = idesc_e4m3_f32<BN>();
             uint32_t it = 0, kbg = 0;
             bool ok = true, issued = false;
             for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
@@ -386,34 +406,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const int s = static_cast<int>(it % S);
                     const uint32_t ph = (it / S) & 1u;
                     const uint32_t buf = kbg % NBUF, tph = (kbg / NBUF) & 1u;
-                    if (!role_wait(full_bar(s), ph)) {
+                    if (!role_wait(full_bar(s), ph) || !role_wait(tempty_bar(buf), tph ^ 1u)) {
                         ok = false;
                         break;
                     }
+                    tc_fence_after_sync();
                     const uint32_t a_addr = smem_addr(stages + s * C::STAGE_BYTES);
                     const uint64_t adesc = smem_desc_sw128(a_addr);
+                    const uint64_t bdesc = smem_desc_sw128(a_addr + C::A_BYTES);
+                    const uint32_t d = tmem_base + buf * BN;
+                    if (leader) {
 #pragma unroll
-                    for (int u = 0; u < NSUB; ++u) {
-                        if (!role_wait(tempty_bar(u, buf), tph ^ 1u)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after_sync();
-                        // sub-tile u reads B rows u*SUBN .. u*SUBN+SUBN-1 (128 bytes each)
-                        const uint64_t bdesc = smem_desc_sw128(a_addr + C::A_BYTES + u * SUBN * BK);
-                        const uint32_t d = tmem_base + (u * NBUF + buf) * SUBN;
-                        if (leader) {
-#pragma unroll
-                            for (int k = 0; k < BK / 32; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
-                                mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
-                            mma_commit(tfull_bar(u, buf));
-                        }
-                        role_sync();
-                        issued = true;
+                        for (int k = 0; k < BK / 32; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
+                            mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+                        mma_commit(tfull_bar(buf));
+                        mma_commit(empty_bar(s));
                     }
-                    if (!ok) break;
-                    if (leader) mma_commit(empty_bar(s));
                     role_sync();
+                    issued = true;
                 }
             }
             if (!ok && issued && leader) {
@@ -425,60 +435,112 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             role_sync();
         }
+    } else if (warp == 2) {
+        // ------------------------------------------------------ scale loader
+        // Per K block, slot it % SR: the A scales of the tile's 128 rows
+        // (rows past the operand read row M-1: never stored), then the B
+        // scales (per-row mode: the tile's BN columns; block modes: the one
+        // or two 128-column blocks).  Issued as 4-byte cp.async copies whose
+        // landing arrives on the slot's full barrier.
+        if (kRing && (kLoaderLanes == 32 || lane == 0) && !aborted_at_start) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
+                Tile ti;
+                if (!get_tile_gm<BN, GM>(p, t, ti)) break;
+                const int64_t nkb = GK ? ti.kb_count : KB;
+                const int64_t kbo = GK ? ti.kb_begin : 0;
+                // block modes: the tile's first 128-column block's scale at K
+                // block 0, and the steps to the next K block / column block
+                const bool blk = p.bmode == FP8_BSCALE_BLOCK128;
+                const int64_t nb0 = ti.n0 / 128;
+                const float* sb_t = p.sb + (GROUPED ? ti.expert * p.sb_expert : 0) +
+                                    (blk ? nb0 * KB : nb0);
+                const int64_t sb_kstep = blk ? 1 : p.N / 128;
+                const int64_t sb_istep = blk ? KB : 1;
+                for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
+                    const int r = static_cast<int>(it % SR);
+                    const uint32_t ph = (it / SR) & 1u;
+                    const bool got = kLoaderLanes == 32 ? wait_bar_warp(sempty_bar(r), ph ^ 1u, abort_flag)
+                                                        : wait_bar(sempty_bar(r), ph ^ 1u, abort_flag);
+                    if (!got) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t slot = smem_addr(ring + r * C::SLOT_FLOATS);
+                    const int64_t kg = kb + kbo;
+                    const float* sa_k = p.sa + kg * p.lds_a;
+                    for (int i = lane; i < BM; i += kLoaderLanes) {
+                        const int64_t row = ti.row0 + i < p.M ? ti.row0 + i : p.M - 1;
+                        cp_async4(slot + 4 * i, sa_k + row);
+                    }
+                    if (ROWSCALE) {
+                        const float* sb_k = p.sb + kg * p.ld_sb + ti.n0;
+                        for (int i = lane; i < BN; i += kLoaderLanes)
+                            cp_async4(slot + 4 * (BM + i), sb_k + i);
+                    } else {
+                        for (int i = lane; i < BN / 128; i += kLoaderLanes)
+                            cp_async4(slot + 4 * (BM + i), sb_t + kg * sb_kstep + i * sb_istep);
+                    }
+                    cp_async_mbar_arrive_noinc(sfull_bar(r));
+                }
+            }
+            cp_async_wait_all();  // nothing in flight when the CTA exits
+            if (kLoaderLanes == 32) __syncwarp();
+        }
     } else if (warp >= kEpiWarp0) {
         // ------------------------------------------------- promotion epilogue
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
         constexpr int COLS = C::COLS;
         constexpr int ELT = OUT_BF16 ? 2 : 4;
-        constexpr int BOX_COLS = 128 / ELT;  // one 128-byte swizzle row per box row
         const int ew = warp - kEpiWarp0;      // 0..7
         const int q = warp & 3;               // TMEM lane quadrant of this warp
         const int cg = ew >> 2;               // column half of the tile
+        constexpr int BOX_COLS = 128 / ELT;  // one 128-byte swizzle row per box row
         uint8_t* my_cstage = cstage + ew * kOutSlots * kBoxBytes;
         uint32_t boxes = 0;  // TMA boxes this warp has stored so far
-        const int KBi = static_cast<int>(KB);
-        const int NB = static_cast<int>(p.N / 128);
-        const int lds_a = static_cast<int>(p.lds_a);
-        // sub-tile of this warp and its first TMEM column within the sub-tile
-        const int u = NSUB == 2 ? cg : 0;
-        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) +
-                                (NSUB == 2 ? 0 : cg * COLS) + u * NBUF * SUBN;
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + cg * COLS;
         uint32_t kbg = 0;
         bool ok = !aborted_at_start;
+        // shared addresses of a thread's entries in slot 0: its row's A
+        // scale, its columns' B scales (slot r adds r * SLOT_FLOATS * 4)
+        const uint32_t sa_addr0 = smem_addr(ring) + 4u * (q * 32 + lane);
+        const uint32_t sb_addr0 =
+            smem_addr(ring) + 4u * (BM + (ROWSCALE ? cg * COLS : (cg * COLS) / 128));
+        auto release_tmem = [&](uint32_t buf) {
+            tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tempty_bar(buf));
+        };
+        auto release_slot = [&](int r) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sempty_bar(r));
+        };
         for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
             Tile ti;
             if (!get_tile_gm<BN, GM>(p, t, ti)) break;
             const int row = static_cast<int>(ti.row0) + q * 32 + lane;
             const int row_end = static_cast<int>(ti.row_end);
             const int ncol0 = static_cast<int>(ti.n0) + cg * COLS;
-            // A-row scales: sa[kb * lds_a + row]; rows past the allocation read 0
-            const float* sa_ptr = p.sa + (row < p.M ? row : 0);
+            const int nkb = GK ? ti.kb_count : static_cast<int>(KB);
+            // block modes: this row's A scales sa[kb * lds_a + row] and the
+            // B scale of this thread's 128-column block, one K block ahead
             const bool row_in_alloc = row < p.M;
-            // B scales: one per (128-column block, K block) for the block modes
-            const float* sb_ptr;
-            int sb_step;
-            if (ROWSCALE) {
-                const int rcol = ew * 32 + lane;  // column this thread stages
-                sb_ptr = p.sb + ti.n0 + (rcol < BN ? rcol : 0);
-                sb_step = static_cast<int>(p.ld_sb);
-            } else {
-                const float* sb_e = p.sb + (GROUPED ? ti.expert * p.sb_expert : 0);
+            const float* sa_g = p.sa + (row_in_alloc ? row : 0);
+            const int lds_a = static_cast<int>(p.lds_a);
+            const float* sb_g = nullptr;
+            int sb_gstep = 0;
+            float sa_next = 0.0f, sb_next = 0.0f;
+            if constexpr (!kRing) {
                 const int nb = ncol0 / 128;
                 const bool blk = p.bmode == FP8_BSCALE_BLOCK128;
-                sb_ptr = sb_e + (blk ? nb * KBi : nb);
-                sb_step = blk ? 1 : NB;
-            }
-            int nkb = KBi;
-            if constexpr (GK) {
-                // this expert's K blocks: its scale rows start at kb_begin
-                nkb = ti.kb_count;
-                sa_ptr += static_cast<int64_t>(ti.kb_begin) * lds_a;
-                sb_ptr += static_cast<int64_t>(ti.kb_begin) * sb_step;
-            }
-            float sa_next = 0.0f, sb_next = 0.0f;
-            if (!GK || nkb > 0) {
-                sa_next = row_in_alloc ? __ldg(sa_ptr) : 0.0f;
-                sb_next = __ldg(sb_ptr);
+                const int KBi = static_cast<int>(KB);
+                sb_g = p.sb + (GROUPED ? ti.expert * p.sb_expert : 0) + (blk ? nb * KBi : nb);
+                sb_gstep = blk ? 1 : static_cast<int>(p.N / 128);
+                if (nkb > 0) {
+                    sa_next = row_in_alloc ? __ldg(sa_g) : 0.0f;
+                    sb_next = __ldg(sb_g);
+                }
             }
 
             uint64_t acc[COLS / 2];
@@ -486,87 +548,86 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < COLS / 2; ++i) acc[i] = 0;
 
             for (int kb = 0; kb < nkb; ++kb, ++kbg) {
-                const float sa_cur = sa_next, sb_cur = sb_next;
-                if (kb + 1 < nkb) {
-                    sa_next = row_in_alloc ? __ldg(sa_ptr + (kb + 1) * lds_a) : 0.0f;
-                    sb_next = __ldg(sb_ptr + (kb + 1) * sb_step);
-                }
+                const int r = static_cast<int>(kbg % SR);
                 const uint32_t buf = kbg % NBUF, tph = (kbg / NBUF) & 1u;
-                const uint32_t rsb = kbg & 1u;
-                if (ROWSCALE) {
-                    // buffer `rsb` was last read in K block kbg-2; every warp
-                    // arrived on the other buffer's barrier for kbg-1 only after
-                    // finishing that read, so it is free to overwrite here.
-                    if (ew * 32 + lane < BN) rscale[rsb * BN + ew * 32 + lane] = sb_cur;
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(rs_bar(rsb));
-                    if (!wait_bar_warp(rs_bar(rsb), (kbg >> 1) & 1u, abort_flag)) {
-                        ok = false;
-                        break;
+                float sa_cur = sa_next, sb_cur = sb_next;
+                if constexpr (!kRing) {
+                    if (kb + 1 < nkb) {
+                        sa_next = row_in_alloc ? __ldg(sa_g + (kb + 1) * lds_a) : 0.0f;
+                        sb_next = __ldg(sb_g + (kb + 1) * sb_gstep);
                     }
                 }
-                if (!wait_bar_warp(tfull_bar(u, buf), tph, abort_flag)) {
+                if ((kRing && !wait_bar_warp(sfull_bar(r), (kbg / SR) & 1u, abort_flag)) ||
+                    !wait_bar_warp(tfull_bar(buf), tph, abort_flag)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after_sync();
-                const uint32_t taddr = t_lane + buf * SUBN;
-                if (!ROWSCALE) {
-                    const float sc = sa_cur * sb_cur;
-                    const uint64_t sc2 = pack2(f2u(sc), f2u(sc));
-                    // 32-column TMEM loads: two in flight from the start, and each
-                    // freed register chunk is refilled at once, so the whole
-                    // partial has landed after two load latencies; the TMEM
-                    // buffer goes back to the MMA before the last FMAs
-                    static_assert(COLS == 64 || COLS == 128, "column chunking");
+                const uint32_t slot_off = static_cast<uint32_t>(r) * (C::SLOT_FLOATS * 4);
+                if constexpr (kRing) sa_cur = lds_f32(sa_addr0 + slot_off);
+                const uint32_t taddr = t_lane + buf * BN;
+                if constexpr (COLS == 64) {
+                    // 64 columns: load all of them, hand the TMEM buffer
+                    // back, then promote from registers
                     uint32_t ra[32], rb[32];
                     tmem_ld32(taddr, ra);
                     tmem_ld32(taddr + 32, rb);
                     tmem_wait_ld(ra);
                     tmem_wait_ld(rb);
-                    auto fma_chunk = [&](uint32_t (&r)[32], int ch) {
+                    release_tmem(buf);
+                    if constexpr (!ROWSCALE) {
+                        const float sc = sa_cur * sb_cur;
+                        const uint64_t sc2 = pack2(f2u(sc), f2u(sc));
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            acc[ch * 16 + i] = ffma2(pack2(r[2 * i], r[2 * i + 1]), sc2, acc[ch * 16 + i]);
-                    };
-                    auto release = [&]() {
-                        tc_fence_before_sync();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(tempty_bar(u, buf));
-                    };
-                    if (COLS == 128) {
-                        fma_chunk(ra, 0);
-                        tmem_ld32(taddr + 64, ra);
-                        fma_chunk(rb, 1);
-                        tmem_ld32(taddr + 96, rb);
-                        tmem_wait_ld(ra);
-                        tmem_wait_ld(rb);
-                        release();
-                        fma_chunk(ra, 2);
-                        fma_chunk(rb, 3);
+                        for (int i = 0; i < 16; ++i) {
+                            acc[i] = ffma2(pack2(ra[2 * i], ra[2 * i + 1]), sc2, acc[i]);
+                            acc[16 + i] = ffma2(pack2(rb[2 * i], rb[2 * i + 1]), sc2, acc[16 + i]);
+                        }
                     } else {
-                        release();
-                        fma_chunk(ra, 0);
-                        fma_chunk(rb, 1);
+                        // per column: (P * sb[col]) * sa + acc
+                        const uint64_t sa2 = pack2(f2u(sa_cur), f2u(sa_cur));
+                        const uint32_t sbp = sb_addr0 + slot_off;
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 b4 = lds_f32x4(sbp + 16 * i);
+                            const uint64_t p0 = fmul2(pack2(ra[4 * i], ra[4 * i + 1]),
+                                                      pack2(f2u(b4.x), f2u(b4.y)));
+                            const uint64_t p1 = fmul2(pack2(ra[4 * i + 2], ra[4 * i + 3]),
+                                                      pack2(f2u(b4.z), f2u(b4.w)));
+                            acc[2 * i] = ffma2(p0, sa2, acc[2 * i]);
+                            acc[2 * i + 1] = ffma2(p1, sa2, acc[2 * i + 1]);
+                        }
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) {
+                            const float4 b4 = lds_f32x4(sbp + 128 + 16 * i);
+                            const uint64_t p0 = fmul2(pack2(rb[4 * i], rb[4 * i + 1]),
+                                                      pack2(f2u(b4.x), f2u(b4.y)));
+                            const uint64_t p1 = fmul2(pack2(rb[4 * i + 2], rb[4 * i + 3]),
+                                                      pack2(f2u(b4.z), f2u(b4.w)));
+                            acc[16 + 2 * i] = ffma2(p0, sa2, acc[16 + 2 * i]);
+                            acc[16 + 2 * i + 1] = ffma2(p1, sa2, acc[16 + 2 * i + 1]);
+                        }
+                        release_slot(r);
                     }
-                } else {
+                } else if constexpr (ROWSCALE) {
+                    // 128 columns, two FP32 operations each: (P * sb[col]) * sa + acc.
+                    // 16-column TMEM loads, two in flight; the TMEM buffer goes
+                    // back once the last pair has landed, the scale slot after
+                    // the last column's arithmetic.
                     const uint64_t sa2 = pack2(f2u(sa_cur), f2u(sa_cur));
-                    const float* rs = rscale + rsb * BN + cg * COLS;
-                    // 16 columns: P * sb[col] (packed), then * sa + acc
-                    auto fma16 = [&](uint32_t (&r)[16], int ch) {
+                    const uint32_t sbp = sb_addr0 + slot_off;
+                    auto fma16 = [&](uint32_t (&rr)[16], int ch) {
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
-                            const float4 b4 = *reinterpret_cast<const float4*>(rs + ch * 16 + 4 * i);
-                            const uint64_t p0 =
-                                fmul2(pack2(r[4 * i], r[4 * i + 1]), pack2(f2u(b4.x), f2u(b4.y)));
-                            const uint64_t p1 = fmul2(pack2(r[4 * i + 2], r[4 * i + 3]),
+                            const float4 b4 = lds_f32x4(sbp + 4u * (ch * 16 + 4 * i));
+                            const uint64_t p0 = fmul2(pack2(rr[4 * i], rr[4 * i + 1]),
+                                                      pack2(f2u(b4.x), f2u(b4.y)));
+                            const uint64_t p1 = fmul2(pack2(rr[4 * i + 2], rr[4 * i + 3]),
                                                       pack2(f2u(b4.z), f2u(b4.w)));
                             acc[ch * 8 + 2 * i] = ffma2(p0, sa2, acc[ch * 8 + 2 * i]);
                             acc[ch * 8 + 2 * i + 1] = ffma2(p1, sa2, acc[ch * 8 + 2 * i + 1]);
                         }
                     };
-                    // two 16-column loads in flight; the TMEM buffer goes back to
-                    // the MMA once the last pair has landed
                     uint32_t r0[16], r1[16];
                     tmem_ld16(taddr, r0);
                     tmem_ld16(taddr + 16, r1);
@@ -580,13 +641,39 @@ __global__ void __launch_bounds__(kThreads, 1)
                             fma16(r1, ch + 1);
                             tmem_ld16(taddr + (ch + 3) * 16, r1);
                         } else {
-                            tc_fence_before_sync();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(tempty_bar(u, buf));
+                            release_tmem(buf);
                             fma16(r0, ch);
                             fma16(r1, ch + 1);
                         }
                     }
+                    release_slot(r);
+                } else {
+                    const float sc = sa_cur * sb_cur;
+                    const uint64_t sc2 = pack2(f2u(sc), f2u(sc));
+                    // 128 columns in 32-column TMEM loads: two in flight from
+                    // the start, and each freed register chunk is refilled at
+                    // once, so the whole partial has landed after two load
+                    // latencies; the TMEM buffer goes back to the MMA before
+                    // the last FMAs
+                    uint32_t ra[32], rb[32];
+                    tmem_ld32(taddr, ra);
+                    tmem_ld32(taddr + 32, rb);
+                    tmem_wait_ld(ra);
+                    tmem_wait_ld(rb);
+                    auto fma_chunk = [&](uint32_t (&rr)[32], int ch) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            acc[ch * 16 + i] = ffma2(pack2(rr[2 * i], rr[2 * i + 1]), sc2, acc[ch * 16 + i]);
+                    };
+                    fma_chunk(ra, 0);
+                    tmem_ld32(taddr + 64, ra);
+                    fma_chunk(rb, 1);
+                    tmem_ld32(taddr + 96, rb);
+                    tmem_wait_ld(ra);
+                    tmem_wait_ld(rb);
+                    release_tmem(buf);
+                    fma_chunk(ra, 2);
+                    fma_chunk(rb, 3);
                 }
             }
             if (!ok) break;
@@ -598,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // whole 32-row box valid: stage with the 128-byte swizzle, TMA store
 #pragma unroll
                 for (int bx = 0; bx < COLS / BOX_COLS; ++bx, ++boxes) {
-                    uint8_t* slot = my_cstage + (boxes % kOutSlots) * kBoxBytes;
+                    uint8_t* slotc = my_cstage + (boxes % kOutSlots) * kBoxBytes;
                     // the store that last used this slot must have read it
                     if (lane == 0 && boxes >= static_cast<uint32_t>(kOutSlots))
                         bulk_wait_group_read<kOutSlots - 1>();
@@ -617,12 +704,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                            static_cast<uint32_t>(acc[a0 + 1]),
                                            static_cast<uint32_t>(acc[a0 + 1] >> 32));
                         }
-                        *reinterpret_cast<uint4*>(slot + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
+                        *reinterpret_cast<uint4*>(slotc + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        tma_store_2d(&tmC, smem_addr(slot), ncol0 + bx * BOX_COLS, wrow0);
+                        tma_store_2d(&tmC, smem_addr(slotc), ncol0 + bx * BOX_COLS, wrow0);
                         bulk_commit_group();
                     }
                 }
@@ -647,6 +734,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         if (lane == 0) bulk_wait_group0();
+
     }
 
     tc_fence_before_sync();
@@ -733,33 +821,33 @@ static int dispatch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_
         return launch<128, false, true, 2>(aq, a_rows, bq, b_rows, p, tiles, stream);
     } else {
         const bool rows = p.bmode == FP8_BSCALE_ROW1x128;
+        if constexpr (!GROUPED) {
+            // per-column B scales (the Wgrad GEMM)
+            if (rows) {
+                if (p.N % 256 == 0) {
+                    const int64_t tiles = mblk_upper * (p.N / 256);
+                    if (out_type == FP8_OUT_BF16)
+                        return launch<256, true, true, 0>(aq, a_rows, bq, b_rows, p, tiles, stream);
+                    return launch<256, false, true, 0>(aq, a_rows, bq, b_rows, p, tiles, stream);
+                }
+                const int64_t tiles = mblk_upper * (p.N / 128);
+                if (out_type == FP8_OUT_BF16)
+                    return launch<128, true, true, 0>(aq, a_rows, bq, b_rows, p, tiles, stream);
+                return launch<128, false, true, 0>(aq, a_rows, bq, b_rows, p, tiles, stream);
+            }
+        }
         // 256-wide tiles halve the shared-memory operand traffic per MMA and
         // run the tensor core at its full rate; 128-wide ones serve N % 256 != 0.
         if (p.N % 256 == 0) {
             const int64_t tiles = mblk_upper * (p.N / 256);
-            if constexpr (!GROUPED) {
-                if (rows) {
-                    if (out_type == FP8_OUT_BF16)
-                        return launch<256, true, true, GM>(aq, a_rows, bq, b_rows, p, tiles, stream);
-                    return launch<256, false, true, GM>(aq, a_rows, bq, b_rows, p, tiles, stream);
-                }
-            }
             if (out_type == FP8_OUT_BF16)
                 return launch<256, true, false, GM>(aq, a_rows, bq, b_rows, p, tiles, stream);
             return launch<256, false, false, GM>(aq, a_rows, bq, b_rows, p, tiles, stream);
         }
         const int64_t tiles = mblk_upper * (p.N / 128);
-        if constexpr (GROUPED) {  // grouped-row calls use 128x128-block B scales
-            if (out_type == FP8_OUT_BF16)
-                return launch<128, true, false, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
-            return launch<128, false, false, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
-        } else {
-            if (out_type == FP8_OUT_BF16)
-                return rows ? launch<128, true, true, 0>(aq, a_rows, bq, b_rows, p, tiles, stream)
-                            : launch<128, true, false, 0>(aq, a_rows, bq, b_rows, p, tiles, stream);
-            return rows ? launch<128, false, true, 0>(aq, a_rows, bq, b_rows, p, tiles, stream)
-                        : launch<128, false, false, 0>(aq, a_rows, bq, b_rows, p, tiles, stream);
-        }
+        if (out_type == FP8_OUT_BF16)
+            return launch<128, true, false, GM>(aq, a_rows, bq, b_rows, p, tiles, stream);
+        return launch<128, false, false, GM>(aq, a_rows, bq, b_rows, p, tiles, stream);
     }
 }
 
