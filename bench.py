@@ -97,10 +97,57 @@ def profiled_traffic(key):
     return float(d["bytes_per_launch"])
 
 
+class _NvmlCtypes:
+    """The few read-only NVML queries the sampler makes, called through ctypes
+    on the driver's libnvidia-ml (used when the pynvml module is absent)."""
+    NVML_CLOCK_SM = 1
+    nvmlClocksEventReasonSwPowerCap = 0x4
+    nvmlClocksEventReasonHwSlowdown = 0x8
+    nvmlClocksEventReasonSwThermalSlowdown = 0x20
+    nvmlClocksEventReasonHwThermalSlowdown = 0x40
+    nvmlClocksEventReasonHwPowerBrakeSlowdown = 0x80
+
+    def __init__(self):
+        import ctypes
+        self.c = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        self._ck(self.lib.nvmlInit_v2(), "nvmlInit_v2")
+
+    def _ck(self, r, what):
+        if r != 0:
+            raise RuntimeError("%s returned %d" % (what, r))
+
+    def nvmlDeviceGetHandleByPciBusId(self, bus):
+        h = self.c.c_void_p()
+        self._ck(self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), self.c.byref(h)),
+                 "nvmlDeviceGetHandleByPciBusId_v2")
+        return h
+
+    def _uint(self, fn, *args):
+        v = self.c.c_uint()
+        self._ck(getattr(self.lib, fn)(*args, self.c.byref(v)), fn)
+        return v.value
+
+    def nvmlDeviceGetMaxClockInfo(self, h, clk):
+        return self._uint("nvmlDeviceGetMaxClockInfo", h, clk)
+
+    def nvmlDeviceGetClockInfo(self, h, clk):
+        return self._uint("nvmlDeviceGetClockInfo", h, clk)
+
+    def nvmlDeviceGetPowerUsage(self, h):
+        return self._uint("nvmlDeviceGetPowerUsage", h)
+
+    def nvmlDeviceGetCurrentClocksEventReasons(self, h):
+        v = self.c.c_ulonglong()
+        self._ck(self.lib.nvmlDeviceGetCurrentClocksThrottleReasons(h, self.c.byref(v)),
+                 "nvmlDeviceGetCurrentClocksThrottleReasons")
+        return v.value
+
+
 class ClockSampler:
     """Read-only NVML samples of the SM clock, power and clock-event reasons,
-    taken every `period` seconds by a background thread for as long as the
-    sampler is open."""
+    taken every `period` seconds by a background thread while a GPU
+    measurement runs (pynvml if installed, else NVML through ctypes)."""
 
     REASONS = (("hw_slowdown", "nvmlClocksEventReasonHwSlowdown"),
                ("hw_thermal_slowdown", "nvmlClocksEventReasonHwThermalSlowdown"),
@@ -117,8 +164,13 @@ class ClockSampler:
         self._stop = threading.Event()
         self._thread = None
         try:
-            import pynvml as nv
-            nv.nvmlInit()
+            try:
+                import pynvml as nv
+                nv.nvmlInit()
+                self.via = "pynvml"
+            except ImportError:
+                nv = _NvmlCtypes()
+                self.via = "libnvidia-ml via ctypes"
             p = torch.cuda.get_device_properties(device)
             bus = "%08x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
             self.h = nv.nvmlDeviceGetHandleByPciBusId(bus)
@@ -127,6 +179,7 @@ class ClockSampler:
             self.masks = {name: getattr(nv, attr, 0) for name, attr in self.REASONS}
         except Exception as e:  # no NVML: the line says so
             self.nv = None
+            self.via = None
             self.err = repr(e)
 
     def _run(self):
@@ -174,8 +227,8 @@ class ClockSampler:
 
     def summary(self, t0=None, t1=None):
         s = [x for x in self.samples if (t0 is None or x[0] >= t0) and (t1 is None or x[0] <= t1)]
-        out = {"source": "NVML, read-only, every %.0f ms while a GPU measurement runs"
-                         % (self.period * 1e3),
+        out = {"source": "NVML (%s), read-only, every %.0f ms while a GPU measurement runs"
+                         % (self.via, self.period * 1e3),
                "samples": len(s), "sm_max_mhz": self.max_mhz}
         if not s:
             out.update({"sm_mhz": None, "reasons": [], "error": self.err})
