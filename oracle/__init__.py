@@ -56,6 +56,15 @@ def _load():
         lib.fo_quant_act_1x128.argtypes = [P, I64, I64, I64, P, I64, P]
         lib.fo_quant_act_128x1.argtypes = [P, I64, I64, I64, P, P]
         lib.fo_quant_weight_128x128.argtypes = [P, I64, I64, I64, P, P, P]
+        lib.fo_e5m6_encode.restype = ctypes.c_uint16
+        lib.fo_e5m6_encode.argtypes = [ctypes.c_float]
+        lib.fo_e5m6_decode.restype = ctypes.c_double
+        lib.fo_e5m6_decode.argtypes = [ctypes.c_uint16]
+        lib.fo_e5m6_encode_array.argtypes = [P, I64, P]
+        lib.fo_e5m6_decode_array.argtypes = [P, I64, P]
+        lib.fo_group_scale_e5m6.restype = ctypes.c_float
+        lib.fo_group_scale_e5m6.argtypes = [ctypes.c_float]
+        lib.fo_quant_act_1x128_e5m6.argtypes = [P, I64, I64, I64, P, I64, P]
         lib.fo_gemm_blockscaled_rows.argtypes = [
             P, I64, P, I64, P, I64, P, I64, ctypes.c_int, I64, I64, I64, P, I64, P,
             ctypes.c_int]
@@ -111,6 +120,54 @@ def group_scale(amax: float) -> np.float32:
     return np.float32(_load().fo_group_scale(float(amax)))
 
 
+def e5m6_encode(x) -> np.ndarray:
+    """E5M6 codes (12-bit values in uint16; RNE, saturating at 65024) of binary32 values."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, np.uint16)
+    _load().fo_e5m6_encode_array(_ptr(x), x.size, _ptr(out))
+    return out
+
+
+def e5m6_decode(c) -> np.ndarray:
+    """binary64 values of E5M6 codes (low 12 bits of uint16)."""
+    c = _c(c, np.uint16)
+    out = np.empty(c.shape, np.float64)
+    _load().fo_e5m6_decode_array(_ptr(c), c.size, _ptr(out))
+    return out
+
+
+def group_scale_e5m6(amax: float) -> np.float32:
+    return np.float32(_load().fo_group_scale_e5m6(float(amax)))
+
+
+def pack_e5m6(codes) -> np.ndarray:
+    """Storage layout of E5M6 rows: element i of a row occupies bits
+    12 i .. 12 i + 11 of the row's bytes, least significant first, so two
+    neighbours (c0, c1) fill three bytes: c0 & 0xFF, (c0 >> 8) | (c1 & 0xF) << 4,
+    c1 >> 4.  codes uint16 [..., K] (K even) -> uint8 [..., 3 K / 2]."""
+    c = _c(codes, np.uint16).astype(np.uint32)
+    assert c.shape[-1] % 2 == 0
+    c0, c1 = c[..., 0::2], c[..., 1::2]
+    out = np.empty(c.shape[:-1] + (c.shape[-1] // 2, 3), np.uint8)
+    out[..., 0] = c0 & 0xFF
+    out[..., 1] = ((c0 >> 8) & 0xF) | ((c1 & 0xF) << 4)
+    out[..., 2] = (c1 >> 4) & 0xFF
+    return out.reshape(c.shape[:-1] + (3 * c.shape[-1] // 2,))
+
+
+def unpack_e5m6(packed) -> np.ndarray:
+    """Inverse of pack_e5m6: uint8 [..., 3 K / 2] -> uint16 codes [..., K]."""
+    b = _c(packed, np.uint8)
+    assert b.shape[-1] % 3 == 0
+    t = b.reshape(b.shape[:-1] + (b.shape[-1] // 3, 3)).astype(np.uint16)
+    c0 = t[..., 0] | ((t[..., 1] & 0xF) << 8)
+    c1 = (t[..., 1] >> 4) | (t[..., 2] << 4)
+    out = np.empty(b.shape[:-1] + (2 * (b.shape[-1] // 3),), np.uint16)
+    out[..., 0::2] = c0
+    out[..., 1::2] = c1
+    return out
+
+
 # ---------------------------------------------------------------- quantisers --
 def quant_act_1x128(x_bf16: np.ndarray):
     """x: uint16 [M, K] bfloat16 bits -> (codes uint8 [M, K], scales f32 [K/128, M])."""
@@ -121,6 +178,18 @@ def quant_act_1x128(x_bf16: np.ndarray):
     sx = np.empty((K // 128, M), np.float32)
     _load().fo_quant_act_1x128(_ptr(x), M, K, K, _ptr(xq), K, _ptr(sx))
     return xq, sx
+
+
+def quant_act_1x128_e5m6(x_bf16: np.ndarray):
+    """x: uint16 [M, K] bfloat16 bits -> (E5M6 codes uint16 [M, K], scales f32 [K/128, M]),
+    s = fl32(amax / 65024) per 1x128 group; pack_e5m6 gives the stored bytes."""
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    assert K % 128 == 0
+    q = np.empty((M, K), np.uint16)
+    sx = np.empty((K // 128, M), np.float32)
+    _load().fo_quant_act_1x128_e5m6(_ptr(x), M, K, K, _ptr(q), K, _ptr(sx))
+    return q, sx
 
 
 def quant_act_128x1(x_bf16: np.ndarray):

@@ -110,6 +110,69 @@ void fo_e4m3_decode_array(const uint8_t* c, int64_t n, double* out)
     for (int64_t i = 0; i < n; ++i) out[i] = fo_e4m3_decode(c[i]);
 }
 
+/* ---------------------------------------------------------------- E5M6 --- */
+
+/*
+ * E5M6: a 12-bit floating-point element with a sign bit, a 5-bit exponent
+ * and a 6-bit mantissa -- the customised format the report adopts for one
+ * class of activations (section 3.3.1, next to E4M3 for the GEMM operands).
+ * The pages give the field widths only; the rest is read as an IEEE-style
+ * format, like the 5-bit-exponent FP16 and E5M2: bias 15, exponent field 31
+ * reserved (mantissa 0 = infinity, else NaN), so the largest finite value is
+ * (1 + 63/64) * 2^15 = 65024 (code 0x7BF), the smallest normal 2^-14 and the
+ * subnormals m * 2^-20 for m = 1..63.  Encoding rounds to nearest, ties to
+ * the even mantissa, and saturates: magnitudes at or above 65024 (and
+ * infinities) give +-65024, as the E4M3 encoder saturates at 448.  Codes are
+ * 12-bit values in a uint16 (sign in bit 11).
+ */
+uint16_t fo_e5m6_encode(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    uint16_t sign = (uint16_t)((u >> 31) << 11);
+    if (isnan(f)) return (uint16_t)(sign | 0x7FF);
+    double a = fabs((double)f);
+    if (a >= 65024.0) return (uint16_t)(sign | 0x7BF);
+    if (a < 0x1p-14) {
+        /* the subnormal grid m * 2^-20, m = 0..64; m = 64 is 2^-14, whose
+         * code (exponent field 1, mantissa 0) is the integer 64 as well */
+        double m = round_half_even(a * 1048576.0);
+        return (uint16_t)(sign | (uint16_t)m);
+    }
+    int ex;
+    double fr = frexp(a, &ex); /* a = fr * 2^ex, fr in [0.5, 1) */
+    int e = ex - 1;            /* a = (2 fr) * 2^e, e in [-14, 15] */
+    double m = round_half_even((2.0 * fr - 1.0) * 64.0);
+    if (m == 64.0) {           /* mantissa carried into the exponent */
+        m = 0.0;
+        e += 1;
+    }
+    /* a < 65024 keeps (e, m) at or below (15, 63): only a >= 65280 would
+     * round up to 2^16 */
+    return (uint16_t)(sign | (uint16_t)(((e + 15) << 6) | (int)m));
+}
+
+/* Value of an E5M6 code (low 12 bits), from the format definition. */
+double fo_e5m6_decode(uint16_t c)
+{
+    int s = (c >> 11) & 1, E = (c >> 6) & 0x1F, m = c & 0x3F;
+    double v;
+    if (E == 31) v = (m == 0) ? INFINITY : NAN;
+    else if (E == 0) v = (double)m * ldexp(1.0, -20);
+    else v = (1.0 + (double)m / 64.0) * ldexp(1.0, E - 15);
+    return s ? -v : v;
+}
+
+void fo_e5m6_encode_array(const float* x, int64_t n, uint16_t* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = fo_e5m6_encode(x[i]);
+}
+
+void fo_e5m6_decode_array(const uint16_t* c, int64_t n, double* out)
+{
+    for (int64_t i = 0; i < n; ++i) out[i] = fo_e5m6_decode(c[i]);
+}
+
 /* ---------------------------------------------------------------- BF16 --- */
 
 /* A bfloat16 is the upper half of a binary32, so widening is exact. */
@@ -174,6 +237,40 @@ void fo_quant_act_1x128(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
             sx[kb * M + m] = s;
             for (int j = 0; j < 128; ++j)
                 xq[m * ldq + kb * 128 + j] = fo_e4m3_encode(bf16_value(g[j]) / s);
+        }
+    }
+}
+
+/* Scale of one E5M6 group: s = fl32(amax / 65024), the format's largest
+ * finite value taking the place of E4M3's 448; an all-zero group gets s = 1. */
+float fo_group_scale_e5m6(float amax)
+{
+    if (amax == 0.0f) { return 1.0f; }
+    return amax / 65024.0f;
+}
+
+/*
+ * 1x128 activation quantisation to E5M6 (the same fine-grained grouping as
+ * fo_quant_act_1x128, section 3.3.2, with the E5M6 element format).
+ * x: bfloat16 [M][K], row stride ldx.  q: 12-bit codes [M][K] (one uint16
+ * each), row stride ldq.  sx: scales [K/128][M].
+ */
+void fo_quant_act_1x128_e5m6(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                             uint16_t* q, int64_t ldq, float* sx)
+{
+    int64_t KB = K / 128;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            const uint16_t* grp = x + m * ldx + kb * 128;
+            float amax = 0.0f;
+            for (int j = 0; j < 128; ++j) {
+                float mag = fabsf(bf16_value(grp[j]));
+                if (mag > amax) amax = mag;
+            }
+            float s = fo_group_scale_e5m6(amax);
+            sx[m + kb * M] = s;
+            for (int j = 0; j < 128; ++j)
+                q[m * ldq + kb * 128 + j] = fo_e5m6_encode(bf16_value(grp[j]) / s);
         }
     }
 }

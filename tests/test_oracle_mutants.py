@@ -6,7 +6,9 @@ exponent bias or subnormal grid, a mantissa carry, a transposed scale or
 code index, a dropped K block, a bfloat16 rounding tie, an amax without the
 absolute value; in the Python layer, the dispatch's token order and expert
 ids, the expert of a boundary row, the padding of short token groups and the
-per-expert scale slice of the grouped Wgrad.  The C mutants are compiled from
+per-expert scale slice of the grouped Wgrad; for E5M6, the exponent bias,
+saturation bound, subnormal grid, mantissa width, sign of zero, divisor,
+scale index, amax and the nibble order of the packed layout.  The C mutants are compiled from
 edited copies of oracle/fp8_oracle.c into temporary libraries, and the
 oracle's pin tests are run against each in a fresh process (the oracle loads
 the library named by FP8FG_ORACLE_LIB); every such run must fail.  The
@@ -28,7 +30,8 @@ from oracle import build as oracle_build
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 PINS = ["tests/test_oracle_quant.py", "tests/test_oracle_gemm.py",
-        "tests/test_oracle_dispatch.py", "tests/test_oracle_e4m3.py"]
+        "tests/test_oracle_dispatch.py", "tests/test_oracle_e4m3.py",
+        "tests/test_oracle_e5m6.py"]
 
 # name -> (exact text of fp8_oracle.c, replacement)
 C_MUTANTS = {
@@ -57,6 +60,23 @@ C_MUTANTS = {
                                  "case FO_BSCALE_BLOCK128: return (double)j->sb[kb * NB + n / 128];"),
     "bf16_ties_away": ("if (lo > 0x8000u || (lo == 0x8000u && (hi & 1u))) hi += 1u;",
                        "if (lo >= 0x8000u) hi += 1u;"),
+    # E5M6
+    "e5m6_decode_bias_16": ("else v = (1.0 + (double)m / 64.0) * ldexp(1.0, E - 15);",
+                            "else v = (1.0 + (double)m / 64.0) * ldexp(1.0, E - 16);"),
+    "e5m6_saturation_bound": ("if (a >= 65024.0) return (uint16_t)(sign | 0x7BF);",
+                              "if (a >= 65536.0) return (uint16_t)(sign | 0x7BF);"),
+    "e5m6_subnormal_grid": ("double m = round_half_even(a * 1048576.0);",
+                            "double m = round_half_even(a * 2097152.0);"),
+    "e5m6_five_mantissa_bits": ("double m = round_half_even((2.0 * fr - 1.0) * 64.0);",
+                                "double m = round_half_even((2.0 * fr - 1.0) * 32.0);"),
+    "e5m6_zero_code_loses_sign": ("return (uint16_t)(sign | (uint16_t)m);",
+                                  "return (uint16_t)(m == 0.0 ? 0 : (sign | (uint16_t)m));"),
+    "e5m6_divisor_65536": ("return amax / 65024.0f;", "return amax / 65536.0f;"),
+    "e5m6_zero_group_scale": ("if (amax == 0.0f) { return 1.0f; }",
+                              "if (amax == 0.0f) { return 0.5f; }"),
+    "e5m6_scale_transposed": ("sx[m + kb * M] = s;", "sx[m * KB + kb] = s;"),
+    "e5m6_amax_without_abs": ("float mag = fabsf(bf16_value(grp[j]));",
+                              "float mag = bf16_value(grp[j]);"),
 }
 
 
@@ -164,6 +184,10 @@ PY_MUTANTS = {  # name -> (exact text of oracle/__init__.py, replacement, pin mo
         "test_oracle_gemm", ["test_grouped_128x1_single_expert_is_the_dense_quantiser",
                              "test_grouped_128x1_short_groups",
                              "test_grouped_wgrad_equals_dequantised_product"]),
+    "e5m6_pack_nibbles_swapped": (
+        "out[..., 1] = ((c0 >> 8) & 0xF) | ((c1 & 0xF) << 4)",
+        "out[..., 1] = (c1 & 0xF) | (((c0 >> 8) & 0xF) << 4)",
+        "test_oracle_e5m6", ["test_packing_bit_layout"]),
     "wgrad_b_scales_of_expert_0": (
         "sb[lo // 128:hi // 128], BSCALE_ROW1x128",
         "sb[:hi // 128 - lo // 128], BSCALE_ROW1x128",
@@ -209,7 +233,7 @@ def test_harness_passes_with_the_unmodified_sources(monkeypatch):
                   acc_pins.test_promotion_keeps_the_error_flat_in_k]:
         check()
     src = open(os.path.join(ROOT, "oracle", "__init__.py")).read()
-    for module in ("test_oracle_dispatch", "test_oracle_gemm"):
+    for module in ("test_oracle_dispatch", "test_oracle_gemm", "test_oracle_e5m6"):
         pins = importlib.import_module(module)
         monkeypatch.setattr(pins, "oracle", _oracle_module(src, "clean"))
         names = {n for _, _, m, ns in PY_MUTANTS.values() if m == module
