@@ -104,6 +104,71 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_1x128_kernel(
     }
 }
 
+// ------------------------------------------------------------- 1x128 E5M6 --
+// The same tiles and lanes as the 1x128 E4M3 kernel; each lane's 32 codes
+// (12 bits each) fill 48 bytes of the packed row, stored as three 16-byte
+// chunks.  Scale s = fl32(amax / 65024).
+__device__ __forceinline__ void quant_1x128_e5m6_tile(int64_t M, int64_t KB,
+                                                      uint8_t* __restrict__ xq, int64_t ldq,
+                                                      float* __restrict__ sx, int64_t t, int row,
+                                                      int l4, const uint4 (&v)[4]) {
+    const int64_t kb = t % KB;
+    const int64_t m = (t / KB) * kQ1Rows + row;
+    uint32_t mx = absmax_bf16x2(v[0].x, v[0].y);
+    mx = absmax_bf16x2(mx, absmax_bf16x2(v[0].z, v[0].w));
+#pragma unroll
+    for (int i = 1; i < 4; ++i) {
+        mx = absmax_bf16x2(mx, absmax_bf16x2(v[i].x, v[i].y));
+        mx = absmax_bf16x2(mx, absmax_bf16x2(v[i].z, v[i].w));
+    }
+    float amax = amax_of_pair(mx);
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+    const float s = amax == 0.0f ? 1.0f : __fdiv_rn(amax, 65024.0f);
+    const GroupDiv dv(s, kE5M6FastMin);
+    if (m < M) {
+        uint32_t w[12];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {  // 16-byte load i: eight elements
+            const uint32_t words[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+            uint32_t c[8];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                float q0, q1;
+                dv.quot2(bf16_lo(words[j]), bf16_hi(words[j]), q0, q1);
+                c[2 * j] = e5m6_code(q0, (words[j] >> 15) & 1u);
+                c[2 * j + 1] = e5m6_code(q1, words[j] >> 31);
+            }
+            pack_e5m6_8(c, w[3 * i], w[3 * i + 1], w[3 * i + 2]);
+        }
+        uint4* dst = reinterpret_cast<uint4*>(xq + m * ldq + kb * 192 + l4 * 48);
+        dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+        dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        dst[2] = make_uint4(w[8], w[9], w[10], w[11]);
+        if (l4 == 0) sx[kb * M + m] = s;
+    }
+}
+
+__global__ void __launch_bounds__(kQuantThreads) quant_act_1x128_e5m6_kernel(
+    const uint16_t* __restrict__ x, int64_t M, int64_t KB, int64_t ldx, uint8_t* __restrict__ xq,
+    int64_t ldq, float* __restrict__ sx, int64_t tiles) {
+    griddep_launch_dependents();
+    const int l4 = threadIdx.x & 3;
+    const int row = threadIdx.x >> 2;  // 0..63
+    int64_t t = blockIdx.x;
+    uint4 v[4];
+    if (t < tiles) load_1x128(x, M, ldx, KB, t, row, l4, v);
+    while (t < tiles) {
+        const int64_t tn = t + gridDim.x;
+        uint4 vn[4];
+        if (tn < tiles) load_1x128(x, M, ldx, KB, tn, row, l4, vn);
+        quant_1x128_e5m6_tile(M, KB, xq, ldq, sx, t, row, l4, v);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = vn[i];
+        t = tn;
+    }
+}
+
 // ------------------------------------------------------------------ 128x1 --
 // Tile: one 128-token group x 64 columns, staged in shared memory; each
 // thread then owns one column and a quarter of the 128 rows.  Tiles are
@@ -515,6 +580,22 @@ extern "C" fp8_status fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, i
     quant_act_1x128_kernel<<<static_cast<unsigned>(quant_grid<quant_act_1x128_kernel>(tiles)), kQuantThreads, 0,
                              static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t*>(x), M, K / 128, ldx, xq, ldq, sx, tiles);
+    return to_status(launch_status());
+}
+
+extern "C" fp8_status fp8_quant_act_1x128_e5m6(const void* x, int64_t M, int64_t K,
+                                               int64_t ldx, uint8_t* xq, int64_t ldq_bytes,
+                                               float* sx, void* stream) {
+    if (M < 0 || K <= 0 || K % 128 != 0 || ldx < K || ldq_bytes < 3 * K / 2) return FP8_ERR_SHAPE;
+    if (M == 0) return FP8_OK;
+    if (x == nullptr || xq == nullptr || sx == nullptr) return FP8_ERR_NULL;
+    if (ldx % 8 != 0 || ldq_bytes % 16 != 0 || !aligned(x, 16) || !aligned(xq, 16) ||
+        !aligned(sx, 4))
+        return FP8_ERR_ALIGN;
+    const int64_t tiles = ((M + kQ1Rows - 1) / kQ1Rows) * (K / 128);
+    quant_act_1x128_e5m6_kernel<<<static_cast<unsigned>(quant_grid<quant_act_1x128_e5m6_kernel>(tiles)),
+                                  kQuantThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t*>(x), M, K / 128, ldx, xq, ldq_bytes, sx, tiles);
     return to_status(launch_status());
 }
 

@@ -47,15 +47,38 @@ __device__ __forceinline__ uint64_t fma2(uint64_t a, uint64_t b, uint64_t c) {
 // quotient, so the corrected path is used for s >= 2^-91 and groups with a
 // smaller scale take the IEEE division.  The tests compare the resulting
 // codes with IEEE division over every (x, amax) bf16 pair.
+//
+// fast_min: the smallest scale for which the corrected path is used.  Below
+// |x| = 2^-102 the residual may be inexact; the path is still right when
+// every such x gives a quotient the target format rounds to zero whatever
+// its last bit: |x / s| < 2^-11 for E4M3 (s >= 2^-91, the default), and
+// |x / s| < 2^-22 for E5M6 (s >= 2^-80, kE5M6FastMin).
+constexpr float kE5M6FastMin = 0x1p-80f;
+
 struct GroupDiv {
     float s;
     uint64_t r2, ns2;
     bool fast;
-    __device__ __forceinline__ explicit GroupDiv(float scale) : s(scale) {
+    __device__ __forceinline__ explicit GroupDiv(float scale, float fast_min = 0x1p-91f)
+        : s(scale) {
         const float r = __frcp_rn(scale);
         r2 = f2x2(r, r);
         ns2 = f2x2(-scale, -scale);
-        fast = scale >= 0x1p-91f;
+        fast = scale >= fast_min;
+    }
+    // Correctly rounded quotients x0 / s, x1 / s (a zero may carry either sign).
+    __device__ __forceinline__ void quot2(float x0, float x1, float& q0, float& q1) const {
+        if (fast) {
+            const uint64_t x2 = f2x2(x0, x1);
+            const uint64_t a = mul2(x2, r2);
+            const uint64_t e = fma2(a, ns2, x2);
+            const uint64_t q = fma2(e, r2, a);
+            q0 = __uint_as_float(static_cast<uint32_t>(q));
+            q1 = __uint_as_float(static_cast<uint32_t>(q >> 32));
+        } else {
+            q0 = __fdiv_rn(x0, s);
+            q1 = __fdiv_rn(x1, s);
+        }
     }
     // E4M3 codes of x0 / s and x1 / s, x0 in the low byte
     __device__ __forceinline__ uint32_t pair(float x0, float x1) const {
@@ -127,6 +150,34 @@ struct GroupDiv {
         return byte_perm(w0, w1, 0xFDB9);
     }
 };
+
+// ------------------------------------------------------------------ E5M6 --
+// E5M6 (sign, 5-bit exponent with bias 15, 6-bit mantissa; exponent field 31
+// reserved; largest finite 65024 = 0x7BF; subnormals m * 2^-20): the 12-bit
+// code of a binary32 magnitude |q| with the given sign bit, rounded to nearest
+// with ties to the even mantissa and saturated at 65024.
+__device__ __forceinline__ uint32_t e5m6_code(float q, uint32_t neg) {
+    const uint32_t a = __float_as_uint(q) & 0x7FFFFFFFu;
+    uint32_t mag;
+    if (a >= 0x477E0000u) {            // |q| >= 65024 (or infinite): saturate
+        mag = 0x7BFu;
+    } else if (a < 0x38800000u) {      // |q| < 2^-14: the grid m * 2^-20, m = 0..64
+        // scaling by 2^20 is exact; m = 64 is 2^-14, whose code is 64 as well
+        mag = __float2uint_rn(__uint_as_float(a) * 1048576.0f);
+    } else {                           // keep 6 of the 23 mantissa bits, RNE
+        const uint32_t r = a + 0xFFFFu + ((a >> 17) & 1u);
+        mag = (r >> 17) - ((127u - 15u) << 6);
+    }
+    return (neg << 11) | mag;
+}
+
+// Eight 12-bit codes packed into three words, element i at bits 12 i .. 12 i + 11.
+__device__ __forceinline__ void pack_e5m6_8(const uint32_t (&c)[8], uint32_t& w0, uint32_t& w1,
+                                            uint32_t& w2) {
+    w0 = c[0] | (c[1] << 12) | (c[2] << 24);
+    w1 = (c[2] >> 8) | (c[3] << 4) | (c[4] << 16) | (c[5] << 28);
+    w2 = (c[5] >> 4) | (c[6] << 8) | (c[7] << 20);
+}
 
 __device__ __forceinline__ uint4 ld_stream_v4(const void* p) {
     return __ldcs(reinterpret_cast<const uint4*>(p));

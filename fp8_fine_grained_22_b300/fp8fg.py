@@ -23,7 +23,8 @@ FP8_BSCALE_BLOCK128_T = 2
 
 # every entry point of include/fp8fg.h
 EXPORTS = ("fp8_status_str", "fp8_device_error", "fp8_selftest_wait_timeout",
-           "fp8_quant_act_1x128", "fp8_quant_act_128x1", "fp8_quant_weight_128x128",
+           "fp8_quant_act_1x128", "fp8_quant_act_1x128_e5m6", "fp8_quant_act_128x1",
+           "fp8_quant_weight_128x128",
            "fp8_quant_fprop_operands",
            "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe", "fp8_grouped_gemm_moe_dgrad",
            "fp8_quant_act_128x1_grouped", "fp8_grouped_gemm_moe_wgrad",
@@ -59,6 +60,8 @@ def lib() -> ctypes.CDLL:
         L.fp8_selftest_wait_timeout.argtypes = [P]
         L.fp8_quant_act_1x128.restype = I
         L.fp8_quant_act_1x128.argtypes = [P, I64, I64, I64, P, I64, P, P]
+        L.fp8_quant_act_1x128_e5m6.restype = I
+        L.fp8_quant_act_1x128_e5m6.argtypes = [P, I64, I64, I64, P, I64, P, P]
         L.fp8_quant_act_128x1.restype = I
         L.fp8_quant_act_128x1.argtypes = [P, I64, I64, I64, P, P, P]
         L.fp8_quant_weight_128x128.restype = I
@@ -138,6 +141,21 @@ def fp8_quant_act_1x128(x, xq=None, sx=None, stream=None):
     assert xq.stride(1) == 1 and sx.is_contiguous()
     _check(lib().fp8_quant_act_1x128(_p(x), M, K, x.stride(0), _p(xq), xq.stride(0), _p(sx),
                                      _stream(stream)), "fp8_quant_act_1x128")
+    return xq, sx
+
+
+def fp8_quant_act_1x128_e5m6(x, xq=None, sx=None, stream=None):
+    """x: bf16 [M, K] -> (xq uint8 [M, 3K/2] packed 12-bit E5M6 codes, sx f32 [K/128, M])."""
+    _cuda(x, "x", torch.bfloat16)
+    assert x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, 3 * K // 2), dtype=torch.uint8, device=x.device)
+    if sx is None:
+        sx = torch.empty((K // 128, M), dtype=torch.float32, device=x.device)
+    assert xq.stride(1) == 1 and sx.is_contiguous()
+    _check(lib().fp8_quant_act_1x128_e5m6(_p(x), M, K, x.stride(0), _p(xq), xq.stride(0),
+                                          _p(sx), _stream(stream)), "fp8_quant_act_1x128_e5m6")
     return xq, sx
 
 

@@ -115,6 +115,26 @@ fp8_status fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, int64_t ldx,
                         uint8_t* xq, int64_t ldq, float* sx, void* stream);
 
 /*
+ * fp8_quant_act_1x128_e5m6 -- 1x128 activation quantisation to the E5M6
+ * format (report section 3.3.1: a customised E5M6 format, 5-bit exponent and
+ * 6-bit mantissa, for one class of activations; the grouping and scaling of
+ * section 3.3.2).  Reading of what the report leaves open: sign bit, exponent
+ * bias 15, exponent field 31 reserved for infinity/NaN, subnormals m * 2^-20,
+ * largest finite value 65024; round to nearest with ties to the even mantissa,
+ * saturating.  Scale s = fl32(amax / 65024) per group (s = 1 for an all-zero
+ * group); code = E5M6(fl32(x / s)), the sign of a zero code taken from x.
+ *   x   : bfloat16 [M][K], row stride ldx.                             (input)
+ *   xq  : packed 12-bit codes, row m at xq + m * ldq_bytes: element k of the
+ *         row occupies bits 12 k .. 12 k + 11 of the row's bytes, least
+ *         significant first (3 K / 2 bytes per row).                  (output)
+ *   sx  : float [K/128][M], as fp8_quant_act_1x128.                    (output)
+ * Requires K % 128 == 0, ldx >= K, ldx % 8 == 0, ldq_bytes >= 3 K / 2,
+ * ldq_bytes % 16 == 0, x and xq 16-byte aligned, sx 4-byte aligned.  M >= 0.
+ */
+fp8_status fp8_quant_act_1x128_e5m6(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                    uint8_t* xq, int64_t ldq_bytes, float* sx, void* stream);
+
+/*
  * fp8_quant_act_128x1 -- 128x1 (token-wise transposed) activation quantisation
  * for the Wgrad GEMM, whose inner dimension is the token dimension M (report
  * sections 3.3.1-3.3.3; transposition moved out of the GEMM per section 3.5.2).
