@@ -65,6 +65,10 @@ def _load():
         lib.fo_group_scale_e5m6.restype = ctypes.c_float
         lib.fo_group_scale_e5m6.argtypes = [ctypes.c_float]
         lib.fo_quant_act_1x128_e5m6.argtypes = [P, I64, I64, I64, P, I64, P]
+        lib.fo_pow2_exponent.restype = ctypes.c_int
+        lib.fo_pow2_exponent.argtypes = [ctypes.c_float]
+        lib.fo_quant_act_1x128_pow2.argtypes = [P, I64, I64, I64, P, I64, P]
+        lib.fo_quant_weight_128x128_pow2.argtypes = [P, I64, I64, I64, P, P]
         lib.fo_gemm_blockscaled_rows.argtypes = [
             P, I64, P, I64, P, I64, P, I64, ctypes.c_int, I64, I64, I64, P, I64, P,
             ctypes.c_int]
@@ -190,6 +194,41 @@ def quant_act_1x128_e5m6(x_bf16: np.ndarray):
     sx = np.empty((K // 128, M), np.float32)
     _load().fo_quant_act_1x128_e5m6(_ptr(x), M, K, K, _ptr(q), K, _ptr(sx))
     return q, sx
+
+
+def pow2_exponent(amax: float) -> int:
+    """e of the power-of-two scale 2^e: the smallest with amax / 2^e <= 448, in [-127, 127]."""
+    return int(_load().fo_pow2_exponent(float(amax)))
+
+
+def e8_scales(se8) -> np.ndarray:
+    """float32 scales 2^(b - 127) of UE8M0 bytes b."""
+    b = np.asarray(se8, dtype=np.int64)
+    return np.ldexp(np.ones(b.shape, np.float64), b - 127).astype(np.float32)
+
+
+def quant_act_1x128_pow2(x_bf16: np.ndarray):
+    """x: uint16 [M, K] -> (codes uint8 [M, K], UE8M0 bytes uint8 [K/128, M]) with
+    power-of-two 1x128 group scales."""
+    x = _c(x_bf16, np.uint16)
+    M, K = x.shape
+    assert K % 128 == 0
+    xq = np.empty((M, K), np.uint8)
+    se8 = np.empty((K // 128, M), np.uint8)
+    _load().fo_quant_act_1x128_pow2(_ptr(x), M, K, K, _ptr(xq), K, _ptr(se8))
+    return xq, se8
+
+
+def quant_weight_128x128_pow2(w_bf16: np.ndarray):
+    """w: uint16 [K, N] -> (wq uint8 [N, K], UE8M0 bytes uint8 [K/128, N], one per row of
+    wq, the block's exponent repeated over its 128 rows)."""
+    w = _c(w_bf16, np.uint16)
+    K, N = w.shape
+    assert K % 128 == 0 and N % 128 == 0
+    wq = np.empty((N, K), np.uint8)
+    se8 = np.empty((K // 128, N), np.uint8)
+    _load().fo_quant_weight_128x128_pow2(_ptr(w), K, N, N, _ptr(wq), _ptr(se8))
+    return wq, se8
 
 
 def quant_act_128x1(x_bf16: np.ndarray):

@@ -275,6 +275,81 @@ void fo_quant_act_1x128_e5m6(const uint16_t* x, int64_t M, int64_t K, int64_t ld
     }
 }
 
+/* ------------------------------------------------ power-of-two scales --- */
+
+/*
+ * Power-of-two group scales, the variant that Blackwell's block-scaled MMA
+ * (MXFP8: one UE8M0 exponent per 32 elements along K) can apply inside the
+ * tensor core.  The report's scale is amax / 448; here the scale is the
+ * smallest power of two s = 2^e with amax / s <= 448, so that x / s is exact
+ * and every code is the E4M3 rounding of an exactly scaled value.  e is kept
+ * in the UE8M0 range [-127, 127] (a group whose amax would need a smaller
+ * exponent keeps e = -127; its codes are then smaller than 448); an all-zero
+ * group gets e = 0.  Written from the definition: the exponent is found by
+ * stepping e upward until 448 * 2^e reaches amax.
+ */
+int fo_pow2_exponent(float amax)
+{
+    if (amax == 0.0f) return 0;
+    int e = -127;
+    while (e < 127 && (double)amax > 448.0 * ldexp(1.0, e)) ++e;
+    return e;
+}
+
+/*
+ * 1x128 activation quantisation with power-of-two scales.  x: bfloat16
+ * [M][K], row stride ldx.  xq: codes [M][K], row stride ldq.  se8: UE8M0
+ * exponent bytes e + 127, [K/128][M].
+ */
+void fo_quant_act_1x128_pow2(const uint16_t* x, int64_t M, int64_t K, int64_t ldx,
+                             uint8_t* xq, int64_t ldq, uint8_t* se8)
+{
+    int64_t KB = K / 128;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            const uint16_t* src = x + m * ldx + kb * 128;
+            float amax = 0.0f;
+            for (int j = 0; j < 128; ++j) {
+                float av = fabsf(bf16_value(src[j]));
+                if (av > amax) amax = av;
+            }
+            int e = fo_pow2_exponent(amax);
+            se8[kb * M + m] = (uint8_t)(e + 127);
+            for (int j = 0; j < 128; ++j) /* x / 2^e: exact in binary64 */
+                xq[m * ldq + kb * 128 + j] = fo_e4m3_encode((float)ldexp((double)bf16_value(src[j]), -e));
+        }
+    }
+}
+
+/*
+ * 128x128 weight quantisation with power-of-two scales.  w: bfloat16 [K][N]
+ * (K = inner dimension), row stride ldw.  wq: codes [N][K].  se8: UE8M0 bytes
+ * [K/128][N], one per row n of wq and K block (the 128 rows of a block share
+ * their block's exponent), the per-row layout a block-scaled MMA reads.
+ */
+void fo_quant_weight_128x128_pow2(const uint16_t* w, int64_t K, int64_t N, int64_t ldw,
+                                  uint8_t* wq, uint8_t* se8)
+{
+    int64_t KB = K / 128, NB = N / 128;
+    for (int64_t nb = 0; nb < NB; ++nb) {
+        for (int64_t kb = 0; kb < KB; ++kb) {
+            float amax = 0.0f;
+            for (int i = 0; i < 128; ++i)
+                for (int j = 0; j < 128; ++j) {
+                    float av = fabsf(bf16_value(w[(kb * 128 + i) * ldw + nb * 128 + j]));
+                    if (av > amax) amax = av;
+                }
+            int e = fo_pow2_exponent(amax);
+            for (int j = 0; j < 128; ++j) se8[kb * N + nb * 128 + j] = (uint8_t)(e + 127);
+            for (int i = 0; i < 128; ++i)
+                for (int j = 0; j < 128; ++j) {
+                    int64_t k = kb * 128 + i, n = nb * 128 + j;
+                    wq[n * K + k] = fo_e4m3_encode((float)ldexp((double)bf16_value(w[k * ldw + n]), -e));
+                }
+        }
+    }
+}
+
 /*
  * 128x1 activation quantisation for the weight-gradient GEMM, whose inner
  * dimension is the token dimension M.  x: bfloat16 [M][K], row stride ldx,

@@ -8,7 +8,9 @@ absolute value; in the Python layer, the dispatch's token order and expert
 ids, the expert of a boundary row, the padding of short token groups and the
 per-expert scale slice of the grouped Wgrad; for E5M6, the exponent bias,
 saturation bound, subnormal grid, mantissa width, sign of zero, divisor,
-scale index, amax and the nibble order of the packed layout.  The C mutants are compiled from
+scale index, amax and the nibble order of the packed layout; for the
+power-of-two scales, a non-minimal exponent, the clamp, the sign of the
+applied exponent and the rows that carry a weight block's exponent.  The C mutants are compiled from
 edited copies of oracle/fp8_oracle.c into temporary libraries, and the
 oracle's pin tests are run against each in a fresh process (the oracle loads
 the library named by FP8FG_ORACLE_LIB); every such run must fail.  The
@@ -31,7 +33,7 @@ from oracle import build as oracle_build
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 PINS = ["tests/test_oracle_quant.py", "tests/test_oracle_gemm.py",
         "tests/test_oracle_dispatch.py", "tests/test_oracle_e4m3.py",
-        "tests/test_oracle_e5m6.py"]
+        "tests/test_oracle_e5m6.py", "tests/test_oracle_pow2.py"]
 
 # name -> (exact text of fp8_oracle.c, replacement)
 C_MUTANTS = {
@@ -74,6 +76,14 @@ C_MUTANTS = {
     "e5m6_divisor_65536": ("return amax / 65024.0f;", "return amax / 65536.0f;"),
     "e5m6_zero_group_scale": ("if (amax == 0.0f) { return 1.0f; }",
                               "if (amax == 0.0f) { return 0.5f; }"),
+    # power-of-two scales
+    "pow2_not_minimal": ("while (e < 127 && (double)amax > 448.0 * ldexp(1.0, e)) ++e;",
+                         "while (e < 127 && (double)amax >= 448.0 * ldexp(1.0, e)) ++e;"),
+    "pow2_clamp_126": ("    int e = -127;\n    while", "    int e = -126;\n    while"),
+    "pow2_scale_not_applied": ("xq[m * ldq + kb * 128 + j] = fo_e4m3_encode((float)ldexp((double)bf16_value(src[j]), -e));",
+                               "xq[m * ldq + kb * 128 + j] = fo_e4m3_encode((float)ldexp((double)bf16_value(src[j]), e));"),
+    "pow2_weight_rows_of_block_0": ("for (int j = 0; j < 128; ++j) se8[kb * N + nb * 128 + j] = (uint8_t)(e + 127);",
+                                    "for (int j = 0; j < 128; ++j) se8[kb * N + j] = (uint8_t)(e + 127);"),
     "e5m6_scale_transposed": ("sx[m + kb * M] = s;", "sx[m * KB + kb] = s;"),
     "e5m6_amax_without_abs": ("float mag = fabsf(bf16_value(grp[j]));",
                               "float mag = bf16_value(grp[j]);"),
