@@ -851,6 +851,379 @@ static int dispatch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_
     }
 }
 
+// ------------------------------------------------------------ MXFP8 variant
+// Block-scaled GEMM for power-of-two group scales (the quantisers of
+// fp8_quant_act_1x128_pow2 / fp8_quant_weight_128x128_pow2).  With such
+// scales the per-group dequantisation can run inside the tensor core, which
+// the report wishes for (section 3.5.2): tcgen05.mma kind::mxf8f6f4 with
+// block scaling multiplies each 32-element K slice of a row of A and of B by
+// its UE8M0 exponent (our 128-wide groups repeat one exponent over four
+// slices) and accumulates the whole K range in FP32 in tensor memory, so the
+// epilogue drains the accumulator once per tile instead of promoting one
+// partial per K block.  Exact only because every scale is a power of two.
+//
+// Roles (384 threads): warp 0 TMA producer (A 128x128, B BNx128 per K block),
+// warp 1 TMEM allocator and MMA issuer, warp 2 scale loader, warps 4..11
+// epilogue.  Per K block the loader writes the scale bytes of the tile's 128
+// A rows and BN B rows as 32-row x 128-bit matrices (row r of a 128-row group
+// at bytes 16 (r % 32) + 4 (r / 32) .. + 3, its exponent repeated in all four
+// bytes) next to the stage, and the MMA warp copies them into tensor memory
+// (tcgen05.cp, four lane quadrants) ahead of the stage's MMAs: a row's scale
+// word ends up at lane r % 32 of each quadrant, column r / 32.
+constexpr int kMxSfSlots = 4;   // tensor-memory scale slots, 16 columns each
+
+template <int BN>
+struct MxCfg {
+    static constexpr int A_BYTES = BM * BK;
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int SF_BYTES = 512 * (1 + BN / 128);  // A's matrix, then B's
+    static constexpr int COLS = BN / 2;
+    static constexpr int CSTAGE_BYTES = kEpiWarps * kOutSlots * kBoxBytes;
+    static constexpr int HEADER = 256;
+    static constexpr int FIXED = HEADER + 1023 + CSTAGE_BYTES;
+    static constexpr int STAGES_FIT = (kSmemLimit - FIXED) / (STAGE_BYTES + SF_BYTES);
+    static constexpr int STAGES = STAGES_FIT > 4 ? 4 : STAGES_FIT;
+    static constexpr int SMEM = FIXED + STAGES * (STAGE_BYTES + SF_BYTES);
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int SF_COL0 = 256;  // scale slots after the accumulator
+    static_assert(STAGES >= 2, "pipeline too shallow");
+    static_assert((2 * STAGES + 3) * 8 <= HEADER - 16, "header too small");
+    static_assert(SF_COL0 + kMxSfSlots * 16 <= TMEM_COLS, "scale slots outside the allocation");
+};
+
+struct MxParams {
+    const uint8_t* sa_e8;  // [K/128][M] UE8M0 bytes
+    const uint8_t* sb_e8;  // [K/128][N]
+    int64_t M, N, K;
+    void* c;
+    int64_t ldc;
+};
+
+// Shared-memory descriptor of a 32-row x 16-byte matrix, rows contiguous (no
+// swizzle): 8-row core groups 128 bytes apart, descriptor version 1.
+__device__ __forceinline__ uint64_t smem_desc_sf(uint32_t addr) {
+    return static_cast<uint64_t>((addr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(128 >> 4) << 32) |
+           (static_cast<uint64_t>(1) << 46);
+}
+
+// Instruction descriptor of the block-scaled MMA: E4M3 x E4M3, A and B
+// K-major, N = BN, M = 128, UE8M0 scales; sf_id picks the byte of the scale
+// words for both operands.
+template <int BN>
+__device__ __forceinline__ uint32_t idesc_mxf8_e4m3(uint32_t sf_id) {
+    return (sf_id << 4) | (static_cast<uint32_t>(BN >> 3) << 17) | (1u << 23) |
+           (static_cast<uint32_t>(BM >> 4) << 24) | (sf_id << 29);
+}
+
+template <int BN, bool OUT_BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    mxfp8_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                      const __grid_constant__ CUtensorMap tmB,
+                      const __grid_constant__ CUtensorMap tmC, const MxParams p) {
+    using C = MxCfg<BN>;
+    constexpr int S = C::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + C::HEADER - 16);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + C::HEADER - 12);
+    uint8_t* base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + C::HEADER + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* stages = base;
+    uint8_t* cstage = base + S * C::STAGE_BYTES;
+    uint8_t* sf_ring = cstage + C::CSTAGE_BYTES;
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t bars_s = smem_addr(bars);
+    auto full_bar = [&](int s) { return bars_s + 8u * s; };              // TMA bytes + scale loader
+    auto empty_bar = [&](int s) { return bars_s + 8u * (S + s); };       // MMAs of the stage done
+    const uint32_t tfull_bar = bars_s + 8u * (2 * S);                    // a tile's accumulator done
+    const uint32_t tempty_bar = bars_s + 8u * (2 * S + 1);               // drained by the epilogue
+    const uint32_t drain_bar = bars_s + 8u * (2 * S + 2);
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 2);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(tfull_bar, 1);
+        mbar_init(tempty_bar, kEpiWarps);
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    griddep_wait();
+    const uint32_t tmem_base = *tmem_slot;
+    const int64_t KB = p.K / BK;
+    const int64_t nblk = p.N / BN;
+    const int64_t tiles = ((p.M + BM - 1) / BM) * nblk;
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        const bool leader = elect_one();
+        uint32_t it = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+            const int row0 = static_cast<int>((t / nblk) * BM), n0 = static_cast<int>((t % nblk) * BN);
+            for (int64_t kb = 0; kb < KB; ++kb, ++it) {
+                const int s = static_cast<int>(it % S);
+                if (!wait_bar_warp(empty_bar(s), ((it / S) & 1u) ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (leader) {
+                    uint8_t* st = stages + s * C::STAGE_BYTES;
+                    mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
+                    tma_load_2d(smem_addr(st), &tmA, full_bar(s), static_cast<int>(kb * BK), row0);
+                    tma_load_2d(smem_addr(st + C::A_BYTES), &tmB, full_bar(s),
+                                static_cast<int>(kb * BK), n0);
+                }
+                __syncwarp();
+            }
+        }
+        if (!ok && leader) {
+            const uint32_t n = it < static_cast<uint32_t>(S) ? it : static_cast<uint32_t>(S);
+            for (uint32_t i = it - n; i < it; ++i) {
+                const long long t0 = clock64();
+                while (!mbar_try_wait(full_bar(static_cast<int>(i % S)), (i / S) & 1u) &&
+                       clock64() - t0 < (1LL << 24)) {
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // --------------------------------------------------------- MMA issuer
+        const bool leader = elect_one();
+        uint32_t it = 0, tc = 0;
+        bool ok = true, issued = false;
+        for (int64_t t = blockIdx.x; ok && t < tiles; t += gridDim.x, ++tc) {
+            // the previous tile's accumulator must have been read
+            if (!wait_bar_warp(tempty_bar, (tc & 1u) ^ 1u, abort_flag)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after_sync();
+            for (int64_t kb = 0; kb < KB; ++kb, ++it) {
+                const int s = static_cast<int>(it % S);
+                if (!wait_bar_warp(full_bar(s), (it / S) & 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const uint32_t a_addr = smem_addr(stages + s * C::STAGE_BYTES);
+                const uint64_t adesc = smem_desc_sw128(a_addr);
+                const uint64_t bdesc = smem_desc_sw128(a_addr + C::A_BYTES);
+                const uint32_t sf_s = smem_addr(sf_ring + s * C::SF_BYTES);
+                const uint32_t sfa = tmem_base + C::SF_COL0 + 16u * (it % kMxSfSlots);
+                const uint32_t sfb = sfa + 4;
+                if (leader) {
+                    tmem_cp_32x128b_warpx4(sfa, smem_desc_sf(sf_s));
+#pragma unroll
+                    for (int c = 0; c < BN / 128; ++c)
+                        tmem_cp_32x128b_warpx4(sfb + 4 * c, smem_desc_sf(sf_s + 512 * (1 + c)));
+#pragma unroll
+                    for (int k = 0; k < BK / 32; ++k)
+                        mma_mxf8f6f4(tmem_base, adesc + 2 * k, bdesc + 2 * k,
+                                     idesc_mxf8_e4m3<BN>(static_cast<uint32_t>(k)), sfa, sfb,
+                                     (kb > 0 || k > 0) ? 1u : 0u);
+                    mma_commit(empty_bar(s));
+                }
+                __syncwarp();
+                issued = true;
+            }
+            if (!ok) break;
+            if (leader) mma_commit(tfull_bar);
+            __syncwarp();
+        }
+        if (!ok && issued && leader) {
+            mma_commit(drain_bar);
+            const long long t0 = clock64();
+            while (!mbar_try_wait(drain_bar, 0) && clock64() - t0 < (1LL << 24)) {
+            }
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ------------------------------------------------------ scale loader
+        uint32_t it = 0;
+        bool ok = true;
+        for (int64_t t = blockIdx.x; ok && t < tiles; t += gridDim.x) {
+            const int64_t row0 = (t / nblk) * BM, n0 = (t % nblk) * BN;
+            for (int64_t kb = 0; kb < KB; ++kb, ++it) {
+                const int s = static_cast<int>(it % S);
+                if (!wait_bar_warp(empty_bar(s), ((it / S) & 1u) ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                uint8_t* sf = sf_ring + s * C::SF_BYTES;
+                const uint8_t* ea = p.sa_e8 + kb * p.M;
+                uint32_t w[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int64_t r = row0 + lane + 32 * j;
+                    w[j] = static_cast<uint32_t>(__ldg(ea + (r < p.M ? r : p.M - 1))) * 0x01010101u;
+                }
+                *reinterpret_cast<uint4*>(sf + 16 * lane) = make_uint4(w[0], w[1], w[2], w[3]);
+                const uint8_t* eb = p.sb_e8 + kb * p.N + n0;
+#pragma unroll
+                for (int c = 0; c < BN / 128; ++c) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        w[j] = static_cast<uint32_t>(__ldg(eb + 128 * c + lane + 32 * j)) * 0x01010101u;
+                    *reinterpret_cast<uint4*>(sf + 512 * (1 + c) + 16 * lane) =
+                        make_uint4(w[0], w[1], w[2], w[3]);
+                }
+                fence_proxy_async_smem();  // the tensor-memory copy reads it
+                __syncwarp();
+                if (lane == 0) mbar_arrive(full_bar(s));
+            }
+        }
+        __syncwarp();
+    } else if (warp >= kEpiWarp0) {
+        // ---------------------------------------------------------- epilogue
+        constexpr int COLS = C::COLS;
+        constexpr int ELT = OUT_BF16 ? 2 : 4;
+        constexpr int BOX_COLS = 128 / ELT;
+        const int ew = warp - kEpiWarp0, q = warp & 3, cg = ew >> 2;
+        uint8_t* my_cstage = cstage + ew * kOutSlots * kBoxBytes;
+        uint32_t boxes = 0, tc = 0;
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + cg * COLS;
+        for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x, ++tc) {
+            if (!wait_bar_warp(tfull_bar, tc & 1u, abort_flag)) break;
+            tc_fence_after_sync();
+            const int row0 = static_cast<int>((t / nblk) * BM);
+            const int ncol0 = static_cast<int>((t % nblk) * BN) + cg * COLS;
+            const int row = row0 + q * 32 + lane;
+            const int wrow0 = row0 + q * 32;
+            const bool whole = wrow0 + 32 <= p.M;
+            // 32 columns at a time; a box (128 bytes of each of 32 rows) is
+            // 64 BF16 or 32 FP32 columns
+#pragma unroll 1
+            for (int ch = 0; ch < COLS / 32; ++ch) {
+                uint32_t r[32];
+                tmem_ld32(t_lane + 32 * ch, r);
+                tmem_wait_ld(r);
+                if (ch == COLS / 32 - 1) {
+                    tc_fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(tempty_bar);  // accumulator free for the next tile
+                }
+                uint4 pc[OUT_BF16 ? 4 : 8];  // this chunk's 16-byte pieces of the row
+#pragma unroll
+                for (int i = 0; i < (OUT_BF16 ? 4 : 8); ++i) {
+                    if (OUT_BF16)
+                        pc[i] = make_uint4(bf16x2(pack2(r[8 * i], r[8 * i + 1])),
+                                           bf16x2(pack2(r[8 * i + 2], r[8 * i + 3])),
+                                           bf16x2(pack2(r[8 * i + 4], r[8 * i + 5])),
+                                           bf16x2(pack2(r[8 * i + 6], r[8 * i + 7])));
+                    else
+                        pc[i] = make_uint4(r[4 * i], r[4 * i + 1], r[4 * i + 2], r[4 * i + 3]);
+                }
+                if (whole) {
+                    // BF16: chunks 2b and 2b+1 fill box b's pieces 0-3 and 4-7
+                    const int box_first = OUT_BF16 ? (ch % 2 == 0) : true;
+                    const int piece0 = OUT_BF16 ? (ch % 2) * 4 : 0;
+                    uint8_t* slotc = my_cstage + (boxes % kOutSlots) * kBoxBytes;
+                    if (box_first) {
+                        if (lane == 0 && boxes >= static_cast<uint32_t>(kOutSlots))
+                            bulk_wait_group_read<kOutSlots - 1>();
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int i = 0; i < (OUT_BF16 ? 4 : 8); ++i) {
+                        const int j = piece0 + i;
+                        *reinterpret_cast<uint4*>(slotc + lane * 128 + ((j ^ (lane & 7)) << 4)) = pc[i];
+                    }
+                    const bool box_done = OUT_BF16 ? (ch % 2 == 1) : true;
+                    if (box_done) {
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int bx_col = ncol0 + (OUT_BF16 ? (ch / 2) * BOX_COLS : ch * BOX_COLS);
+                            tma_store_2d(&tmC, smem_addr(slotc), bx_col, wrow0);
+                            bulk_commit_group();
+                        }
+                        ++boxes;
+                    }
+                } else if (row < p.M) {
+                    uint4* dst = reinterpret_cast<uint4*>(
+                        static_cast<uint8_t*>(p.c) + (static_cast<int64_t>(row) * p.ldc + ncol0 + 32 * ch) * ELT);
+#pragma unroll
+                    for (int i = 0; i < (OUT_BF16 ? 4 : 8); ++i) dst[i] = pc[i];
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_group0();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+template <int BN, bool OUT_BF16>
+static int mx_launch(const uint8_t* aq, const uint8_t* bq, const MxParams& p, cudaStream_t stream) {
+    using C = MxCfg<BN>;
+    auto kern = mxfp8_gemm_kernel<BN, OUT_BF16>;
+    const int sms = sm_count_current();
+    if (sms <= 0) return FP8_ERR_CUDA;
+    static ContextCache<int> attr_cache;
+    int ok = 0;
+    const int ast = attr_cache.get(&ok, [&](int* v) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+            cudaSuccess)
+            return static_cast<int>(FP8_ERR_CUDA);
+        *v = 1;
+        return static_cast<int>(FP8_OK);
+    });
+    if (ast != FP8_OK) return ast;
+    CUtensorMap ta, tb, tc;
+    int st;
+    if ((st = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, p.K, p.M, p.K, BK, BM,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != FP8_OK)
+        return st;
+    if ((st = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bq, p.K, p.N, p.K, BK, BN,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != FP8_OK)
+        return st;
+    constexpr int ELT = OUT_BF16 ? 2 : 4;
+    if ((st = make_map(&tc, OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                       p.c, p.N, p.M, p.ldc * ELT, 128 / ELT, 32, CU_TENSOR_MAP_SWIZZLE_128B)) !=
+        FP8_OK)
+        return st;
+    const int64_t tiles = ((p.M + BM - 1) / BM) * (p.N / BN);
+    const int64_t grid = tiles < sms ? tiles : sms;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return FP8_ERR_CUDA;
+    }
+    return launch_status();
+}
+
 }  // namespace fp8fg
 
 using namespace fp8fg;
@@ -922,6 +1295,27 @@ static int grouped_gemm(const uint8_t* aq, const float* sa, const uint8_t* bq, c
     // every expert adds at most one ragged M block
     return dispatch<1>(aq, T, bq, static_cast<int64_t>(E) * N, p, out_type,
                           (T + BM - 1) / BM + E, static_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp8_status fp8_gemm_mxfp8(const uint8_t* aq, const uint8_t* sa_e8, const uint8_t* bq,
+                                     const uint8_t* sb_e8, int64_t M, int64_t N, int64_t K,
+                                     void* c, int64_t ldc, fp8_out_t out_type, void* stream) {
+    if (M < 0 || N <= 0 || N % 128 != 0 || K <= 0 || K % 128 != 0 || ldc < N) return FP8_ERR_SHAPE;
+    if (out_type != FP8_OUT_F32 && out_type != FP8_OUT_BF16) return FP8_ERR_UNSUPPORTED;
+    if (M == 0) return FP8_OK;
+    if (aq == nullptr || sa_e8 == nullptr || bq == nullptr || sb_e8 == nullptr || c == nullptr)
+        return FP8_ERR_NULL;
+    const int64_t elt = out_type == FP8_OUT_BF16 ? 2 : 4;
+    if (!aligned(aq, 16) || !aligned(bq, 16) || !aligned(c, 16) || (ldc * elt) % 16 != 0)
+        return FP8_ERR_ALIGN;
+    if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL) return FP8_ERR_UNSUPPORTED;
+    MxParams p{sa_e8, sb_e8, M, N, K, c, ldc};
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (N % 256 == 0)
+        return to_status(out_type == FP8_OUT_BF16 ? mx_launch<256, true>(aq, bq, p, s)
+                                                  : mx_launch<256, false>(aq, bq, p, s));
+    return to_status(out_type == FP8_OUT_BF16 ? mx_launch<128, true>(aq, bq, p, s)
+                                              : mx_launch<128, false>(aq, bq, p, s));
 }
 
 extern "C" fp8_status fp8_grouped_gemm_moe(const uint8_t* aq, const float* sa, const uint8_t* bq,

@@ -226,6 +226,32 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// D[tmem] (+)= (A * sfA) * (B * sfB)^T, E4M3 x E4M3 -> FP32, one CTA,
+// block-scaled (MXFP8): each row of A and of B carries one UE8M0 exponent per
+// 32 elements of K, read from tensor memory at sfa_tmem / sfb_tmem; the
+// instruction descriptor selects the byte of each scale word.
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                             uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                             uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem),
+        "r"(sfb_tmem)
+        : "memory");
+}
+
+// Copy a 32-row x 128-bit matrix from shared memory (descriptor s_desc) into
+// tensor memory at taddr, the same 32 rows into each of the four 32-lane
+// quadrants: row r goes to lanes r, 32 + r, 64 + r, 96 + r, its four 32-bit
+// words to columns taddr .. taddr + 3.  Ordered with this thread's
+// tcgen05.mma in issue order.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t s_desc) {
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(s_desc)
+                 : "memory");
+}
+
 // Arrive once on `bar` when all previously issued tcgen05.mma of this thread
 // have completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar) {

@@ -169,6 +169,130 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_1x128_e5m6_kernel(
     }
 }
 
+// ---------------------------------------------- power-of-two-scale 1x128 --
+// As the 1x128 kernel, with the scale the smallest power of two 2^e such that
+// amax / 2^e <= 448; writes the UE8M0 byte e + 127 instead of an FP32 scale.
+__global__ void __launch_bounds__(kQuantThreads) quant_act_1x128_pow2_kernel(
+    const uint16_t* __restrict__ x, int64_t M, int64_t KB, int64_t ldx, uint8_t* __restrict__ xq,
+    int64_t ldq, uint8_t* __restrict__ se8, int64_t tiles) {
+    griddep_launch_dependents();
+    const int l4 = threadIdx.x & 3;
+    const int row = threadIdx.x >> 2;
+    int64_t t = blockIdx.x;
+    uint4 v[4];
+    if (t < tiles) load_1x128(x, M, ldx, KB, t, row, l4, v);
+    while (t < tiles) {
+        const int64_t tn = t + gridDim.x;
+        uint4 vn[4];
+        if (tn < tiles) load_1x128(x, M, ldx, KB, tn, row, l4, vn);
+        const int64_t kb = t % KB;
+        const int64_t m = (t / KB) * kQ1Rows + row;
+        uint32_t mx = absmax_bf16x2(v[0].x, v[0].y);
+        mx = absmax_bf16x2(mx, absmax_bf16x2(v[0].z, v[0].w));
+#pragma unroll
+        for (int i = 1; i < 4; ++i) {
+            mx = absmax_bf16x2(mx, absmax_bf16x2(v[i].x, v[i].y));
+            mx = absmax_bf16x2(mx, absmax_bf16x2(v[i].z, v[i].w));
+        }
+        float amax = amax_of_pair(mx);
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        const int e = pow2_exponent(amax);
+        const float r = pow2_inverse(e);
+        if (m < M) {
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                o[2 * i] = e4m3_scaled_pair(bf16_lo(v[i].x), bf16_hi(v[i].x), r) |
+                           (e4m3_scaled_pair(bf16_lo(v[i].y), bf16_hi(v[i].y), r) << 16);
+                o[2 * i + 1] = e4m3_scaled_pair(bf16_lo(v[i].z), bf16_hi(v[i].z), r) |
+                               (e4m3_scaled_pair(bf16_lo(v[i].w), bf16_hi(v[i].w), r) << 16);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(xq + m * ldq + kb * 128 + l4 * 32);
+            dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+            dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+            if (l4 == 0) se8[kb * M + m] = static_cast<uint8_t>(e + 127);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = vn[i];
+        t = tn;
+    }
+}
+
+// ------------------------------------------- power-of-two-scale 128x128 --
+// One CTA (256 threads) per 128x128 block: the block is staged in shared
+// memory, its amax reduced, and the codes written K-major (wq[n][k]) through
+// an XOR-swizzled shared transpose; the block's UE8M0 byte is written for
+// each of its 128 rows n (se8[kb][n]).
+__global__ void __launch_bounds__(256) quant_weight_128x128_pow2_kernel(
+    const uint16_t* __restrict__ w, int64_t K, int64_t N, int64_t ldw, uint8_t* __restrict__ wq,
+    uint8_t* __restrict__ se8) {
+    griddep_launch_dependents();
+    __shared__ __align__(16) uint16_t tile[128][128];
+    __shared__ float part[8];
+    const int t0 = threadIdx.x, lane = t0 & 31, warp = t0 >> 5;
+    const int64_t NB = N / 128;
+    const int64_t nb = blockIdx.x % NB, kb = blockIdx.x / NB;
+    const int64_t n0 = nb * 128, k0 = kb * 128;
+    const int ch = t0 & 15;
+    uint32_t mx = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = (t0 >> 4) + 16 * i;
+        const uint4 u = ld_stream_v4(w + (k0 + r) * ldw + n0 + ch * 8);
+        *reinterpret_cast<uint4*>(&tile[r][ch * 8]) = u;
+        mx = absmax_bf16x2(mx, absmax_bf16x2(u.x, u.y));
+        mx = absmax_bf16x2(mx, absmax_bf16x2(u.z, u.w));
+    }
+    float amax = amax_of_pair(mx);
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) part[warp] = amax;
+    __syncthreads();
+    amax = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
+                 fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
+    const int e = pow2_exponent(amax);
+    const float r = pow2_inverse(e);
+    if (t0 < 128) se8[kb * N + n0 + t0] = static_cast<uint8_t>(e + 127);
+    // thread: column pair (2cp, 2cp+1), rows rq*32 .. rq*32+31 -> 32 codes of
+    // each of the two columns (wq rows n = 2cp, 2cp+1), k contiguous
+    const int cp = t0 & 63, rq = t0 >> 6;
+    uint32_t ca[8], cb[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const uint32_t w0 = *reinterpret_cast<const uint32_t*>(&tile[rq * 32 + 4 * i + 2 * j][2 * cp]);
+            const uint32_t w1 = *reinterpret_cast<const uint32_t*>(&tile[rq * 32 + 4 * i + 2 * j + 1][2 * cp]);
+            // k = rq*32 + 4i + 2j and +1: column 2cp (lo halves), 2cp+1 (hi halves)
+            lo |= e4m3_scaled_pair(bf16_lo(w0), bf16_lo(w1), r) << (16 * j);
+            hi |= e4m3_scaled_pair(bf16_hi(w0), bf16_hi(w1), r) << (16 * j);
+        }
+        ca[i] = lo;
+        cb[i] = hi;
+    }
+    __syncthreads();  // every value has been read: reuse the tile for the codes
+    uint8_t* codes = reinterpret_cast<uint8_t*>(tile);  // [128 n][128 k], 16-byte chunks swizzled
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int c = rq * 2 + h;  // 16-byte chunk of the k row
+        const int na = 2 * cp, nbb = 2 * cp + 1;
+        *reinterpret_cast<uint4*>(&codes[na * 128 + ((c ^ (na & 7)) << 4)]) =
+            make_uint4(ca[4 * h], ca[4 * h + 1], ca[4 * h + 2], ca[4 * h + 3]);
+        *reinterpret_cast<uint4*>(&codes[nbb * 128 + ((c ^ (nbb & 7)) << 4)]) =
+            make_uint4(cb[4 * h], cb[4 * h + 1], cb[4 * h + 2], cb[4 * h + 3]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int j = t0 + 256 * i;
+        const int n = j >> 3, c = j & 7;
+        *reinterpret_cast<uint4*>(wq + (n0 + n) * K + k0 + c * 16) =
+            *reinterpret_cast<const uint4*>(&codes[n * 128 + ((c ^ (n & 7)) << 4)]);
+    }
+}
+
 // ------------------------------------------------------------------ 128x1 --
 // Tile: one 128-token group x 64 columns, staged in shared memory; each
 // thread then owns one column and a quarter of the 128 rows.  Tiles are
@@ -596,6 +720,35 @@ extern "C" fp8_status fp8_quant_act_1x128_e5m6(const void* x, int64_t M, int64_t
     quant_act_1x128_e5m6_kernel<<<static_cast<unsigned>(quant_grid<quant_act_1x128_e5m6_kernel>(tiles)),
                                   kQuantThreads, 0, static_cast<cudaStream_t>(stream)>>>(
         static_cast<const uint16_t*>(x), M, K / 128, ldx, xq, ldq_bytes, sx, tiles);
+    return to_status(launch_status());
+}
+
+extern "C" fp8_status fp8_quant_act_1x128_pow2(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                               uint8_t* xq, int64_t ldq, uint8_t* se8,
+                                               void* stream) {
+    if (M < 0 || K <= 0 || K % 128 != 0 || ldx < K || ldq < K) return FP8_ERR_SHAPE;
+    if (M == 0) return FP8_OK;
+    if (x == nullptr || xq == nullptr || se8 == nullptr) return FP8_ERR_NULL;
+    if (ldx % 8 != 0 || ldq % 16 != 0 || !aligned(x, 16) || !aligned(xq, 16)) return FP8_ERR_ALIGN;
+    const int64_t tiles = ((M + kQ1Rows - 1) / kQ1Rows) * (K / 128);
+    quant_act_1x128_pow2_kernel<<<static_cast<unsigned>(quant_grid<quant_act_1x128_pow2_kernel>(tiles)),
+                                  kQuantThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t*>(x), M, K / 128, ldx, xq, ldq, se8, tiles);
+    return to_status(launch_status());
+}
+
+extern "C" fp8_status fp8_quant_weight_128x128_pow2(const void* w, int64_t K, int64_t N,
+                                                   int64_t ldw, uint8_t* wq, uint8_t* se8,
+                                                   void* stream) {
+    if (K < 0 || K % 128 != 0 || N < 0 || N % 128 != 0 || ldw < N) return FP8_ERR_SHAPE;
+    if (K == 0 || N == 0) return FP8_OK;
+    if (w == nullptr || wq == nullptr || se8 == nullptr) return FP8_ERR_NULL;
+    if (ldw % 8 != 0 || !aligned(w, 16) || !aligned(wq, 16)) return FP8_ERR_ALIGN;
+    const int64_t blocks = (N / 128) * (K / 128);
+    if (blocks > 0x7fffffffLL) return FP8_ERR_UNSUPPORTED;
+    quant_weight_128x128_pow2_kernel<<<static_cast<unsigned>(blocks), 256, 0,
+                                       static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t*>(w), K, N, ldw, wq, se8);
     return to_status(launch_status());
 }
 

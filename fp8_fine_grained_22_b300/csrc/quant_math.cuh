@@ -151,6 +151,30 @@ struct GroupDiv {
     }
 };
 
+// ---------------------------------------------------- power-of-two scales --
+// The smallest e with amax <= 448 * 2^e, clamped to the UE8M0 range
+// [-127, 127]; e = 0 for amax = 0.  amax is a bfloat16 value (1 + m/128) 2^E:
+// 448 = 1.75 * 2^8, so e = E - 8 when m <= 96 (mantissa <= 1.75) and E - 7
+// otherwise; bfloat16 subnormals (and everything below 448 * 2^-128) clamp.
+__device__ __forceinline__ int pow2_exponent(float amax) {
+    const uint32_t b = __float_as_uint(amax);
+    const int ef = static_cast<int>((b >> 23) & 0xFF);
+    if (b == 0) return 0;
+    if (ef == 0) return -127;
+    const int e = ef - 127 - 8 + (((b >> 16) & 0x7F) > 96 ? 1 : 0);
+    return e < -127 ? -127 : (e > 127 ? 127 : e);
+}
+// 2^-e as a binary32 (e in [-127, 127]: 2^127 down to the subnormal 2^-127)
+__device__ __forceinline__ float pow2_inverse(int e) {
+    return e >= 127 ? 0x1p-127f : __uint_as_float(static_cast<uint32_t>(127 - e) << 23);
+}
+// E4M3 codes of x0 * r, x1 * r (r a power of two: the products are exact
+// wherever the code can be nonzero), x0 in the low byte.
+__device__ __forceinline__ uint32_t e4m3_scaled_pair(float x0, float x1, float r) {
+    return static_cast<uint32_t>(
+        __nv_cvt_float2_to_fp8x2(make_float2(x0 * r, x1 * r), __NV_SATFINITE, __NV_E4M3));
+}
+
 // ------------------------------------------------------------------ E5M6 --
 // E5M6 (sign, 5-bit exponent with bias 15, 6-bit mantissa; exponent field 31
 // reserved; largest finite 65024 = 0x7BF; subnormals m * 2^-20): the 12-bit

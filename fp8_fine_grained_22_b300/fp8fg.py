@@ -25,7 +25,8 @@ FP8_BSCALE_BLOCK128_T = 2
 EXPORTS = ("fp8_status_str", "fp8_device_error", "fp8_selftest_wait_timeout",
            "fp8_quant_act_1x128", "fp8_quant_act_1x128_e5m6", "fp8_quant_act_128x1",
            "fp8_quant_weight_128x128",
-           "fp8_quant_fprop_operands",
+           "fp8_quant_fprop_operands", "fp8_quant_act_1x128_pow2",
+           "fp8_quant_weight_128x128_pow2", "fp8_gemm_mxfp8",
            "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe", "fp8_grouped_gemm_moe_dgrad",
            "fp8_quant_act_128x1_grouped", "fp8_grouped_gemm_moe_wgrad",
            "fp8_moe_dispatch_workspace_size", "fp8_moe_dispatch_quant",
@@ -62,6 +63,12 @@ def lib() -> ctypes.CDLL:
         L.fp8_quant_act_1x128.argtypes = [P, I64, I64, I64, P, I64, P, P]
         L.fp8_quant_act_1x128_e5m6.restype = I
         L.fp8_quant_act_1x128_e5m6.argtypes = [P, I64, I64, I64, P, I64, P, P]
+        L.fp8_quant_act_1x128_pow2.restype = I
+        L.fp8_quant_act_1x128_pow2.argtypes = [P, I64, I64, I64, P, I64, P, P]
+        L.fp8_quant_weight_128x128_pow2.restype = I
+        L.fp8_quant_weight_128x128_pow2.argtypes = [P, I64, I64, I64, P, P, P]
+        L.fp8_gemm_mxfp8.restype = I
+        L.fp8_gemm_mxfp8.argtypes = [P, P, P, P, I64, I64, I64, P, I64, I, P]
         L.fp8_quant_act_128x1.restype = I
         L.fp8_quant_act_128x1.argtypes = [P, I64, I64, I64, P, P, P]
         L.fp8_quant_weight_128x128.restype = I
@@ -239,6 +246,55 @@ def fp8_gemm_blockscaled(aq, sa, bq, sb, bmode=FP8_BSCALE_BLOCK128, out_dtype=to
     _check(lib().fp8_gemm_blockscaled(_p(aq), _p(sa), _p(bq), _p(sb), int(bmode), M, N, K, _p(c),
                                       c.stride(0), out_type, _stream(stream)),
            "fp8_gemm_blockscaled")
+    return c
+
+
+# ------------------------------------------------ MXFP8 (power-of-two) variant --
+def fp8_quant_act_1x128_pow2(x, xq=None, se8=None, stream=None):
+    """x: bf16 [M, K] -> (xq uint8 [M, K], se8 uint8 [K/128, M] UE8M0 exponents)."""
+    _cuda(x, "x", torch.bfloat16)
+    assert x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if se8 is None:
+        se8 = torch.empty((K // 128, M), dtype=torch.uint8, device=x.device)
+    assert xq.stride(1) == 1 and se8.is_contiguous()
+    _check(lib().fp8_quant_act_1x128_pow2(_p(x), M, K, x.stride(0), _p(xq), xq.stride(0),
+                                          _p(se8), _stream(stream)), "fp8_quant_act_1x128_pow2")
+    return xq, se8
+
+
+def fp8_quant_weight_128x128_pow2(w, wq=None, se8=None, stream=None):
+    """w: bf16 [K, N] -> (wq uint8 [N, K], se8 uint8 [K/128, N] per-row UE8M0 exponents)."""
+    _cuda(w, "w", torch.bfloat16)
+    assert w.dim() == 2 and w.stride(1) == 1
+    K, N = w.shape
+    if wq is None:
+        wq = torch.empty((N, K), dtype=torch.uint8, device=w.device)
+    if se8 is None:
+        se8 = torch.empty((K // 128, N), dtype=torch.uint8, device=w.device)
+    assert wq.is_contiguous() and se8.is_contiguous()
+    _check(lib().fp8_quant_weight_128x128_pow2(_p(w), K, N, w.stride(0), _p(wq), _p(se8),
+                                               _stream(stream)), "fp8_quant_weight_128x128_pow2")
+    return wq, se8
+
+
+def fp8_gemm_mxfp8(aq, sa_e8, bq, sb_e8, out_dtype=torch.bfloat16, c=None, stream=None):
+    """C[M, N] on the block-scaled tensor-core path; aq uint8 [M, K], sa_e8 uint8 [K/128, M],
+    bq uint8 [N, K], sb_e8 uint8 [K/128, N]."""
+    for t, n in ((aq, "aq"), (sa_e8, "sa_e8"), (bq, "bq"), (sb_e8, "sb_e8")):
+        _cuda(t, n, torch.uint8)
+    M, K = aq.shape
+    N = bq.shape[0]
+    assert aq.is_contiguous() and bq.is_contiguous() and bq.shape[1] == K
+    assert sa_e8.is_contiguous() and sb_e8.is_contiguous()
+    out_type = FP8_OUT_BF16 if out_dtype == torch.bfloat16 else FP8_OUT_F32
+    if c is None:
+        c = torch.empty((M, N), dtype=out_dtype, device=aq.device)
+    assert c.stride(1) == 1
+    _check(lib().fp8_gemm_mxfp8(_p(aq), _p(sa_e8), _p(bq), _p(sb_e8), M, N, K, _p(c), c.stride(0),
+                                out_type, _stream(stream)), "fp8_gemm_mxfp8")
     return c
 
 

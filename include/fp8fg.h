@@ -199,6 +199,64 @@ fp8_status fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, const uint8_
                          void* c, int64_t ldc, fp8_out_t out_type, void* stream);
 
 /*
+ * The MXFP8 variant (power-of-two scales).  The report wishes that the
+ * per-group dequantisation could be completed inside the tensor cores
+ * (section 3.5.2); Blackwell's block-scaled MMA does that, but only with
+ * power-of-two scales (UE8M0 exponents).  These three calls quantise with the
+ * smallest power-of-two scale 2^e such that amax / 2^e <= 448 (e in
+ * [-127, 127]; e = 0 for an all-zero group) and multiply with the scales
+ * applied inside the tensor core, accumulating the whole K range in FP32 in
+ * tensor memory.  With such scales the result is the same block-scaled
+ * product as fp8_gemm_blockscaled computes; the codes differ from the amax/448
+ * quantisers' (a different scale), so the variant is an alternative
+ * quantisation, not a drop-in for the other calls' outputs.
+ */
+
+/*
+ * fp8_quant_act_1x128_pow2 -- 1x128 activation quantisation with power-of-two
+ * scales.
+ *   x   : bfloat16 [M][K], row stride ldx.                             (input)
+ *   xq  : E4M3 codes [M][K], row stride ldq; code = E4M3_RNE_satfinite(x / 2^e),
+ *         x / 2^e exact.                                               (output)
+ *   se8 : UE8M0 bytes [K/128][M]: e + 127 of row m, K group kb at se8[kb*M + m]. (output)
+ * Requires K % 128 == 0, ldx >= K, ldq >= K, ldx % 8 == 0, ldq % 16 == 0,
+ * x and xq 16-byte aligned.  M >= 0.
+ */
+fp8_status fp8_quant_act_1x128_pow2(const void* x, int64_t M, int64_t K, int64_t ldx,
+                                    uint8_t* xq, int64_t ldq, uint8_t* se8, void* stream);
+
+/*
+ * fp8_quant_weight_128x128_pow2 -- 128x128 weight quantisation with
+ * power-of-two scales.
+ *   w   : bfloat16 [K][N], row stride ldw.                             (input)
+ *   wq  : E4M3 codes [N][K] (K contiguous).                            (output)
+ *   se8 : UE8M0 bytes [K/128][N]: the exponent of the block holding row n of
+ *         wq, K group kb, at se8[kb*N + n] (each block's byte on its 128 rows:
+ *         the per-row layout fp8_gemm_mxfp8 reads).                   (output)
+ * Requires K % 128 == 0, N % 128 == 0, ldw >= N, ldw % 8 == 0, w and wq
+ * 16-byte aligned.
+ */
+fp8_status fp8_quant_weight_128x128_pow2(const void* w, int64_t K, int64_t N, int64_t ldw,
+                                         uint8_t* wq, uint8_t* se8, void* stream);
+
+/*
+ * fp8_gemm_mxfp8 -- C[M][N] = sum over k of (aq[m][k] 2^ea) (bq[n][k] 2^eb),
+ * ea = sa_e8[k/128][m] - 127, eb = sb_e8[k/128][n] - 127, on the block-scaled
+ * tensor-core path (tcgen05.mma kind::mxf8f6f4): each 32-element K slice of a
+ * row carries its exponent into the MMA and the whole K range accumulates in
+ * FP32 in tensor memory.
+ *   aq    : E4M3 [M][K], K contiguous.  sa_e8: uint8 [K/128][M].       (input)
+ *   bq    : E4M3 [N][K], K contiguous.  sb_e8: uint8 [K/128][N].       (input)
+ *   c     : [M][N] row stride ldc, float or bfloat16 RNE per out_type. (output)
+ * Requires K % 128 == 0, K > 0, N % 128 == 0, ldc >= N, ldc*elt % 16 == 0,
+ * aq/bq/c 16-byte aligned, M >= 0.  Launched with programmatic stream
+ * serialisation like the other GEMMs.
+ */
+fp8_status fp8_gemm_mxfp8(const uint8_t* aq, const uint8_t* sa_e8, const uint8_t* bq,
+                          const uint8_t* sb_e8, int64_t M, int64_t N, int64_t K, void* c,
+                          int64_t ldc, fp8_out_t out_type, void* stream);
+
+/*
  * fp8_grouped_gemm_moe -- per-expert block-scaled GEMM over rows grouped by
  * expert (report section 3.4: MoE expert GEMMs; section 3.4.2: decode-time
  * batches of at most a few hundred tokens per expert are memory bound).
