@@ -659,7 +659,40 @@ def measure_configs(args, d, peaks, tr):
     out["cfg4_moe_prefill_t16384_top8of256_e32"] = moe.pop("result")
     out["cfg5_moe_decode_e32_t1to256"] = cfg5(d, peaks, moe)
     out["quantisers"] = quantisers(d, peaks, tr, moe)
+    out["mxfp8_variant (power-of-two scales)"] = mxfp8_variant(d, peaks, tr)
     return out
+
+
+def mxfp8_variant(d, peaks, tr):
+    """The MXFP8 variant (power-of-two group scales, dequantisation inside the
+    tensor core): its quantisers and block-scaled GEMM at the dense Fprop and
+    the trio Fprop sizes, beside the promotion GEMM at the same sizes."""
+    from fp8_fine_grained_22_b300 import fp8fg
+    s = d.stream
+    res = {}
+    wl = inputs.fprop_dense(seed=0)
+    cases = [("fprop_m8192_n7168_k2048_bf16", wl.x.to(d.dev), wl.w.to(d.dev)),
+             ("trio_fprop_m8192_n4096_k7168_bf16", tr.x, tr.w)]
+    for name, x, w in cases:
+        M, K = x.shape
+        N = w.shape[1]
+        xq, sx8 = fp8fg.fp8_quant_act_1x128_pow2(x)
+        wq, sw8 = fp8fg.fp8_quant_weight_128x128_pow2(w)
+        y = torch.empty((M, N), dtype=torch.bfloat16, device=d.dev)
+        gm = d.kernel_ms(lambda: fp8fg.fp8_gemm_mxfp8(xq, sx8, wq, sw8, c=y, stream=s), reps=20)
+        qx = d.kernel_ms(lambda: fp8fg.fp8_quant_act_1x128_pow2(x, xq, sx8, stream=s), reps=20)
+        qw = d.kernel_ms(lambda: fp8fg.fp8_quant_weight_128x128_pow2(w, wq, sw8, stream=s), reps=20)
+        f = 2.0 * M * N * K
+        tf = tflops(f, gm)
+        qxb = M * K * 3 + (K // 128) * M
+        qwb = K * N * 3 + (K // 128) * N
+        res[name] = {"gemm_ms": round(gm, 5), "gemm_tflops": round(tf, 2),
+                     "gemm_frac": frac_set(tf, peaks),
+                     "quant_act_ms": round(qx, 5),
+                     "quant_act_frac_hbm": round(gbs(qxb, qx) / peaks["hbm"], 4),
+                     "quant_weight_ms": round(qw, 5),
+                     "quant_weight_frac_hbm": round(gbs(qwb, qw) / peaks["hbm"], 4)}
+    return res
 
 
 def cfg1(d, peaks):
