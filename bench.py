@@ -1055,6 +1055,46 @@ def run_reference(args):
     }
 
 
+def probe_gemms():
+    """For an ncu capture: one warm-up launch, then one launch with L2 flushed
+    before it, of each GEMM the profiles cover (trio Fprop, Dgrad, Wgrad; the
+    dense Fprop; the MoE decode grouped GEMM; the MXFP8 dense Fprop)."""
+    from fp8_fine_grained_22_b300 import fp8fg
+    d = Dev(0)
+    fp8fg.lib()
+    tr = Trio(d, inputs.training_trio(seed=0))
+    for fn in tr.launches()[:4]:
+        fn()
+    wl = inputs.fprop_dense(seed=0)
+    x2, w2 = wl.x.to(d.dev), wl.w.to(d.dev)
+    xq2, sx2, wq2, _, sw2 = fp8fg.fp8_quant_fprop_operands(x2, w2)
+    y2 = torch.empty((wl.M, wl.N), dtype=torch.bfloat16, device=d.dev)
+    dec = inputs.moe_decode(seed=0, device=d.dev)
+    dxq, dsx = fp8fg.fp8_quant_act_1x128(dec.x.to(d.dev))
+    dwq = torch.empty((dec.E, dec.N, dec.K), dtype=torch.uint8, device=d.dev)
+    dsw = torch.empty((dec.E, dec.N // 128, dec.K // 128), dtype=torch.float32, device=d.dev)
+    for e in range(dec.E):
+        fp8fg.fp8_quant_weight_128x128(dec.w[e], wq=dwq[e], sw=dsw[e])
+    off = torch.from_numpy(np.asarray(dec.offsets, np.int32)).to(d.dev)
+    yd = torch.empty((int(dec.offsets[-1]), dec.N), dtype=torch.bfloat16, device=d.dev)
+    mxq, mx8 = fp8fg.fp8_quant_act_1x128_pow2(x2)
+    mwq, mw8 = fp8fg.fp8_quant_weight_128x128_pow2(w2)
+    runs = tr.launches()[4:] + [
+        lambda: fp8fg.fp8_gemm_blockscaled(xq2, sx2, wq2, sw2, c=y2),
+        lambda: fp8fg.fp8_grouped_gemm_moe(dxq, dsx, dwq, dsw, off, c=yd),
+        lambda: fp8fg.fp8_gemm_mxfp8(mxq, mx8, mwq, mw8, c=y2)]
+    for r in runs:
+        r()
+    for r in runs:
+        d.flush_l2()
+        torch.cuda.synchronize()
+        r()
+    torch.cuda.synchronize()
+    if fp8fg.device_error() != 0:
+        raise RuntimeError("device-side error")
+    print(json.dumps({"probe": "gemms", "launches": 2 * len(runs)}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1070,7 +1110,13 @@ def main():
                     help="tokens of the trio the cpu_baseline oracle run covers (multiple of 128)")
     ap.add_argument("--workload", default="trio",
                     choices=["trio", "fprop_dense", "moe_prefill", "moe_decode", "moe_backward"])
+    ap.add_argument("--probe", choices=["gemms"], default=None,
+                    help="launch each profiled GEMM twice (warm-up, then L2 flushed) and exit: "
+                         "the program the committed ncu summaries capture")
     args = ap.parse_args()
+    if args.probe == "gemms":
+        probe_gemms()
+        return
     if args.ref_tokens % 128 or args.cpu_tokens % 128:
         ap.error("--ref-tokens and --cpu-tokens must be multiples of 128")
     if args.warmup < 3 and args.impl == "ours":
