@@ -36,6 +36,7 @@
 
 #include "common.cuh"
 #include "ptx.cuh"
+#include "quant_math.cuh"
 #include "tensormap.cuh"
 
 namespace fp8fg {
@@ -1224,6 +1225,472 @@ static int mx_launch(const uint8_t* aq, const uint8_t* bq, const MxParams& p, cu
     return launch_status();
 }
 
+// ------------------------------------------------ activation cast fused in
+// The report wishes the FP8 conversion of activations were fused with the
+// TMA access that brings them in (section 3.5.2).  This GEMM takes A as
+// bfloat16 and quantises it 1x128 inside the kernel: per K block the producer
+// TMA-loads the BF16 A tile (two 64-column boxes, 128-byte swizzle) into one
+// of two staging slots, and a converter warpgroup (four warps) converts it
+// with the arithmetic of fp8_quant_act_1x128 (four lanes per row,
+// amax by shuffles, the same correctly rounded quotients), writing the E4M3
+// codes straight into the stage's swizzled A tile the MMA reads and the row
+// scales into a ring the epilogue reads.  Codes and scales are the bits the
+// 1x128 quantiser produces, so the output is bitwise the output of
+// quantise-then-fp8_gemm_blockscaled.  B is the pre-quantised weight (block
+// scales, Fprop or the transposed Dgrad layout); tiles are 128 x 256.
+// 512 threads: warpgroup 0 producer / MMA issuer (warps 2-3 idle), warpgroup
+// 1 the converter (four warps), warpgroups 2-3 the epilogue.  Register split
+// (setmaxnreg) within the launch's 512 x 128: 128 x 40 + 128 x 64 + 256 x 200
+// = 64512.  The host refuses a build whose register count is not 128.
+constexpr int kFzThreads = 512;
+constexpr int kFzLaunchRegs = 128;
+constexpr int kFzConvRegs = 64;
+constexpr int kFzEpiRegs = 200;
+constexpr int kFzConvWarp0 = 4, kFzConvWarps = 4, kFzEpiWarp0 = 8;
+static_assert(128 * kCtrlRegs + 128 * kFzConvRegs + 256 * kFzEpiRegs <= kFzThreads * kFzLaunchRegs,
+              "fused register split");
+constexpr int kFzStages = 2;   // operand stages (FP8 A tile + B tile)
+constexpr int kFzSlots = 2;    // BF16 A staging slots
+constexpr int kFzSR = 8;       // A-scale ring slots
+constexpr int kFzOutSlots = 1;
+
+struct FzCfg {
+    static constexpr int BN = 256;
+    static constexpr int A_BYTES = BM * BK;              // FP8 A tile
+    static constexpr int B_BYTES = BN * BK;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr int X_BYTES = BM * BK * 2;           // BF16 A tile (two boxes)
+    static constexpr int COLS = BN / 2;
+    static constexpr int CSTAGE_BYTES = kEpiWarps * kFzOutSlots * kBoxBytes;
+    static constexpr int RING_BYTES = kFzSR * BM * 4;
+    static constexpr int HEADER = 512;
+    static constexpr int SMEM = HEADER + 1023 + kFzStages * STAGE_BYTES + kFzSlots * X_BYTES +
+                                CSTAGE_BYTES + RING_BYTES;
+    static constexpr int NBUF = 2;
+    static constexpr int NBARS = 2 * kFzStages + 2 * kFzSlots + 2 * NBUF + 1 + 2 * kFzSR;
+    static_assert(SMEM <= kSmemLimit, "fused GEMM does not fit shared memory");
+    static_assert(NBARS * 8 <= HEADER - 16, "header too small");
+};
+
+template <bool OUT_BF16, int GM>
+__global__ void __launch_bounds__(kFzThreads, 1)
+    gemm_fused_act_kernel(const __grid_constant__ CUtensorMap tmX,
+                          const __grid_constant__ CUtensorMap tmB,
+                          const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
+    constexpr bool GROUPED = GM == 1;
+    using C = FzCfg;
+    constexpr int BN = C::BN, S = kFzStages, SX = kFzSlots, SR = kFzSR, NBUF = C::NBUF;
+    extern __shared__ uint8_t smem_raw[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + C::HEADER - 16);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + C::HEADER - 12);
+    uint8_t* base = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + C::HEADER + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t* stages = base;
+    uint8_t* xslots = stages + S * C::STAGE_BYTES;
+    uint8_t* cstage = xslots + SX * C::X_BYTES;
+    float* ring = reinterpret_cast<float*>(cstage + C::CSTAGE_BYTES);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t bars_s = smem_addr(bars);
+    auto bar_at = [bars_s](int i) { return bars_s + 8u * static_cast<uint32_t>(i); };
+    // stage full: B bytes + both converter warps; stage empty: MMAs done
+    auto full_bar = [&](int s) { return bar_at(s); };
+    auto empty_bar = [&](int s) { return bar_at(S + s); };
+    // BF16 slot full: A bytes landed; slot empty: both converter warps read it
+    auto xfull_bar = [&](int x) { return bar_at(2 * S + x); };
+    auto xempty_bar = [&](int x) { return bar_at(2 * S + SX + x); };
+    auto tfull_bar = [&](int b) { return bar_at(2 * S + 2 * SX + b); };
+    auto tempty_bar = [&](int b) { return bar_at(2 * S + 2 * SX + NBUF + b); };
+    const uint32_t drain_bar = bar_at(2 * S + 2 * SX + 2 * NBUF);
+    // A-scale ring: full (both converter warps wrote), empty (all epilogue warps read)
+    auto sfull_bar = [&](int r) { return bar_at(2 * S + 2 * SX + 2 * NBUF + 1 + r); };
+    auto sempty_bar = [&](int r) { return bar_at(2 * S + 2 * SX + 2 * NBUF + 1 + SR + r); };
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(full_bar(s), 1 + kFzConvWarps);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int x = 0; x < SX; ++x) {
+            mbar_init(xfull_bar(x), 1);
+            mbar_init(xempty_bar(x), kFzConvWarps);
+        }
+        for (int b = 0; b < NBUF; ++b) {
+            mbar_init(tfull_bar(b), 1);
+            mbar_init(tempty_bar(b), kEpiWarps);
+        }
+        mbar_init(drain_bar, 1);
+        for (int r = 0; r < SR; ++r) {
+            mbar_init(sfull_bar(r), kFzConvWarps);
+            mbar_init(sempty_bar(r), kEpiWarps);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmC);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_addr(tmem_slot), 512);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    griddep_wait();
+    if (GROUPED) {
+        bool bad = false;
+        if (threadIdx.x == 0) bad = (__ldg(p.offsets) != 0) || (__ldg(p.offsets + p.E) > p.M);
+        for (int e = threadIdx.x; e < p.E; e += kFzThreads)
+            bad |= __ldg(p.offsets + e + 1) < __ldg(p.offsets + e);
+        if (bad) raise_error(abort_flag, kErrBadOffsets);
+        __syncthreads();
+    }
+    const uint32_t tmem_base = *tmem_slot;
+    const int64_t KB = p.K / BK;
+    const bool aborted_at_start = *abort_flag != 0;
+    if (warp < kFzConvWarp0)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
+    else if (warp < kFzEpiWarp0)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kFzConvRegs));
+    constexpr bool kWarpRoles = !GROUPED;
+    auto role_wait = [&](uint32_t bar, uint32_t parity) {
+        return kWarpRoles ? wait_bar_warp(bar, parity, abort_flag) : wait_bar(bar, parity, abort_flag);
+    };
+    auto role_sync = [&]() {
+        if (kWarpRoles) __syncwarp();
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if ((kWarpRoles || lane == 0) && !aborted_at_start) {
+            const bool leader = kWarpRoles ? elect_one() : true;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
+                Tile ti;
+                if (!get_tile<BN, GROUPED>(p, t, ti)) break;
+                for (int64_t kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = static_cast<int>(it % S), x = static_cast<int>(it % SX);
+                    if (!role_wait(empty_bar(s), ((it / S) & 1u) ^ 1u) ||
+                        !role_wait(xempty_bar(x), ((it / SX) & 1u) ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    if (leader) {
+                        uint8_t* st = stages + s * C::STAGE_BYTES;
+                        mbar_arrive_expect_tx(full_bar(s), C::B_BYTES);
+                        tma_load_2d(smem_addr(st + C::A_BYTES), &tmB, full_bar(s),
+                                    static_cast<int>(kb * BK), static_cast<int>(ti.b_row0));
+                        uint8_t* xs = xslots + x * C::X_BYTES;
+                        mbar_arrive_expect_tx(xfull_bar(x), C::X_BYTES);
+                        tma_load_2d(smem_addr(xs), &tmX, xfull_bar(x), static_cast<int>(kb * BK),
+                                    static_cast<int>(ti.row0));
+                        tma_load_2d(smem_addr(xs + C::X_BYTES / 2), &tmX, xfull_bar(x),
+                                    static_cast<int>(kb * BK + 64), static_cast<int>(ti.row0));
+                    }
+                    role_sync();
+                }
+            }
+            role_sync();
+        }
+    } else if (warp == 1) {
+        // --------------------------------------------------------- MMA issuer
+        if ((kWarpRoles || lane == 0) && !aborted_at_start) {
+            const bool leader = kWarpRoles ? elect_one() : true;
+            const uint32_t idesc = idesc_e4m3_f32<BN>();
+            uint32_t it = 0;
+            bool ok = true, issued = false;
+            for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
+                Tile ti;
+                if (!get_tile<BN, GROUPED>(p, t, ti)) break;
+                for (int64_t kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = static_cast<int>(it % S);
+                    const uint32_t buf = it % NBUF, tph = (it / NBUF) & 1u;
+                    if (!role_wait(full_bar(s), (it / S) & 1u) || !role_wait(tempty_bar(buf), tph ^ 1u)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after_sync();
+                    const uint32_t a_addr = smem_addr(stages + s * C::STAGE_BYTES);
+                    const uint64_t adesc = smem_desc_sw128(a_addr);
+                    const uint64_t bdesc = smem_desc_sw128(a_addr + C::A_BYTES);
+                    const uint32_t d = tmem_base + buf * BN;
+                    if (leader) {
+#pragma unroll
+                        for (int k = 0; k < BK / 32; ++k)
+                            mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+                        mma_commit(tfull_bar(buf));
+                        mma_commit(empty_bar(s));
+                    }
+                    role_sync();
+                    issued = true;
+                }
+            }
+            if (!ok && issued && leader) {
+                mma_commit(drain_bar);
+                const long long t0 = clock64();
+                while (!mbar_try_wait(drain_bar, 0) && clock64() - t0 < (1LL << 24)) {
+                }
+            }
+            role_sync();
+        }
+    } else if (warp >= kFzConvWarp0 && warp < kFzEpiWarp0) {
+        // ------------------------------------------------ 1x128 A converter
+        // Per pass 32 rows (8 per warp), four lanes per row, 32 elements per
+        // lane held in registers (one 64-column box holds a lane pair's 64).
+        if (!aborted_at_start) {
+            const int w = warp - kFzConvWarp0, l4 = lane & 3, box = l4 >> 1, half = l4 & 1;
+            uint32_t it = 0;
+            bool ok = true;
+            for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
+                Tile ti;
+                if (!get_tile<BN, GROUPED>(p, t, ti)) break;
+                for (int64_t kb = 0; kb < KB; ++kb, ++it) {
+                    const int s = static_cast<int>(it % S), x = static_cast<int>(it % SX);
+                    const int r8 = static_cast<int>(it % SR);
+                    if (!wait_bar_warp(xfull_bar(x), (it / SX) & 1u, abort_flag) ||
+                        !wait_bar_warp(empty_bar(s), ((it / S) & 1u) ^ 1u, abort_flag) ||
+                        !wait_bar_warp(sempty_bar(r8), ((it / SR) & 1u) ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t xs = smem_addr(xslots + x * C::X_BYTES) + box * (C::X_BYTES / 2);
+                    const uint32_t as = smem_addr(stages + s * C::STAGE_BYTES);
+                    const uint32_t sa_slot = smem_addr(ring + r8 * BM);
+#pragma unroll 1
+                    for (int pass = 0; pass < BM / (8 * kFzConvWarps); ++pass) {
+                        const int r = pass * 8 * kFzConvWarps + w * 8 + (lane >> 2);
+                        const uint32_t rowx = xs + r * 128;
+                        uint32_t v[16];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float4 f = lds_f32x4(rowx + (((half * 4 + i) ^ (r & 7)) << 4));
+                            v[4 * i] = __float_as_uint(f.x);
+                            v[4 * i + 1] = __float_as_uint(f.y);
+                            v[4 * i + 2] = __float_as_uint(f.z);
+                            v[4 * i + 3] = __float_as_uint(f.w);
+                        }
+                        uint32_t mx = absmax_bf16x2(v[0], v[1]);
+#pragma unroll
+                        for (int i = 1; i < 8; ++i) mx = absmax_bf16x2(mx, absmax_bf16x2(v[2 * i], v[2 * i + 1]));
+                        float amax = amax_of_pair(mx);
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+                        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+                        const float sc = group_scale(amax);
+                        const GroupDiv dv(sc);
+                        uint32_t o[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) o[i] = dv.quad_words(v[2 * i], v[2 * i + 1]);
+                        // the row's 128 codes: 16-byte chunks 2 l4 and 2 l4 + 1 (swizzled)
+                        const uint32_t rowa = as + r * 128;
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                         rowa + (((2 * l4) ^ (r & 7)) << 4)),
+                                     "r"(o[0]), "r"(o[1]), "r"(o[2]), "r"(o[3])
+                                     : "memory");
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(
+                                         rowa + (((2 * l4 + 1) ^ (r & 7)) << 4)),
+                                     "r"(o[4]), "r"(o[5]), "r"(o[6]), "r"(o[7])
+                                     : "memory");
+                        if (l4 == 0)
+                            asm volatile("st.shared.f32 [%0], %1;" ::"r"(sa_slot + 4u * r), "f"(sc)
+                                         : "memory");
+                    }
+                    fence_proxy_async_smem();  // the MMA reads the codes through the async proxy
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(xempty_bar(x));
+                        mbar_arrive(sfull_bar(r8));
+                        mbar_arrive(full_bar(s));
+                    }
+                }
+            }
+            __syncwarp();
+        }
+    } else if (warp >= kFzEpiWarp0) {
+        // ------------------------------------------------- promotion epilogue
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kFzEpiRegs));
+        constexpr int COLS = C::COLS;
+        constexpr int ELT = OUT_BF16 ? 2 : 4;
+        constexpr int BOX_COLS = 128 / ELT;
+        const int ew = warp - kFzEpiWarp0, q = warp & 3, cg = ew >> 2;
+        uint8_t* my_cstage = cstage + ew * kFzOutSlots * kBoxBytes;
+        uint32_t boxes = 0, it = 0;
+        const uint32_t t_lane = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + cg * COLS;
+        const uint32_t sa_addr0 = smem_addr(ring) + 4u * (q * 32 + lane);
+        bool ok = !aborted_at_start;
+        for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
+            Tile ti;
+            if (!get_tile<BN, GROUPED>(p, t, ti)) break;
+            const int row = static_cast<int>(ti.row0) + q * 32 + lane;
+            const int row_end = static_cast<int>(ti.row_end);
+            const int ncol0 = static_cast<int>(ti.n0) + cg * COLS;
+            const int KBi = static_cast<int>(KB);
+            const int nb = ncol0 / 128;
+            const bool blk = p.bmode == FP8_BSCALE_BLOCK128;
+            const float* sb_g = p.sb + (GROUPED ? ti.expert * p.sb_expert : 0) + (blk ? nb * KBi : nb);
+            const int sb_step = blk ? 1 : static_cast<int>(p.N / 128);
+            float sb_next = __ldg(sb_g);
+            uint64_t acc[COLS / 2];
+#pragma unroll
+            for (int i = 0; i < COLS / 2; ++i) acc[i] = 0;
+            for (int kb = 0; kb < KBi; ++kb, ++it) {
+                const float sb_cur = sb_next;
+                if (kb + 1 < KBi) sb_next = __ldg(sb_g + (kb + 1) * sb_step);
+                const int r8 = static_cast<int>(it % SR);
+                const uint32_t buf = it % NBUF, tph = (it / NBUF) & 1u;
+                if (!wait_bar_warp(sfull_bar(r8), (it / SR) & 1u, abort_flag) ||
+                    !wait_bar_warp(tfull_bar(buf), tph, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after_sync();
+                const float sc = lds_f32(sa_addr0 + 4u * BM * r8) * sb_cur;
+                __syncwarp();
+                if (lane == 0) mbar_arrive(sempty_bar(r8));
+                const uint64_t sc2 = pack2(f2u(sc), f2u(sc));
+                const uint32_t taddr = t_lane + buf * BN;
+                // 16-column TMEM loads, two in flight (the 200-register budget)
+                auto fma16 = [&](uint32_t (&rr)[16], int ch) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        acc[ch * 8 + i] = ffma2(pack2(rr[2 * i], rr[2 * i + 1]), sc2, acc[ch * 8 + i]);
+                };
+                uint32_t r0[16], r1[16];
+                tmem_ld16(taddr, r0);
+                tmem_ld16(taddr + 16, r1);
+#pragma unroll
+                for (int ch = 0; ch < COLS / 16; ch += 2) {
+                    tmem_wait_ld16(r0);
+                    tmem_wait_ld16(r1);
+                    if (ch + 2 < COLS / 16) {
+                        fma16(r0, ch);
+                        tmem_ld16(taddr + (ch + 2) * 16, r0);
+                        fma16(r1, ch + 1);
+                        tmem_ld16(taddr + (ch + 3) * 16, r1);
+                    } else {
+                        tc_fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(tempty_bar(buf));
+                        fma16(r0, ch);
+                        fma16(r1, ch + 1);
+                    }
+                }
+            }
+            if (!ok) break;
+            const int wrow0 = static_cast<int>(ti.row0) + q * 32;
+            if (wrow0 + 32 <= row_end) {
+#pragma unroll
+                for (int bx = 0; bx < COLS / BOX_COLS; ++bx, ++boxes) {
+                    uint8_t* slotc = my_cstage + (boxes % kFzOutSlots) * kBoxBytes;
+                    if (lane == 0 && boxes >= static_cast<uint32_t>(kFzOutSlots))
+                        bulk_wait_group_read<kFzOutSlots - 1>();
+                    __syncwarp();
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        uint4 v;
+                        if (OUT_BF16) {
+                            const int a0 = (bx * BOX_COLS + j * 8) / 2;
+                            v = make_uint4(bf16x2(acc[a0]), bf16x2(acc[a0 + 1]), bf16x2(acc[a0 + 2]),
+                                           bf16x2(acc[a0 + 3]));
+                        } else {
+                            const int a0 = (bx * BOX_COLS + j * 4) / 2;
+                            v = make_uint4(static_cast<uint32_t>(acc[a0]), static_cast<uint32_t>(acc[a0] >> 32),
+                                           static_cast<uint32_t>(acc[a0 + 1]),
+                                           static_cast<uint32_t>(acc[a0 + 1] >> 32));
+                        }
+                        *reinterpret_cast<uint4*>(slotc + lane * 128 + ((j ^ (lane & 7)) << 4)) = v;
+                    }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        tma_store_2d(&tmC, smem_addr(slotc), ncol0 + bx * BOX_COLS, wrow0);
+                        bulk_commit_group();
+                    }
+                }
+            } else if (row < row_end) {
+                uint8_t* dst = static_cast<uint8_t*>(p.c) + (static_cast<int64_t>(row) * p.ldc + ncol0) * ELT;
+#pragma unroll
+                for (int j = 0; j < COLS * ELT / 16; ++j) {
+                    uint4 v;
+                    if (OUT_BF16)
+                        v = make_uint4(bf16x2(acc[4 * j]), bf16x2(acc[4 * j + 1]), bf16x2(acc[4 * j + 2]),
+                                       bf16x2(acc[4 * j + 3]));
+                    else
+                        v = make_uint4(static_cast<uint32_t>(acc[2 * j]), static_cast<uint32_t>(acc[2 * j] >> 32),
+                                       static_cast<uint32_t>(acc[2 * j + 1]),
+                                       static_cast<uint32_t>(acc[2 * j + 1] >> 32));
+                    reinterpret_cast<uint4*>(dst)[j] = v;
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_group0();
+    }
+
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after_sync();
+        tmem_dealloc(tmem_base, 512);
+    }
+}
+
+template <bool OUT_BF16, int GM>
+static int fz_launch(const void* x, int64_t ldx, int64_t x_rows, const uint8_t* bq, int64_t b_rows,
+                     const GemmParams& p, int64_t tiles_upper, cudaStream_t stream) {
+    using C = FzCfg;
+    auto kern = gemm_fused_act_kernel<OUT_BF16, GM>;
+    const int sms = sm_count_current();
+    if (sms <= 0) return FP8_ERR_CUDA;
+    static ContextCache<int> attr_cache;
+    int ok = 0;
+    const int ast = attr_cache.get(&ok, [&](int* v) {
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return static_cast<int>(FP8_ERR_CUDA);
+        if (fa.numRegs != kFzLaunchRegs) return static_cast<int>(FP8_ERR_UNSUPPORTED);
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
+            cudaSuccess)
+            return static_cast<int>(FP8_ERR_CUDA);
+        *v = 1;
+        return static_cast<int>(FP8_OK);
+    });
+    if (ast != FP8_OK) return ast;
+    CUtensorMap tx, tb, tc;
+    int st;
+    // BF16 A: boxes of 64 columns (128 bytes) x 128 rows, 128-byte swizzle
+    if ((st = make_map(&tx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, p.K, x_rows, ldx * 2, 64, BM,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != FP8_OK)
+        return st;
+    if ((st = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bq, p.K, b_rows, p.K, BK, C::BN,
+                       CU_TENSOR_MAP_SWIZZLE_128B)) != FP8_OK)
+        return st;
+    constexpr int ELT = OUT_BF16 ? 2 : 4;
+    if ((st = make_map(&tc, OUT_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                       p.c, p.N, p.M, p.ldc * ELT, 128 / ELT, 32, CU_TENSOR_MAP_SWIZZLE_128B)) != FP8_OK)
+        return st;
+    const int64_t grid = tiles_upper < sms ? tiles_upper : sms;
+    if (grid <= 0) return FP8_OK;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(kFzThreads);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tx, tb, tc, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return FP8_ERR_CUDA;
+    }
+    return launch_status();
+}
+
 }  // namespace fp8fg
 
 using namespace fp8fg;
@@ -1316,6 +1783,68 @@ extern "C" fp8_status fp8_gemm_mxfp8(const uint8_t* aq, const uint8_t* sa_e8, co
                                                   : mx_launch<256, false>(aq, bq, p, s));
     return to_status(out_type == FP8_OUT_BF16 ? mx_launch<128, true>(aq, bq, p, s)
                                               : mx_launch<128, false>(aq, bq, p, s));
+}
+
+extern "C" fp8_status fp8_gemm_blockscaled_bf16a(const void* x, int64_t ldx, const uint8_t* bq,
+                                                 const float* sb, fp8_bscale_t bmode, int64_t M,
+                                                 int64_t N, int64_t K, void* c, int64_t ldc,
+                                                 fp8_out_t out_type, void* stream) {
+    if (M < 0 || N <= 0 || N % 256 != 0 || K <= 0 || K % 128 != 0 || ldc < N || ldx < K)
+        return FP8_ERR_SHAPE;
+    if (bmode != FP8_BSCALE_BLOCK128 && bmode != FP8_BSCALE_BLOCK128_T) return FP8_ERR_UNSUPPORTED;
+    if (out_type != FP8_OUT_F32 && out_type != FP8_OUT_BF16) return FP8_ERR_UNSUPPORTED;
+    if (M == 0) return FP8_OK;
+    if (x == nullptr || bq == nullptr || sb == nullptr || c == nullptr) return FP8_ERR_NULL;
+    const int64_t elt = out_type == FP8_OUT_BF16 ? 2 : 4;
+    if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(bq, 16) || !aligned(c, 16) ||
+        !aligned(sb, 4) || (ldc * elt) % 16 != 0)
+        return FP8_ERR_ALIGN;
+    if (M > 0x7fffffffLL || N > 0x7fffffffLL || K > 0x7fffffffLL) return FP8_ERR_UNSUPPORTED;
+    GemmParams p{};
+    p.sb = sb;
+    p.bmode = bmode;
+    p.M = M;
+    p.N = N;
+    p.K = K;
+    p.c = c;
+    p.ldc = ldc;
+    const int64_t tiles = ((M + BM - 1) / BM) * (N / 256);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return to_status(out_type == FP8_OUT_BF16 ? fz_launch<true, 0>(x, ldx, M, bq, N, p, tiles, s)
+                                              : fz_launch<false, 0>(x, ldx, M, bq, N, p, tiles, s));
+}
+
+extern "C" fp8_status fp8_grouped_gemm_moe_bf16a(const void* x, int64_t ldx, const uint8_t* bq,
+                                                 const float* sb, const int32_t* offsets,
+                                                 int32_t E, int64_t T, int64_t N, int64_t K,
+                                                 void* c, fp8_out_t out_type, void* stream) {
+    if (E < 1 || E > 65536 || T < 0 || N <= 0 || N % 256 != 0 || K <= 0 || K % 128 != 0 || ldx < K)
+        return FP8_ERR_SHAPE;
+    if (out_type != FP8_OUT_F32 && out_type != FP8_OUT_BF16) return FP8_ERR_UNSUPPORTED;
+    if (T == 0) return FP8_OK;
+    if (x == nullptr || bq == nullptr || sb == nullptr || offsets == nullptr || c == nullptr)
+        return FP8_ERR_NULL;
+    if (!aligned(x, 16) || ldx % 8 != 0 || !aligned(bq, 16) || !aligned(c, 16) || !aligned(sb, 4) ||
+        !aligned(offsets, 4))
+        return FP8_ERR_ALIGN;
+    if (T > 0x7fffffffLL || static_cast<int64_t>(E) * N > 0x7fffffffLL || K > 0x7fffffffLL)
+        return FP8_ERR_UNSUPPORTED;
+    GemmParams p{};
+    p.sb = sb;
+    p.sb_expert = (N / 128) * (K / 128);
+    p.bmode = FP8_BSCALE_BLOCK128;
+    p.M = T;
+    p.N = N;
+    p.K = K;
+    p.c = c;
+    p.ldc = N;
+    p.offsets = offsets;
+    p.E = E;
+    const int64_t tiles = ((T + BM - 1) / BM + E) * (N / 256);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const int64_t b_rows = static_cast<int64_t>(E) * N;
+    return to_status(out_type == FP8_OUT_BF16 ? fz_launch<true, 1>(x, ldx, T, bq, b_rows, p, tiles, s)
+                                              : fz_launch<false, 1>(x, ldx, T, bq, b_rows, p, tiles, s));
 }
 
 extern "C" fp8_status fp8_grouped_gemm_moe(const uint8_t* aq, const float* sa, const uint8_t* bq,

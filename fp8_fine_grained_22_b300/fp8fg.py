@@ -28,6 +28,7 @@ EXPORTS = ("fp8_status_str", "fp8_device_error", "fp8_selftest_wait_timeout",
            "fp8_quant_fprop_operands", "fp8_quant_act_1x128_pow2",
            "fp8_quant_weight_128x128_pow2", "fp8_gemm_mxfp8",
            "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe", "fp8_grouped_gemm_moe_dgrad",
+           "fp8_gemm_blockscaled_bf16a", "fp8_grouped_gemm_moe_bf16a",
            "fp8_quant_act_128x1_grouped", "fp8_grouped_gemm_moe_wgrad",
            "fp8_moe_dispatch_workspace_size", "fp8_moe_dispatch_quant",
            "fp8_moe_dispatch_quant_noalloc")
@@ -67,6 +68,10 @@ def lib() -> ctypes.CDLL:
         L.fp8_quant_act_1x128_pow2.argtypes = [P, I64, I64, I64, P, I64, P, P]
         L.fp8_quant_weight_128x128_pow2.restype = I
         L.fp8_quant_weight_128x128_pow2.argtypes = [P, I64, I64, I64, P, P, P]
+        L.fp8_gemm_blockscaled_bf16a.restype = I
+        L.fp8_gemm_blockscaled_bf16a.argtypes = [P, I64, P, P, I, I64, I64, I64, P, I64, I, P]
+        L.fp8_grouped_gemm_moe_bf16a.restype = I
+        L.fp8_grouped_gemm_moe_bf16a.argtypes = [P, I64, P, P, P, I32, I64, I64, I64, P, I, P]
         L.fp8_gemm_mxfp8.restype = I
         L.fp8_gemm_mxfp8.argtypes = [P, P, P, P, I64, I64, I64, P, I64, I, P]
         L.fp8_quant_act_128x1.restype = I
@@ -246,6 +251,45 @@ def fp8_gemm_blockscaled(aq, sa, bq, sb, bmode=FP8_BSCALE_BLOCK128, out_dtype=to
     _check(lib().fp8_gemm_blockscaled(_p(aq), _p(sa), _p(bq), _p(sb), int(bmode), M, N, K, _p(c),
                                       c.stride(0), out_type, _stream(stream)),
            "fp8_gemm_blockscaled")
+    return c
+
+
+# ------------------------------------------- activation quantisation fused in --
+def fp8_gemm_blockscaled_bf16a(x, bq, sb, bmode=FP8_BSCALE_BLOCK128, out_dtype=torch.bfloat16,
+                               c=None, stream=None):
+    """C[M, N] from bf16 x [M, K] (quantised 1x128 inside the GEMM) and bq uint8 [N, K]."""
+    _cuda(x, "x", torch.bfloat16)
+    _cuda(bq, "bq", torch.uint8)
+    _cuda(sb, "sb", torch.float32)
+    assert x.dim() == 2 and x.stride(1) == 1 and bq.is_contiguous()
+    M, K = x.shape
+    N = bq.shape[0]
+    out_type = FP8_OUT_BF16 if out_dtype == torch.bfloat16 else FP8_OUT_F32
+    if c is None:
+        c = torch.empty((M, N), dtype=out_dtype, device=x.device)
+    assert c.stride(1) == 1
+    _check(lib().fp8_gemm_blockscaled_bf16a(_p(x), x.stride(0), _p(bq), _p(sb), int(bmode), M, N,
+                                            K, _p(c), c.stride(0), out_type, _stream(stream)),
+           "fp8_gemm_blockscaled_bf16a")
+    return c
+
+
+def fp8_grouped_gemm_moe_bf16a(x, bq, sb, offsets, out_dtype=torch.bfloat16, c=None,
+                               stream=None):
+    """Y[T, N] per expert from bf16 x [T, K] (quantised 1x128 inside the GEMM)."""
+    _cuda(x, "x", torch.bfloat16)
+    for t, n in ((bq, "bq"), (sb, "sb"), (offsets, "offsets")):
+        _cuda(t, n)
+    assert x.dim() == 2 and x.stride(1) == 1 and offsets.dtype == torch.int32
+    T, K = x.shape
+    E, N, _ = bq.shape
+    out_type = FP8_OUT_BF16 if out_dtype == torch.bfloat16 else FP8_OUT_F32
+    if c is None:
+        c = torch.empty((T, N), dtype=out_dtype, device=x.device)
+    assert c.is_contiguous()
+    _check(lib().fp8_grouped_gemm_moe_bf16a(_p(x), x.stride(0), _p(bq), _p(sb), _p(offsets), E, T,
+                                            N, K, _p(c), out_type, _stream(stream)),
+           "fp8_grouped_gemm_moe_bf16a")
     return c
 
 

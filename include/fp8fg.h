@@ -199,6 +199,38 @@ fp8_status fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, const uint8_
                          void* c, int64_t ldc, fp8_out_t out_type, void* stream);
 
 /*
+ * fp8_gemm_blockscaled_bf16a -- fp8_gemm_blockscaled with the activation
+ * quantisation fused into the GEMM: A is read as bfloat16 and quantised 1x128
+ * inside the kernel, on its way from the TMA copy to the tensor cores (report
+ * section 3.5.2: the fusion of FP8 format conversion with TMA access).  The
+ * codes and scales are those of fp8_quant_act_1x128, so C is bitwise the
+ * result of fp8_quant_act_1x128 followed by fp8_gemm_blockscaled.
+ *   x  : bfloat16 [M][K], row stride ldx (the activation).            (input)
+ *   bq, sb, bmode : as fp8_gemm_blockscaled (FP8_BSCALE_BLOCK128 or
+ *        FP8_BSCALE_BLOCK128_T).                                       (input)
+ *   c  : [M][N] row stride ldc, float or bfloat16 per out_type.        (output)
+ * Requires N % 256 == 0, K % 128 == 0, K > 0, ldx >= K, ldx % 8 == 0,
+ * ldc >= N, ldc*elt % 16 == 0, x/bq/c 16-byte aligned, sb 4-byte aligned.
+ */
+fp8_status fp8_gemm_blockscaled_bf16a(const void* x, int64_t ldx, const uint8_t* bq,
+                                      const float* sb, fp8_bscale_t bmode, int64_t M, int64_t N,
+                                      int64_t K, void* c, int64_t ldc, fp8_out_t out_type,
+                                      void* stream);
+
+/*
+ * fp8_grouped_gemm_moe_bf16a -- fp8_grouped_gemm_moe with the activation
+ * quantisation fused in the same way: the expert-grouped rows x [T][K] are
+ * read as bfloat16 (row stride ldx) and quantised 1x128 in the kernel; C is
+ * bitwise fp8_quant_act_1x128 followed by fp8_grouped_gemm_moe.  Other
+ * arguments, checks and the device-side offset validation as
+ * fp8_grouped_gemm_moe; requires N % 256 == 0.
+ */
+fp8_status fp8_grouped_gemm_moe_bf16a(const void* x, int64_t ldx, const uint8_t* bq,
+                                      const float* sb, const int32_t* offsets, int32_t E,
+                                      int64_t T, int64_t N, int64_t K, void* c,
+                                      fp8_out_t out_type, void* stream);
+
+/*
  * The MXFP8 variant (power-of-two scales).  The report wishes that the
  * per-group dequantisation could be completed inside the tensor cores
  * (section 3.5.2); Blackwell's block-scaled MMA does that, but only with
