@@ -185,6 +185,25 @@ __device__ __forceinline__ bool get_tile_gk(const GemmParams& p, int64_t t, Tile
     return true;
 }
 
+// Dense tiles of a cluster of CM CTAs along M: cluster tile t covers the CM
+// row blocks CM*mg .. CM*mg+CM-1 of one BN-wide column block; CTA `rank`
+// takes row block CM*mg + rank (past M when M has fewer blocks: its rows read
+// as zeros and are not stored, but it keeps the cluster's schedule).
+template <int BN, int CM>
+__device__ __forceinline__ bool get_tile_cluster(const GemmParams& p, int64_t t, uint32_t rank,
+                                                 Tile& ti) {
+    const int64_t nblk = p.N / BN;
+    const int64_t mgroups = ((p.M + BM - 1) / BM + CM - 1) / CM;
+    if (t >= mgroups * nblk) return false;
+    const int64_t mg = t / nblk, nb = t % nblk;
+    ti.row0 = (mg * CM + rank) * BM;
+    ti.row_end = p.M;
+    ti.n0 = nb * BN;
+    ti.b_row0 = ti.n0;
+    ti.expert = 0;
+    return true;
+}
+
 // GM: 0 dense, 1 grouped over rows (MoE Fprop/Dgrad), 2 grouped over K (MoE Wgrad)
 template <int BN, int GM>
 __device__ __forceinline__ bool get_tile_gm(const GemmParams& p, int64_t t, Tile& ti) {
@@ -192,6 +211,15 @@ __device__ __forceinline__ bool get_tile_gm(const GemmParams& p, int64_t t, Tile
         return get_tile_gk<BN>(p, t, ti);
     else
         return get_tile<BN, GM == 1>(p, t, ti);
+}
+
+// CM > 1: dense cluster tiles, this CTA's share by its rank in the cluster
+template <int BN, int GM, int CM>
+__device__ __forceinline__ bool get_tile_any(const GemmParams& p, int64_t t, Tile& ti) {
+    if constexpr (CM > 1)
+        return get_tile_cluster<BN, CM>(p, t, cluster_ctarank(), ti);
+    else
+        return get_tile_gm<BN, GM>(p, t, ti);
 }
 
 // Shared-memory matrix descriptor of a K-major operand tile whose rows are
@@ -231,13 +259,22 @@ __device__ __forceinline__ uint32_t bf16x2(uint64_t pair) {
     return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-template <int BN, bool OUT_BF16, bool ROWSCALE, int GM>
+template <int BN, bool OUT_BF16, bool ROWSCALE, int GM, int CM>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_blockscaled_kernel(const __grid_constant__ CUtensorMap tmA,
                             const __grid_constant__ CUtensorMap tmB,
                             const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
     constexpr bool GROUPED = GM == 1;  // tiles walk the expert row offsets
     constexpr bool GK = GM == 2;       // every expert contracts over its own K range
+    // CM > 1 (dense only): a cluster of CM CTAs along M shares each K block's
+    // B tile.  Every CTA loads its own A tile and BN/CM rows of B, multicast
+    // into the same stage of all CM CTAs, so each SM pulls A + B/CM bytes
+    // per K block from L2 instead of A + B.  A stage is refilled only after
+    // the MMAs of every CTA of the cluster have read it: each MMA commit
+    // arrives on that stage's empty barrier in all CM CTAs.
+    constexpr bool MC = CM > 1;
+    static_assert(!MC || GM == 0, "clusters serve the dense kernels");
+    static_assert(BN % (8 * CM) == 0, "B slice must be whole 8-row swizzle atoms");
     using C = Cfg<BN, ROWSCALE>;
     constexpr int S = C::STAGES;
     constexpr int NBUF = C::NBUF;
@@ -279,7 +316,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), 1);
+            mbar_init(empty_bar(s), CM);
         }
         for (int b = 0; b < NBUF; ++b) {
             mbar_init(tfull_bar(b), 1);
@@ -305,6 +342,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
+    // the other CTAs' barriers are initialised before any multicast targets them
+    if constexpr (MC) cluster_sync();
     // Nothing above reads global memory.  The operands, scales and offsets
     // may come from the kernel launched just before this one (the launch
     // allows a programmatic dependency), so wait for it here.
@@ -350,15 +389,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto role_sync = [&]() {
         if (kWarpRoles) __syncwarp();
     };
+    // Tile schedule: a cluster (or a lone CTA, CM = 1) walks the tiles
+    // blockIdx.x / CM, + gridDim.x / CM, ...; every role walks the same list.
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if ((kWarpRoles || lane == 0) && !aborted_at_start) {
             const bool leader = kWarpRoles ? elect_one() : true;
             uint32_t it = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
+            for (int64_t t = blockIdx.x / CM; ok; t += gridDim.x / CM) {
                 Tile ti;
-                if (!get_tile_gm<BN, GM>(p, t, ti)) break;
+                if (!get_tile_any<BN, GM, CM>(p, t, ti)) break;
                 const int64_t nkb = GK ? ti.kb_count : KB;
                 const int64_t kbo = GK ? ti.kb_begin : 0;
                 for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
@@ -373,9 +414,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
                         tma_load_2d(smem_addr(st), &tmA, full_bar(s),
                                     static_cast<int>((kb + kbo) * BK), static_cast<int>(ti.row0));
-                        tma_load_2d(smem_addr(st + C::A_BYTES), &tmB, full_bar(s),
-                                    static_cast<int>((kb + kbo) * BK),
-                                    static_cast<int>(ti.b_row0));
+                        if constexpr (MC) {
+                            constexpr int SLICE = BN / CM;  // B rows this CTA loads for all
+                            const uint32_t rank = cluster_ctarank();
+                            tma_load_2d_mc(smem_addr(st + C::A_BYTES + rank * SLICE * BK), &tmB,
+                                           full_bar(s), static_cast<int>((kb + kbo) * BK),
+                                           static_cast<int>(ti.b_row0 + rank * SLICE),
+                                           static_cast<uint16_t>((1u << CM) - 1u));
+                        } else {
+                            tma_load_2d(smem_addr(st + C::A_BYTES), &tmB, full_bar(s),
+                                        static_cast<int>((kb + kbo) * BK),
+                                        static_cast<int>(ti.b_row0));
+                        }
                     }
                     role_sync();
                 }
@@ -390,6 +440,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            if (MC && ok && leader) {
+                // every CTA's MMA has released the last stages: no commit of
+                // another CTA is still on its way to this CTA's barriers
+                const uint32_t n = it < static_cast<uint32_t>(S) ? it : static_cast<uint32_t>(S);
+                for (uint32_t i = it - n; i < it; ++i)
+                    if (!wait_bar(empty_bar(static_cast<int>(i % S)), (i / S) & 1u, abort_flag)) break;
+            }
             role_sync();
         }
     } else if (warp == 1) {
@@ -399,9 +456,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t idesc = idesc_e4m3_f32<BN>();
             uint32_t it = 0, kbg = 0;
             bool ok = true, issued = false;
-            for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
+            for (int64_t t = blockIdx.x / CM; ok; t += gridDim.x / CM) {
                 Tile ti;
-                if (!get_tile_gm<BN, GM>(p, t, ti)) break;
+                if (!get_tile_any<BN, GM, CM>(p, t, ti)) break;
                 const int64_t nkb = GK ? ti.kb_count : KB;
                 for (int64_t kb = 0; kb < nkb; ++kb, ++it, ++kbg) {
                     const int s = static_cast<int>(it % S);
@@ -421,7 +478,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         for (int k = 0; k < BK / 32; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
                             mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
                         mma_commit(tfull_bar(buf));
-                        mma_commit(empty_bar(s));
+                        if constexpr (MC)
+                            mma_commit_mc(empty_bar(s), static_cast<uint16_t>((1u << CM) - 1u));
+                        else
+                            mma_commit(empty_bar(s));
                     }
                     role_sync();
                     issued = true;
@@ -446,9 +506,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (kRing && (kLoaderLanes == 32 || lane == 0) && !aborted_at_start) {
             uint32_t it = 0;
             bool ok = true;
-            for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
+            for (int64_t t = blockIdx.x / CM; ok; t += gridDim.x / CM) {
                 Tile ti;
-                if (!get_tile_gm<BN, GM>(p, t, ti)) break;
+                if (!get_tile_any<BN, GM, CM>(p, t, ti)) break;
                 const int64_t nkb = GK ? ti.kb_count : KB;
                 const int64_t kbo = GK ? ti.kb_begin : 0;
                 // block modes: the tile's first 128-column block's scale at K
@@ -517,9 +577,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(sempty_bar(r));
         };
-        for (int64_t t = blockIdx.x; ok; t += gridDim.x) {
+        for (int64_t t = blockIdx.x / CM; ok; t += gridDim.x / CM) {
             Tile ti;
-            if (!get_tile_gm<BN, GM>(p, t, ti)) break;
+            if (!get_tile_any<BN, GM, CM>(p, t, ti)) break;
             const int row = static_cast<int>(ti.row0) + q * 32 + lane;
             const int row_end = static_cast<int>(ti.row_end);
             const int ncol0 = static_cast<int>(ti.n0) + cg * COLS;
@@ -744,21 +804,29 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after_sync();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
+    // no CTA leaves while another may still write to its shared memory
+    if constexpr (MC) cluster_sync();
 }
 
 // -------------------------------------------------------------------- host --
-template <int BN, bool OUT_BF16, bool ROWSCALE, int GM>
+// Launch configuration of one kernel instance, per context: the register
+// check, the shared-memory opt-in (a kernel attribute belongs to the context
+// it was set in) and, for clusters, how many can be resident at once.
+struct LaunchInfo {
+    int ok;
+    int max_clusters;  // CM > 1 only
+};
+
+template <int BN, bool OUT_BF16, bool ROWSCALE, int GM, int CM>
 static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t b_rows,
                   const GemmParams& p, int64_t tiles_upper, cudaStream_t stream) {
     using C = Cfg<BN, ROWSCALE>;
-    auto kern = gemm_blockscaled_kernel<BN, OUT_BF16, ROWSCALE, GM>;
+    auto kern = gemm_blockscaled_kernel<BN, OUT_BF16, ROWSCALE, GM, CM>;
     const int sms = sm_count_current();
     if (sms <= 0) return FP8_ERR_CUDA;
-    // Per context: the register check and the shared-memory opt-in (a kernel
-    // attribute belongs to the context it was set in).
-    static ContextCache<int> attr_cache;
-    int ok = 0;
-    const int ast = attr_cache.get(&ok, [&](int* v) {
+    static ContextCache<LaunchInfo> info_cache;
+    LaunchInfo info{};
+    const int ast = info_cache.get(&info, [&](LaunchInfo* v) {
         // the setmaxnreg split is only safe for the register count it was sized for
         cudaFuncAttributes fa;
         if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return static_cast<int>(FP8_ERR_CUDA);
@@ -766,7 +834,27 @@ static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t 
         if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) !=
             cudaSuccess)
             return static_cast<int>(FP8_ERR_CUDA);
-        *v = 1;
+        v->ok = 1;
+        v->max_clusters = 0;
+        if (CM > 1) {
+            cudaLaunchAttribute ca[1];
+            ca[0].id = cudaLaunchAttributeClusterDimension;
+            ca[0].val.clusterDim.x = CM;
+            ca[0].val.clusterDim.y = 1;
+            ca[0].val.clusterDim.z = 1;
+            cudaLaunchConfig_t qc = {};
+            qc.gridDim = dim3(static_cast<unsigned>(CM * (sms / CM)));
+            qc.blockDim = dim3(kThreads);
+            qc.dynamicSmemBytes = C::SMEM;
+            qc.attrs = ca;
+            qc.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &qc) != cudaSuccess || n <= 0) {
+                (void)cudaGetLastError();
+                return static_cast<int>(FP8_ERR_UNSUPPORTED);
+            }
+            v->max_clusters = n;
+        }
         return static_cast<int>(FP8_OK);
     });
     if (ast != FP8_OK) return ast;
@@ -775,7 +863,8 @@ static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t 
     if ((st = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, p.K, a_rows, p.K, BK, BM,
                        CU_TENSOR_MAP_SWIZZLE_128B)) != FP8_OK)
         return st;
-    if ((st = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bq, p.K, b_rows, p.K, BK, BN,
+    // with a cluster each CTA loads (and multicasts) BN / CM rows of B
+    if ((st = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bq, p.K, b_rows, p.K, BK, BN / CM,
                        CU_TENSOR_MAP_SWIZZLE_128B)) != FP8_OK)
         return st;
     constexpr int ELT = OUT_BF16 ? 2 : 4;
@@ -784,27 +873,38 @@ static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t 
                        p.c, p.N, c_rows, p.ldc * ELT, 128 / ELT, 32,
                        CU_TENSOR_MAP_SWIZZLE_128B)) != FP8_OK)
         return st;
-    const int64_t grid = tiles_upper < sms ? tiles_upper : sms;
+    // CM > 1: tiles_upper counts cluster tiles, and the grid holds whole
+    // clusters, no more than can be resident at once
+    const int64_t slots = CM > 1 ? info.max_clusters : sms;
+    const int64_t grid = CM * (tiles_upper < slots ? tiles_upper : slots);
     if (grid <= 0) return FP8_OK;
     // Programmatic stream serialisation: the CTAs may be scheduled while the
     // previous kernel on the stream finishes (once it allows it); they set
     // up barriers and tensor memory, then wait for it in griddep_wait.
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = CM;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = stream;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = CM > 1 ? 2 : 1;
     if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p) != cudaSuccess) {
         (void)cudaGetLastError();
         return FP8_ERR_CUDA;
     }
     return launch_status();
 }
+
+// CTAs per cluster along M in the dense 256-wide kernels (they share B)
+constexpr int kClusterM = 2;
+static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 template <int GM>
 static int dispatch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t b_rows,
@@ -816,39 +916,51 @@ static int dispatch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_
         (void)mblk_upper;
         if (p.N % 256 == 0) {
             const int64_t tiles = static_cast<int64_t>(p.E) * (p.M / BM) * (p.N / 256);
-            return launch<256, false, true, 2>(aq, a_rows, bq, b_rows, p, tiles, stream);
+            return launch<256, false, true, 2, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
         }
         const int64_t tiles = static_cast<int64_t>(p.E) * (p.M / BM) * (p.N / 128);
-        return launch<128, false, true, 2>(aq, a_rows, bq, b_rows, p, tiles, stream);
+        return launch<128, false, true, 2, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
     } else {
         const bool rows = p.bmode == FP8_BSCALE_ROW1x128;
         if constexpr (!GROUPED) {
             // per-column B scales (the Wgrad GEMM)
             if (rows) {
                 if (p.N % 256 == 0) {
-                    const int64_t tiles = mblk_upper * (p.N / 256);
+                    const int64_t tiles = ceil_div(mblk_upper, kClusterM) * (p.N / 256);
                     if (out_type == FP8_OUT_BF16)
-                        return launch<256, true, true, 0>(aq, a_rows, bq, b_rows, p, tiles, stream);
-                    return launch<256, false, true, 0>(aq, a_rows, bq, b_rows, p, tiles, stream);
+                        return launch<256, true, true, 0, kClusterM>(aq, a_rows, bq, b_rows, p, tiles,
+                                                                     stream);
+                    return launch<256, false, true, 0, kClusterM>(aq, a_rows, bq, b_rows, p, tiles,
+                                                                  stream);
                 }
                 const int64_t tiles = mblk_upper * (p.N / 128);
                 if (out_type == FP8_OUT_BF16)
-                    return launch<128, true, true, 0>(aq, a_rows, bq, b_rows, p, tiles, stream);
-                return launch<128, false, true, 0>(aq, a_rows, bq, b_rows, p, tiles, stream);
+                    return launch<128, true, true, 0, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
+                return launch<128, false, true, 0, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
+            }
+            // 256-wide tiles halve the shared-memory operand traffic per MMA
+            // and, with kClusterM CTAs sharing each B tile, the L2 traffic too
+            if (p.N % 256 == 0) {
+                const int64_t tiles = ceil_div(mblk_upper, kClusterM) * (p.N / 256);
+                if (out_type == FP8_OUT_BF16)
+                    return launch<256, true, false, 0, kClusterM>(aq, a_rows, bq, b_rows, p, tiles,
+                                                                  stream);
+                return launch<256, false, false, 0, kClusterM>(aq, a_rows, bq, b_rows, p, tiles,
+                                                               stream);
             }
         }
-        // 256-wide tiles halve the shared-memory operand traffic per MMA and
-        // run the tensor core at its full rate; 128-wide ones serve N % 256 != 0.
+        // grouped rows, or dense with N % 256 != 0: one CTA per tile, 256 or
+        // 128 columns wide
         if (p.N % 256 == 0) {
             const int64_t tiles = mblk_upper * (p.N / 256);
             if (out_type == FP8_OUT_BF16)
-                return launch<256, true, false, GM>(aq, a_rows, bq, b_rows, p, tiles, stream);
-            return launch<256, false, false, GM>(aq, a_rows, bq, b_rows, p, tiles, stream);
+                return launch<256, true, false, GM, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
+            return launch<256, false, false, GM, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
         }
         const int64_t tiles = mblk_upper * (p.N / 128);
         if (out_type == FP8_OUT_BF16)
-            return launch<128, true, false, GM>(aq, a_rows, bq, b_rows, p, tiles, stream);
-        return launch<128, false, false, GM>(aq, a_rows, bq, b_rows, p, tiles, stream);
+            return launch<128, true, false, GM, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
+        return launch<128, false, false, GM, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
     }
 }
 
@@ -972,6 +1084,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int64_t nblk = p.N / BN;
     const int64_t tiles = ((p.M + BM - 1) / BM) * nblk;
 
+    // Tile schedule: a cluster (or a lone CTA, CM = 1) walks the tiles
+    // blockIdx.x / CM, + gridDim.x / CM, ...; every role walks the same list.
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         const bool leader = elect_one();
@@ -1365,6 +1479,8 @@ __global__ void __launch_bounds__(kFzThreads, 1)
         if (kWarpRoles) __syncwarp();
     };
 
+    // Tile schedule: a cluster (or a lone CTA, CM = 1) walks the tiles
+    // blockIdx.x / CM, + gridDim.x / CM, ...; every role walks the same list.
     if (warp == 0) {
         // ------------------------------------------------------ TMA producer
         if ((kWarpRoles || lane == 0) && !aborted_at_start) {

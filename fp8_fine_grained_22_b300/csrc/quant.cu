@@ -295,8 +295,10 @@ __global__ void __launch_bounds__(256) quant_weight_128x128_pow2_kernel(
 
 // ------------------------------------------------------------------ 128x1 --
 // Tile: one 128-token group x 64 columns, staged in shared memory; each
-// thread then owns one column and a quarter of the 128 rows.  Tiles are
-// numbered column-block fastest.
+// thread then owns a pair of adjacent columns (one 32-bit word per row: the
+// warp reads a whole 128-byte row, no bank conflicts) and 16 of the 128
+// rows, and converts both columns with one permute per four sign bits.
+// Tiles are numbered column-block fastest.
 __device__ __forceinline__ void load_128x1(const uint16_t* __restrict__ x, int64_t ldx,
                                            int64_t KC, int64_t t, int tid, uint4 (&v)[4]) {
     const int64_t k0 = (t % KC) * 64;
@@ -314,16 +316,16 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_128x1_kernel(
     float* __restrict__ sxT, int64_t tiles) {
     griddep_launch_dependents();  // the GEMM that follows may set up meanwhile
     __shared__ __align__(16) uint16_t tile[128][64];
-    __shared__ float part[4][64];
+    __shared__ float part[8][64];
     const int t0 = threadIdx.x;
     const int64_t KC = K / 64;
+    const int cp = t0 & 31, rg = t0 >> 5;
     int64_t t = blockIdx.x;
     uint4 v[4];
     if (t < tiles) load_128x1(x, ldx, KC, t, t0, v);
     while (t < tiles) {
         const int64_t k0 = (t % KC) * 64;
         const int64_t mb = t / KC;
-        const int64_t m0 = mb * 128;
         {
             const int ch = t0 & 7;
 #pragma unroll
@@ -335,33 +337,36 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_128x1_kernel(
         const int64_t tn = t + gridDim.x;
         if (tn < tiles) load_128x1(x, ldx, KC, tn, t0, v);  // next tile's loads in flight
         __syncthreads();
-        const int c = t0 & 63;
-        const int qr = t0 >> 6;
-        float f[32];
-        float amax = 0.0f;
+        uint32_t w[16];
+        uint32_t mx = 0;
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            f[i] = __uint_as_float(static_cast<uint32_t>(tile[qr * 32 + i][c]) << 16);
-            amax = fmaxf(amax, fabsf(f[i]));
+        for (int i = 0; i < 16; ++i) {
+            w[i] = *reinterpret_cast<const uint32_t*>(&tile[rg * 16 + i][2 * cp]);
+            mx = absmax_bf16x2(mx, w[i]);  // per column: low half and high half
         }
-        part[qr][c] = amax;
+        part[rg][2 * cp] = bf16_lo(mx);
+        part[rg][2 * cp + 1] = bf16_hi(mx);
         __syncthreads();
-        amax = fmaxf(fmaxf(part[0][c], part[1][c]), fmaxf(part[2][c], part[3][c]));
-        const float s = group_scale(amax);
-        const GroupDiv dv(s);
-        if (qr == 0) sxT[mb * K + k0 + c] = s;
-        uint4 o0, o1;
-        o0.x = dv.quad(f[0], f[1], f[2], f[3]);
-        o0.y = dv.quad(f[4], f[5], f[6], f[7]);
-        o0.z = dv.quad(f[8], f[9], f[10], f[11]);
-        o0.w = dv.quad(f[12], f[13], f[14], f[15]);
-        o1.x = dv.quad(f[16], f[17], f[18], f[19]);
-        o1.y = dv.quad(f[20], f[21], f[22], f[23]);
-        o1.z = dv.quad(f[24], f[25], f[26], f[27]);
-        o1.w = dv.quad(f[28], f[29], f[30], f[31]);
-        uint8_t* dst = xqT + (k0 + c) * M + m0 + qr * 32;
-        reinterpret_cast<uint4*>(dst)[0] = o0;
-        reinterpret_cast<uint4*>(dst)[1] = o1;
+        float amax_a = part[0][2 * cp], amax_b = part[0][2 * cp + 1];
+#pragma unroll
+        for (int j = 1; j < 8; ++j) {
+            amax_a = fmaxf(amax_a, part[j][2 * cp]);
+            amax_b = fmaxf(amax_b, part[j][2 * cp + 1]);
+        }
+        const float sa = group_scale(amax_a), sb = group_scale(amax_b);
+        const GroupDiv da(sa), db(sb);
+        if (rg == 0) {
+            sxT[mb * K + k0 + 2 * cp] = sa;
+            sxT[mb * K + k0 + 2 * cp + 1] = sb;
+        }
+        uint4 oa, ob;
+        GroupDiv::halves(da, db, w[0], w[1], w[2], w[3], oa.x, ob.x);
+        GroupDiv::halves(da, db, w[4], w[5], w[6], w[7], oa.y, ob.y);
+        GroupDiv::halves(da, db, w[8], w[9], w[10], w[11], oa.z, ob.z);
+        GroupDiv::halves(da, db, w[12], w[13], w[14], w[15], oa.w, ob.w);
+        const int64_t r0 = mb * 128 + rg * 16;
+        *reinterpret_cast<uint4*>(xqT + (k0 + 2 * cp) * M + r0) = oa;
+        *reinterpret_cast<uint4*>(xqT + (k0 + 2 * cp + 1) * M + r0) = ob;
         __syncthreads();  // tile and part are rewritten by the next iteration
         t = tn;
     }

@@ -73,7 +73,11 @@ def test_small_fp32_workload():
     _compare(out, aq, sa, bq, sw, 0)
 
 
-SHAPES = [(1, 128, 128), (37, 384, 256), (130, 256, 1024), (257, 512, 384), (300, 640, 128)]
+# N % 256 == 0 runs the dense kernel with two CTAs per cluster sharing B:
+# (1, 256, 128) and (257, 512, 384) give clusters whose second CTA has no
+# valid row, (640, 768, 256) an odd number of 128-row blocks.
+SHAPES = [(1, 128, 128), (37, 384, 256), (130, 256, 1024), (257, 512, 384), (300, 640, 128),
+          (1, 256, 128), (640, 768, 256)]
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
@@ -83,6 +87,16 @@ def test_shapes(M, N, K, bmode, out_dtype):
     aq, sa, bq, sb = _operands(M, N, K, bmode, seed=M + N + K + bmode)
     out = _run(aq, sa, bq, sb, bmode, out_dtype)
     _compare(out, aq, sa, bq, sb, bmode)
+
+
+@pytest.mark.parametrize("bmode", [0, 1, 2])
+def test_clusters_walk_many_tiles(bmode):
+    """More cluster tiles than clusters fit on the GPU (each cluster walks
+    several), a ragged last row block: rows sampled from every row block."""
+    M, N, K = 4096 + 128 + 5, 1024, 256
+    aq, sa, bq, sb = _operands(M, N, K, bmode, seed=90 + bmode)
+    out = _run(aq, sa, bq, sb, bmode, torch.float32)
+    _compare(out, aq, sa, bq, sb, bmode, rows=sample_rows(M, 256, seed=bmode))
 
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
