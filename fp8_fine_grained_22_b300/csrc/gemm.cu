@@ -75,10 +75,11 @@ constexpr int kBoxBytes = 32 * 128;
 // barrier couples its warps.
 constexpr int kScaleSlots = 8;
 
-template <int BN, bool ROWSCALE>
+// BSPLIT = 2: a CTA pair shares the tile's B rows, each stage holds half
+template <int BN, bool ROWSCALE, int BSPLIT = 1>
 struct Cfg {
     static constexpr int A_BYTES = BM * BK;
-    static constexpr int B_BYTES = BN * BK;
+    static constexpr int B_BYTES = BN / BSPLIT * BK;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     static constexpr int COLS = BN / 2;           // columns per epilogue thread
     // Tensor memory holds NBUF partial buffers of the whole tile (all 512
@@ -96,7 +97,7 @@ struct Cfg {
     static constexpr int STAGES_FIT = (kSmemLimit - FIXED) / STAGE_BYTES;
     static constexpr int STAGES = STAGES_FIT > 6 ? 6 : STAGES_FIT;
     static constexpr int SMEM = FIXED + STAGES * STAGE_BYTES;
-    static constexpr int NBARS = 2 * STAGES + 2 * NBUF + 1 + 2 * kScaleSlots;
+    static constexpr int NBARS = 2 * STAGES + 2 * NBUF + 2 + 2 * kScaleSlots;
     static_assert(STAGES >= 2, "pipeline too shallow");
     static_assert(NBARS * 8 <= HEADER - 16, "header too small for barriers");
     static_assert(TMEM_COLS == 512, "TMEM allocation must be a power of 2");
@@ -188,7 +189,8 @@ __device__ __forceinline__ bool get_tile_gk(const GemmParams& p, int64_t t, Tile
 // Dense tiles of a cluster of CM CTAs along M: cluster tile t covers the CM
 // row blocks CM*mg .. CM*mg+CM-1 of one BN-wide column block; CTA `rank`
 // takes row block CM*mg + rank (past M when M has fewer blocks: its rows read
-// as zeros and are not stored, but it keeps the cluster's schedule).
+// as zeros and are not stored, but it keeps the cluster's schedule) and, in
+// a CTA pair, B rows n0 + rank*BN/2 .. + BN/2 - 1.
 template <int BN, int CM>
 __device__ __forceinline__ bool get_tile_cluster(const GemmParams& p, int64_t t, uint32_t rank,
                                                  Tile& ti) {
@@ -213,7 +215,7 @@ __device__ __forceinline__ bool get_tile_gm(const GemmParams& p, int64_t t, Tile
         return get_tile<BN, GM == 1>(p, t, ti);
 }
 
-// CM > 1: dense cluster tiles, this CTA's share by its rank in the cluster
+// CM = 2: dense tiles of a CTA pair, this CTA's share by its rank
 template <int BN, int GM, int CM>
 __device__ __forceinline__ bool get_tile_any(const GemmParams& p, int64_t t, Tile& ti) {
     if constexpr (CM > 1)
@@ -232,11 +234,12 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
            (static_cast<uint64_t>(2) << 61);
 }
 
-// Instruction descriptor: E4M3 x E4M3 -> FP32, A and B K-major, M = 128, N = BN.
-template <int BN>
+// Instruction descriptor: E4M3 x E4M3 -> FP32, A and B K-major, M x N = MM x BN
+// (MM = 256 for a CTA pair).
+template <int BN, int MM = BM>
 __device__ __forceinline__ uint32_t idesc_e4m3_f32() {
     return (1u << 4) | (static_cast<uint32_t>(BN >> 3) << 17) |
-           (static_cast<uint32_t>(BM >> 4) << 24);
+           (static_cast<uint32_t>(MM >> 4) << 24);
 }
 
 __device__ __forceinline__ void raise_error(volatile int* abort_flag, unsigned bits) {
@@ -253,6 +256,17 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ float u2f(uint32_t u) { return __uint_as_float(u); }
 __device__ __forceinline__ uint32_t f2u(float f) { return __float_as_uint(f); }
 
+// Block-mode promotion of an accumulator pair (two FP32 values in one 64-bit
+// word, low half first): acc += p * s as two scalar FFMAs.  The packed
+// fma.rn.f32x2 form measured slower in the epilogue (it keeps one FMA pipe
+// busy for twice as long); every lane is the same IEEE round-to-nearest
+// operation either way.
+__device__ __forceinline__ uint64_t fma_pair(uint32_t p0, uint32_t p1, float s, uint64_t acc) {
+    const float lo = fmaf(__uint_as_float(p0), s, __uint_as_float(static_cast<uint32_t>(acc)));
+    const float hi = fmaf(__uint_as_float(p1), s, __uint_as_float(static_cast<uint32_t>(acc >> 32)));
+    return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+
 __device__ __forceinline__ uint32_t bf16x2(uint64_t pair) {
     const __nv_bfloat162 h = __floats2bfloat162_rn(u2f(static_cast<uint32_t>(pair)),
                                                    u2f(static_cast<uint32_t>(pair >> 32)));
@@ -266,16 +280,23 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const __grid_constant__ CUtensorMap tmC, const GemmParams p) {
     constexpr bool GROUPED = GM == 1;  // tiles walk the expert row offsets
     constexpr bool GK = GM == 2;       // every expert contracts over its own K range
-    // CM > 1 (dense only): a cluster of CM CTAs along M shares each K block's
-    // B tile.  Every CTA loads its own A tile and BN/CM rows of B, multicast
-    // into the same stage of all CM CTAs, so each SM pulls A + B/CM bytes
-    // per K block from L2 instead of A + B.  A stage is refilled only after
-    // the MMAs of every CTA of the cluster have read it: each MMA commit
-    // arrives on that stage's empty barrier in all CM CTAs.
-    constexpr bool MC = CM > 1;
-    static_assert(!MC || GM == 0, "clusters serve the dense kernels");
-    static_assert(BN % (8 * CM) == 0, "B slice must be whole 8-row swizzle atoms");
-    using C = Cfg<BN, ROWSCALE>;
+    // CM = 2 (dense only): a cluster of two CTAs on neighbouring SMs whose
+    // tensor cores work as one (tcgen05 cta_group::2) on a 256 x BN tile.
+    // Each CTA loads its 128 rows of A and half of the tile's BN rows of B;
+    // the even CTA issues M = 256 MMAs that read both CTAs' shared memory
+    // and write each CTA's 128 rows of D into its own tensor memory.  Per SM
+    // and K block the shared memory then takes A + B/2 bytes from TMA and
+    // gives A + B/2 to the tensor core, instead of A + B each way.
+    //   full[s]    (even CTA) both CTAs' TMA bytes of stage s
+    //   empty[s]   (both) the pair's MMAs have read stage s: one commit,
+    //              multicast to both CTAs
+    //   tfull[b]   (both) partial buffer b written: multicast commit
+    //   tempty[b]  (even CTA) every epilogue warp of both CTAs has read b
+    // The epilogue, the scale ring and the output store are per CTA.
+    constexpr bool PAIR = CM == 2;
+    static_assert(CM == 1 || PAIR, "one CTA, or a CTA pair");
+    static_assert(!PAIR || GM == 0, "CTA pairs serve the dense kernels");
+    using C = Cfg<BN, ROWSCALE, CM>;
     constexpr int S = C::STAGES;
     constexpr int NBUF = C::NBUF;
     constexpr int SR = kScaleSlots;
@@ -301,9 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto empty_bar = [&](int s) { return bar_at(S + s); };
     auto tfull_bar = [&](int b) { return bar_at(2 * S + b); };
     auto tempty_bar = [&](int b) { return bar_at(2 * S + NBUF + b); };
-    const uint32_t drain_bar = bar_at(2 * S + 2 * NBUF);
-    auto sfull_bar = [&](int r) { return bar_at(2 * S + 2 * NBUF + 1 + r); };
-    auto sempty_bar = [&](int r) { return bar_at(2 * S + 2 * NBUF + 1 + SR + r); };
+    const uint32_t drain_bar = bar_at(2 * S + 2 * NBUF);  // and the next one: one per MMA issuer
+    auto sfull_bar = [&](int r) { return bar_at(2 * S + 2 * NBUF + 2 + r); };
+    auto sempty_bar = [&](int r) { return bar_at(2 * S + 2 * NBUF + 2 + SR + r); };
     // The scale loader runs as a whole warp in the dense and grouped-K
     // kernels and as one lane in the grouped-row kernels (whose tile walk
     // over the expert offsets is kept to single lanes).
@@ -316,15 +337,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(full_bar(s), 1);
-            mbar_init(empty_bar(s), CM);
+            mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < NBUF; ++b) {
             mbar_init(tfull_bar(b), 1);
-            mbar_init(tempty_bar(b), kEpiWarps);
+            mbar_init(tempty_bar(b), CM * kEpiWarps);
         }
         mbar_init(drain_bar, 1);
+        mbar_init(drain_bar + 8u, 1);
         for (int r = 0; r < SR; ++r) {
-            mbar_init(sfull_bar(r), kLoaderLanes);
+            mbar_init(sfull_bar(r), 1);
             mbar_init(sempty_bar(r), kEpiWarps);
         }
         *abort_flag = 0;
@@ -336,14 +358,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_prefetch_desc(&tmC);
     }
     if (warp == 1) {
-        tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(smem_addr(tmem_slot), C::TMEM_COLS);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_addr(tmem_slot), C::TMEM_COLS);
+            tmem_relinquish();
+        }
     }
     tc_fence_before_sync();
     __syncthreads();
     tc_fence_after_sync();
-    // the other CTAs' barriers are initialised before any multicast targets them
-    if constexpr (MC) cluster_sync();
+    // the peer's barriers are initialised before any arrival targets them
+    if constexpr (PAIR) cluster_sync();
     // Nothing above reads global memory.  The operands, scales and offsets
     // may come from the kernel launched just before this one (the launch
     // allows a programmatic dependency), so wait for it here.
@@ -383,6 +410,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // keep single-lane roles: their tile walk over the expert offsets does not
     // fit the control warps' registers when run warp-wide.
     constexpr bool kWarpRoles = !GROUPED;  // dense and grouped-K tiles are cheap to walk
+    constexpr bool kTwoIssuers = GM == 0;
     auto role_wait = [&](uint32_t bar, uint32_t parity) {
         return kWarpRoles ? wait_bar_warp(bar, parity, abort_flag) : wait_bar(bar, parity, abort_flag);
     };
@@ -395,7 +423,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------ TMA producer
         if ((kWarpRoles || lane == 0) && !aborted_at_start) {
             const bool leader = kWarpRoles ? elect_one() : true;
-            uint32_t it = 0;
+            uint32_t it = 0;          // K blocks issued
+            int s = 0;                // stage of K block it, and its ring pass parity
+            uint32_t ph = 0;
             bool ok = true;
             for (int64_t t = blockIdx.x / CM; ok; t += gridDim.x / CM) {
                 Tile ti;
@@ -403,34 +433,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t nkb = GK ? ti.kb_count : KB;
                 const int64_t kbo = GK ? ti.kb_begin : 0;
                 for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
-                    const int s = static_cast<int>(it % S);
-                    const uint32_t ph = (it / S) & 1u;
                     if (!role_wait(empty_bar(s), ph ^ 1u)) {
                         ok = false;
                         break;
                     }
                     if (leader) {
                         uint8_t* st = stages + s * C::STAGE_BYTES;
-                        mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
-                        tma_load_2d(smem_addr(st), &tmA, full_bar(s),
-                                    static_cast<int>((kb + kbo) * BK), static_cast<int>(ti.row0));
-                        if constexpr (MC) {
-                            constexpr int SLICE = BN / CM;  // B rows this CTA loads for all
+                        const int kx = static_cast<int>((kb + kbo) * BK);
+                        if constexpr (PAIR) {
+                            // both CTAs' bytes land on the even CTA's barrier
                             const uint32_t rank = cluster_ctarank();
-                            tma_load_2d_mc(smem_addr(st + C::A_BYTES + rank * SLICE * BK), &tmB,
-                                           full_bar(s), static_cast<int>((kb + kbo) * BK),
-                                           static_cast<int>(ti.b_row0 + rank * SLICE),
-                                           static_cast<uint16_t>((1u << CM) - 1u));
+                            if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * C::STAGE_BYTES);
+                            const uint32_t fb = mapa_shared(full_bar(s), 0);
+                            tma_load_2d_pair(smem_addr(st), &tmA, fb, kx, static_cast<int>(ti.row0));
+                            tma_load_2d_pair(smem_addr(st + C::A_BYTES), &tmB, fb, kx,
+                                             static_cast<int>(ti.b_row0 + rank * (BN / 2)));
                         } else {
-                            tma_load_2d(smem_addr(st + C::A_BYTES), &tmB, full_bar(s),
-                                        static_cast<int>((kb + kbo) * BK),
+                            mbar_arrive_expect_tx(full_bar(s), C::STAGE_BYTES);
+                            tma_load_2d(smem_addr(st), &tmA, full_bar(s), kx, static_cast<int>(ti.row0));
+                            tma_load_2d(smem_addr(st + C::A_BYTES), &tmB, full_bar(s), kx,
                                         static_cast<int>(ti.b_row0));
                         }
                     }
                     role_sync();
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
-            if (!ok && leader) {
+            if (!PAIR && !ok && leader) {
                 // let copies already issued land before the CTA can exit
                 const uint32_t n = it < static_cast<uint32_t>(S) ? it : static_cast<uint32_t>(S);
                 for (uint32_t i = it - n; i < it; ++i) {
@@ -440,30 +472,48 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
             }
-            if (MC && ok && leader) {
-                // every CTA's MMA has released the last stages: no commit of
-                // another CTA is still on its way to this CTA's barriers
+            if (PAIR && leader) {
+                // The pair's MMAs have released the last stages: every copy
+                // into this CTA has been read (so has landed) and the even
+                // CTA's last commits to this CTA's barriers have arrived.
                 const uint32_t n = it < static_cast<uint32_t>(S) ? it : static_cast<uint32_t>(S);
                 for (uint32_t i = it - n; i < it; ++i)
                     if (!wait_bar(empty_bar(static_cast<int>(i % S)), (i / S) & 1u, abort_flag)) break;
             }
             role_sync();
         }
-    } else if (warp == 1) {
-        // --------------------------------------------------------- MMA issuer
-        if ((kWarpRoles || lane == 0) && !aborted_at_start) {
+    } else if (warp == 1 || (kTwoIssuers && warp == 3)) {
+        // -------------------------------------------------------- MMA issuers
+        // Dense kernels: warp 1 issues the even K blocks (global count), warp
+        // 3 the odd ones.  Issuing tcgen05.mma holds up the tensor-memory
+        // loads of the epilogue warps on the issuing warp's SM sub-partition,
+        // so the load is split between two sub-partitions.  Every K block's
+        // MMAs and commits come from one thread, and consecutive K blocks use
+        // different TMEM buffers.  The grouped kernels issue from warp 1
+        // alone (their tile walk leaves no registers for the split).  A CTA
+        // pair: the even CTA issues for both.
+        const uint32_t mine = warp == 1 ? 0u : 1u;
+        if ((kWarpRoles || lane == 0) && !aborted_at_start && (!PAIR || cluster_ctarank() == 0)) {
             const bool leader = kWarpRoles ? elect_one() : true;
-            const uint32_t idesc = idesc_e4m3_f32<BN>();
-            uint32_t it = 0, kbg = 0;
+            const uint32_t idesc = idesc_e4m3_f32<BN, CM * BM>();
+            uint32_t kbg = 0;  // K blocks walked (both issuers walk all)
+            int s = 0;         // stage of K block kbg and its ring pass parity
+            uint32_t ph = 0;
             bool ok = true, issued = false;
             for (int64_t t = blockIdx.x / CM; ok; t += gridDim.x / CM) {
                 Tile ti;
                 if (!get_tile_any<BN, GM, CM>(p, t, ti)) break;
                 const int64_t nkb = GK ? ti.kb_count : KB;
-                for (int64_t kb = 0; kb < nkb; ++kb, ++it, ++kbg) {
-                    const int s = static_cast<int>(it % S);
-                    const uint32_t ph = (it / S) & 1u;
+                for (int64_t kb = 0; kb < nkb; ++kb, ++kbg) {
+                    if (kTwoIssuers && (kbg & 1u) != mine) {
+                        if (++s == S) {
+                            s = 0;
+                            ph ^= 1u;
+                        }
+                        continue;
+                    }
                     const uint32_t buf = kbg % NBUF, tph = (kbg / NBUF) & 1u;
+                    // tempty: in a pair the peer's epilogue warps arrive from the other CTA
                     if (!role_wait(full_bar(s), ph) || !role_wait(tempty_bar(buf), tph ^ 1u)) {
                         ok = false;
                         break;
@@ -474,35 +524,60 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint64_t bdesc = smem_desc_sw128(a_addr + C::A_BYTES);
                     const uint32_t d = tmem_base + buf * BN;
                     if (leader) {
+                        if constexpr (PAIR) {
 #pragma unroll
-                        for (int k = 0; k < BK / 32; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
-                            mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
-                        mma_commit(tfull_bar(buf));
-                        if constexpr (MC)
-                            mma_commit_mc(empty_bar(s), static_cast<uint16_t>((1u << CM) - 1u));
-                        else
+                            for (int k = 0; k < BK / 32; ++k)
+                                mma_f8f6f4_pair(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+                            mma_commit_pair_mc(tfull_bar(buf), 3);
+                            mma_commit_pair_mc(empty_bar(s), 3);
+                        } else {
+#pragma unroll
+                            for (int k = 0; k < BK / 32; ++k)  // K = 32 bytes per MMA: +2 in 16-byte units
+                                mma_f8f6f4(d, adesc + 2 * k, bdesc + 2 * k, idesc, k > 0 ? 1u : 0u);
+                            mma_commit(tfull_bar(buf));
                             mma_commit(empty_bar(s));
+                        }
                     }
                     role_sync();
                     issued = true;
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
             }
             if (!ok && issued && leader) {
-                // wait (bounded) for every MMA already issued before TMEM is freed
-                mma_commit(drain_bar);
+                // wait (bounded) for every MMA this thread issued before TMEM is freed
+                const uint32_t db = drain_bar + 8u * mine;
+                if constexpr (PAIR)
+                    mma_commit_pair(db);
+                else
+                    mma_commit(db);
                 const long long t0 = clock64();
-                while (!mbar_try_wait(drain_bar, 0) && clock64() - t0 < (1LL << 24)) {
+                while (!mbar_try_wait(db, 0) && clock64() - t0 < (1LL << 24)) {
                 }
+            }
+            if (PAIR && ok && leader) {
+                // every epilogue warp of both CTAs has read this issuer's last
+                // partials: no arrival from the peer is still on its way here
+                const uint32_t nb = kbg < static_cast<uint32_t>(NBUF) ? kbg : static_cast<uint32_t>(NBUF);
+                for (uint32_t j = kbg - nb; j < kbg; ++j)
+                    if ((!kTwoIssuers || (j & 1u) == mine) &&
+                        !wait_bar(tempty_bar(static_cast<int>(j % NBUF)), (j / NBUF) & 1u, abort_flag))
+                        break;
             }
             role_sync();
         }
     } else if (warp == 2) {
         // ------------------------------------------------------ scale loader
-        // Per K block, slot it % SR: the A scales of the tile's 128 rows
-        // (rows past the operand read row M-1: never stored), then the B
-        // scales (per-row mode: the tile's BN columns; block modes: the one
-        // or two 128-column blocks).  Issued as 4-byte cp.async copies whose
-        // landing arrives on the slot's full barrier.
+        // (per-column B scales only) Per K block, slot it % SR receives the
+        // A scales of the tile's 128 rows, then the B scales of its BN
+        // columns.  Where both runs are 16-byte aligned and all the tile's
+        // rows are inside the operand, one lane copies each run with one
+        // bulk copy counted on the slot's full barrier.  Otherwise (a ragged
+        // last row block, unaligned scale arrays) the lanes copy 4-byte
+        // elements (rows past the operand read row M-1: never stored), wait
+        // for them, and one lane arrives.
         if (kRing && (kLoaderLanes == 32 || lane == 0) && !aborted_at_start) {
             uint32_t it = 0;
             bool ok = true;
@@ -511,14 +586,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!get_tile_any<BN, GM, CM>(p, t, ti)) break;
                 const int64_t nkb = GK ? ti.kb_count : KB;
                 const int64_t kbo = GK ? ti.kb_begin : 0;
-                // block modes: the tile's first 128-column block's scale at K
-                // block 0, and the steps to the next K block / column block
-                const bool blk = p.bmode == FP8_BSCALE_BLOCK128;
-                const int64_t nb0 = ti.n0 / 128;
-                const float* sb_t = p.sb + (GROUPED ? ti.expert * p.sb_expert : 0) +
-                                    (blk ? nb0 * KB : nb0);
-                const int64_t sb_kstep = blk ? 1 : p.N / 128;
-                const int64_t sb_istep = blk ? KB : 1;
                 for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
                     const int r = static_cast<int>(it % SR);
                     const uint32_t ph = (it / SR) & 1u;
@@ -530,24 +597,30 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     const uint32_t slot = smem_addr(ring + r * C::SLOT_FLOATS);
                     const int64_t kg = kb + kbo;
-                    const float* sa_k = p.sa + kg * p.lds_a;
-                    for (int i = lane; i < BM; i += kLoaderLanes) {
-                        const int64_t row = ti.row0 + i < p.M ? ti.row0 + i : p.M - 1;
-                        cp_async4(slot + 4 * i, sa_k + row);
-                    }
-                    if (ROWSCALE) {
-                        const float* sb_k = p.sb + kg * p.ld_sb + ti.n0;
+                    const float* sa_k = p.sa + kg * p.lds_a + ti.row0;
+                    const float* sb_k = p.sb + kg * p.ld_sb + ti.n0;
+                    const bool bulk = ti.row0 + BM <= p.M &&
+                                      ((reinterpret_cast<uintptr_t>(sa_k) |
+                                        reinterpret_cast<uintptr_t>(sb_k)) & 15u) == 0;
+                    if (bulk) {
+                        if (lane == 0) {
+                            mbar_arrive_expect_tx(sfull_bar(r), 4 * (BM + BN));
+                            bulk_load(slot, sa_k, 4 * BM, sfull_bar(r));
+                            bulk_load(slot + 4 * BM, sb_k, 4 * BN, sfull_bar(r));
+                        }
+                    } else {
+                        const int64_t last = p.M - 1 - ti.row0;  // offset of row M-1
+                        for (int i = lane; i < BM; i += kLoaderLanes)
+                            cp_async4(slot + 4 * i, sa_k + (i <= last ? i : last));
                         for (int i = lane; i < BN; i += kLoaderLanes)
                             cp_async4(slot + 4 * (BM + i), sb_k + i);
-                    } else {
-                        for (int i = lane; i < BN / 128; i += kLoaderLanes)
-                            cp_async4(slot + 4 * (BM + i), sb_t + kg * sb_kstep + i * sb_istep);
+                        cp_async_wait_all();
+                        if (kLoaderLanes == 32) __syncwarp();
+                        if (lane == 0) mbar_arrive(sfull_bar(r));
                     }
-                    cp_async_mbar_arrive_noinc(sfull_bar(r));
+                    if (kLoaderLanes == 32) __syncwarp();
                 }
             }
-            cp_async_wait_all();  // nothing in flight when the CTA exits
-            if (kLoaderLanes == 32) __syncwarp();
         }
     } else if (warp >= kEpiWarp0) {
         // ------------------------------------------------- promotion epilogue
@@ -568,10 +641,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t sa_addr0 = smem_addr(ring) + 4u * (q * 32 + lane);
         const uint32_t sb_addr0 =
             smem_addr(ring) + 4u * (BM + (ROWSCALE ? cg * COLS : (cg * COLS) / 128));
+        // a pair's tempty barriers are the even CTA's (8 bytes apart there too)
+        const uint32_t tempty0 = PAIR ? mapa_shared(tempty_bar(0), 0) : tempty_bar(0);
         auto release_tmem = [&](uint32_t buf) {
             tc_fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(tempty_bar(buf));
+            if (lane == 0) {
+                if constexpr (PAIR)
+                    mbar_arrive_remote(tempty0 + 8u * buf);
+                else
+                    mbar_arrive(tempty_bar(buf));
+            }
         };
         auto release_slot = [&](int r) {
             __syncwarp();
@@ -638,14 +718,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     release_tmem(buf);
                     if constexpr (!ROWSCALE) {
                         const float sc = sa_cur * sb_cur;
-                        const uint64_t sc2 = pack2(f2u(sc), f2u(sc));
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
-                            acc[i] = ffma2(pack2(ra[2 * i], ra[2 * i + 1]), sc2, acc[i]);
-                            acc[16 + i] = ffma2(pack2(rb[2 * i], rb[2 * i + 1]), sc2, acc[16 + i]);
+                            acc[i] = fma_pair(ra[2 * i], ra[2 * i + 1], sc, acc[i]);
+                            acc[16 + i] = fma_pair(rb[2 * i], rb[2 * i + 1], sc, acc[16 + i]);
                         }
                     } else {
-                        // per column: (P * sb[col]) * sa + acc
+                        // per column: (P * sb[col]) * sa + acc, packed FP32 pairs
                         const uint64_t sa2 = pack2(f2u(sa_cur), f2u(sa_cur));
                         const uint32_t sbp = sb_addr0 + slot_off;
 #pragma unroll
@@ -675,6 +754,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // 16-column TMEM loads, two in flight; the TMEM buffer goes
                     // back once the last pair has landed, the scale slot after
                     // the last column's arithmetic.
+                    // (packed FP32 pairs here: the scalar form needs more registers)
                     const uint64_t sa2 = pack2(f2u(sa_cur), f2u(sa_cur));
                     const uint32_t sbp = sb_addr0 + slot_off;
                     auto fma16 = [&](uint32_t (&rr)[16], int ch) {
@@ -710,7 +790,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     release_slot(r);
                 } else {
                     const float sc = sa_cur * sb_cur;
-                    const uint64_t sc2 = pack2(f2u(sc), f2u(sc));
                     // 128 columns in 32-column TMEM loads: two in flight from
                     // the start, and each freed register chunk is refilled at
                     // once, so the whole partial has landed after two load
@@ -724,7 +803,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     auto fma_chunk = [&](uint32_t (&rr)[32], int ch) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
-                            acc[ch * 16 + i] = ffma2(pack2(rr[2 * i], rr[2 * i + 1]), sc2, acc[ch * 16 + i]);
+                            acc[ch * 16 + i] = fma_pair(rr[2 * i], rr[2 * i + 1], sc, acc[ch * 16 + i]);
                     };
                     fma_chunk(ra, 0);
                     tmem_ld32(taddr + 64, ra);
@@ -800,12 +879,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     tc_fence_before_sync();
     __syncthreads();
+    // a pair frees its tensor memory together, once both CTAs are done with
+    // it; neither leaves while the other may still write to its barriers
+    if constexpr (PAIR) cluster_sync();
     if (warp == 1) {
         tc_fence_after_sync();
-        tmem_dealloc(tmem_base, C::TMEM_COLS);
+        if constexpr (PAIR)
+            tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
+        else
+            tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
-    // no CTA leaves while another may still write to its shared memory
-    if constexpr (MC) cluster_sync();
 }
 
 // -------------------------------------------------------------------- host --
@@ -820,7 +903,7 @@ struct LaunchInfo {
 template <int BN, bool OUT_BF16, bool ROWSCALE, int GM, int CM>
 static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t b_rows,
                   const GemmParams& p, int64_t tiles_upper, cudaStream_t stream) {
-    using C = Cfg<BN, ROWSCALE>;
+    using C = Cfg<BN, ROWSCALE, CM>;
     auto kern = gemm_blockscaled_kernel<BN, OUT_BF16, ROWSCALE, GM, CM>;
     const int sms = sm_count_current();
     if (sms <= 0) return FP8_ERR_CUDA;
@@ -863,7 +946,7 @@ static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t 
     if ((st = make_map(&ta, CU_TENSOR_MAP_DATA_TYPE_UINT8, aq, p.K, a_rows, p.K, BK, BM,
                        CU_TENSOR_MAP_SWIZZLE_128B)) != FP8_OK)
         return st;
-    // with a cluster each CTA loads (and multicasts) BN / CM rows of B
+    // in a CTA pair each CTA loads BN / 2 rows of B
     if ((st = make_map(&tb, CU_TENSOR_MAP_DATA_TYPE_UINT8, bq, p.K, b_rows, p.K, BK, BN / CM,
                        CU_TENSOR_MAP_SWIZZLE_128B)) != FP8_OK)
         return st;
@@ -902,7 +985,7 @@ static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t 
     return launch_status();
 }
 
-// CTAs per cluster along M in the dense 256-wide kernels (they share B)
+// The dense 256-wide kernels run as CTA pairs (cta_group::2)
 constexpr int kClusterM = 2;
 static int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -938,8 +1021,8 @@ static int dispatch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_
                     return launch<128, true, true, 0, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
                 return launch<128, false, true, 0, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
             }
-            // 256-wide tiles halve the shared-memory operand traffic per MMA
-            // and, with kClusterM CTAs sharing each B tile, the L2 traffic too
+            // 256-wide tiles on CTA pairs: per SM and K block, shared memory
+            // moves A + B/2 each way instead of A + B
             if (p.N % 256 == 0) {
                 const int64_t tiles = ceil_div(mblk_upper, kClusterM) * (p.N / 256);
                 if (out_type == FP8_OUT_BF16)
@@ -949,13 +1032,15 @@ static int dispatch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_
                                                                stream);
             }
         }
-        // grouped rows, or dense with N % 256 != 0: one CTA per tile, 256 or
-        // 128 columns wide
-        if (p.N % 256 == 0) {
-            const int64_t tiles = mblk_upper * (p.N / 256);
-            if (out_type == FP8_OUT_BF16)
-                return launch<256, true, false, GM, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
-            return launch<256, false, false, GM, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
+        // grouped rows (256 or 128 columns wide), or dense with N % 256 != 0
+        // (128 wide): one CTA per tile
+        if constexpr (GROUPED) {
+            if (p.N % 256 == 0) {
+                const int64_t tiles = mblk_upper * (p.N / 256);
+                if (out_type == FP8_OUT_BF16)
+                    return launch<256, true, false, GM, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
+                return launch<256, false, false, GM, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
+            }
         }
         const int64_t tiles = mblk_upper * (p.N / 128);
         if (out_type == FP8_OUT_BF16)
