@@ -11,23 +11,31 @@
 // threads in three warpgroups:
 //   warp 0      TMA producer: A tile 128x128 and B tile BNx128 (E4M3, 128-byte
 //               swizzle) per K block into a STAGES-deep shared-memory ring.
-//   warp 1      TMEM allocator and MMA issuer: four tcgen05.mma kind::f8f6f4
-//               (K = 32 each) per K block into one of the TMEM partial buffers
-//               (two of 256 FP32 columns, or four of 128), then tcgen05.commit
-//               to release the smem stage and to signal the epilogue.  In the
-//               dense kernels both roles run as whole warps with one elected
-//               lane issuing; the grouped-row kernels use one lane.
-//   warps 2, 3  idle (they complete the control warpgroup for setmaxnreg).
+//   warps 1, 3  MMA issuers (warp 1 also allocates TMEM): four tcgen05.mma
+//               kind::f8f6f4 (K = 32 each) per K block into one of the TMEM
+//               partial buffers (two of 256 FP32 columns, or four of 128),
+//               then tcgen05.commit to release the smem stage and to signal
+//               the epilogue.  Dense kernels alternate K blocks between warps
+//               1 and 3; the grouped kernels issue from warp 1.  Dense and
+//               grouped-K roles run as whole warps with one elected lane
+//               issuing; the grouped-row kernels use one lane.
+//   warp 2      scale loader of the per-column (Wgrad) mode: each K block's
+//               A and B scales into a shared-memory ring by bulk copies.
 //   warps 4..11 promotion epilogue, two per TMEM lane quadrant: tcgen05.ld the
 //               partial of K block kb, acc += partial * (sa[m,kb] * sb[kb])
-//               (or * sb[n,kb] per column in the Wgrad mode) with packed FP32
-//               FMAs in registers, release the TMEM buffer; after the last K
+//               (or * sb[n,kb] per column in the Wgrad mode) with FP32 FMAs
+//               in registers, release the TMEM buffer; after the last K
 //               block, convert and store the tile through a swizzled
 //               shared-memory staging buffer and TMA bulk stores.
+// The dense 256-wide kernels run on CTA pairs (clusters of two) whose tensor
+// cores act as one on a 256 x 256 tile (tcgen05 cta_group::2): each CTA
+// loads its 128 rows of A and half of B, so shared memory moves A + B/2 per
+// K block in each direction instead of A + B.
 // Group modes: dense; grouped over rows (MoE Fprop and Dgrad: tiles walk the
 // expert row offsets); grouped over K (MoE Wgrad: every expert has the same
 // output tiles and contracts over its own padded token range).
-// The kernel is persistent: one CTA per SM walks a static tile schedule.
+// The kernel is persistent: one CTA (or CTA pair) per SM (pair of SMs) walks
+// a static tile schedule.
 // Every barrier wait is bounded; on expiry the kernel records
 // FP8_ERR_TIMEOUT in a device error word, unwinds and frees its TMEM.
 #include <cuda.h>
