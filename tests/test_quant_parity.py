@@ -96,6 +96,18 @@ def test_128x1_full_size(which):
     _assert_128x1(x)
 
 
+def test_128x1_strided_input():
+    """A column window of a wider matrix (row stride 512 elements), with a
+    64-column last tile: the loader's row stride and its zero-filled tail."""
+    big = _act(256, 512, 17)
+    x = big[:, 64:64 + 192]
+    xqT, sxT = fp8fg.fp8_quant_act_128x1(big.to(DEV)[:, 64:64 + 192])
+    torch.cuda.synchronize()
+    oq, os_ = oracle.quant_act_128x1(bits(x.contiguous()))
+    np.testing.assert_array_equal(xqT.cpu().numpy(), oq)
+    np.testing.assert_array_equal(sxT.cpu().numpy().view(np.uint32), os_.view(np.uint32))
+
+
 def test_128x1_edge_groups():
     x = _edge_matrix().T.contiguous()  # [256, 8]: pad to 64 columns
     xp = torch.zeros(256, 64, dtype=torch.bfloat16)
