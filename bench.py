@@ -10,6 +10,8 @@ One step = one pass of the path over the training trio of an expert MLP
   5. Fprop  Y  = X . W          -> BF16 [8192, 4096]   (fp8_gemm_blockscaled)
   6. Dgrad  dX = dY . W^T       -> BF16 [8192, 7168]   (transposed block scales)
   7. Wgrad  dW = X^T . dY       -> FP32 [7168, 4096]   (per-row B scales)
+(the GEMMs get the split-K workspace; of the three only the Wgrad's short last
+wave is split)
 (The one-launch form of steps 1-2, fp8_quant_fprop_operands, is timed among
 the quantisers in `configs`; as two launches they measured faster.)
 The metric is the step's FP8 GEMM throughput: 3 * 2 * 8192 * 7168 * 4096
@@ -421,6 +423,9 @@ class Trio:
         self.dx = e((M, K), torch.bfloat16)
         self.dw = e((K, N), f32)
         self.gemm_flops = 2.0 * M * N * K
+        # split-K workspace of the GEMMs (zero-filled once; each call leaves it so)
+        self.ws = torch.zeros(fp8fg.fp8_gemm_blockscaled_workspace_size(), dtype=torch.uint8,
+                              device=dev)
 
     NAMES = ("fp8_quant_act_1x128 (X)", "fp8_quant_weight_128x128 (W, wq and wqT)",
              "fp8_quant_act_1x128 (dY)", "fp8_quant_act_128x1 (X)", "fp8_quant_act_128x1 (dY)",
@@ -444,13 +449,16 @@ class Trio:
             lambda: f.fp8_quant_act_128x1(dy, self.dyqT, self.sdyT, stream=s),
             lambda: f.fp8_gemm_blockscaled(self.xq, self.sx, self.wq, self.sw,
                                            bmode=f.FP8_BSCALE_BLOCK128,
-                                           out_dtype=torch.bfloat16, c=y, stream=s),
+                                           out_dtype=torch.bfloat16, c=y, stream=s,
+                                           workspace=self.ws),
             lambda: f.fp8_gemm_blockscaled(self.dyq, self.sdy, self.wqT, self.sw,
                                            bmode=f.FP8_BSCALE_BLOCK128_T,
-                                           out_dtype=torch.bfloat16, c=dx, stream=s),
+                                           out_dtype=torch.bfloat16, c=dx, stream=s,
+                                           workspace=self.ws),
             lambda: f.fp8_gemm_blockscaled(self.xqT, self.sxT, self.dyqT, self.sdyT,
                                            bmode=f.FP8_BSCALE_ROW1x128,
-                                           out_dtype=torch.float32, c=dw, stream=s),
+                                           out_dtype=torch.float32, c=dw, stream=s,
+                                           workspace=self.ws),
         ]
 
     def step(self, ev=None, **bufs):

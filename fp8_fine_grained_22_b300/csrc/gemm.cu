@@ -124,6 +124,13 @@ struct GemmParams {
     int64_t ldc;          // elements
     const int32_t* offsets;  // grouped only
     int E;
+    // Split-K tail of the dense CTA-pair kernels: tiles >= full_tiles (the
+    // last, partial wave) are split along K into sk chunks; each chunk's FP32
+    // partial goes to ws, and the last chunk of a tile to finish sums them.
+    int64_t full_tiles;   // tiles computed whole (all of them when sk == 1)
+    int sk;               // K chunks per tail tile (1: no split)
+    float* ws;            // [tail unit][CTA rank][BM][BN] FP32 partials
+    int* ws_cnt;          // [tail tile][CTA rank] arrivals; zero between launches
 };
 
 struct Tile {
@@ -132,10 +139,11 @@ struct Tile {
     int64_t b_row0;   // first row of B (expert-major for grouped)
     int64_t n0;       // first output column
     int expert;
-    // grouped-K (per-expert contraction) tiles only:
-    int64_t c_row0;   // first row of C (expert-major)
-    int kb_begin;     // first K block of the expert
-    int kb_count;     // K blocks of the expert (0: the tile is written as zeros)
+    // grouped-K (per-expert contraction) and split-K tail tiles:
+    int64_t c_row0;   // first row of C (expert-major; grouped-K only)
+    int kb_begin;     // first K block of the range
+    int kb_count;     // K blocks of the range (grouped-K: 0 writes the tile as zeros)
+    int64_t split;    // split-K tail unit index, or -1
 };
 
 template <int BN, bool GROUPED>
@@ -200,15 +208,32 @@ __device__ __forceinline__ bool get_tile_gk(const GemmParams& p, int64_t t, Tile
 // as zeros and are not stored, but it keeps the cluster's schedule) and, in
 // a CTA pair, B rows n0 + rank*BN/2 .. + BN/2 - 1.
 template <int BN, int CM>
-__device__ __forceinline__ bool get_tile_cluster(const GemmParams& p, int64_t t, uint32_t rank,
+__device__ __forceinline__ bool get_tile_cluster(const GemmParams& p, int64_t t64, uint32_t rank,
                                                  Tile& ti) {
-    const int64_t nblk = p.N / BN;
-    const int64_t mgroups = ((p.M + BM - 1) / BM + CM - 1) / CM;
-    if (t >= mgroups * nblk) return false;
-    const int64_t mg = t / nblk, nb = t % nblk;
-    ti.row0 = (mg * CM + rank) * BM;
+    // 32-bit arithmetic throughout (the host keeps every count below 2^31):
+    // the control warps walk this at 40 registers.
+    const int t = static_cast<int>(t64);
+    const int nblk = static_cast<int>(p.N / BN);
+    const int mgroups = static_cast<int>(((p.M + BM - 1) / BM + CM - 1) / CM);
+    const int KBt = static_cast<int>(p.K / BK);
+    const int full = static_cast<int>(p.full_tiles);
+    int tile = t;
+    ti.split = -1;
+    ti.kb_begin = 0;
+    ti.kb_count = KBt;
+    if (t >= full) {  // a K chunk of a tail tile
+        const int u = t - full;
+        const int c = u % p.sk;
+        tile = full + u / p.sk;
+        ti.kb_begin = (c * KBt) / p.sk;
+        ti.kb_count = ((c + 1) * KBt) / p.sk - ti.kb_begin;
+        ti.split = u;
+    }
+    if (tile >= mgroups * nblk) return false;
+    const int mg = tile / nblk, nb = tile % nblk;
+    ti.row0 = static_cast<int64_t>(mg * CM + static_cast<int>(rank)) * BM;
     ti.row_end = p.M;
-    ti.n0 = nb * BN;
+    ti.n0 = static_cast<int64_t>(nb) * BN;
     ti.b_row0 = ti.n0;
     ti.expert = 0;
     return true;
@@ -253,6 +278,11 @@ __device__ __forceinline__ uint32_t idesc_e4m3_f32() {
 __device__ __forceinline__ void raise_error(volatile int* abort_flag, unsigned bits) {
     raise_device_error(abort_flag, &g_dev_error, bits);
 }
+// Barrier over the eight epilogue warps (named barrier 1, 256 threads).
+__device__ __forceinline__ void epilogue_sync() {
+    asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag) {
     return wait_bounded(bar, parity, abort_flag, &g_dev_error);
 }
@@ -312,6 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem_raw);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem_raw + C::HEADER - 16);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem_raw + C::HEADER - 12);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(smem_raw + C::HEADER - 8);
     uint8_t* base = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + C::HEADER + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t* stages = base;
@@ -419,6 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // fit the control warps' registers when run warp-wide.
     constexpr bool kWarpRoles = !GROUPED;  // dense and grouped-K tiles are cheap to walk
     constexpr bool kTwoIssuers = GM == 0;
+    constexpr bool kKRange = GK || PAIR;  // tiles carry their own K range
     auto role_wait = [&](uint32_t bar, uint32_t parity) {
         return kWarpRoles ? wait_bar_warp(bar, parity, abort_flag) : wait_bar(bar, parity, abort_flag);
     };
@@ -438,8 +470,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int64_t t = blockIdx.x / CM; ok; t += gridDim.x / CM) {
                 Tile ti;
                 if (!get_tile_any<BN, GM, CM>(p, t, ti)) break;
-                const int64_t nkb = GK ? ti.kb_count : KB;
-                const int64_t kbo = GK ? ti.kb_begin : 0;
+                const int64_t nkb = kKRange ? ti.kb_count : KB;
+                const int64_t kbo = kKRange ? ti.kb_begin : 0;
                 for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
                     if (!role_wait(empty_bar(s), ph ^ 1u)) {
                         ok = false;
@@ -511,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int64_t t = blockIdx.x / CM; ok; t += gridDim.x / CM) {
                 Tile ti;
                 if (!get_tile_any<BN, GM, CM>(p, t, ti)) break;
-                const int64_t nkb = GK ? ti.kb_count : KB;
+                const int64_t nkb = kKRange ? ti.kb_count : KB;
                 for (int64_t kb = 0; kb < nkb; ++kb, ++kbg) {
                     if (kTwoIssuers && (kbg & 1u) != mine) {
                         if (++s == S) {
@@ -592,8 +624,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int64_t t = blockIdx.x / CM; ok; t += gridDim.x / CM) {
                 Tile ti;
                 if (!get_tile_any<BN, GM, CM>(p, t, ti)) break;
-                const int64_t nkb = GK ? ti.kb_count : KB;
-                const int64_t kbo = GK ? ti.kb_begin : 0;
+                const int64_t nkb = kKRange ? ti.kb_count : KB;
+                const int64_t kbo = kKRange ? ti.kb_begin : 0;
                 for (int64_t kb = 0; kb < nkb; ++kb, ++it) {
                     const int r = static_cast<int>(it % SR);
                     const uint32_t ph = (it / SR) & 1u;
@@ -671,12 +703,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int row = static_cast<int>(ti.row0) + q * 32 + lane;
             const int row_end = static_cast<int>(ti.row_end);
             const int ncol0 = static_cast<int>(ti.n0) + cg * COLS;
-            const int nkb = GK ? ti.kb_count : static_cast<int>(KB);
+            const int nkb = kKRange ? ti.kb_count : static_cast<int>(KB);
+            const int kbo = kKRange ? ti.kb_begin : 0;
             // block modes: this row's A scales sa[kb * lds_a + row] and the
             // B scale of this thread's 128-column block, one K block ahead
             const bool row_in_alloc = row < p.M;
-            const float* sa_g = p.sa + (row_in_alloc ? row : 0);
             const int lds_a = static_cast<int>(p.lds_a);
+            const float* sa_g = p.sa + static_cast<int64_t>(kbo) * lds_a + (row_in_alloc ? row : 0);
             const float* sb_g = nullptr;
             int sb_gstep = 0;
             float sa_next = 0.0f, sb_next = 0.0f;
@@ -684,8 +717,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int nb = ncol0 / 128;
                 const bool blk = p.bmode == FP8_BSCALE_BLOCK128;
                 const int KBi = static_cast<int>(KB);
-                sb_g = p.sb + (GROUPED ? ti.expert * p.sb_expert : 0) + (blk ? nb * KBi : nb);
                 sb_gstep = blk ? 1 : static_cast<int>(p.N / 128);
+                sb_g = p.sb + (GROUPED ? ti.expert * p.sb_expert : 0) + (blk ? nb * KBi : nb) +
+                       static_cast<int64_t>(kbo) * sb_gstep;
                 if (nkb > 0) {
                     sa_next = row_in_alloc ? __ldg(sa_g) : 0.0f;
                     sb_next = __ldg(sb_g);
@@ -826,6 +860,55 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!ok) break;
 
+            if constexpr (PAIR) {
+                if (ti.split >= 0) {
+                    // Split-K tail: park this K chunk's partial; the last chunk
+                    // of the tile to arrive (per CTA half) sums all of them in
+                    // chunk order and stores the tile.  Nothing waits.
+                    const uint32_t rank = cluster_ctarank();
+                    const int64_t tail = ti.split / p.sk;
+                    // A CTA's partial is [warp][16-byte chunk][lane]: a warp's
+                    // store or load of one chunk index covers 512 contiguous bytes.
+                    constexpr int kChunks = COLS / 4;
+                    auto part_at = [&](int64_t unit) {
+                        return reinterpret_cast<float4*>(p.ws) +
+                               ((unit * CM + rank) * kEpiWarps + ew) * (kChunks * 32) + lane;
+                    };
+                    float4* mine_p = part_at(ti.split);
+#pragma unroll
+                    for (int i = 0; i < kChunks; ++i)
+                        mine_p[i * 32] = make_float4(u2f(static_cast<uint32_t>(acc[2 * i])),
+                                                     u2f(static_cast<uint32_t>(acc[2 * i] >> 32)),
+                                                     u2f(static_cast<uint32_t>(acc[2 * i + 1])),
+                                                     u2f(static_cast<uint32_t>(acc[2 * i + 1] >> 32)));
+                    epilogue_sync();
+                    if (ew == 0 && lane == 0) {
+                        __threadfence();
+                        const int old = atomicAdd(p.ws_cnt + tail * CM + rank, 1);
+                        *last_flag = old == p.sk - 1;
+                    }
+                    epilogue_sync();
+                    if (!*last_flag) continue;  // another chunk completes the tile
+                    __threadfence();
+#pragma unroll
+                    for (int i = 0; i < COLS / 2; ++i) acc[i] = 0;
+                    for (int c = 0; c < p.sk; ++c) {
+                        const float4* src = part_at(tail * p.sk + c);
+#pragma unroll
+                        for (int i = 0; i < kChunks; ++i) {
+                            const float4 v = __ldcg(src + i * 32);
+                            acc[2 * i] = pack2(f2u(u2f(static_cast<uint32_t>(acc[2 * i])) + v.x),
+                                               f2u(u2f(static_cast<uint32_t>(acc[2 * i] >> 32)) + v.y));
+                            acc[2 * i + 1] =
+                                pack2(f2u(u2f(static_cast<uint32_t>(acc[2 * i + 1])) + v.z),
+                                      f2u(u2f(static_cast<uint32_t>(acc[2 * i + 1] >> 32)) + v.w));
+                        }
+                    }
+                    epilogue_sync();  // every thread has read the counter's flag
+                    if (ew == 0 && lane == 0) p.ws_cnt[tail * CM + rank] = 0;  // for the next launch
+                }
+            }
+
             // ---------------------------------------------------- tile store
             // grouped-K: C is [E][M][N], the tile's rows start at c_row0 and are all valid
             const int wrow0 = static_cast<int>(GK ? ti.c_row0 : ti.row0) + q * 32;
@@ -900,6 +983,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // -------------------------------------------------------------------- host --
+// Split-K workspace of the dense CTA-pair kernels: 4 KB of arrival counters
+// (two per tail tile, zero between launches), then one 128 x 256 FP32
+// partial per CTA of each tail unit.  A tail has at most one unit per pair.
+constexpr int64_t kSplitCounterBytes = 4096;
+constexpr int64_t kSplitPartialBytes = 128 * 256 * 4;
+static int64_t kSplitUnitsMax(int sms) { return sms / 2; }
+static int64_t split_workspace_bytes(int sms) {
+    return kSplitCounterBytes + kSplitUnitsMax(sms) * 2 * kSplitPartialBytes;
+}
+
 // Launch configuration of one kernel instance, per context: the register
 // check, the shared-memory opt-in (a kernel attribute belongs to the context
 // it was set in) and, for clusters, how many can be resident at once.
@@ -969,6 +1062,29 @@ static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t 
     const int64_t slots = CM > 1 ? info.max_clusters : sms;
     const int64_t grid = CM * (tiles_upper < slots ? tiles_upper : slots);
     if (grid <= 0) return FP8_OK;
+    GemmParams q = p;
+    q.full_tiles = tiles_upper;
+    q.sk = 1;
+    if (CM > 1 && p.ws != nullptr) {
+        // Split-K tail: when the last wave of whole tiles would leave at least
+        // half the pairs idle, its tiles are cut along K into sk chunks and
+        // reduced by the last chunk to finish.  Summing one chunk's partial
+        // costs about three K blocks of MMA time (measured), so the tail
+        // takes about KB/sk + 3 sk K blocks: sk ~ sqrt(KB/3), and only deep
+        // contractions (48 K blocks or more) gain.
+        const int64_t P = grid / CM;
+        const int64_t full = (tiles_upper / P) * P, rem = tiles_upper - full;
+        const int64_t KBt = p.K / BK;
+        int64_t cap = 1;
+        while (3 * (cap + 1) * (cap + 1) <= KBt + 3 * cap) ++cap;  // round(sqrt(KB / 3))
+        int64_t sk = rem > 0 ? P / rem : 0;
+        if (sk > cap) sk = cap;
+        if (KBt >= 48 && sk >= 2 && rem * sk <= kSplitUnitsMax(sms) &&
+            rem * CM * 4 <= kSplitCounterBytes) {
+            q.full_tiles = full;
+            q.sk = static_cast<int>(sk);
+        }
+    }
     // Programmatic stream serialisation: the CTAs may be scheduled while the
     // previous kernel on the stream finishes (once it allows it); they set
     // up barriers and tensor memory, then wait for it in griddep_wait.
@@ -986,7 +1102,7 @@ static int launch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_t 
     cfg.stream = stream;
     cfg.attrs = attr;
     cfg.numAttrs = CM > 1 ? 2 : 1;
-    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, p) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, q) != cudaSuccess) {
         (void)cudaGetLastError();
         return FP8_ERR_CUDA;
     }
@@ -1016,7 +1132,7 @@ static int dispatch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_
         if constexpr (!GROUPED) {
             // per-column B scales (the Wgrad GEMM)
             if (rows) {
-                if (p.N % 256 == 0) {
+                if (p.N % 256 == 0 && ceil_div(mblk_upper, kClusterM) * (p.N / 256) < (1LL << 30)) {
                     const int64_t tiles = ceil_div(mblk_upper, kClusterM) * (p.N / 256);
                     if (out_type == FP8_OUT_BF16)
                         return launch<256, true, true, 0, kClusterM>(aq, a_rows, bq, b_rows, p, tiles,
@@ -1031,7 +1147,7 @@ static int dispatch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_
             }
             // 256-wide tiles on CTA pairs: per SM and K block, shared memory
             // moves A + B/2 each way instead of A + B
-            if (p.N % 256 == 0) {
+            if (p.N % 256 == 0 && ceil_div(mblk_upper, kClusterM) * (p.N / 256) < (1LL << 30)) {
                 const int64_t tiles = ceil_div(mblk_upper, kClusterM) * (p.N / 256);
                 if (out_type == FP8_OUT_BF16)
                     return launch<256, true, false, 0, kClusterM>(aq, a_rows, bq, b_rows, p, tiles,
@@ -1904,9 +2020,11 @@ static int fz_launch(const void* x, int64_t ldx, int64_t x_rows, const uint8_t* 
 
 using namespace fp8fg;
 
-extern "C" fp8_status fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, const uint8_t* bq,
-                                    const float* sb, fp8_bscale_t bmode, int64_t M, int64_t N, int64_t K,
-                                    void* c, int64_t ldc, fp8_out_t out_type, void* stream) {
+// Shared body of fp8_gemm_blockscaled and fp8_gemm_blockscaled_ws (ws: the
+// split-K workspace, or null).
+static int dense_gemm(const uint8_t* aq, const float* sa, const uint8_t* bq, const float* sb,
+                      int bmode, int64_t M, int64_t N, int64_t K, void* c, int64_t ldc, int out_type,
+                      void* ws, int64_t ws_bytes, void* stream) {
     if (M < 0 || N <= 0 || N % 128 != 0 || K <= 0 || K % 128 != 0 || ldc < N)
         return FP8_ERR_SHAPE;
     if (bmode < FP8_BSCALE_BLOCK128 || bmode > FP8_BSCALE_BLOCK128_T) return FP8_ERR_UNSUPPORTED;
@@ -1933,8 +2051,36 @@ extern "C" fp8_status fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, c
     p.ldc = ldc;
     p.offsets = nullptr;
     p.E = 0;
-    return to_status(dispatch<0>(aq, M, bq, N, p, out_type, (M + BM - 1) / BM,
-                           static_cast<cudaStream_t>(stream)));
+    if (ws != nullptr) {
+        const int sms = sm_count_current();
+        if (sms <= 0) return FP8_ERR_CUDA;
+        if (!aligned(ws, 16)) return FP8_ERR_ALIGN;
+        if (ws_bytes < split_workspace_bytes(sms)) return FP8_ERR_SHAPE;
+        p.ws_cnt = static_cast<int*>(ws);
+        p.ws = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kSplitCounterBytes);
+    }
+    return dispatch<0>(aq, M, bq, N, p, out_type, (M + BM - 1) / BM,
+                       static_cast<cudaStream_t>(stream));
+}
+
+extern "C" fp8_status fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, const uint8_t* bq,
+                                    const float* sb, fp8_bscale_t bmode, int64_t M, int64_t N, int64_t K,
+                                    void* c, int64_t ldc, fp8_out_t out_type, void* stream) {
+    return to_status(dense_gemm(aq, sa, bq, sb, bmode, M, N, K, c, ldc, out_type, nullptr, 0, stream));
+}
+
+extern "C" fp8_status fp8_gemm_blockscaled_ws(const uint8_t* aq, const float* sa, const uint8_t* bq,
+                                       const float* sb, fp8_bscale_t bmode, int64_t M, int64_t N,
+                                       int64_t K, void* c, int64_t ldc, fp8_out_t out_type,
+                                       void* workspace, int64_t workspace_bytes, void* stream) {
+    if (workspace == nullptr) return FP8_ERR_NULL;
+    return to_status(dense_gemm(aq, sa, bq, sb, bmode, M, N, K, c, ldc, out_type, workspace,
+                                workspace_bytes, stream));
+}
+
+extern "C" int64_t fp8_gemm_blockscaled_workspace_size(void) {
+    const int sms = sm_count_current();
+    return sms > 0 ? split_workspace_bytes(sms) : -1;
 }
 
 // Shared body of the grouped entry points; bmode is BLOCK128 (Fprop: per-expert

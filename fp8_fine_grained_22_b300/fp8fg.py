@@ -27,7 +27,8 @@ EXPORTS = ("fp8_status_str", "fp8_device_error", "fp8_selftest_wait_timeout",
            "fp8_quant_weight_128x128",
            "fp8_quant_fprop_operands", "fp8_quant_act_1x128_pow2",
            "fp8_quant_weight_128x128_pow2", "fp8_gemm_mxfp8",
-           "fp8_gemm_blockscaled", "fp8_grouped_gemm_moe", "fp8_grouped_gemm_moe_dgrad",
+           "fp8_gemm_blockscaled", "fp8_gemm_blockscaled_ws", "fp8_gemm_blockscaled_workspace_size",
+           "fp8_grouped_gemm_moe", "fp8_grouped_gemm_moe_dgrad",
            "fp8_gemm_blockscaled_bf16a", "fp8_grouped_gemm_moe_bf16a",
            "fp8_quant_act_128x1_grouped", "fp8_grouped_gemm_moe_wgrad",
            "fp8_moe_dispatch_workspace_size", "fp8_moe_dispatch_quant",
@@ -83,6 +84,10 @@ def lib() -> ctypes.CDLL:
                                                P, P]
         L.fp8_gemm_blockscaled.restype = I
         L.fp8_gemm_blockscaled.argtypes = [P, P, P, P, I, I64, I64, I64, P, I64, I, P]
+        L.fp8_gemm_blockscaled_ws.restype = I
+        L.fp8_gemm_blockscaled_ws.argtypes = [P, P, P, P, I, I64, I64, I64, P, I64, I, P, I64, P]
+        L.fp8_gemm_blockscaled_workspace_size.restype = I64
+        L.fp8_gemm_blockscaled_workspace_size.argtypes = []
         L.fp8_grouped_gemm_moe.restype = I
         L.fp8_grouped_gemm_moe.argtypes = [P, P, P, P, P, I32, I64, I64, I64, P, I, P]
         L.fp8_quant_act_128x1_grouped.restype = I
@@ -236,9 +241,19 @@ def fp8_quant_fprop_operands(x, w, xq=None, sx=None, wq=None, wqT=None, sw=None,
 
 
 # -------------------------------------------------------------------- GEMMs --
+def fp8_gemm_blockscaled_workspace_size():
+    """Bytes of the split-K workspace on the current device."""
+    n = lib().fp8_gemm_blockscaled_workspace_size()
+    if n < 0:
+        raise Fp8Error(5, "fp8_gemm_blockscaled_workspace_size")  # FP8_ERR_CUDA
+    return n
+
+
 def fp8_gemm_blockscaled(aq, sa, bq, sb, bmode=FP8_BSCALE_BLOCK128, out_dtype=torch.bfloat16,
-                         c=None, stream=None):
-    """C[M, N] of the block-scaled product; aq uint8 [M, K], bq uint8 [N, K]."""
+                         c=None, stream=None, workspace=None):
+    """C[M, N] of the block-scaled product; aq uint8 [M, K], bq uint8 [N, K].
+    workspace: a zero-filled uint8 device tensor of
+    fp8_gemm_blockscaled_workspace_size() bytes enables the split-K tail."""
     for t, n in ((aq, "aq"), (sa, "sa"), (bq, "bq"), (sb, "sb")):
         _cuda(t, n)
     M, K = aq.shape
@@ -248,9 +263,16 @@ def fp8_gemm_blockscaled(aq, sa, bq, sb, bmode=FP8_BSCALE_BLOCK128, out_dtype=to
     if c is None:
         c = torch.empty((M, N), dtype=out_dtype, device=aq.device)
     assert c.stride(1) == 1
-    _check(lib().fp8_gemm_blockscaled(_p(aq), _p(sa), _p(bq), _p(sb), int(bmode), M, N, K, _p(c),
-                                      c.stride(0), out_type, _stream(stream)),
-           "fp8_gemm_blockscaled")
+    if workspace is None:
+        _check(lib().fp8_gemm_blockscaled(_p(aq), _p(sa), _p(bq), _p(sb), int(bmode), M, N, K,
+                                          _p(c), c.stride(0), out_type, _stream(stream)),
+               "fp8_gemm_blockscaled")
+    else:
+        _cuda(workspace, "workspace", torch.uint8)
+        _check(lib().fp8_gemm_blockscaled_ws(_p(aq), _p(sa), _p(bq), _p(sb), int(bmode), M, N, K,
+                                             _p(c), c.stride(0), out_type, _p(workspace),
+                                             workspace.numel(), _stream(stream)),
+               "fp8_gemm_blockscaled_ws")
     return c
 
 

@@ -199,6 +199,38 @@ fp8_status fp8_gemm_blockscaled(const uint8_t* aq, const float* sa, const uint8_
                          void* c, int64_t ldc, fp8_out_t out_type, void* stream);
 
 /*
+ * fp8_gemm_blockscaled_ws -- fp8_gemm_blockscaled with a split-K workspace for
+ * the dense 256-column kernels (N % 256 == 0), which run on pairs of SMs.
+ * When the last wave of whole 256 x 256 tiles would leave at least half of
+ * the pairs idle, its tiles are cut along K into chunks computed on the idle
+ * pairs; each chunk parks its FP32 partial in the workspace, and the last
+ * chunk of a tile to finish adds the partials in chunk order and stores the
+ * tile.  The sum of the chunks is a different FP32 rounding order than the
+ * unsplit tile's (within the same error bound); it is the same for every call
+ * with the same shape on the same device.
+ *   workspace       : device memory, 16-byte aligned, at least
+ *                     fp8_gemm_blockscaled_workspace_size() bytes, zero-filled
+ *                     before its first use (each call leaves its counters zero
+ *                     again).  Owned by the caller.
+ *   workspace_bytes : its size.
+ * Calls that share one workspace must not run concurrently (they reuse its
+ * counters and partials).  Returns FP8_ERR_NULL for a NULL workspace,
+ * FP8_ERR_ALIGN for a misaligned one, FP8_ERR_SHAPE for one that is too small;
+ * everything else as fp8_gemm_blockscaled.
+ */
+fp8_status fp8_gemm_blockscaled_ws(const uint8_t* aq, const float* sa, const uint8_t* bq,
+                                   const float* sb, fp8_bscale_t bmode, int64_t M, int64_t N,
+                                   int64_t K, void* c, int64_t ldc, fp8_out_t out_type,
+                                   void* workspace, int64_t workspace_bytes, void* stream);
+
+/*
+ * fp8_gemm_blockscaled_workspace_size -- bytes of the split-K workspace for the
+ * current device (4 KB of counters + 256 KB per pair of SMs), or -1 if the
+ * device cannot be queried.
+ */
+int64_t fp8_gemm_blockscaled_workspace_size(void);
+
+/*
  * fp8_gemm_blockscaled_bf16a -- fp8_gemm_blockscaled with the activation
  * quantisation fused into the GEMM: A is read as bfloat16 and quantised 1x128
  * inside the kernel, on its way from the TMA copy to the tensor cores (report
