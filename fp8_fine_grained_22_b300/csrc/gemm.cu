@@ -249,9 +249,43 @@ __device__ __forceinline__ bool get_tile_gm(const GemmParams& p, int64_t t, Tile
 }
 
 // CM = 2: dense tiles of a CTA pair, this CTA's share by its rank
+// Grouped-row tiles of a CTA pair: every expert's rows are cut into 256-row
+// pair blocks (the last one ragged), times N / BN column blocks; CTA `rank`
+// takes the pair block's 128-row half `rank` (rows at or past the expert's
+// end are computed from whatever A holds there and not stored).  32-bit
+// arithmetic: the control warps walk this at 40 registers.
+template <int BN, int CM>
+__device__ __forceinline__ bool get_tile_grouped_pair(const GemmParams& p, int64_t t64, uint32_t rank,
+                                                      Tile& ti) {
+    const int t = static_cast<int>(t64);
+    const int nblk = static_cast<int>(p.N / BN);
+    int base = 0;
+    for (int e = 0; e < p.E; ++e) {
+        const int lo = __ldg(p.offsets + e), hi = __ldg(p.offsets + e + 1);
+        const int n_e = ((hi - lo + CM * BM - 1) / (CM * BM)) * nblk;
+        if (t < base + n_e) {
+            const int local = t - base;
+            const int mp = local / nblk, nb = local % nblk;
+            ti.row0 = lo + (mp * CM + static_cast<int>(rank)) * BM;
+            ti.row_end = hi;
+            ti.n0 = static_cast<int64_t>(nb) * BN;
+            ti.b_row0 = static_cast<int64_t>(e) * p.N + ti.n0;
+            ti.expert = e;
+            ti.kb_begin = 0;
+            ti.kb_count = static_cast<int>(p.K / BK);
+            ti.split = -1;
+            return true;
+        }
+        base += n_e;
+    }
+    return false;
+}
+
 template <int BN, int GM, int CM>
 __device__ __forceinline__ bool get_tile_any(const GemmParams& p, int64_t t, Tile& ti) {
-    if constexpr (CM > 1)
+    if constexpr (CM > 1 && GM == 1)
+        return get_tile_grouped_pair<BN, CM>(p, t, cluster_ctarank(), ti);
+    else if constexpr (CM > 1)
         return get_tile_cluster<BN, CM>(p, t, cluster_ctarank(), ti);
     else
         return get_tile_gm<BN, GM>(p, t, ti);
@@ -333,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // The epilogue, the scale ring and the output store are per CTA.
     constexpr bool PAIR = CM == 2;
     static_assert(CM == 1 || PAIR, "one CTA, or a CTA pair");
-    static_assert(!PAIR || GM == 0, "CTA pairs serve the dense kernels");
+    static_assert(!PAIR || GM != 2, "CTA pairs serve the dense and grouped-row kernels");
     using C = Cfg<BN, ROWSCALE, CM>;
     constexpr int S = C::STAGES;
     constexpr int NBUF = C::NBUF;
@@ -448,8 +482,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tcgen05.mma costs about twice the issue cycles).  The grouped kernels
     // keep single-lane roles: their tile walk over the expert offsets does not
     // fit the control warps' registers when run warp-wide.
-    constexpr bool kWarpRoles = !GROUPED;  // dense and grouped-K tiles are cheap to walk
-    constexpr bool kTwoIssuers = GM == 0;
+    // Whole-warp roles and two MMA issuers where the tile walk is cheap enough
+    // for the control warps' 40 registers: dense, grouped-K, and the grouped-
+    // row pairs (32-bit walk); the one-CTA grouped-row kernels keep one lane.
+    constexpr bool kWarpRoles = !GROUPED || PAIR;
+    constexpr bool kTwoIssuers = GM == 0 || (GROUPED && PAIR);
     constexpr bool kKRange = GK || PAIR;  // tiles carry their own K range
     auto role_wait = [&](uint32_t bar, uint32_t parity) {
         return kWarpRoles ? wait_bar_warp(bar, parity, abort_flag) : wait_bar(bar, parity, abort_flag);
@@ -793,9 +830,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 } else if constexpr (ROWSCALE) {
                     // 128 columns, two FP32 operations each: (P * sb[col]) * sa + acc.
-                    // 16-column TMEM loads, two in flight; the TMEM buffer goes
-                    // back once the last pair has landed, the scale slot after
-                    // the last column's arithmetic.
+                    // 16-column TMEM loads, three in flight (three load latencies
+                    // per K block; more staging registers than this do not fit);
+                    // the TMEM buffer goes back once the last loads have landed,
+                    // the scale slot after the last column's arithmetic.
                     // (packed FP32 pairs here: the scalar form needs more registers)
                     const uint64_t sa2 = pack2(f2u(sa_cur), f2u(sa_cur));
                     const uint32_t sbp = sb_addr0 + slot_off;
@@ -811,24 +849,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                             acc[ch * 8 + 2 * i + 1] = ffma2(p1, sa2, acc[ch * 8 + 2 * i + 1]);
                         }
                     };
-                    uint32_t r0[16], r1[16];
+                    // 16-column loads, three in flight: chunks 0-2, 3-5, 6-7
+                    uint32_t r0[16], r1[16], r2[16];
                     tmem_ld16(taddr, r0);
                     tmem_ld16(taddr + 16, r1);
-#pragma unroll
-                    for (int ch = 0; ch < COLS / 16; ch += 2) {
-                        tmem_wait_ld16(r0);
-                        tmem_wait_ld16(r1);
-                        if (ch + 2 < COLS / 16) {
-                            fma16(r0, ch);
-                            tmem_ld16(taddr + (ch + 2) * 16, r0);
-                            fma16(r1, ch + 1);
-                            tmem_ld16(taddr + (ch + 3) * 16, r1);
-                        } else {
-                            release_tmem(buf);
-                            fma16(r0, ch);
-                            fma16(r1, ch + 1);
-                        }
-                    }
+                    tmem_ld16(taddr + 32, r2);
+                    tmem_wait_ld16(r0);
+                    tmem_wait_ld16(r1);
+                    tmem_wait_ld16(r2);
+                    fma16(r0, 0);
+                    tmem_ld16(taddr + 48, r0);
+                    fma16(r1, 1);
+                    tmem_ld16(taddr + 64, r1);
+                    fma16(r2, 2);
+                    tmem_ld16(taddr + 80, r2);
+                    tmem_wait_ld16(r0);
+                    tmem_wait_ld16(r1);
+                    tmem_wait_ld16(r2);
+                    fma16(r0, 3);
+                    tmem_ld16(taddr + 96, r0);
+                    fma16(r1, 4);
+                    tmem_ld16(taddr + 112, r1);
+                    fma16(r2, 5);
+                    tmem_wait_ld16(r0);
+                    tmem_wait_ld16(r1);
+                    release_tmem(buf);
+                    fma16(r0, 6);
+                    fma16(r1, 7);
                     release_slot(r);
                 } else {
                     const float sc = sa_cur * sb_cur;
@@ -1156,8 +1203,24 @@ static int dispatch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_
                                                                stream);
             }
         }
-        // grouped rows (256 or 128 columns wide), or dense with N % 256 != 0
-        // (128 wide): one CTA per tile
+        // grouped rows, 256 columns wide: CTA pairs over 256-row blocks of
+        // each expert (at most one ragged block per expert) when the experts
+        // average 192 rows or more.  With fewer (decode-sized batches) most
+        // pairs would hold one expert's rows in one CTA only: measured 20 %
+        // slower there than one CTA per 128-row tile, which stays.
+        if constexpr (GROUPED) {
+            const int64_t pair_blocks = (p.M + kClusterM * BM - 1) / (kClusterM * BM) + p.E;
+            if (p.N % 256 == 0 && p.M >= 192 * static_cast<int64_t>(p.E) &&
+                pair_blocks * (p.N / 256) < (1LL << 30)) {
+                const int64_t tiles = pair_blocks * (p.N / 256);
+                if (out_type == FP8_OUT_BF16)
+                    return launch<256, true, false, GM, kClusterM>(aq, a_rows, bq, b_rows, p, tiles,
+                                                                   stream);
+                return launch<256, false, false, GM, kClusterM>(aq, a_rows, bq, b_rows, p, tiles,
+                                                                stream);
+            }
+        }
+        // grouped rows with few rows per expert: one CTA per 128 x 256 tile
         if constexpr (GROUPED) {
             if (p.N % 256 == 0) {
                 const int64_t tiles = mblk_upper * (p.N / 256);
@@ -1166,6 +1229,7 @@ static int dispatch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_
                 return launch<256, false, false, GM, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
             }
         }
+        // N % 256 != 0: one CTA per 128 x 128 tile
         const int64_t tiles = mblk_upper * (p.N / 128);
         if (out_type == FP8_OUT_BF16)
             return launch<128, true, false, GM, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);

@@ -63,7 +63,11 @@ def _compare(out, aq, sa, bq, sb, offsets, rows, bmode=oracle.BSCALE_BLOCK128):
 
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("counts", [[3, 0, 130, 1], [0, 0, 1], [128, 256, 127, 129, 5],
-                                    [0, 300, 0]])
+                                    [0, 300, 0],
+                                    # 192+ rows per expert on average, N = 256: CTA pairs
+                                    # over 256-row blocks (ragged second halves, a
+                                    # one-row expert, an empty one)
+                                    [300, 0, 450], [1, 600, 7]])
 def test_grouped_small(counts, out_dtype):
     g = torch.Generator().manual_seed(sum(counts) + len(counts))
     E, K, N = len(counts), 384, 256 if len(counts) % 2 else 384
@@ -159,6 +163,26 @@ def test_grouped_dgrad_small(counts, out_dtype):
     offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
     T = int(offsets[-1])
     dy = inputs.grad(max(T, 1), Nf, g)[:T]
+    w = torch.stack([inputs.weight(Kf, Nf, g) for _ in range(E)])
+    dq, sd = oracle.quant_act_1x128(bits(dy))
+    bqT, sw = _quant_experts_T(w)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(DEV)
+    off = torch.from_numpy(offsets.astype(np.int32)).to(DEV)
+    dx = fp8fg.fp8_grouped_gemm_moe_dgrad(t(dq), t(sd), t(bqT), t(sw), off, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert fp8fg.device_error() == 0
+    _compare(dx, dq, sd, bqT, sw, offsets, np.arange(T), bmode=oracle.BSCALE_BLOCK128_T)
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
+def test_grouped_dgrad_pairs(out_dtype):
+    """Dgrad with 512 output columns and 250 rows per expert: the CTA-pair path."""
+    counts = [300, 0, 450]
+    g = torch.Generator().manual_seed(41)
+    E, Kf, Nf = len(counts), 512, 256
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    T = int(offsets[-1])
+    dy = inputs.grad(T, Nf, g)
     w = torch.stack([inputs.weight(Kf, Nf, g) for _ in range(E)])
     dq, sd = oracle.quant_act_1x128(bits(dy))
     bqT, sw = _quant_experts_T(w)
