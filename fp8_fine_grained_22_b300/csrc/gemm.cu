@@ -15,10 +15,9 @@
 //               kind::f8f6f4 (K = 32 each) per K block into one of the TMEM
 //               partial buffers (two of 256 FP32 columns, or four of 128),
 //               then tcgen05.commit to release the smem stage and to signal
-//               the epilogue.  Dense kernels alternate K blocks between warps
-//               1 and 3; the grouped kernels issue from warp 1.  Dense and
-//               grouped-K roles run as whole warps with one elected lane
-//               issuing; the grouped-row kernels use one lane.
+//               the epilogue.  Dense and pair kernels alternate K blocks
+//               between warps 1 and 3; the others issue from warp 1.  Roles
+//               run as whole warps with one elected lane issuing.
 //   warp 2      scale loader of the per-column (Wgrad) mode: each K block's
 //               A and B scales into a shared-memory ring by bulk copies.
 //   warps 4..11 promotion epilogue, two per TMEM lane quadrant: tcgen05.ld the
@@ -160,16 +159,18 @@ __device__ __forceinline__ bool get_tile(const GemmParams& p, int64_t t, Tile& t
         ti.expert = 0;
         return true;
     } else {
-        int64_t base = 0;
+        // 32-bit arithmetic (the host keeps the tile count below 2^30)
+        const int t32 = static_cast<int>(t), nb32 = static_cast<int>(nblk);
+        int base = 0;
         for (int e = 0; e < p.E; ++e) {
-            const int64_t lo = __ldg(p.offsets + e), hi = __ldg(p.offsets + e + 1);
-            const int64_t n_e = ((hi - lo + BM - 1) / BM) * nblk;
-            if (t < base + n_e) {
-                const int64_t local = t - base;
-                const int64_t mb = local / nblk, nb = local % nblk;
+            const int lo = __ldg(p.offsets + e), hi = __ldg(p.offsets + e + 1);
+            const int n_e = ((hi - lo + BM - 1) / BM) * nb32;
+            if (t32 < base + n_e) {
+                const int local = t32 - base;
+                const int mb = local / nb32, nb = local % nb32;
                 ti.row0 = lo + mb * BM;
                 ti.row_end = hi;
-                ti.n0 = nb * BN;
+                ti.n0 = static_cast<int64_t>(nb) * BN;
                 ti.b_row0 = static_cast<int64_t>(e) * p.N + ti.n0;
                 ti.expert = e;
                 return true;
@@ -482,10 +483,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     // tcgen05.mma costs about twice the issue cycles).  The grouped kernels
     // keep single-lane roles: their tile walk over the expert offsets does not
     // fit the control warps' registers when run warp-wide.
-    // Whole-warp roles and two MMA issuers where the tile walk is cheap enough
-    // for the control warps' 40 registers: dense, grouped-K, and the grouped-
-    // row pairs (32-bit walk); the one-CTA grouped-row kernels keep one lane.
-    constexpr bool kWarpRoles = !GROUPED || PAIR;
+    // Producer and MMA issuer run as whole warps (one elected lane issuing)
+    // in every kernel: the 32-bit tile walks fit the control warps' 40
+    // registers.  Two MMA issuers in the dense and grouped-row pair kernels.
+    constexpr bool kWarpRoles = true;
     constexpr bool kTwoIssuers = GM == 0 || (GROUPED && PAIR);
     constexpr bool kKRange = GK || PAIR;  // tiles carry their own K range
     auto role_wait = [&](uint32_t bar, uint32_t parity) {
