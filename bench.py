@@ -282,7 +282,10 @@ class Dev:
         self.clk = clk
         self.dev = torch.device("cuda", local)
         torch.cuda.set_device(self.dev)
-        self.stream = torch.cuda.current_stream(self.dev)
+        # a stream of its own, current for everything the bench issues: CUDA
+        # graphs are captured on it (the legacy default stream cannot capture)
+        self.stream = torch.cuda.Stream(self.dev)
+        torch.cuda.set_stream(self.stream)
         self._flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=self.dev)
         self._sink = torch.empty((), dtype=torch.float32, device=self.dev)
 
@@ -294,14 +297,27 @@ class Dev:
         self._flush.zero_()
         torch.sum(self._flush, dim=0, out=self._sink)
 
+    def graph(self, fn):
+        """fn's launches captured once as a CUDA graph on the bench's stream
+        (after one eager call, so that first-call attribute setup is done):
+        a replay issues them with no host work between them."""
+        fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.stream):
+            fn()
+        torch.cuda.synchronize()
+        return g
+
     def kernel_ms(self, fn, reps=20, flush=True):
-        """Mean device time of fn's launches (CUDA events on the launching
-        stream), with L2 flushed before each repetition."""
+        """Mean device time of fn's launches, replayed from a CUDA graph with
+        CUDA events on the launching stream around each replay and L2
+        flushed before it."""
+        g = self.graph(fn)
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(reps)]
-        fn()  # warm-up (first-call attribute setup stays out of the timing)
         with self.busy():
-            self._reps(fn, ev, flush)
+            self._reps(g.replay, ev, flush)
         return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
     def busy(self):
@@ -502,20 +518,36 @@ def run_trio(args, rank, world, local):
         raise RuntimeError("device-side error during warm-up")
 
     nk = len(Trio.NAMES)
-    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nk + 1)]
-              for _ in range(args.steps)]
+    # The step as a CUDA graph of its eight launches, and a second graph of
+    # the same launches with an event before each and after the last: the
+    # per-kernel times.  Events between the kernels cost the programmatic
+    # overlap of each GEMM's set-up with the kernel before it, so the step
+    # time comes from the plain graph and the kernel times from the
+    # instrumented one; every timed iteration replays both.
+    g_step = d.graph(tr.step)
+    inner = [torch.cuda.Event(enable_timing=True, external=True) for _ in range(nk + 1)]
+    g_inst = d.graph(lambda: tr.step(inner))
+    outer = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+             for _ in range(args.steps)]
+    per_runs, inst_steps = [], []
     rank_barrier()
     torch.cuda.synchronize()
     with d.busy():
         t_start = time.perf_counter()
         for i in range(args.steps):
             d.flush_l2()  # between steps, outside the step's events
-            tr.step(events[i])
-        torch.cuda.synchronize()
+            outer[i][0].record(d.stream)
+            g_step.replay()
+            outer[i][1].record(d.stream)
+            d.flush_l2()
+            g_inst.replay()
+            torch.cuda.synchronize()  # the inner events are read before the next replay
+            per_runs.append([inner[j].elapsed_time(inner[j + 1]) for j in range(nk)])
+            inst_steps.append(inner[0].elapsed_time(inner[nk]))
         t_end = time.perf_counter()
     rank_barrier()
-    per = [statistics.mean(e[j].elapsed_time(e[j + 1]) for e in events) for j in range(nk)]
-    step_ms = statistics.mean(e[0].elapsed_time(e[nk]) for e in events)
+    per = [statistics.mean(r[j] for r in per_runs) for j in range(nk)]
+    step_ms = statistics.mean(a.elapsed_time(b) for a, b in outer)
     ms_step = reduce_max(step_ms, d.dev)
     if fp8fg.device_error() != 0:
         raise RuntimeError("device-side error in the timed steps")
@@ -576,9 +608,14 @@ def run_trio(args, rank, world, local):
                    "parallelism": "replicas (dp%d, no collective)" % world,
                    "l2": "flushed between steps (%d MB written, then read back); the step's "
                          "operands (~0.8 GB) are larger than L2" % (2 * L2_BYTES >> 20),
-                   "step": list(Trio.NAMES)},
+                   "step": list(Trio.NAMES),
+                   "timing": "each timed step replays a CUDA graph of the step's eight launches "
+                             "between two events (ms_per_step), then, L2 flushed again, a graph "
+                             "of the same launches with an event between kernels (kernels, "
+                             "roofline; ms_per_step_instrumented)"},
+        "ms_per_step_instrumented": round(statistics.mean(inst_steps), 5),
         "e2e": e2e,
-        "gpu_launches": nk * args.steps,
+        "gpu_launches": 2 * nk * args.steps,
         "roofline": roofline,
         "kernels": kernels,
         "peaks": peaks,
@@ -1107,6 +1144,26 @@ def probe_gemms():
     print(json.dumps({"probe": "gemms", "launches": 2 * len(runs)}))
 
 
+def probe_quant():
+    """For an ncu capture: the trio's quantiser launches once, then each again
+    with L2 flushed before it."""
+    from fp8_fine_grained_22_b300 import fp8fg
+    d = Dev(0)
+    fp8fg.lib()
+    tr = Trio(d, inputs.training_trio(seed=0))
+    runs = tr.launches()[:Trio.N_QUANT]
+    for r in runs:
+        r()
+    for r in runs:
+        d.flush_l2()
+        torch.cuda.synchronize()
+        r()
+    torch.cuda.synchronize()
+    if fp8fg.device_error() != 0:
+        raise RuntimeError("device-side error")
+    print(json.dumps({"probe": "quant", "launches": 2 * len(runs)}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1122,12 +1179,16 @@ def main():
                     help="tokens of the trio the cpu_baseline oracle run covers (multiple of 128)")
     ap.add_argument("--workload", default="trio",
                     choices=["trio", "fprop_dense", "moe_prefill", "moe_decode", "moe_backward"])
-    ap.add_argument("--probe", choices=["gemms"], default=None,
-                    help="launch each profiled GEMM twice (warm-up, then L2 flushed) and exit: "
-                         "the program the committed ncu summaries capture")
+    ap.add_argument("--probe", choices=["gemms", "quant"], default=None,
+                    help="launch each profiled GEMM (gemms) or the trio's quantisers (quant) "
+                         "twice (warm-up, then L2 flushed) and exit: the programs the committed "
+                         "ncu summaries capture")
     args = ap.parse_args()
     if args.probe == "gemms":
         probe_gemms()
+        return
+    if args.probe == "quant":
+        probe_quant()
         return
     if args.ref_tokens % 128 or args.cpu_tokens % 128:
         ap.error("--ref-tokens and --cpu-tokens must be multiples of 128")

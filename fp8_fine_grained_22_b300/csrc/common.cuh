@@ -139,4 +139,8 @@ class ContextCache {
     Slot slots_[kMaxDevices];
 };
 
+// Device address of the library's error word (the one fp8_device_error reads
+// and clears) in the current context; nullptr if it cannot be looked up.
+unsigned* device_error_word();
+
 }  // namespace fp8fg

@@ -2335,6 +2335,22 @@ extern "C" fp8_status fp8_selftest_wait_timeout(void* stream) {
     return to_status(launch_status());
 }
 
+// Device address of the error word in the current context, for kernels of
+// the other translation units (the library is built without relocatable
+// device code, so they cannot name g_dev_error themselves).
+unsigned* fp8fg::device_error_word() {
+    static ContextCache<unsigned*> cache;
+    unsigned* p = nullptr;
+    if (cache.get(&p, [](unsigned** v) {
+            void* a = nullptr;
+            if (cudaGetSymbolAddress(&a, g_dev_error) != cudaSuccess) return static_cast<int>(FP8_ERR_CUDA);
+            *v = static_cast<unsigned*>(a);
+            return static_cast<int>(FP8_OK);
+        }) != FP8_OK)
+        return nullptr;
+    return p;
+}
+
 extern "C" fp8_status fp8_device_error(void* stream) {
     if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
         return FP8_ERR_CUDA;

@@ -18,6 +18,7 @@
 #include "common.cuh"
 #include "ptx.cuh"
 #include "quant_math.cuh"
+#include "tensormap.cuh"
 
 namespace fp8fg {
 
@@ -35,8 +36,17 @@ constexpr int kQuantCtasPerSm = 4;
 // K-group fastest.
 constexpr int kQ1Rows = 64;
 
-__device__ __forceinline__ void load_1x128(const uint16_t* __restrict__ x, int64_t M, int64_t ldx,
-                                           int64_t KB, int64_t t, int row, int l4, uint4 (&v)[4]) {
+// Loads this lane's 32 elements of row m, K group kb (zeros past row M).
+__device__ __forceinline__ void load_1x128(const uint16_t* __restrict__ x, uint32_t M, int64_t ldx,
+                                           uint32_t kb, uint32_t m, int l4, uint4 (&v)[4]) {
+    const uint16_t* src = x + static_cast<size_t>(m) * ldx + kb * 128 + l4 * 32;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = (m < M) ? ld_stream_v4(src + 8 * i) : make_uint4(0, 0, 0, 0);
+}
+
+// The same for tile t (64 rows x one K group, K group fastest), row `row`.
+__device__ __forceinline__ void load_1x128_tile(const uint16_t* __restrict__ x, int64_t M, int64_t ldx,
+                                                int64_t KB, int64_t t, int row, int l4, uint4 (&v)[4]) {
     const int64_t kb = t % KB;
     const int64_t m = (t / KB) * kQ1Rows + row;
     const uint16_t* src = x + m * ldx + kb * 128 + l4 * 32;
@@ -44,63 +54,75 @@ __device__ __forceinline__ void load_1x128(const uint16_t* __restrict__ x, int64
     for (int i = 0; i < 4; ++i) v[i] = (m < M) ? ld_stream_v4(src + 8 * i) : make_uint4(0, 0, 0, 0);
 }
 
-// Quantises the 1x128 tile whose bf16 values this thread holds in v (row
-// `row` of the tile, lanes l4 = 0..3 of its four-lane group).
-__device__ __forceinline__ void quant_1x128_tile(int64_t M, int64_t KB, uint8_t* __restrict__ xq,
-                                                 int64_t ldq, float* __restrict__ sx, int64_t t,
-                                                 int row, int l4, const uint4 (&v)[4]) {
-    const int64_t kb = t % KB;
-    const int64_t m = (t / KB) * kQ1Rows + row;
-    uint32_t mx = absmax_bf16x2(v[0].x, v[0].y);
-    mx = absmax_bf16x2(mx, absmax_bf16x2(v[0].z, v[0].w));
+// Codes of 16 consecutive elements (eight words, memory order) of a group,
+// sign bits flipped back, as one 16-byte store.
+template <bool FAST>
+__device__ __forceinline__ uint4 codes_1x128(const NegDiv& dv, const uint4& a, const uint4& b) {
+    auto quad = [&](uint32_t w0, uint32_t w1) {
+        return prmt(dv.ncodes2<FAST>(bf16x2_to_f2(w0)), dv.ncodes2<FAST>(bf16x2_to_f2(w1)), 0x5410u) ^
+               kSignFlip4;
+    };
+    return make_uint4(quad(a.x, a.y), quad(a.z, a.w), quad(b.x, b.y), quad(b.z, b.w));
+}
+
+// Quantises the group (row m, K group kb) whose 32 bf16 values per lane
+// this thread holds in v (lanes l4 = 0..3 of the row's four-lane group).
+__device__ __forceinline__ void quant_1x128_group(uint32_t M, uint8_t* __restrict__ xq, int64_t ldq,
+                                                  float* __restrict__ sx, uint32_t kb, uint32_t m, int l4,
+                                                  const uint4 (&v)[4]) {
+    uint32_t mx = 0;
 #pragma unroll
-    for (int i = 1; i < 4; ++i) {
-        mx = absmax_bf16x2(mx, absmax_bf16x2(v[i].x, v[i].y));
-        mx = absmax_bf16x2(mx, absmax_bf16x2(v[i].z, v[i].w));
+    for (int i = 0; i < 4; ++i) {
+        mx = absmax_acc(mx, v[i].x);
+        mx = absmax_acc(mx, v[i].y);
+        mx = absmax_acc(mx, v[i].z);
+        mx = absmax_acc(mx, v[i].w);
     }
-    float amax = amax_of_pair(mx);
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-    amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    const float s = group_scale(amax);
-    const GroupDiv dv(s);
+    mx &= 0x7FFF7FFFu;
+    mx = absmax_acc(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = absmax_acc(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float s = group_scale(amax_of_pair(mx));
+    const NegDiv dv(s, __frcp_rn(s));
     if (m < M) {
-        uint4 o[2];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t a = dv.quad_words(v[i].x, v[i].y);
-            const uint32_t b = dv.quad_words(v[i].z, v[i].w);
-            if (i & 1) {
-                o[i >> 1].z = a;
-                o[i >> 1].w = b;
-            } else {
-                o[i >> 1].x = a;
-                o[i >> 1].y = b;
-            }
+        uint4 o0, o1;
+        if (s >= 0x1p-91f) {
+            o0 = codes_1x128<true>(dv, v[0], v[1]);
+            o1 = codes_1x128<true>(dv, v[2], v[3]);
+        } else {
+            o0 = codes_1x128<false>(dv, v[0], v[1]);
+            o1 = codes_1x128<false>(dv, v[2], v[3]);
         }
-        uint4* dst = reinterpret_cast<uint4*>(xq + m * ldq + kb * 128 + l4 * 32);
-        dst[0] = o[0];
-        dst[1] = o[1];
-        if (l4 == 0) sx[kb * M + m] = s;
+        uint4* dst = reinterpret_cast<uint4*>(xq + static_cast<size_t>(m) * ldq + kb * 128 + l4 * 32);
+        dst[0] = o0;
+        dst[1] = o1;
+        if (l4 == 0) sx[static_cast<size_t>(kb) * M + m] = s;
     }
 }
 
 __global__ void __launch_bounds__(kQuantThreads) quant_act_1x128_kernel(
-    const uint16_t* __restrict__ x, int64_t M, int64_t KB, int64_t ldx, uint8_t* __restrict__ xq,
-    int64_t ldq, float* __restrict__ sx, int64_t tiles) {
+    const uint16_t* __restrict__ x, uint32_t M, uint32_t KB, int64_t ldx, uint8_t* __restrict__ xq,
+    int64_t ldq, float* __restrict__ sx, uint32_t tiles) {
     griddep_launch_dependents();  // the GEMM that follows may set up meanwhile
     const int l4 = threadIdx.x & 3;
     const int row = threadIdx.x >> 2;  // 0..63
-    int64_t t = blockIdx.x;
+    // tile t = mb * KB + kb, walked with the grid stride without division
+    const uint32_t step = gridDim.x, step_q = step / KB, step_r = step % KB;
+    uint32_t kb = blockIdx.x % KB, mb = blockIdx.x / KB;
     uint4 v[4];
-    if (t < tiles) load_1x128(x, M, ldx, KB, t, row, l4, v);
-    while (t < tiles) {
-        const int64_t tn = t + gridDim.x;
+    if (blockIdx.x < tiles) load_1x128(x, M, ldx, kb, mb * kQ1Rows + row, l4, v);
+    for (uint32_t t = blockIdx.x; t < tiles; t += step) {
+        uint32_t kbn = kb + step_r, mbn = mb + step_q;
+        if (kbn >= KB) {
+            kbn -= KB;
+            ++mbn;
+        }
         uint4 vn[4];
-        if (tn < tiles) load_1x128(x, M, ldx, KB, tn, row, l4, vn);
-        quant_1x128_tile(M, KB, xq, ldq, sx, t, row, l4, v);
+        if (t + step < tiles) load_1x128(x, M, ldx, kbn, mbn * kQ1Rows + row, l4, vn);  // in flight
+        quant_1x128_group(M, xq, ldq, sx, kb, mb * kQ1Rows + row, l4, v);
 #pragma unroll
         for (int i = 0; i < 4; ++i) v[i] = vn[i];
-        t = tn;
+        kb = kbn;
+        mb = mbn;
     }
 }
 
@@ -157,11 +179,11 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_1x128_e5m6_kernel(
     const int row = threadIdx.x >> 2;  // 0..63
     int64_t t = blockIdx.x;
     uint4 v[4];
-    if (t < tiles) load_1x128(x, M, ldx, KB, t, row, l4, v);
+    if (t < tiles) load_1x128_tile(x, M, ldx, KB, t, row, l4, v);
     while (t < tiles) {
         const int64_t tn = t + gridDim.x;
         uint4 vn[4];
-        if (tn < tiles) load_1x128(x, M, ldx, KB, tn, row, l4, vn);
+        if (tn < tiles) load_1x128_tile(x, M, ldx, KB, tn, row, l4, vn);
         quant_1x128_e5m6_tile(M, KB, xq, ldq, sx, t, row, l4, v);
 #pragma unroll
         for (int i = 0; i < 4; ++i) v[i] = vn[i];
@@ -180,11 +202,11 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_1x128_pow2_kernel(
     const int row = threadIdx.x >> 2;
     int64_t t = blockIdx.x;
     uint4 v[4];
-    if (t < tiles) load_1x128(x, M, ldx, KB, t, row, l4, v);
+    if (t < tiles) load_1x128_tile(x, M, ldx, KB, t, row, l4, v);
     while (t < tiles) {
         const int64_t tn = t + gridDim.x;
         uint4 vn[4];
-        if (tn < tiles) load_1x128(x, M, ldx, KB, tn, row, l4, vn);
+        if (tn < tiles) load_1x128_tile(x, M, ldx, KB, tn, row, l4, vn);
         const int64_t kb = t % KB;
         const int64_t m = (t / KB) * kQ1Rows + row;
         uint32_t mx = absmax_bf16x2(v[0].x, v[0].y);
@@ -294,81 +316,167 @@ __global__ void __launch_bounds__(256) quant_weight_128x128_pow2_kernel(
 }
 
 // ------------------------------------------------------------------ 128x1 --
-// Tile: one 128-token group x 64 columns, staged in shared memory; each
-// thread then owns a pair of adjacent columns (one 32-bit word per row: the
-// warp reads a whole 128-byte row, no bank conflicts) and 16 of the 128
-// rows, and converts both columns with one permute per four sign bits.
-// Tiles are numbered column-block fastest.
-__device__ __forceinline__ void load_128x1(const uint16_t* __restrict__ x, int64_t ldx,
-                                           int64_t KC, int64_t t, int tid, uint4 (&v)[4]) {
-    const int64_t k0 = (t % KC) * 64;
-    const int64_t m0 = (t / KC) * 128;
-    const int ch = tid & 7;
+// Tile: one 128-token group x 64 columns (16 KB of bf16), brought by TMA
+// with the 128-byte swizzle into a ring of kQ128x1Stages slots.  Warp w owns
+// the tile's columns 8w .. 8w+7 (one 16-byte chunk of every row); lane
+// (cp = lane & 3, g = lane >> 2) owns the column pair 8w+2cp, 8w+2cp+1 and
+// rows 16g .. 16g+15.  The warps never wait for one another:
+// - lane g reads its rows in the order 16g + (i ^ g), i = 0..15, so at every
+//   step the eight lanes of a column pair read rows with different swizzle
+//   phases, i.e. eight different bank groups (no conflicts);
+// - a column's maximum is combined across its eight lanes by shuffles, and
+//   the eight columns' scales are computed once each, by lanes 0-7;
+// - the last warp to finish reading a slot (a shared counter) issues the
+//   slot's next load.
+// A lane's 16 codes per column leave in one 16-byte store, the XOR order
+// undone by the byte permute that packs them; the eight lanes of a column
+// write its 128-byte row of xqT together.  Tiles are numbered column-block
+// fastest.
+constexpr int kQ128x1Stages = 3;
+constexpr int kQ128x1TileBytes = 128 * 64 * 2;
+// 1 KB of slack to align the ring to the swizzle pattern; then the ring, the
+// full barriers, the slot counters (reads done, loads issued) and the abort flag
+constexpr int kQ128x1Smem = 1024 + kQ128x1Stages * (kQ128x1TileBytes + 16) + 16;
+
+// Wait for a TMA load still in flight when the CTA gives up, so that the ring
+// is not released under it; bounded like every other wait.
+__device__ __forceinline__ void drain_load(uint32_t bar, uint32_t parity) {
+    const long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity))
+        if (clock64() - t0 > kWaitLimit) return;
+}
+
+// Codes of 16 rows of two columns held as bf16 pairs (column a in the low
+// halves of w[0..15], b in the high ones), sign bits flipped back.  Word m
+// of oa packs the codes of w[4m .. 4m+3] through the byte selector sel
+// (0x5410: memory order; the 128x1 kernel passes a lane-dependent order).
+template <bool FAST>
+__device__ __forceinline__ void codes_cols16(const NegDiv& da, const NegDiv& db, const uint32_t* w,
+                                             uint32_t sel, uint32_t* oa, uint32_t* ob) {
 #pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const int row = (tid >> 3) + 32 * p;
-        v[p] = ld_stream_v4(x + (m0 + row) * ldx + k0 + ch * 8);
+    for (int m = 0; m < 4; ++m) {
+        const uint32_t a01 = da.ncodes2<FAST>(bf16_lo2(w[4 * m], w[4 * m + 1]));
+        const uint32_t a23 = da.ncodes2<FAST>(bf16_lo2(w[4 * m + 2], w[4 * m + 3]));
+        const uint32_t b01 = db.ncodes2<FAST>(bf16_hi2(w[4 * m], w[4 * m + 1]));
+        const uint32_t b23 = db.ncodes2<FAST>(bf16_hi2(w[4 * m + 2], w[4 * m + 3]));
+        oa[m] = prmt(a01, a23, sel) ^ kSignFlip4;
+        ob[m] = prmt(b01, b23, sel) ^ kSignFlip4;
     }
 }
 
 __global__ void __launch_bounds__(kQuantThreads) quant_act_128x1_kernel(
-    const uint16_t* __restrict__ x, int64_t M, int64_t K, int64_t ldx, uint8_t* __restrict__ xqT,
-    float* __restrict__ sxT, int64_t tiles) {
+    const __grid_constant__ CUtensorMap xmap, uint32_t M, uint32_t K, uint8_t* __restrict__ xqT,
+    float* __restrict__ sxT, uint32_t tiles, unsigned* err_word) {
     griddep_launch_dependents();  // the GEMM that follows may set up meanwhile
-    __shared__ __align__(16) uint16_t tile[128][64];
-    __shared__ float part[8][64];
-    const int t0 = threadIdx.x;
-    const int64_t KC = K / 64;
-    const int cp = t0 & 31, rg = t0 >> 5;
-    int64_t t = blockIdx.x;
-    uint4 v[4];
-    if (t < tiles) load_128x1(x, ldx, KC, t, t0, v);
-    while (t < tiles) {
-        const int64_t k0 = (t % KC) * 64;
-        const int64_t mb = t / KC;
-        {
-            const int ch = t0 & 7;
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-                const int row = (t0 >> 3) + 32 * p;
-                *reinterpret_cast<uint4*>(&tile[row][ch * 8]) = v[p];
-            }
+    extern __shared__ __align__(16) uint8_t smem_q1[];
+    uint8_t* ring = smem_q1 + ((1024u - (smem_addr(smem_q1) & 1023u)) & 1023u);
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + kQ128x1Stages * kQ128x1TileBytes);
+    uint32_t* done = reinterpret_cast<uint32_t*>(full + kQ128x1Stages);  // warps done reading, per slot
+    uint32_t* issued = done + kQ128x1Stages;                              // loads issued, per slot
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(issued + kQ128x1Stages);
+    const int t0 = threadIdx.x, warp = t0 >> 5, lane = t0 & 31;
+    const int cp = lane & 3, g = lane >> 2;
+    const uint32_t KC = K / 64;
+    const uint32_t step = gridDim.x;
+    auto issue = [&](uint32_t tt, int s) {
+        const uint32_t bar = smem_addr(&full[s]);
+        mbar_arrive_expect_tx(bar, kQ128x1TileBytes);
+        tma_load_2d(smem_addr(ring + s * kQ128x1TileBytes), &xmap, bar, static_cast<int>((tt % KC) * 64),
+                    static_cast<int>((tt / KC) * 128));
+        atomicAdd(&issued[s], 1u);
+    };
+    if (t0 == 0) {
+        for (int s = 0; s < kQ128x1Stages; ++s) {
+            mbar_init(smem_addr(&full[s]), 1);
+            done[s] = 0;
+            issued[s] = 0;
         }
-        const int64_t tn = t + gridDim.x;
-        if (tn < tiles) load_128x1(x, ldx, KC, tn, t0, v);  // next tile's loads in flight
-        __syncthreads();
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&xmap);
+        for (int s = 0; s < kQ128x1Stages; ++s)
+            if (blockIdx.x + s * step < tiles) issue(blockIdx.x + s * step, s);
+    }
+    __syncthreads();
+    // Byte offsets of this lane's words in a slot, for i & 7 = j (rows
+    // 16g + (j ^ g), +8 for i >= 8): row 16g + u sits at 128 (16g + u) and its
+    // chunk w at 16 (w ^ (row & 7)) = 16 (w ^ u).
+    uint32_t off[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int u = j ^ g;
+        off[j] = 2048 * g + 128 * u + 16 * (warp ^ u) + 4 * cp;
+    }
+    // Packing selector: the codes of rows i = 4m + t (t = 0, 1 in the first
+    // source's low bytes, t = 2, 3 in the second's) go to byte t ^ (g & 3).
+    uint32_t sel = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const int t = b ^ (g & 3);
+        sel |= static_cast<uint32_t>((t & 1) | ((t >> 1) << 2)) << (4 * b);
+    }
+    const bool swap_words = (g & 4) != 0;
+    const uint32_t step_q = step / KC, step_r = step % KC;
+    uint32_t kc = blockIdx.x % KC, mb = blockIdx.x / KC;
+    uint32_t it = 0;
+    for (uint32_t t = blockIdx.x; t < tiles; t += step, ++it) {
+        const int s = static_cast<int>(it % kQ128x1Stages);
+        if (!wait_bounded_warp(smem_addr(&full[s]), (it / kQ128x1Stages) & 1u, abort_flag, err_word)) break;
+        const uint8_t* slot = ring + s * kQ128x1TileBytes;
         uint32_t w[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) w[i] = *reinterpret_cast<const uint32_t*>(slot + off[i & 7] + 128 * (i & 8));
+        // the last warp to finish with the slot refills it
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            const uint32_t prev = atomicAdd(&done[s], 1u);
+            const uint32_t tn = t + kQ128x1Stages * step;
+            if (prev == 8u * (it / kQ128x1Stages) + 7u && tn < tiles) issue(tn, s);
+        }
         uint32_t mx = 0;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            w[i] = *reinterpret_cast<const uint32_t*>(&tile[rg * 16 + i][2 * cp]);
-            mx = absmax_bf16x2(mx, w[i]);  // per column: low half and high half
+        for (int i = 0; i < 16; ++i) mx = absmax_acc(mx, w[i]);
+        mx &= 0x7FFF7FFFu;
+        mx = absmax_acc(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = absmax_acc(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = absmax_acc(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        // lanes c = 0..7 (and their copies) take column 8w + c: its maximum
+        // is half c & 1 of lane c >> 1's pair
+        const int c8 = lane & 7;
+        const uint32_t m2 = __shfl_sync(0xffffffffu, mx, c8 >> 1);
+        const float sc = group_scale((c8 & 1) ? bf16_hi(m2) : bf16_lo(m2));
+        const float rc = __frcp_rn(sc);
+        const uint32_t k0 = kc * 64 + 8 * warp;
+        if (lane < 8) sxT[static_cast<size_t>(mb) * K + k0 + lane] = sc;
+        const float sa = __shfl_sync(0xffffffffu, sc, 2 * cp), ra = __shfl_sync(0xffffffffu, rc, 2 * cp);
+        const float sb = __shfl_sync(0xffffffffu, sc, 2 * cp + 1), rb = __shfl_sync(0xffffffffu, rc, 2 * cp + 1);
+        const NegDiv da(sa, ra), db(sb, rb);
+        uint32_t oa[4], ob[4];
+        if (sa >= 0x1p-91f && sb >= 0x1p-91f)
+            codes_cols16<true>(da, db, w, sel, oa, ob);
+        else
+            codes_cols16<false>(da, db, w, sel, oa, ob);
+        const uint4 va = swap_words ? make_uint4(oa[1], oa[0], oa[3], oa[2]) : make_uint4(oa[0], oa[1], oa[2], oa[3]);
+        const uint4 vb = swap_words ? make_uint4(ob[1], ob[0], ob[3], ob[2]) : make_uint4(ob[0], ob[1], ob[2], ob[3]);
+        uint8_t* dst = xqT + static_cast<size_t>(k0 + 2 * cp) * M + mb * 128 + 16 * g;
+        *reinterpret_cast<uint4*>(dst) = va;
+        *reinterpret_cast<uint4*>(dst + M) = vb;
+        kc += step_r;
+        mb += step_q;
+        if (kc >= KC) {
+            kc -= KC;
+            ++mb;
         }
-        part[rg][2 * cp] = bf16_lo(mx);
-        part[rg][2 * cp + 1] = bf16_hi(mx);
-        __syncthreads();
-        float amax_a = part[0][2 * cp], amax_b = part[0][2 * cp + 1];
-#pragma unroll
-        for (int j = 1; j < 8; ++j) {
-            amax_a = fmaxf(amax_a, part[j][2 * cp]);
-            amax_b = fmaxf(amax_b, part[j][2 * cp + 1]);
+    }
+    // A timed-out wait ends the loop early: a load still in flight into a
+    // slot (at most one per slot) must land before the CTA releases the ring.
+    __syncthreads();
+    if (t0 == 0 && *abort_flag) {
+        for (int s = 0; s < kQ128x1Stages; ++s) {
+            const uint32_t n = *reinterpret_cast<volatile uint32_t*>(&issued[s]);
+            if (n > 0) drain_load(smem_addr(&full[s]), (n - 1) & 1u);
         }
-        const float sa = group_scale(amax_a), sb = group_scale(amax_b);
-        const GroupDiv da(sa), db(sb);
-        if (rg == 0) {
-            sxT[mb * K + k0 + 2 * cp] = sa;
-            sxT[mb * K + k0 + 2 * cp + 1] = sb;
-        }
-        uint4 oa, ob;
-        GroupDiv::halves(da, db, w[0], w[1], w[2], w[3], oa.x, ob.x);
-        GroupDiv::halves(da, db, w[4], w[5], w[6], w[7], oa.y, ob.y);
-        GroupDiv::halves(da, db, w[8], w[9], w[10], w[11], oa.z, ob.z);
-        GroupDiv::halves(da, db, w[12], w[13], w[14], w[15], oa.w, ob.w);
-        const int64_t r0 = mb * 128 + rg * 16;
-        *reinterpret_cast<uint4*>(xqT + (k0 + 2 * cp) * M + r0) = oa;
-        *reinterpret_cast<uint4*>(xqT + (k0 + 2 * cp + 1) * M + r0) = ob;
-        __syncthreads();  // tile and part are rewritten by the next iteration
-        t = tn;
     }
 }
 
@@ -506,6 +614,10 @@ struct PairArgs {
     uint8_t* wqT;
     float* sw;
     int64_t KB;  // K / 128, shared by both operands
+    // ceil(w_tiles 2^32 / (w_tiles + act_tiles)): the weight blocks among
+    // items 0..n-1 number floor(n w_frac / 2^32), which steps by 0 or 1 and
+    // reaches w_tiles at n = total
+    uint64_t w_frac;
 };
 
 __device__ __forceinline__ void cp_async_commit() {
@@ -516,24 +628,23 @@ __device__ __forceinline__ void cp_async_wait_prev() {  // all groups but the ne
 }
 
 // Item i of the list is a weight block when the count of weight blocks
-// among items 0..i, floor((i + 1) W / total), steps up at i; *idx is then
+// among items 0..i, floor((i + 1) w_frac / 2^32), steps up at i; *idx is then
 // the block's index, else the activation tile's.
-__device__ __forceinline__ bool pair_item(const PairArgs& p, int64_t i, int64_t* idx) {
-    const int64_t total = p.w_tiles + p.act_tiles;
-    const int64_t w_upto = ((i + 1) * p.w_tiles) / total;
-    const bool is_w = w_upto > (i * p.w_tiles) / total;
+__device__ __forceinline__ bool pair_item(const PairArgs& p, uint32_t i, uint32_t* idx) {
+    const uint32_t w_upto = static_cast<uint32_t>(((i + 1ull) * p.w_frac) >> 32);
+    const bool is_w = w_upto > static_cast<uint32_t>((static_cast<uint64_t>(i) * p.w_frac) >> 32);
     *idx = is_w ? w_upto - 1 : i - w_upto;
     return is_w;
 }
 
 // Starts the loads of item t: weight block t into `tile`, or activation
 // tile t into v.
-__device__ __forceinline__ void pair_issue(const PairArgs& p, bool is_w, int64_t t,
+__device__ __forceinline__ void pair_issue(const PairArgs& p, bool is_w, uint32_t t,
                                            uint16_t (*tile)[128], int row, int l4,
                                            uint4 (&v)[4]) {
     if (is_w) {
-        const int64_t NB = p.N / 128;
-        const int64_t n0 = (t % NB) * 128, k0 = (t / NB) * 128;
+        const uint32_t NB = static_cast<uint32_t>(p.N / 128);
+        const size_t n0 = static_cast<size_t>(t % NB) * 128, k0 = static_cast<size_t>(t / NB) * 128;
         const int ch = threadIdx.x & 15;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
@@ -541,89 +652,86 @@ __device__ __forceinline__ void pair_issue(const PairArgs& p, bool is_w, int64_t
             cp_async16(&tile[r][ch * 8], p.w + (k0 + r) * p.ldw + n0 + ch * 8);
         }
     } else {
-        load_1x128(p.x, p.M, p.ldx, p.KB, t, row, l4, v);
+        const uint32_t KB = static_cast<uint32_t>(p.KB);
+        load_1x128(p.x, static_cast<uint32_t>(p.M), p.ldx, t % KB, (t / KB) * kQ1Rows + row, l4, v);
     }
 }
 
-// Converts the weight block t staged in `tile` (all 256 threads).  The
-// transposed codes are staged in the first 16 KB of `tile` once every
-// thread has read its values.  Ends with a barrier, after which `tile` and
-// `part` may be reused.
-__device__ __forceinline__ void pair_weight_block(const PairArgs& p, int64_t t,
+// Converts the weight block t staged in `tile` (all 256 threads).  Thread
+// (cp = t0 & 63, rq = t0 >> 6) reads the two columns n = 2cp, 2cp+1 over
+// the rows k = 32 rq .. 32 rq + 31 and converts each element once; its codes
+// then go to two staging areas over `tile` (the block is in registers by
+// then): [n][k] rows for wq, with 16-byte chunks XOR-swizzled by (n >> 1) & 7,
+// and [k][n] rows for wqT, two bytes per row.  Both leave as 16-byte rows
+// pieces.  Ends with a barrier, after which `tile` and `part` may be reused.
+__device__ __forceinline__ void pair_weight_block(const PairArgs& p, uint32_t t,
                                                   uint16_t (*tile)[128], float* part) {
     const int t0 = threadIdx.x;
     const int lane = t0 & 31, warp = t0 >> 5;
-    const int ch = t0 & 15;
-    const int64_t NB = p.N / 128, K = p.KB * 128;
-    const int64_t nb = t % NB, kb = t / NB;
-    const int64_t n0 = nb * 128, k0 = kb * 128;
+    const uint32_t NB = static_cast<uint32_t>(p.N / 128), KB = static_cast<uint32_t>(p.KB);
+    const uint32_t nb = t % NB, kb = t / NB;
+    const size_t n0 = static_cast<size_t>(nb) * 128, k0 = static_cast<size_t>(kb) * 128;
+    const size_t K = static_cast<size_t>(KB) * 128;
+    const int cp = t0 & 63, rq = t0 >> 6;
+    uint32_t w[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = *reinterpret_cast<const uint32_t*>(&tile[32 * rq + i][2 * cp]);
     uint32_t mx = 0;
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-        const uint4 u = *reinterpret_cast<const uint4*>(&tile[(t0 >> 4) + 16 * q][ch * 8]);
-        mx = absmax_bf16x2(mx, absmax_bf16x2(u.x, u.y));
-        mx = absmax_bf16x2(mx, absmax_bf16x2(u.z, u.w));
-    }
-    float amax = amax_of_pair(mx);
+    for (int i = 0; i < 32; ++i) mx = absmax_acc(mx, w[i]);
+    mx &= 0x7FFF7FFFu;
 #pragma unroll
-    for (int off = 16; off >= 1; off >>= 1)
-        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    if (lane == 0) part[warp] = amax;
-    __syncthreads();
-    amax = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
-                 fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
+    for (int off = 16; off >= 1; off >>= 1) mx = absmax_acc(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) part[warp] = amax_of_pair(mx);
+    __syncthreads();  // the block maxima are published and every value is in registers
+    const float amax = fmaxf(fmaxf(fmaxf(part[0], part[1]), fmaxf(part[2], part[3])),
+                             fmaxf(fmaxf(part[4], part[5]), fmaxf(part[6], part[7])));
     const float s = group_scale(amax);
-    const GroupDiv dv(s);
-    if (t0 == 0) p.sw[nb * p.KB + kb] = s;
-    if (p.wqT != nullptr) {
-#pragma unroll 4
-        for (int q = 0; q < 8; ++q) {
-            const int r = (t0 >> 4) + 16 * q;
-            const uint4 u = *reinterpret_cast<const uint4*>(&tile[r][ch * 8]);
-            uint2 o;
-            o.x = dv.quad_words(u.x, u.y);
-            o.y = dv.quad_words(u.z, u.w);
-            *reinterpret_cast<uint2*>(p.wqT + (k0 + r) * p.N + n0 + ch * 8) = o;
+    const NegDiv dv(s, __frcp_rn(s));
+    if (t0 == 0) p.sw[static_cast<size_t>(nb) * KB + kb] = s;
+    uint32_t A[8], B[8];  // column 2cp / 2cp+1: word m holds rows 32rq + 4m .. +3
+    if (s >= 0x1p-91f) {
+        codes_cols16<true>(dv, dv, w, 0x5410u, A, B);
+        codes_cols16<true>(dv, dv, w + 16, 0x5410u, A + 4, B + 4);
+    } else {
+        codes_cols16<false>(dv, dv, w, 0x5410u, A, B);
+        codes_cols16<false>(dv, dv, w + 16, 0x5410u, A + 4, B + 4);
+    }
+    uint8_t* cq = reinterpret_cast<uint8_t*>(tile);  // wq codes [128 n][128 k]
+    uint8_t* cqT = cq + 128 * 128;                     // wqT codes [128 k][128 n]
+    if (p.wq != nullptr) {
+        const int na = 2 * cp, nb2 = 2 * cp + 1;
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int c = 2 * rq + h;  // 16-byte chunk of the 128-byte k row
+            *reinterpret_cast<uint4*>(&cq[na * 128 + ((c ^ ((na >> 1) & 7)) << 4)]) =
+                make_uint4(A[4 * h], A[4 * h + 1], A[4 * h + 2], A[4 * h + 3]);
+            *reinterpret_cast<uint4*>(&cq[nb2 * 128 + ((c ^ ((nb2 >> 1) & 7)) << 4)]) =
+                make_uint4(B[4 * h], B[4 * h + 1], B[4 * h + 2], B[4 * h + 3]);
         }
     }
-    if (p.wq != nullptr) {
-        // columns 2cp, 2cp+1; rows rq*32 .. rq*32+31 in two chunks of 16
-        // k values; codes staged as [n][k] rows with 16-byte chunks
-        // XOR-swizzled by n & 7, then written out as 128-byte rows of wq.
-        const int cp = t0 & 63;
-        const int rq = t0 >> 6;
-        uint4 oc[2][2];
+    if (p.wqT != nullptr) {
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            uint32_t wv[16];
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-                wv[i] = *reinterpret_cast<const uint32_t*>(&tile[rq * 32 + h * 16 + i][2 * cp]);
-            uint4 o0, o1;
-            dv.quad_halves(wv[0], wv[1], wv[2], wv[3], o0.x, o1.x);
-            dv.quad_halves(wv[4], wv[5], wv[6], wv[7], o0.y, o1.y);
-            dv.quad_halves(wv[8], wv[9], wv[10], wv[11], o0.z, o1.z);
-            dv.quad_halves(wv[12], wv[13], wv[14], wv[15], o0.w, o1.w);
-            oc[h][0] = o0;
-            oc[h][1] = o1;
+        for (int m = 0; m < 8; ++m) {
+            const uint32_t lo = prmt(A[m], B[m], 0x5140u), hi = prmt(A[m], B[m], 0x7362u);
+            uint8_t* d = cqT + (32 * rq + 4 * m) * 128 + 2 * cp;
+            *reinterpret_cast<uint16_t*>(d) = static_cast<uint16_t>(lo);
+            *reinterpret_cast<uint16_t*>(d + 128) = static_cast<uint16_t>(lo >> 16);
+            *reinterpret_cast<uint16_t*>(d + 256) = static_cast<uint16_t>(hi);
+            *reinterpret_cast<uint16_t*>(d + 384) = static_cast<uint16_t>(hi >> 16);
         }
-        __syncthreads();  // every value of the block has been read
-        uint8_t* codes = reinterpret_cast<uint8_t*>(tile);
+    }
+    __syncthreads();
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int c = rq * 2 + h;  // 16-byte chunk of the 128-byte k row
-            const int n_a = 2 * cp, n_b = 2 * cp + 1;
-            *reinterpret_cast<uint4*>(&codes[n_a * 128 + ((c ^ (n_a & 7)) << 4)]) = oc[h][0];
-            *reinterpret_cast<uint4*>(&codes[n_b * 128 + ((c ^ (n_b & 7)) << 4)]) = oc[h][1];
-        }
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int j = t0 + kPairThreads * i;  // chunk j: row n = j / 8, chunk c = j % 8
-            const int n = j >> 3, c = j & 7;
-            const uint4 v = *reinterpret_cast<const uint4*>(&codes[n * 128 + ((c ^ (n & 7)) << 4)]);
-            *reinterpret_cast<uint4*>(p.wq + (n0 + n) * K + k0 + c * 16) = v;
-        }
+    for (int i = 0; i < 4; ++i) {
+        const int j = t0 + kPairThreads * i;  // chunk j: row j / 8, chunk j % 8
+        const int r = j >> 3, c = j & 7;
+        if (p.wq != nullptr)
+            *reinterpret_cast<uint4*>(p.wq + (n0 + r) * K + k0 + c * 16) =
+                *reinterpret_cast<const uint4*>(&cq[r * 128 + ((c ^ ((r >> 1) & 7)) << 4)]);
+        if (p.wqT != nullptr)
+            *reinterpret_cast<uint4*>(p.wqT + (k0 + r) * static_cast<size_t>(p.N) + n0 + c * 16) =
+                *reinterpret_cast<const uint4*>(&cqT[r * 128 + c * 16]);
     }
     __syncthreads();
 }
@@ -635,11 +743,12 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm) quant_fprop_pair
     uint16_t (*tiles)[128][128] = reinterpret_cast<uint16_t (*)[128][128]>(pair_smem);
     const int l4 = threadIdx.x & 3;
     const int row = threadIdx.x >> 2;  // 0..63
-    const int64_t total = p.w_tiles + p.act_tiles;
-    int64_t i = blockIdx.x;  // item; the same in every thread of the CTA
+    const uint32_t total = static_cast<uint32_t>(p.w_tiles + p.act_tiles);
+    const uint32_t KB = static_cast<uint32_t>(p.KB);
+    uint32_t i = blockIdx.x;  // item; the same in every thread of the CTA
     int buf = 0;
     uint4 v[4];
-    int64_t idx = 0;
+    uint32_t idx = 0;
     bool is_w = false;
     if (i < total) {
         is_w = pair_item(p, i, &idx);
@@ -647,9 +756,9 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm) quant_fprop_pair
     }
     cp_async_commit();
     while (i < total) {
-        const int64_t in = i + gridDim.x;
+        const uint32_t in = i + gridDim.x;
         uint4 vn[4];
-        int64_t idx_n = 0;
+        uint32_t idx_n = 0;
         bool is_w_n = false;
         if (in < total) {
             is_w_n = pair_item(p, in, &idx_n);
@@ -661,7 +770,8 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm) quant_fprop_pair
             __syncthreads();
             pair_weight_block(p, idx, tiles[buf], part);
         } else {
-            quant_1x128_tile(p.M, p.KB, p.xq, p.ldq, p.sx, idx, row, l4, v);
+            quant_1x128_group(static_cast<uint32_t>(p.M), p.xq, p.ldq, p.sx, idx % KB,
+                              (idx / KB) * kQ1Rows + row, l4, v);
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) v[k] = vn[k];
@@ -675,21 +785,29 @@ __global__ void __launch_bounds__(kPairThreads, kPairCtasPerSm) quant_fprop_pair
 
 // Persistent grid: as many CTAs as can be resident at once (cached per
 // kernel and device), never more than there are tiles.
+// Persistent grid: as many CTAs as are resident (at most kQuantCtasPerSm per
+// SM), never more than there are tiles.  A kernel with dynamic shared memory
+// gets its size limit raised here, once per context; 0 if that fails.
 template <auto kern>
-static int64_t quant_grid(int64_t tiles) {
+static int64_t quant_grid(int64_t tiles, int smem = 0) {
     static ContextCache<int> per_sm;
     const int sms = sm_count_current();
     int n = 0;
-    if (sms <= 0 || per_sm.get(&n, [](int* v) {
-            int b = 0;
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, kQuantThreads, 0) !=
-                    cudaSuccess ||
-                b <= 0)
-                b = 1;
-            *v = b < kQuantCtasPerSm ? b : kQuantCtasPerSm;
-            return static_cast<int>(FP8_OK);
-        }) != FP8_OK)
+    const int st = sms <= 0 ? static_cast<int>(FP8_ERR_CUDA) : per_sm.get(&n, [smem](int* v) {
+        if (smem > 0 &&
+            cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+            return static_cast<int>(FP8_ERR_CUDA);
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, kern, kQuantThreads, smem) != cudaSuccess ||
+            b <= 0)
+            b = 1;
+        *v = b < kQuantCtasPerSm ? b : kQuantCtasPerSm;
+        return static_cast<int>(FP8_OK);
+    });
+    if (st != FP8_OK) {
+        if (smem > 0) return 0;
         return tiles < 1024 ? tiles : 1024;
+    }
     const int64_t cap = static_cast<int64_t>(sms) * n;
     return tiles < cap ? tiles : cap;
 }
@@ -706,9 +824,11 @@ extern "C" fp8_status fp8_quant_act_1x128(const void* x, int64_t M, int64_t K, i
     if (ldx % 8 != 0 || ldq % 16 != 0 || !aligned(x, 16) || !aligned(xq, 16) || !aligned(sx, 4))
         return FP8_ERR_ALIGN;
     const int64_t tiles = ((M + kQ1Rows - 1) / kQ1Rows) * (K / 128);
+    if (M > 0x7fffffffLL || tiles > 0x7fffffffLL) return FP8_ERR_UNSUPPORTED;  // 32-bit tile walk
     quant_act_1x128_kernel<<<static_cast<unsigned>(quant_grid<quant_act_1x128_kernel>(tiles)), kQuantThreads, 0,
                              static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(x), M, K / 128, ldx, xq, ldq, sx, tiles);
+        static_cast<const uint16_t*>(x), static_cast<uint32_t>(M), static_cast<uint32_t>(K / 128), ldx, xq,
+        ldq, sx, static_cast<uint32_t>(tiles));
     return to_status(launch_status());
 }
 
@@ -764,10 +884,22 @@ extern "C" fp8_status fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, i
     if (x == nullptr || xqT == nullptr || sxT == nullptr) return FP8_ERR_NULL;
     if (ldx % 8 != 0 || !aligned(x, 16) || !aligned(xqT, 16) || !aligned(sxT, 4))
         return FP8_ERR_ALIGN;
+    // 32-bit tile walk and TMA coordinates
     const int64_t tiles = (M / 128) * (K / 64);
-    quant_act_128x1_kernel<<<static_cast<unsigned>(quant_grid<quant_act_128x1_kernel>(tiles)), kQuantThreads, 0,
+    if (M > 0x7fffffffLL || K > 0x7fffffffLL || tiles > 0x7fffffffLL) return FP8_ERR_UNSUPPORTED;
+    unsigned* err = device_error_word();
+    if (err == nullptr) return FP8_ERR_CUDA;
+    CUtensorMap xmap;
+    if (make_map(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(K),
+                 static_cast<uint64_t>(M), static_cast<uint64_t>(ldx) * 2, 64, 128,
+                 CU_TENSOR_MAP_SWIZZLE_128B) != FP8_OK)
+        return FP8_ERR_CUDA;
+    const int64_t grid = quant_grid<quant_act_128x1_kernel>(tiles, kQ128x1Smem);
+    if (grid <= 0) return FP8_ERR_CUDA;
+    quant_act_128x1_kernel<<<static_cast<unsigned>(grid), kQuantThreads, kQ128x1Smem,
                              static_cast<cudaStream_t>(stream)>>>(
-        static_cast<const uint16_t*>(x), M, K, ldx, xqT, sxT, tiles);
+        xmap, static_cast<uint32_t>(M), static_cast<uint32_t>(K), xqT, sxT,
+        static_cast<uint32_t>(tiles), err);
     return to_status(launch_status());
 }
 
@@ -800,6 +932,12 @@ extern "C" fp8_status fp8_quant_act_128x1_grouped(const void* x, int64_t T, int6
 static int launch_pair(const PairArgs& p, cudaStream_t stream) {
     const int64_t total = p.act_tiles + p.w_tiles;
     if (total == 0) return FP8_OK;
+    // 32-bit item walk and row indices
+    if (total > 0x7fffffffLL || p.M > 0x7fffffffLL || p.N / 128 > 0x7fffffffLL || p.KB > 0x7fffffffLL)
+        return FP8_ERR_UNSUPPORTED;
+    PairArgs q = p;
+    q.w_frac = ((static_cast<uint64_t>(p.w_tiles) << 32) + static_cast<uint64_t>(total) - 1) /
+               static_cast<uint64_t>(total);
     static ContextCache<int> per_sm;
     const int sms = sm_count_current();
     if (sms <= 0) return FP8_ERR_CUDA;
@@ -821,7 +959,7 @@ static int launch_pair(const PairArgs& p, cudaStream_t stream) {
     if (st != FP8_OK) return st;
     const int64_t cap = static_cast<int64_t>(sms) * n;
     const int64_t grid = total < cap ? total : cap;
-    quant_fprop_pair_kernel<<<static_cast<unsigned>(grid), kPairThreads, kPairSmem, stream>>>(p);
+    quant_fprop_pair_kernel<<<static_cast<unsigned>(grid), kPairThreads, kPairSmem, stream>>>(q);
     return launch_status();
 }
 

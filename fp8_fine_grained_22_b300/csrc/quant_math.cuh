@@ -66,6 +66,12 @@ struct GroupDiv {
         ns2 = f2x2(-scale, -scale);
         fast = scale >= fast_min;
     }
+    // From a scale and its reciprocal computed elsewhere (r = RN(1 / scale)).
+    __device__ __forceinline__ GroupDiv(float scale, float r, float fast_min) : s(scale) {
+        r2 = f2x2(r, r);
+        ns2 = f2x2(-scale, -scale);
+        fast = scale >= fast_min;
+    }
     // Correctly rounded quotients x0 / s, x1 / s (a zero may carry either sign).
     __device__ __forceinline__ void quot2(float x0, float x1, float& q0, float& q1) const {
         if (fast) {
@@ -148,7 +154,6 @@ struct GroupDiv {
     }
 
   private:
-
     __device__ __forceinline__ static uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
         uint32_t d;
         asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
@@ -160,6 +165,60 @@ struct GroupDiv {
         return byte_perm(w0, w1, 0xFDB9);
     }
 };
+
+// ------------------------------------------------ negated-quotient codes --
+// The streaming quantisers compute codes of the negated quotient and flip
+// the sign bits afterwards.  With r = RN(1/s) and nr = -r:
+//   a = RN(x nr) = -RN(x r),  e = RN(x + a s) = x - RN(x r) s (exact, as in
+//   Markstein's correction above),  RN(e nr + a) = -RN(x / s),
+// so the same three operations give the negated correctly rounded quotient,
+// and a zero x gives a zero of the opposite sign (+0 + -0 rounds to +0 at
+// the last step).  The E4M3 conversion is odd (RNE and saturation treat both
+// signs alike), so code(x / s) = code(-(x / s)) ^ 0x80 for every finite x,
+// signed zeros included, with no per-element sign repair.  The slow path
+// (scales below the fast-path threshold) divides by -s in IEEE arithmetic,
+// which is the same negated quotient.
+struct NegDiv {
+    uint64_t nr2, s2;
+    float ns;
+    __device__ __forceinline__ NegDiv(float scale, float r)
+        : nr2(f2x2(-r, -r)), s2(f2x2(scale, scale)), ns(-scale) {}
+    // Codes of -(x0 / s), -(x1 / s) (x0 in the low half of x2) in the low
+    // two bytes, x0's first.
+    template <bool FAST>
+    __device__ __forceinline__ uint32_t ncodes2(uint64_t x2) const {
+        uint64_t q;
+        if (FAST) {
+            const uint64_t a = mul2(x2, nr2);
+            const uint64_t e = fma2(a, s2, x2);
+            q = fma2(e, nr2, a);
+        } else {
+            q = f2x2(__fdiv_rn(__uint_as_float(static_cast<uint32_t>(x2)), ns),
+                     __fdiv_rn(__uint_as_float(static_cast<uint32_t>(x2 >> 32)), ns));
+        }
+        return static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(
+            make_float2(__uint_as_float(static_cast<uint32_t>(q)), __uint_as_float(static_cast<uint32_t>(q >> 32))),
+            __NV_SATFINITE, __NV_E4M3));
+    }
+};
+constexpr uint32_t kSignFlip4 = 0x80808080u;
+
+// The two bf16 values of a word as a packed FP32 pair (low half first).
+__device__ __forceinline__ uint64_t bf16x2_to_f2(uint32_t w) {
+    return f2x2(bf16_lo(w), bf16_hi(w));
+}
+// The low (or high) halves of two words as a packed FP32 pair, w0's first.
+__device__ __forceinline__ uint64_t bf16_lo2(uint32_t w0, uint32_t w1) {
+    return f2x2(bf16_lo(w0), bf16_lo(w1));
+}
+__device__ __forceinline__ uint64_t bf16_hi2(uint32_t w0, uint32_t w1) {
+    return f2x2(bf16_hi(w0), bf16_hi(w1));
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
 
 // ---------------------------------------------------- power-of-two scales --
 // The smallest e with amax <= 448 * 2^e, clamped to the UE8M0 range
@@ -223,6 +282,15 @@ __device__ __forceinline__ uint32_t absmax_bf16x2(uint32_t a, uint32_t b) {
     const __nv_bfloat162 r = __hmax2(__habs2(*reinterpret_cast<const __nv_bfloat162*>(&a)),
                                      __habs2(*reinterpret_cast<const __nv_bfloat162*>(&b)));
     return *reinterpret_cast<const uint32_t*>(&r);
+}
+// Running maximum of magnitudes over words of bf16 pairs, one instruction a
+// word: max.xorsign.abs gives max(|a|, |b|) per half with the XOR of the
+// signs, so the magnitudes are exact and the sign bits meaningless until
+// masked with 0x7FFF7FFF.
+__device__ __forceinline__ uint32_t absmax_acc(uint32_t acc, uint32_t w) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(acc), "r"(w));
+    return d;
 }
 __device__ __forceinline__ float amax_of_pair(uint32_t w) {
     return fmaxf(bf16_lo(w), bf16_hi(w));  // both halves already non-negative
