@@ -750,7 +750,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const float* sa_g = p.sa + static_cast<int64_t>(kbo) * lds_a + (row_in_alloc ? row : 0);
             const float* sb_g = nullptr;
             int sb_gstep = 0;
-            float sa_next = 0.0f, sb_next = 0.0f;
+            // scales of K blocks kb+1 and kb+2 (loaded two blocks ahead)
+            float sa_next = 0.0f, sb_next = 0.0f, sa_next2 = 0.0f, sb_next2 = 0.0f;
             if constexpr (!kRing) {
                 const int nb = ncol0 / 128;
                 const bool blk = p.bmode == FP8_BSCALE_BLOCK128;
@@ -761,6 +762,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (nkb > 0) {
                     sa_next = row_in_alloc ? __ldg(sa_g) : 0.0f;
                     sb_next = __ldg(sb_g);
+                }
+                if (nkb > 1) {
+                    sa_next2 = row_in_alloc ? __ldg(sa_g + lds_a) : 0.0f;
+                    sb_next2 = __ldg(sb_g + sb_gstep);
                 }
             }
 
@@ -773,9 +778,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t buf = kbg % NBUF, tph = (kbg / NBUF) & 1u;
                 float sa_cur = sa_next, sb_cur = sb_next;
                 if constexpr (!kRing) {
-                    if (kb + 1 < nkb) {
-                        sa_next = row_in_alloc ? __ldg(sa_g + (kb + 1) * lds_a) : 0.0f;
-                        sb_next = __ldg(sb_g + (kb + 1) * sb_gstep);
+                    sa_next = sa_next2;
+                    sb_next = sb_next2;
+                    if (kb + 2 < nkb) {
+                        sa_next2 = row_in_alloc ? __ldg(sa_g + (kb + 2) * lds_a) : 0.0f;
+                        sb_next2 = __ldg(sb_g + (kb + 2) * sb_gstep);
                     }
                 }
                 if ((kRing && !wait_bar_warp(sfull_bar(r), (kbg / SR) & 1u, abort_flag)) ||

@@ -64,6 +64,10 @@ def _compare(out, aq, sa, bq, sb, offsets, rows, bmode=oracle.BSCALE_BLOCK128):
 @pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("counts", [[3, 0, 130, 1], [0, 0, 1], [128, 256, 127, 129, 5],
                                     [0, 300, 0],
+                                    # fewer than 192 rows per expert on average: one CTA
+                                    # per 128-row tile, experts ending on and around
+                                    # tile edges and one spanning three tiles
+                                    [16, 17, 33, 64, 65, 255, 257],
                                     # 192+ rows per expert on average, N = 256: CTA pairs
                                     # over 256-row blocks (ragged second halves, a
                                     # one-row expert, an empty one)
