@@ -2,18 +2,20 @@
 """Benchmark of the fine-grained FP8 hot path on one (or N independent) B300s.
 
 One step = one pass of the path over the training trio of an expert MLP
-(hidden 7168, intermediate 4096, 8192 tokens; BF16 inputs drawn seeded):
-  1. X [8192, 7168] 1x128                         (fp8_quant_act_1x128)
+(hidden 7168, intermediate 4096, 8192 tokens; BF16 inputs drawn seeded), six
+launches:
+  1. X [8192, 7168] 1x128, and 128x1 transposed for the Wgrad
+                                                  (fp8_quant_act_dual: one read of X)
   2. W [7168, 4096] 128x128, both orientations    (fp8_quant_weight_128x128)
-  3. dY [8192, 4096] 1x128                        (fp8_quant_act_1x128)
-  4. X and dY 128x1, transposed, for the Wgrad    (fp8_quant_act_128x1, twice)
-  5. Fprop  Y  = X . W          -> BF16 [8192, 4096]   (fp8_gemm_blockscaled)
-  6. Dgrad  dX = dY . W^T       -> BF16 [8192, 7168]   (transposed block scales)
-  7. Wgrad  dW = X^T . dY       -> FP32 [7168, 4096]   (per-row B scales)
+  3. dY [8192, 4096] 1x128 and 128x1              (fp8_quant_act_dual)
+  4. Fprop  Y  = X . W          -> BF16 [8192, 4096]   (fp8_gemm_blockscaled)
+  5. Dgrad  dX = dY . W^T       -> BF16 [8192, 7168]   (transposed block scales)
+  6. Wgrad  dW = X^T . dY       -> FP32 [7168, 4096]   (per-row B scales)
 (the GEMMs get the split-K workspace; of the three only the Wgrad's short last
 wave is split)
-(The one-launch form of steps 1-2, fp8_quant_fprop_operands, is timed among
-the quantisers in `configs`; as two launches they measured faster.)
+(The separate quantisers -- fp8_quant_act_1x128, fp8_quant_act_128x1 -- and the
+one-launch operand form fp8_quant_fprop_operands are timed among the
+quantisers in `configs`.)
 The metric is the step's FP8 GEMM throughput: 3 * 2 * 8192 * 7168 * 4096
 FLOP / step time (TFLOP/s).  The JSON line also carries each kernel's time in
 the step, the roofline of the kernel that takes the most time, an end-to-end
@@ -408,6 +410,11 @@ def q128x1_bytes(M, K):
     return M * K * 3 + (M // 128) * K * 4
 
 
+def qdual_bytes(M, K):
+    """fp8_quant_act_dual: the input read once, both codes and both scale sets written."""
+    return M * K * 4 + (K // 128) * M * 4 + (M // 128) * K * 4
+
+
 def q128x128_bytes(K, N, both):
     return K * N * (2 + (2 if both else 1)) + (K // 128) * (N // 128) * 4
 
@@ -418,7 +425,7 @@ def gemm_bytes(M, N, K, out_elt, a_scales, b_scales):
 
 # -------------------------------------------------------------- the trio --
 class Trio:
-    """Device buffers of the training trio and its seven launches."""
+    """Device buffers of the training trio and its six launches."""
 
     def __init__(self, d: Dev, wl):
         from fp8_fine_grained_22_b300 import fp8fg
@@ -443,11 +450,15 @@ class Trio:
         self.ws = torch.zeros(fp8fg.fp8_gemm_blockscaled_workspace_size(), dtype=torch.uint8,
                               device=dev)
 
-    NAMES = ("fp8_quant_act_1x128 (X)", "fp8_quant_weight_128x128 (W, wq and wqT)",
-             "fp8_quant_act_1x128 (dY)", "fp8_quant_act_128x1 (X)", "fp8_quant_act_128x1 (dY)",
+    NAMES = ("fp8_quant_act_dual (X: 1x128 and 128x1)", "fp8_quant_weight_128x128 (W, wq and wqT)",
+             "fp8_quant_act_dual (dY: 1x128 and 128x1)",
              "fp8_gemm_blockscaled Fprop", "fp8_gemm_blockscaled Dgrad",
              "fp8_gemm_blockscaled Wgrad")
-    N_QUANT = 5  # launches before the GEMMs
+    N_QUANT = 3  # launches before the GEMMs
+    QUANT_TRAFFIC = ("quant_act_dual_m8192_k7168", "quant_weight_128x128_k7168_n4096",
+                     "quant_act_dual_m8192_k4096")
+    GEMM_TRAFFIC = ("gemm_fprop_m8192_n4096_k7168", "gemm_dgrad_m8192_n7168_k4096",
+                    "gemm_wgrad_m7168_n4096_k8192")
 
     def launches(self, x=None, w=None, dy=None, y=None, dx=None, dw=None):
         f, s = self.fp8fg, self.d.stream
@@ -458,11 +469,9 @@ class Trio:
         dx = self.dx if dx is None else dx
         dw = self.dw if dw is None else dw
         return [
-            lambda: f.fp8_quant_act_1x128(x, self.xq, self.sx, stream=s),
+            lambda: f.fp8_quant_act_dual(x, self.xq, self.sx, self.xqT, self.sxT, stream=s),
             lambda: f.fp8_quant_weight_128x128(w, wq=self.wq, wqT=self.wqT, sw=self.sw, stream=s),
-            lambda: f.fp8_quant_act_1x128(dy, self.dyq, self.sdy, stream=s),
-            lambda: f.fp8_quant_act_128x1(x, self.xqT, self.sxT, stream=s),
-            lambda: f.fp8_quant_act_128x1(dy, self.dyqT, self.sdyT, stream=s),
+            lambda: f.fp8_quant_act_dual(dy, self.dyq, self.sdy, self.dyqT, self.sdyT, stream=s),
             lambda: f.fp8_gemm_blockscaled(self.xq, self.sx, self.wq, self.sw,
                                            bmode=f.FP8_BSCALE_BLOCK128,
                                            out_dtype=torch.bfloat16, c=y, stream=s,
@@ -489,8 +498,7 @@ class Trio:
         """Algorithmic work of launch i of the step, its rate and roofline fraction."""
         M, K, N = self.M, self.K, self.N
         if i < self.N_QUANT:
-            nbytes = [q1x128_bytes(M, K), q128x128_bytes(K, N, True), q1x128_bytes(M, N),
-                      q128x1_bytes(M, K), q128x1_bytes(M, N)][i]
+            nbytes = [qdual_bytes(M, K), q128x128_bytes(K, N, True), qdual_bytes(M, N)][i]
             g = gbs(nbytes, ms)
             return {"ms": round(ms, 5), "bound": "hbm", "algorithmic_bytes": nbytes,
                     "gbs": round(g, 1), "frac_hbm": round(g / peaks["hbm"], 4)}
@@ -518,7 +526,7 @@ def run_trio(args, rank, world, local):
         raise RuntimeError("device-side error during warm-up")
 
     nk = len(Trio.NAMES)
-    # The step as a CUDA graph of its eight launches, and a second graph of
+    # The step as a CUDA graph of its six launches, and a second graph of
     # the same launches with an event before each and after the last: the
     # per-kernel times.  Events between the kernels cost the programmatic
     # overlap of each GEMM's set-up with the kernel before it, so the step
@@ -558,13 +566,10 @@ def run_trio(args, rank, world, local):
     dk = kernels[Trio.NAMES[dom]]
     if dk["bound"] == "tensor":
         achieved, peak, unit = dk["tflops"], peaks["fp8_from_bf16"], "TFLOP/s"
-        traffic_key = ["", "", "", "", "", "gemm_fprop_m8192_n4096_k7168",
-                       "gemm_dgrad_m8192_n7168_k4096", "gemm_wgrad_m7168_n4096_k8192"][dom]
+        traffic_key = Trio.GEMM_TRAFFIC[dom - Trio.N_QUANT]
     else:
         achieved, peak, unit = dk["gbs"], peaks["hbm"], "GB/s"
-        traffic_key = ["quant_act_1x128_m8192_k7168", "quant_weight_128x128_k7168_n4096",
-                       "quant_act_1x128_m8192_k4096", "quant_act_128x1_m8192_k7168",
-                       "quant_act_128x1_m8192_k4096"][dom]
+        traffic_key = Trio.QUANT_TRAFFIC[dom]
     roofline = {"kernel": Trio.NAMES[dom], "bound": dk["bound"], "achieved": achieved,
                 "peak": peak, "unit": unit, "frac": round(achieved / peak, 4),
                 "peak_source": peaks["fp8_from_bf16_source"] if unit == "TFLOP/s"
@@ -609,7 +614,7 @@ def run_trio(args, rank, world, local):
                    "l2": "flushed between steps (%d MB written, then read back); the step's "
                          "operands (~0.8 GB) are larger than L2" % (2 * L2_BYTES >> 20),
                    "step": list(Trio.NAMES),
-                   "timing": "each timed step replays a CUDA graph of the step's eight launches "
+                   "timing": "each timed step replays a CUDA graph of the step's six launches "
                              "between two events (ms_per_step), then, L2 flushed again, a graph "
                              "of the same launches with an event between kernels (kernels, "
                              "roofline; ms_per_step_instrumented)"},
@@ -930,6 +935,12 @@ def quantisers(d, peaks, tr, moe):
     add("128x128 W[7168,4096] wq+wqT",
         lambda: fp8fg.fp8_quant_weight_128x128(tr.w, wq=tr.wq, wqT=tr.wqT, sw=tr.sw, stream=s),
         q128x128_bytes(K, N, True))
+    add("1x128 + 128x1 X[8192,7168] in one launch (fp8_quant_act_dual)",
+        lambda: fp8fg.fp8_quant_act_dual(tr.x, tr.xq, tr.sx, tr.xqT, tr.sxT, stream=s),
+        qdual_bytes(M, K))
+    add("1x128 + 128x1 dY[8192,4096] in one launch (fp8_quant_act_dual)",
+        lambda: fp8fg.fp8_quant_act_dual(tr.dy, tr.dyq, tr.sdy, tr.dyqT, tr.sdyT, stream=s),
+        qdual_bytes(M, N))
     add("operands X 1x128 + W 128x128 wq+wqT (trio)",
         lambda: fp8fg.fp8_quant_fprop_operands(tr.x, tr.w, xq=tr.xq, sx=tr.sx, wq=tr.wq,
                                                wqT=tr.wqT, sw=tr.sw, stream=s),

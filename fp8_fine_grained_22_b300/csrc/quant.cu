@@ -480,6 +480,182 @@ __global__ void __launch_bounds__(kQuantThreads) quant_act_128x1_kernel(
     }
 }
 
+// ------------------------------------------------------- 1x128 and 128x1 --
+// Both quantisations of one activation from a single read of it (the Fprop
+// operand and the transposed Wgrad operand of the same X or dY).  Tiles of
+// 128 tokens x 128 columns arrive by TMA as two 64-column boxes with the
+// 128-byte swizzle, in a two-slot ring.  Per tile:
+// - 128x1: every warp does, for each 64-column half, what a warp of
+//   quant_act_128x1_kernel does with its tile (column chunk w, XOR row order);
+// - 1x128: the thread pair (2r, 2r+1) takes row r's 128-wide group, one half
+//   each.  The odd thread walks its chunks in the order j ^ 4, so the pair's
+//   reads of one row fall on different bank groups;
+// - the last warp to finish with the slot issues its next two loads.
+// Codes and scales are those of fp8_quant_act_1x128 and fp8_quant_act_128x1,
+// bit for bit (the same per-group arithmetic).
+constexpr int kQDualStages = 2;
+constexpr int kQDualHalfBytes = 128 * 64 * 2;
+constexpr int kQDualTileBytes = 2 * kQDualHalfBytes;
+constexpr int kQDualSmem = 1024 + kQDualStages * (kQDualTileBytes + 16) + 16;
+
+__global__ void __launch_bounds__(kQuantThreads) quant_act_dual_kernel(
+    const __grid_constant__ CUtensorMap xmap, uint32_t M, uint32_t K, uint8_t* __restrict__ xq,
+    int64_t ldq, float* __restrict__ sx, uint8_t* __restrict__ xqT, float* __restrict__ sxT,
+    uint32_t tiles, unsigned* err_word) {
+    griddep_launch_dependents();  // the GEMM that follows may set up meanwhile
+    constexpr int S = kQDualStages;
+    extern __shared__ __align__(16) uint8_t smem_qd[];
+    uint8_t* ring = smem_qd + ((1024u - (smem_addr(smem_qd) & 1023u)) & 1023u);
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + S * kQDualTileBytes);
+    uint32_t* done = reinterpret_cast<uint32_t*>(full + S);  // warps done reading, per slot
+    uint32_t* issued = done + S;                              // loads issued, per slot
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(issued + S);
+    const int t0 = threadIdx.x, warp = t0 >> 5, lane = t0 & 31;
+    const int cp = lane & 3, g = lane >> 2;
+    const uint32_t KC = K / 128;
+    const uint32_t step = gridDim.x;
+    auto issue = [&](uint32_t tt, int s) {
+        const uint32_t bar = smem_addr(&full[s]);
+        const uint32_t dst = smem_addr(ring + s * kQDualTileBytes);
+        const int kx = static_cast<int>((tt % KC) * 128), my = static_cast<int>((tt / KC) * 128);
+        mbar_arrive_expect_tx(bar, kQDualTileBytes);
+        tma_load_2d(dst, &xmap, bar, kx, my);
+        tma_load_2d(dst + kQDualHalfBytes, &xmap, bar, kx + 64, my);
+        atomicAdd(&issued[s], 1u);
+    };
+    if (t0 == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(smem_addr(&full[s]), 1);
+            done[s] = 0;
+            issued[s] = 0;
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&xmap);
+        for (int s = 0; s < S; ++s)
+            if (blockIdx.x + s * step < tiles) issue(blockIdx.x + s * step, s);
+    }
+    __syncthreads();
+    // 128x1 part: this lane's word offsets in a 64-column half, packing
+    // selector and word order, as in quant_act_128x1_kernel
+    uint32_t off[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int u = j ^ g;
+        off[j] = 2048 * g + 128 * u + 16 * (warp ^ u) + 4 * cp;
+    }
+    uint32_t sel = 0;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const int t = b ^ (g & 3);
+        sel |= static_cast<uint32_t>((t & 1) | ((t >> 1) << 2)) << (4 * b);
+    }
+    const bool swap_words = (g & 4) != 0;
+    // 1x128 part: row r, half h; chunk j of the half read in the order j ^ 4h
+    const int r1 = t0 >> 1, h1 = t0 & 1;
+    const uint32_t step_q = step / KC, step_r = step % KC;
+    uint32_t kc = blockIdx.x % KC, mb = blockIdx.x / KC;
+    uint32_t it = 0;
+    uint32_t t = blockIdx.x;
+    for (; t < tiles; t += step, ++it) {
+        const int s = static_cast<int>(it % S);
+        if (!wait_bounded_warp(smem_addr(&full[s]), (it / S) & 1u, abort_flag, err_word)) break;
+        const uint8_t* slot = ring + s * kQDualTileBytes;
+        // ---- 128x1: both halves
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+            const uint8_t* half = slot + h * kQDualHalfBytes;
+            uint32_t w[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                w[i] = *reinterpret_cast<const uint32_t*>(half + off[i & 7] + 128 * (i & 8));
+            uint32_t mx = 0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) mx = absmax_acc(mx, w[i]);
+            mx &= 0x7FFF7FFFu;
+            mx = absmax_acc(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = absmax_acc(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = absmax_acc(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const int c8 = lane & 7;
+            const uint32_t m2 = __shfl_sync(0xffffffffu, mx, c8 >> 1);
+            const float sc = group_scale((c8 & 1) ? bf16_hi(m2) : bf16_lo(m2));
+            const float rc = __frcp_rn(sc);
+            const uint32_t k0 = kc * 128 + 64 * h + 8 * warp;
+            if (lane < 8) sxT[static_cast<size_t>(mb) * K + k0 + lane] = sc;
+            const float sa = __shfl_sync(0xffffffffu, sc, 2 * cp), ra = __shfl_sync(0xffffffffu, rc, 2 * cp);
+            const float sb = __shfl_sync(0xffffffffu, sc, 2 * cp + 1), rb = __shfl_sync(0xffffffffu, rc, 2 * cp + 1);
+            const NegDiv da(sa, ra), db(sb, rb);
+            uint32_t oa[4], ob[4];
+            if (sa >= 0x1p-91f && sb >= 0x1p-91f)
+                codes_cols16<true>(da, db, w, sel, oa, ob);
+            else
+                codes_cols16<false>(da, db, w, sel, oa, ob);
+            const uint4 va = swap_words ? make_uint4(oa[1], oa[0], oa[3], oa[2]) : make_uint4(oa[0], oa[1], oa[2], oa[3]);
+            const uint4 vb = swap_words ? make_uint4(ob[1], ob[0], ob[3], ob[2]) : make_uint4(ob[0], ob[1], ob[2], ob[3]);
+            uint8_t* dst = xqT + static_cast<size_t>(k0 + 2 * cp) * M + mb * 128 + 16 * g;
+            *reinterpret_cast<uint4*>(dst) = va;
+            *reinterpret_cast<uint4*>(dst + M) = vb;
+        }
+        // ---- 1x128: row r1's group, half h1
+        {
+            const uint8_t* rowp = slot + h1 * kQDualHalfBytes + r1 * 128;
+            uint4 v[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[j] = *reinterpret_cast<const uint4*>(rowp + (((j ^ (4 * h1)) ^ (r1 & 7)) << 4));
+            uint32_t mx = 0;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                mx = absmax_acc(mx, v[j].x);
+                mx = absmax_acc(mx, v[j].y);
+                mx = absmax_acc(mx, v[j].z);
+                mx = absmax_acc(mx, v[j].w);
+            }
+            mx &= 0x7FFF7FFFu;
+            mx = absmax_acc(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            const float sc = group_scale(amax_of_pair(mx));
+            const NegDiv dv(sc, __frcp_rn(sc));
+            const uint32_t m = mb * 128 + r1;
+            // v[2i], v[2i+1] hold chunks 2i ^ 4h1 and its successor: 16 codes
+            // for bytes 16 (i ^ 2h1) .. of this half of the row
+            uint8_t* dst = xq + static_cast<size_t>(m) * ldq + kc * 128 + 64 * h1;
+            if (sc >= 0x1p-91f) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<uint4*>(dst + 16 * (i ^ (2 * h1))) = codes_1x128<true>(dv, v[2 * i], v[2 * i + 1]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    *reinterpret_cast<uint4*>(dst + 16 * (i ^ (2 * h1))) = codes_1x128<false>(dv, v[2 * i], v[2 * i + 1]);
+            }
+            if (h1 == 0) sx[static_cast<size_t>(kc) * M + m] = sc;
+        }
+        // the last warp to finish with the slot refills it
+        __syncwarp();
+        if (lane == 0) {
+            __threadfence_block();
+            const uint32_t prev = atomicAdd(&done[s], 1u);
+            const uint32_t tn = t + S * step;
+            if (prev == 8u * (it / S) + 7u && tn < tiles) issue(tn, s);
+        }
+        kc += step_r;
+        mb += step_q;
+        if (kc >= KC) {
+            kc -= KC;
+            ++mb;
+        }
+    }
+    // A timed-out wait ends the loop early: a load still in flight into a
+    // slot (at most one per slot) must land before the CTA releases the ring.
+    __syncthreads();
+    if (t0 == 0 && *abort_flag) {
+        for (int s = 0; s < S; ++s) {
+            const uint32_t n = *reinterpret_cast<volatile uint32_t*>(&issued[s]);
+            if (n > 0) drain_load(smem_addr(&full[s]), (n - 1) & 1u);
+        }
+    }
+}
+
 // ---------------------------------------------------- 128x1, per expert --
 // The 128x1 grouping for a grouped Wgrad GEMM, whose contraction runs over
 // each expert's own tokens: expert e's rows offsets[e] .. offsets[e+1]-1 of
@@ -899,6 +1075,34 @@ extern "C" fp8_status fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, i
     quant_act_128x1_kernel<<<static_cast<unsigned>(grid), kQuantThreads, kQ128x1Smem,
                              static_cast<cudaStream_t>(stream)>>>(
         xmap, static_cast<uint32_t>(M), static_cast<uint32_t>(K), xqT, sxT,
+        static_cast<uint32_t>(tiles), err);
+    return to_status(launch_status());
+}
+
+extern "C" fp8_status fp8_quant_act_dual(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
+                                         int64_t ldq, float* sx, uint8_t* xqT, float* sxT, void* stream) {
+    if (M < 0 || M % 128 != 0 || K <= 0 || K % 128 != 0 || ldx < K || ldq < K) return FP8_ERR_SHAPE;
+    if (M == 0) return FP8_OK;
+    if (x == nullptr || xq == nullptr || sx == nullptr || xqT == nullptr || sxT == nullptr)
+        return FP8_ERR_NULL;
+    if (ldx % 8 != 0 || ldq % 16 != 0 || !aligned(x, 16) || !aligned(xq, 16) || !aligned(xqT, 16) ||
+        !aligned(sx, 4) || !aligned(sxT, 4))
+        return FP8_ERR_ALIGN;
+    // 32-bit tile walk and TMA coordinates
+    const int64_t tiles = (M / 128) * (K / 128);
+    if (M > 0x7fffffffLL || K > 0x7fffffffLL || tiles > 0x7fffffffLL) return FP8_ERR_UNSUPPORTED;
+    unsigned* err = device_error_word();
+    if (err == nullptr) return FP8_ERR_CUDA;
+    CUtensorMap xmap;
+    if (make_map(&xmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, static_cast<uint64_t>(K),
+                 static_cast<uint64_t>(M), static_cast<uint64_t>(ldx) * 2, 64, 128,
+                 CU_TENSOR_MAP_SWIZZLE_128B) != FP8_OK)
+        return FP8_ERR_CUDA;
+    const int64_t grid = quant_grid<quant_act_dual_kernel>(tiles, kQDualSmem);
+    if (grid <= 0) return FP8_ERR_CUDA;
+    quant_act_dual_kernel<<<static_cast<unsigned>(grid), kQuantThreads, kQDualSmem,
+                            static_cast<cudaStream_t>(stream)>>>(
+        xmap, static_cast<uint32_t>(M), static_cast<uint32_t>(K), xq, ldq, sx, xqT, sxT,
         static_cast<uint32_t>(tiles), err);
     return to_status(launch_status());
 }

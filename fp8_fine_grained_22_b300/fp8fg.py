@@ -24,6 +24,7 @@ FP8_BSCALE_BLOCK128_T = 2
 # every entry point of include/fp8fg.h
 EXPORTS = ("fp8_status_str", "fp8_device_error", "fp8_selftest_wait_timeout",
            "fp8_quant_act_1x128", "fp8_quant_act_1x128_e5m6", "fp8_quant_act_128x1",
+           "fp8_quant_act_dual",
            "fp8_quant_weight_128x128",
            "fp8_quant_fprop_operands", "fp8_quant_act_1x128_pow2",
            "fp8_quant_weight_128x128_pow2", "fp8_gemm_mxfp8",
@@ -77,6 +78,8 @@ def lib() -> ctypes.CDLL:
         L.fp8_gemm_mxfp8.argtypes = [P, P, P, P, I64, I64, I64, P, I64, I, P]
         L.fp8_quant_act_128x1.restype = I
         L.fp8_quant_act_128x1.argtypes = [P, I64, I64, I64, P, P, P]
+        L.fp8_quant_act_dual.restype = I
+        L.fp8_quant_act_dual.argtypes = [P, I64, I64, I64, P, I64, P, P, P, P]
         L.fp8_quant_weight_128x128.restype = I
         L.fp8_quant_weight_128x128.argtypes = [P, I64, I64, I64, P, P, P, P]
         L.fp8_quant_fprop_operands.restype = I
@@ -189,6 +192,26 @@ def fp8_quant_act_128x1(x, xqT=None, sxT=None, stream=None):
     _check(lib().fp8_quant_act_128x1(_p(x), M, K, x.stride(0), _p(xqT), _p(sxT),
                                      _stream(stream)), "fp8_quant_act_128x1")
     return xqT, sxT
+
+
+def fp8_quant_act_dual(x, xq=None, sx=None, xqT=None, sxT=None, stream=None):
+    """x: bf16 [M, K] -> (xq uint8 [M, K], sx f32 [K/128, M], xqT uint8 [K, M],
+    sxT f32 [M/128, K]): fp8_quant_act_1x128 and fp8_quant_act_128x1 in one launch."""
+    _cuda(x, "x", torch.bfloat16)
+    assert x.dim() == 2 and x.stride(1) == 1
+    M, K = x.shape
+    if xq is None:
+        xq = torch.empty((M, K), dtype=torch.uint8, device=x.device)
+    if sx is None:
+        sx = torch.empty((K // 128, M), dtype=torch.float32, device=x.device)
+    if xqT is None:
+        xqT = torch.empty((K, M), dtype=torch.uint8, device=x.device)
+    if sxT is None:
+        sxT = torch.empty((M // 128, K), dtype=torch.float32, device=x.device)
+    assert xq.stride(1) == 1 and sx.is_contiguous() and xqT.is_contiguous() and sxT.is_contiguous()
+    _check(lib().fp8_quant_act_dual(_p(x), M, K, x.stride(0), _p(xq), xq.stride(0), _p(sx),
+                                    _p(xqT), _p(sxT), _stream(stream)), "fp8_quant_act_dual")
+    return xq, sx, xqT, sxT
 
 
 def fp8_quant_weight_128x128(w, wq=None, wqT=None, sw=None, want_wq=True, want_wqT=False,

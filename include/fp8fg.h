@@ -149,6 +149,20 @@ fp8_status fp8_quant_act_128x1(const void* x, int64_t M, int64_t K, int64_t ldx,
                         uint8_t* xqT, float* sxT, void* stream);
 
 /*
+ * fp8_quant_act_dual -- fp8_quant_act_1x128 and fp8_quant_act_128x1 of the same
+ * activation in one launch that reads it once (the Fprop or Dgrad operand and
+ * the transposed Wgrad operand of X or dY, report sections 3.3.1-3.3.3).
+ *   x        : bfloat16 [M][K], row stride ldx.                          (input)
+ *   xq, sx   : as fp8_quant_act_1x128 (xq row stride ldq).               (output)
+ *   xqT, sxT : as fp8_quant_act_128x1.                                   (output)
+ * The outputs are bit for bit those of the two separate calls.  Requires
+ * M % 128 == 0, K % 128 == 0, ldx >= K, ldx % 8 == 0, ldq >= K, ldq % 16 == 0,
+ * x, xq, xqT 16-byte aligned, sx, sxT 4-byte aligned.  M >= 0.
+ */
+fp8_status fp8_quant_act_dual(const void* x, int64_t M, int64_t K, int64_t ldx, uint8_t* xq,
+                              int64_t ldq, float* sx, uint8_t* xqT, float* sxT, void* stream);
+
+/*
  * fp8_quant_weight_128x128 -- 128x128 block weight quantisation (report
  * section 3.3.2; block size 128x128).
  *   w   : bfloat16 [K][N] (K = inner dimension of the Fprop GEMM), row stride ldw. (input)
