@@ -415,6 +415,15 @@ def qdual_bytes(M, K):
     return M * K * 4 + (K // 128) * M * 4 + (M // 128) * K * 4
 
 
+def padded_rows(offsets, E):
+    """Rows the grouped GEMM computes: per expert, its rows rounded up to the
+    tile height the library picks (256-row CTA-pair blocks when the experts
+    average 192 rows or more, 128-row tiles otherwise)."""
+    cnt = np.diff(np.asarray(offsets, np.int64))
+    h = 256 if cnt.sum() >= 192 * E else 128
+    return int(sum(((c + h - 1) // h) * h for c in cnt))
+
+
 def q128x128_bytes(K, N, both):
     return K * N * (2 + (2 if both else 1)) + (K // 128) * (N // 128) * 4
 
@@ -870,6 +879,13 @@ def cfg4(d, peaks):
            "dispatch_frac_hbm": round(gbs(disp_bytes, dp) / peaks["hbm"], 4),
            "grouped_gemm_ms": round(gm, 5), "grouped_gemm_tflops": round(tf, 2),
            "grouped_gemm_frac": frac_set(tf, peaks),
+           # the tiles the kernel computes: each expert's rows padded to whole
+           # 256-row CTA-pair blocks (the library's choice at 192+ rows per expert
+           # on average, else 128-row tiles): the rate on computed FLOPs is the
+           # kernel's own efficiency, the gap to the above is the padding
+           "grouped_gemm_padded_rows": padded_rows(wl.offsets, E),
+           "grouped_gemm_frac_of_computed": frac_set(
+               tflops(2.0 * padded_rows(wl.offsets, E) * N * K, gm), peaks),
            "weight_quant_ms (32 experts, static, outside the step)": round(wq_ms, 5),
            "weight_quant_gbs": round(gbs(wbytes, wq_ms), 1),
            "weight_quant_frac_hbm": round(gbs(wbytes, wq_ms) / peaks["hbm"], 4),
