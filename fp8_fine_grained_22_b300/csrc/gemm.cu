@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kLoaderLanes = GROUPED ? 1 : 32;
     // The ring carries the per-column B scales of the Wgrad mode.  In the
     // block modes the epilogue needs two scalars per K block and prefetches
-    // them from global memory one K block ahead instead.
+    // them from global memory two K blocks ahead instead.
     constexpr bool kRing = ROWSCALE;
 
     if (threadIdx.x == 0) {
@@ -476,16 +476,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp < kEpiWarp0) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kCtrlRegs));
     }
-    // Dense kernels run the producer and the MMA issuer as whole warps: every
-    // lane walks the schedule and waits on the barriers, so descriptors and
-    // coordinates are warp-uniform and one elected lane issues the
+    // The producer and the MMA issuer run as whole warps in every kernel:
+    // every lane walks the schedule and waits on the barriers, so descriptors
+    // and coordinates are warp-uniform and one elected lane issues the
     // asynchronous operations (issued from a single divergent lane, each
-    // tcgen05.mma costs about twice the issue cycles).  The grouped kernels
-    // keep single-lane roles: their tile walk over the expert offsets does not
-    // fit the control warps' registers when run warp-wide.
-    // Producer and MMA issuer run as whole warps (one elected lane issuing)
-    // in every kernel: the 32-bit tile walks fit the control warps' 40
-    // registers.  Two MMA issuers in the dense and grouped-row pair kernels.
+    // tcgen05.mma costs about twice the issue cycles).  The 32-bit tile walks
+    // fit the control warps' 40 registers.  Two MMA issuers in the dense and
+    // grouped-row pair kernels.
     constexpr bool kWarpRoles = true;
     constexpr bool kTwoIssuers = GM == 0 || (GROUPED && PAIR);
     constexpr bool kKRange = GK || PAIR;  // tiles carry their own K range
@@ -744,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int nkb = kKRange ? ti.kb_count : static_cast<int>(KB);
             const int kbo = kKRange ? ti.kb_begin : 0;
             // block modes: this row's A scales sa[kb * lds_a + row] and the
-            // B scale of this thread's 128-column block, one K block ahead
+            // B scale of this thread's 128-column block, two K blocks ahead
             const bool row_in_alloc = row < p.M;
             const int lds_a = static_cast<int>(p.lds_a);
             const float* sa_g = p.sa + static_cast<int64_t>(kbo) * lds_a + (row_in_alloc ? row : 0);
