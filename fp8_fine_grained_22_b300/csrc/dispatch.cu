@@ -211,7 +211,10 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
     }
 
     // 1x128 groups (token, kb) of this K slice: four lanes per group, 32
-    // elements per lane, the arithmetic of the 1x128 quantiser
+    // elements per lane, the arithmetic of the 1x128 quantiser.  Item it is
+    // (active token it / nkb, K block kb0 + it % nkb); each group walks its
+    // items with a fixed stride, advancing the pair without division, and
+    // issues the next item's loads before it converts the current one.
     const int kb0 = blockIdx.y * kb_per_slice;
     const int kb1 = static_cast<int>(KB < kb0 + kb_per_slice ? KB : kb0 + kb_per_slice);
     const int nkb = kb1 - kb0;
@@ -219,47 +222,71 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
     const int l4 = tid & 3;
     const uint32_t gmask = 0xFu << (lane & ~3);
     const int64_t K = KB * 128;
-    for (int it = tid >> 2; it < items; it += kPackThreads / 4) {
-        const int tl = s_active[it / nkb];
-        const int kb = kb0 + it % nkb;
-        const uint16_t* src = x + (t0 + tl) * ldx + static_cast<int64_t>(kb) * 128 + l4 * 32;
-        uint4 q[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) q[i] = ld_stream_v4(src + 8 * i);
-        uint32_t mx = absmax_bf16x2(q[0].x, q[0].y);
-        mx = absmax_bf16x2(mx, absmax_bf16x2(q[0].z, q[0].w));
-#pragma unroll
-        for (int i = 1; i < 4; ++i) {
-            mx = absmax_bf16x2(mx, absmax_bf16x2(q[i].x, q[i].y));
-            mx = absmax_bf16x2(mx, absmax_bf16x2(q[i].z, q[i].w));
+    constexpr int kStep = kPackThreads / 4;
+    const int step_q = kStep / nkb, step_r = kStep % nkb;
+    int it = tid >> 2;
+    int ia = it / nkb, ib = it % nkb;  // active-token index and K block within the slice
+    uint4 q0 = make_uint4(0, 0, 0, 0), q1 = q0, q2 = q0, q3 = q0;
+    if (it < items) {
+        const uint16_t* src = x + (t0 + s_active[ia]) * ldx + static_cast<int64_t>(kb0 + ib) * 128 + l4 * 32;
+        q0 = ld_stream_v4(src);
+        q1 = ld_stream_v4(src + 8);
+        q2 = ld_stream_v4(src + 16);
+        q3 = ld_stream_v4(src + 24);
+    }
+    for (; it < items; it += kStep) {
+        int na = ia + step_q, nb = ib + step_r;
+        if (nb >= nkb) {
+            nb -= nkb;
+            ++na;
         }
-        float amax = amax_of_pair(mx);
-        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(gmask, amax, 2));
-        const float s = group_scale(amax);
-        const GroupDiv dv(s);
-        uint4 o[2];
+        uint4 n0 = make_uint4(0, 0, 0, 0), n1 = n0, n2 = n0, n3 = n0;
+        if (it + kStep < items) {  // the next item's loads, in flight during the conversion
+            const uint16_t* src = x + (t0 + s_active[na]) * ldx + static_cast<int64_t>(kb0 + nb) * 128 + l4 * 32;
+            n0 = ld_stream_v4(src);
+            n1 = ld_stream_v4(src + 8);
+            n2 = ld_stream_v4(src + 16);
+            n3 = ld_stream_v4(src + 24);
+        }
+        const uint4 q[4] = {q0, q1, q2, q3};
+        uint32_t mx = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const uint32_t a = dv.quad_words(q[i].x, q[i].y);
-            const uint32_t b = dv.quad_words(q[i].z, q[i].w);
-            if (i & 1) {
-                o[i >> 1].z = a;
-                o[i >> 1].w = b;
-            } else {
-                o[i >> 1].x = a;
-                o[i >> 1].y = b;
-            }
+            mx = absmax_acc(mx, q[i].x);
+            mx = absmax_acc(mx, q[i].y);
+            mx = absmax_acc(mx, q[i].z);
+            mx = absmax_acc(mx, q[i].w);
         }
+        mx &= 0x7FFF7FFFu;
+        mx = absmax_acc(mx, __shfl_xor_sync(gmask, mx, 1));
+        mx = absmax_acc(mx, __shfl_xor_sync(gmask, mx, 2));
+        const float s = group_scale(amax_of_pair(mx));
+        const NegDiv dv(s, __frcp_rn(s));
+        uint4 o0, o1;
+        if (s >= 0x1p-91f) {
+            o0 = codes_1x128<true>(dv, q[0], q[1]);
+            o1 = codes_1x128<true>(dv, q[2], q[3]);
+        } else {
+            o0 = codes_1x128<false>(dv, q[0], q[1]);
+            o1 = codes_1x128<false>(dv, q[2], q[3]);
+        }
+        const int tl = s_active[ia];
+        const int kb = kb0 + ib;
         for (int j = 0; j < topk; ++j) {
             const int d = s_dest[tl * topk + j];
             if (d < 0) continue;
             uint4* dst = reinterpret_cast<uint4*>(xq + static_cast<int64_t>(d) * K +
                                                   static_cast<int64_t>(kb) * 128 + l4 * 32);
-            dst[0] = o[0];
-            dst[1] = o[1];
+            dst[0] = o0;
+            dst[1] = o1;
             if (l4 == 0) sx[static_cast<int64_t>(kb) * cap + d] = s;
         }
+        q0 = n0;
+        q1 = n1;
+        q2 = n2;
+        q3 = n3;
+        ia = na;
+        ib = nb;
     }
 }
 

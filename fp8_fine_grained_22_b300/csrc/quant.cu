@@ -54,17 +54,6 @@ __device__ __forceinline__ void load_1x128_tile(const uint16_t* __restrict__ x, 
     for (int i = 0; i < 4; ++i) v[i] = (m < M) ? ld_stream_v4(src + 8 * i) : make_uint4(0, 0, 0, 0);
 }
 
-// Codes of 16 consecutive elements (eight words, memory order) of a group,
-// sign bits flipped back, as one 16-byte store.
-template <bool FAST>
-__device__ __forceinline__ uint4 codes_1x128(const NegDiv& dv, const uint4& a, const uint4& b) {
-    auto quad = [&](uint32_t w0, uint32_t w1) {
-        return prmt(dv.ncodes2<FAST>(bf16x2_to_f2(w0)), dv.ncodes2<FAST>(bf16x2_to_f2(w1)), 0x5410u) ^
-               kSignFlip4;
-    };
-    return make_uint4(quad(a.x, a.y), quad(a.z, a.w), quad(b.x, b.y), quad(b.z, b.w));
-}
-
 // Quantises the group (row m, K group kb) whose 32 bf16 values per lane
 // this thread holds in v (lanes l4 = 0..3 of the row's four-lane group).
 __device__ __forceinline__ void quant_1x128_group(uint32_t M, uint8_t* __restrict__ xq, int64_t ldq,

@@ -220,6 +220,17 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return d;
 }
 
+// Codes of 16 consecutive elements (eight words, memory order) of a group,
+// sign bits flipped back, as one 16-byte store.
+template <bool FAST>
+__device__ __forceinline__ uint4 codes_1x128(const NegDiv& dv, const uint4& a, const uint4& b) {
+    auto quad = [&](uint32_t w0, uint32_t w1) {
+        return prmt(dv.ncodes2<FAST>(bf16x2_to_f2(w0)), dv.ncodes2<FAST>(bf16x2_to_f2(w1)), 0x5410u) ^
+               kSignFlip4;
+    };
+    return make_uint4(quad(a.x, a.y), quad(a.z, a.w), quad(b.x, b.y), quad(b.z, b.w));
+}
+
 // ---------------------------------------------------- power-of-two scales --
 // The smallest e with amax <= 448 * 2^e, clamped to the UE8M0 range
 // [-127, 127]; e = 0 for amax = 0.  amax is a bfloat16 value (1 + m/128) 2^E:
