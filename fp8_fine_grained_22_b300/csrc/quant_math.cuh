@@ -134,25 +134,6 @@ struct GroupDiv {
                            (pair_unsigned(bf16_lo(w1), bf16_hi(w1)) << 16);
         return c | (sign_bytes(w0, w1) & 0x80808080u);
     }
-    // Codes of the low halves (lo) and of the high halves (hi) of four words.
-    __device__ __forceinline__ void quad_halves(uint32_t w0, uint32_t w1, uint32_t w2, uint32_t w3,
-                                                uint32_t& lo, uint32_t& hi) const {
-        halves(*this, *this, w0, w1, w2, w3, lo, hi);
-    }
-    // As quad_halves(), the low halves divided by da's scale and the high
-    // halves by db's: two columns held as bfloat16 pairs, one scale each.
-    __device__ __forceinline__ static void halves(const GroupDiv& da, const GroupDiv& db, uint32_t w0,
-                                                  uint32_t w1, uint32_t w2, uint32_t w3, uint32_t& lo,
-                                                  uint32_t& hi) {
-        const uint32_t s01 = sign_bytes(w0, w1), s23 = sign_bytes(w2, w3);
-        lo = da.pair_unsigned(bf16_lo(w0), bf16_lo(w1)) |
-             (da.pair_unsigned(bf16_lo(w2), bf16_lo(w3)) << 16);
-        hi = db.pair_unsigned(bf16_hi(w0), bf16_hi(w1)) |
-             (db.pair_unsigned(bf16_hi(w2), bf16_hi(w3)) << 16);
-        lo |= byte_perm(s01, s23, 0x6420) & 0x80808080u;
-        hi |= byte_perm(s01, s23, 0x7531) & 0x80808080u;
-    }
-
   private:
     __device__ __forceinline__ static uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
         uint32_t d;
