@@ -1191,6 +1191,37 @@ def probe_quant():
     print(json.dumps({"probe": "quant", "launches": 2 * len(runs)}))
 
 
+def probe_dispatch():
+    """For an ncu capture: the MoE prefill dispatch (count, scan and pack
+    launches) once, then again with L2 flushed before it."""
+    from fp8_fine_grained_22_b300 import fp8fg
+    d = Dev(0)
+    fp8fg.lib()
+    wl = inputs.moe_prefill(seed=0, device=d.dev)
+    x = wl.extra["x_tokens"].to(d.dev)
+    ids = wl.extra["topk_ids"].to(torch.int32).contiguous().to(d.dev)
+    E, rows = wl.E, int(wl.offsets[-1])
+    del wl  # the expert weights: the capture keeps only what the dispatch touches
+    torch.cuda.empty_cache()
+    T, K = x.shape
+    cap = T * min(ids.shape[1], E)
+    ws = fp8fg.moe_dispatch_workspace(T, E, d.dev)
+    xq = torch.empty((cap, K), dtype=torch.uint8, device=d.dev)
+    sx = torch.empty((K // 128, cap), dtype=torch.float32, device=d.dev)
+    off = torch.empty(E + 1, dtype=torch.int32, device=d.dev)
+    tok = torch.empty(cap, dtype=torch.int32, device=d.dev)
+    for flush in (False, True):
+        if flush:
+            d.flush_l2()
+            torch.cuda.synchronize()
+        fp8fg.fp8_moe_dispatch_quant(x, ids, 0, E, cap=cap, xq=xq, sx=sx, offsets=off,
+                                     token_ids=tok, workspace=ws, stream=d.stream)
+    torch.cuda.synchronize()
+    if int(off[-1].item()) != rows or fp8fg.device_error() != 0:
+        raise RuntimeError("dispatch check failed")
+    print(json.dumps({"probe": "dispatch", "launches": 6}))
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -1206,16 +1237,19 @@ def main():
                     help="tokens of the trio the cpu_baseline oracle run covers (multiple of 128)")
     ap.add_argument("--workload", default="trio",
                     choices=["trio", "fprop_dense", "moe_prefill", "moe_decode", "moe_backward"])
-    ap.add_argument("--probe", choices=["gemms", "quant"], default=None,
-                    help="launch each profiled GEMM (gemms) or the trio's quantisers (quant) "
-                         "twice (warm-up, then L2 flushed) and exit: the programs the committed "
-                         "ncu summaries capture")
+    ap.add_argument("--probe", choices=["gemms", "quant", "dispatch"], default=None,
+                    help="launch each profiled GEMM (gemms), the trio's quantisers (quant) or "
+                         "the MoE prefill dispatch (dispatch) twice (warm-up, then L2 flushed) "
+                         "and exit: the programs the committed ncu summaries capture")
     args = ap.parse_args()
     if args.probe == "gemms":
         probe_gemms()
         return
     if args.probe == "quant":
         probe_quant()
+        return
+    if args.probe == "dispatch":
+        probe_dispatch()
         return
     if args.ref_tokens % 128 or args.cpu_tokens % 128:
         ap.error("--ref-tokens and --cpu-tokens must be multiples of 128")

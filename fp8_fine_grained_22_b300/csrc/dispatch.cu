@@ -18,13 +18,15 @@
 //          into counts[e][chunk];
 //   scan   one warp per expert: exclusive prefix of counts over the chunks
 //          (in place) and the expert's total;
-//   pack   one CTA per (chunk, K slice): the exclusive scan of the totals
-//          gives offsets; the first warp ranks the chunk's (token, expert)
-//          pairs in token order with shared-memory lane masks and lists the
-//          tokens that have a local expert; all warps quantise those tokens'
-//          1x128 groups (the arithmetic of fp8_quant_act_1x128) and store
-//          each group's codes and scale at every destination row.  Tokens
-//          routed only to other experts are not read.
+//   pack   one CTA per (chunk, K slice), as many as are resident at once
+//          (one wave): the exclusive scan of the totals gives offsets; the
+//          chunk's (token, expert) pairs are ranked in token order in two
+//          parallel passes over a 64-bit token mask per expert, and the
+//          tokens that have a local expert are listed; then all warps
+//          quantise those tokens' 1x128 groups (the arithmetic of
+//          fp8_quant_act_1x128) and store each group's codes and scale at
+//          every destination row.  Tokens routed only to other experts are
+//          not read.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -35,10 +37,13 @@
 
 namespace fp8fg {
 
-constexpr int kChunk = 64;          // tokens per chunk (ranked by one warp, 32 at a time)
+constexpr int kChunk = 64;          // tokens per chunk (one 64-bit token mask per expert)
 constexpr int kMaxTopk = 16;
 constexpr int kMaxLocal = 1024;     // local experts
 constexpr int kPackThreads = 256;   // 64 four-lane groups
+constexpr int kCountThreads = 256;  // four lanes per token of a chunk
+static_assert(kPackThreads == 4 * kChunk && kCountThreads == 4 * kChunk,
+              "four lanes per token of a chunk");
 
 // Local expert index of slot j of a token's top-k row, or -1 when the expert
 // is not local or repeats an earlier slot of the same row.
@@ -50,24 +55,28 @@ __device__ __forceinline__ int local_slot(const int32_t* ids, int j, int expert_
     return static_cast<int>(e);
 }
 
-__global__ void __launch_bounds__(kChunk) moe_count_kernel(const int32_t* __restrict__ topk_ids,
-                                                           int64_t T, int topk, int expert_begin,
-                                                           int E, int nchunks,
-                                                           int32_t* __restrict__ counts) {
+// The chunk's top-k rows are read coalesced into shared memory; lane
+// (token, sub) then takes the token's slots sub, sub + 4, ...
+__global__ void __launch_bounds__(kCountThreads) moe_count_kernel(
+    const int32_t* __restrict__ topk_ids, int64_t T, int topk, int expert_begin, int E,
+    int nchunks, int32_t* __restrict__ counts) {
     __shared__ int hist[kMaxLocal];
-    for (int e = threadIdx.x; e < E; e += kChunk) hist[e] = 0;
+    __shared__ int32_t s_ids[kChunk * kMaxTopk];
+    const int tid = threadIdx.x;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kChunk;
+    const int n_tok = static_cast<int>(T - t0 < kChunk ? T - t0 : kChunk);
+    for (int e = tid; e < E; e += kCountThreads) hist[e] = 0;
+    for (int i = tid; i < n_tok * topk; i += kCountThreads) s_ids[i] = __ldg(topk_ids + t0 * topk + i);
     __syncthreads();
-    const int64_t t = static_cast<int64_t>(blockIdx.x) * kChunk + threadIdx.x;
-    if (t < T) {
-        int32_t ids[kMaxTopk];
-        for (int j = 0; j < topk; ++j) ids[j] = __ldg(topk_ids + t * topk + j);
-        for (int j = 0; j < topk; ++j) {
-            const int e = local_slot(ids, j, expert_begin, E);
+    const int tl = tid >> 2, sub = tid & 3;
+    if (tl < n_tok) {
+        for (int j = sub; j < topk; j += 4) {
+            const int e = local_slot(&s_ids[tl * topk], j, expert_begin, E);
             if (e >= 0) atomicAdd(&hist[e], 1);
         }
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < E; e += kChunk)
+    for (int e = tid; e < E; e += kCountThreads)
         counts[static_cast<int64_t>(e) * nchunks + blockIdx.x] = hist[e];
 }
 
@@ -79,20 +88,26 @@ __global__ void __launch_bounds__(256) moe_scan_kernel(int32_t* __restrict__ cou
     const int e = blockIdx.x * 8 + warp;
     if (e >= E) return;  // whole warp
     int32_t* row = counts + static_cast<int64_t>(e) * nchunks;
-    int running = 0;
-    for (int c0 = 0; c0 < nchunks; c0 += 32) {
-        const int c = c0 + lane;
-        const int v = c < nchunks ? row[c] : 0;
-        int incl = v;
+    // lane l takes the consecutive chunks c0 .. c1-1: its sum (independent
+    // loads), an exclusive scan of the lane sums, then its prefixes
+    const int per = (nchunks + 31) / 32;
+    const int c0 = lane * per < nchunks ? lane * per : nchunks;
+    const int c1 = c0 + per < nchunks ? c0 + per : nchunks;
+    int sum = 0;
+    for (int c = c0; c < c1; ++c) sum += row[c];
+    int incl = sum;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int n = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += n;
-        }
-        if (c < nchunks) row[c] = running + incl - v;
-        running += __shfl_sync(0xffffffffu, incl, 31);
+    for (int o = 1; o < 32; o <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += n;
     }
-    if (lane == 0) totals[e] = running;
+    int run = incl - sum;
+    for (int c = c0; c < c1; ++c) {
+        const int v = row[c];
+        row[c] = run;
+        run += v;
+    }
+    if (lane == 31) totals[e] = incl;
 }
 
 __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
@@ -105,11 +120,10 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
     __shared__ int32_t s_ids[kChunk * kMaxTopk];
     __shared__ int32_t s_dest[kChunk * kMaxTopk];
     __shared__ int32_t s_base[kMaxLocal];
-    __shared__ uint32_t s_mask[kMaxLocal];
-    __shared__ int32_t s_run[kMaxLocal];
+    __shared__ unsigned long long s_tok[kMaxLocal];  // per expert: its tokens of the chunk
     __shared__ int32_t s_wsum[kPackThreads / 32];
     __shared__ int32_t s_active[kChunk];  // chunk tokens with a local expert, ascending
-    __shared__ int32_t s_n_active;
+    __shared__ unsigned long long s_act;  // the same tokens as a mask
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
     const int64_t t0 = static_cast<int64_t>(c) * kChunk;
@@ -117,6 +131,7 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
     const bool first_cta = c == 0 && blockIdx.y == 0;
 
     for (int i = tid; i < n_tok * topk; i += kPackThreads) s_ids[i] = __ldg(topk_ids + t0 * topk + i);
+    if (tid == 0) s_act = 0ull;
 
     // exclusive scan of the expert totals (four experts per thread) -> offsets
     int v[4], sum = 0;
@@ -150,8 +165,7 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
         const int e = tid * 4 + i;
         if (e < E) {
             s_base[e] = excl + __ldg(chunk_base + static_cast<int64_t>(e) * nchunks + c);
-            s_mask[e] = 0;
-            s_run[e] = 0;
+            s_tok[e] = 0ull;
             if (first_cta) offsets[e] = excl;
         }
         excl += v[i];
@@ -159,49 +173,37 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
     if (first_cta && tid == 0) offsets[E] = s_wsum[kPackThreads / 32 - 1];
     __syncthreads();
 
-    // rank the (token, local expert) pairs of the chunk in token order
-    if (warp == 0) {
-        for (int b = 0; b < kChunk; b += 32) {
-            const int tl = b + lane;
-            const bool valid = tl < n_tok;
-            int le[kMaxTopk];
-            for (int j = 0; j < topk; ++j) {
-                le[j] = valid ? local_slot(&s_ids[tl * topk], j, expert_begin, E) : -1;
-                if (le[j] >= 0) atomicOr(&s_mask[le[j]], 1u << lane);
+    // Rank the chunk's (token, local expert) pairs in token order, lane
+    // (token, sub) taking the token's slots sub, sub + 4, ...  Pass 1: each
+    // slot's local expert (or -1) into s_dest, and the token's bit in its
+    // expert's mask and in the mask of tokens with a local expert.  Pass 2:
+    // the destination row is the expert's first row for this chunk plus the
+    // number of the expert's tokens ahead of this one in the chunk.
+    const int tl = tid >> 2, sub = tid & 3;
+    const unsigned long long below = (1ull << tl) - 1ull;
+    if (tl < n_tok) {
+        bool any = false;
+        for (int j = sub; j < topk; j += 4) {
+            const int e = local_slot(&s_ids[tl * topk], j, expert_begin, E);
+            s_dest[tl * topk + j] = e;
+            if (e >= 0) {
+                atomicOr(&s_tok[e], 1ull << tl);
+                any = true;
             }
-            __syncwarp();
-            for (int j = 0; j < topk; ++j) {
-                if (le[j] >= 0) {
-                    const uint32_t m = s_mask[le[j]];
-                    s_dest[tl * topk + j] =
-                        s_base[le[j]] + s_run[le[j]] + __popc(m & ((1u << lane) - 1u));
-                } else if (valid) {
-                    s_dest[tl * topk + j] = -1;
-                }
-            }
-            __syncwarp();
-            // the highest lane of each expert's mask advances its running count
-            bool any = false;
-            for (int j = 0; j < topk; ++j) {
-                if (le[j] >= 0) {
-                    any = true;
-                    const uint32_t m = s_mask[le[j]];
-                    if (m != 0 && 31 - __clz(m) == lane) {
-                        s_run[le[j]] += __popc(m);
-                        s_mask[le[j]] = 0;
-                    }
-                }
-            }
-            // tokens with no local expert are never read
-            const uint32_t act = __ballot_sync(0xffffffffu, any);
-            const int n_before = b == 0 ? 0 : s_n_active;
-            __syncwarp();
-            if (any) s_active[n_before + __popc(act & ((1u << lane) - 1u))] = tl;
-            if (lane == 0) s_n_active = n_before + __popc(act);
-            __syncwarp();
         }
+        if (any) atomicOr(&s_act, 1ull << tl);
     }
     __syncthreads();
+    if (tl < n_tok) {
+        for (int j = sub; j < topk; j += 4) {
+            const int e = s_dest[tl * topk + j];
+            if (e >= 0) s_dest[tl * topk + j] = s_base[e] + __popcll(s_tok[e] & below);
+        }
+        // tokens with no local expert are never read
+        if (sub == 0 && ((s_act >> tl) & 1ull) != 0) s_active[__popcll(s_act & below)] = tl;
+    }
+    __syncthreads();
+    const int n_active = __popcll(s_act);
 
     if (blockIdx.y == 0) {
         for (int i = tid; i < n_tok * topk; i += kPackThreads) {
@@ -218,7 +220,7 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
     const int kb0 = blockIdx.y * kb_per_slice;
     const int kb1 = static_cast<int>(KB < kb0 + kb_per_slice ? KB : kb0 + kb_per_slice);
     const int nkb = kb1 - kb0;
-    const int items = s_n_active * nkb;
+    const int items = n_active * nkb;
     const int l4 = tid & 3;
     const uint32_t gmask = 0xFu << (lane & ~3);
     const int64_t K = KB * 128;
@@ -324,15 +326,33 @@ static int dispatch_launch(const void* x, int64_t T, int64_t K, int64_t ldx,
     const DispatchPlan d = dispatch_plan(T, n_local);
     int32_t* counts = scratch;
     int32_t* totals = scratch + d.count_ints;
-    moe_count_kernel<<<d.nchunks, kChunk, 0, stream>>>(topk_ids, T, topk, expert_begin, n_local,
-                                                        d.nchunks, counts);
-    moe_scan_kernel<<<(n_local + 7) / 8, 256, 0, stream>>>(counts, totals, n_local, d.nchunks);
+    // (chunk, K slice) CTAs of the pack: as many slices per chunk as fit in
+    // one wave of resident CTAs (a second, partial wave measured 20 % slower)
     const int sms = sm_count_current();
+    if (sms <= 0) return FP8_ERR_CUDA;
+    static ContextCache<int> per_sm;
+    int resident = 0;
+    const int ost = per_sm.get(&resident, [](int* v) {
+        int b = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, moe_pack_quant_kernel, kPackThreads, 0) !=
+                cudaSuccess ||
+            b < 1)
+            return static_cast<int>(FP8_ERR_CUDA);
+        *v = b;
+        return static_cast<int>(FP8_OK);
+    });
+    if (ost != FP8_OK) return ost;
     const int64_t KB = K / 128;
-    int64_t slices = (4LL * (sms > 0 ? sms : 148) + d.nchunks - 1) / d.nchunks;
+    int64_t slices = static_cast<int64_t>(resident) * sms / d.nchunks;
     slices = std::max<int64_t>(1, std::min<int64_t>(slices, KB));
     const int kb_per_slice = static_cast<int>((KB + slices - 1) / slices);
     slices = (KB + kb_per_slice - 1) / kb_per_slice;
+
+    moe_count_kernel<<<d.nchunks, kCountThreads, 0, stream>>>(topk_ids, T, topk, expert_begin,
+                                                               n_local, d.nchunks, counts);
+    moe_scan_kernel<<<(n_local + 7) / 8, 256, 0, stream>>>(counts, totals, n_local, d.nchunks);
+    // (launching these two with programmatic stream serialisation, each
+    // waiting for the one before in griddepcontrol.wait, measured 2 us slower)
     const dim3 grid(static_cast<unsigned>(d.nchunks), static_cast<unsigned>(slices));
     moe_pack_quant_kernel<<<grid, kPackThreads, 0, stream>>>(
         static_cast<const uint16_t*>(x), T, KB, ldx, topk_ids, topk, expert_begin, n_local,
