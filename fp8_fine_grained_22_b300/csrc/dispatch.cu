@@ -124,6 +124,9 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
     __shared__ int32_t s_wsum[kPackThreads / 32];
     __shared__ int32_t s_active[kChunk];  // chunk tokens with a local expert, ascending
     __shared__ unsigned long long s_act;  // the same tokens as a mask
+    __shared__ uint32_t s_vmask[kChunk];  // per token: its slots with a local expert
+    __shared__ int32_t s_nd[kChunk];      // per active token: its destination rows,
+    __shared__ int32_t s_dl[kChunk * kMaxTopk];  // in slot order
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int c = blockIdx.x;
     const int64_t t0 = static_cast<int64_t>(c) * kChunk;
@@ -132,6 +135,7 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
 
     for (int i = tid; i < n_tok * topk; i += kPackThreads) s_ids[i] = __ldg(topk_ids + t0 * topk + i);
     if (tid == 0) s_act = 0ull;
+    if (tid < kChunk) s_vmask[tid] = 0u;
 
     // exclusive scan of the expert totals (four experts per thread) -> offsets
     int v[4], sum = 0;
@@ -175,10 +179,12 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
 
     // Rank the chunk's (token, local expert) pairs in token order, lane
     // (token, sub) taking the token's slots sub, sub + 4, ...  Pass 1: each
-    // slot's local expert (or -1) into s_dest, and the token's bit in its
-    // expert's mask and in the mask of tokens with a local expert.  Pass 2:
-    // the destination row is the expert's first row for this chunk plus the
-    // number of the expert's tokens ahead of this one in the chunk.
+    // slot's local expert (or -1) into s_dest, the token's bit in its
+    // expert's mask and in the mask of tokens with a local expert, and the
+    // slot's bit in the token's slot mask.  Pass 2: the destination row is the
+    // expert's first row for this chunk plus the number of the expert's tokens
+    // ahead of this one in the chunk; each active token's rows are also listed
+    // compactly, so that the quantising groups store without scanning slots.
     const int tl = tid >> 2, sub = tid & 3;
     const unsigned long long below = (1ull << tl) - 1ull;
     if (tl < n_tok) {
@@ -188,6 +194,7 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
             s_dest[tl * topk + j] = e;
             if (e >= 0) {
                 atomicOr(&s_tok[e], 1ull << tl);
+                atomicOr(&s_vmask[tl], 1u << j);
                 any = true;
             }
         }
@@ -195,12 +202,22 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
     }
     __syncthreads();
     if (tl < n_tok) {
+        const bool act = ((s_act >> tl) & 1ull) != 0;
+        const int a = __popcll(s_act & below);  // the token's index among the active ones
+        const uint32_t vm = s_vmask[tl];
         for (int j = sub; j < topk; j += 4) {
             const int e = s_dest[tl * topk + j];
-            if (e >= 0) s_dest[tl * topk + j] = s_base[e] + __popcll(s_tok[e] & below);
+            if (e >= 0) {
+                const int d = s_base[e] + __popcll(s_tok[e] & below);
+                s_dest[tl * topk + j] = d;
+                s_dl[a * kMaxTopk + __popc(vm & ((1u << j) - 1u))] = d;
+            }
         }
         // tokens with no local expert are never read
-        if (sub == 0 && ((s_act >> tl) & 1ull) != 0) s_active[__popcll(s_act & below)] = tl;
+        if (sub == 0 && act) {
+            s_active[a] = tl;
+            s_nd[a] = __popc(vm);
+        }
     }
     __syncthreads();
     const int n_active = __popcll(s_act);
@@ -272,11 +289,10 @@ __global__ void __launch_bounds__(kPackThreads) moe_pack_quant_kernel(
             o0 = codes_1x128<false>(dv, q[0], q[1]);
             o1 = codes_1x128<false>(dv, q[2], q[3]);
         }
-        const int tl = s_active[ia];
         const int kb = kb0 + ib;
-        for (int j = 0; j < topk; ++j) {
-            const int d = s_dest[tl * topk + j];
-            if (d < 0) continue;
+        const int nd = s_nd[ia];
+        for (int k = 0; k < nd; ++k) {
+            const int d = s_dl[ia * kMaxTopk + k];
             uint4* dst = reinterpret_cast<uint4*>(xq + static_cast<int64_t>(d) * K +
                                                   static_cast<int64_t>(kb) * 128 + l4 * 32);
             dst[0] = o0;
