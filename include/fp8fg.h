@@ -65,6 +65,21 @@ typedef enum {
     FP8_ERR_DEVICE_SHAPE = 7 /* a kernel found invalid device-side data (offsets) */
 } fp8_status;
 
+/*
+ * FP8_ERR_UNSUPPORTED, in detail.  A call returns it, launching nothing, for:
+ *   - sizes beyond the kernels' 32-bit tile and row walks (a dimension or a
+ *     tile count of 2^31 or more), or a dispatch problem larger than the
+ *     fixed scratch of fp8_moe_dispatch_quant_noalloc;
+ *   - an fp8_out_t or fp8_bscale_t value the entry point does not take;
+ *   - (GEMMs) a library build whose GEMM kernels were given a different
+ *     register count than the one their per-warp-role register split is
+ *     sized for (a build made with another CUDA compiler version): the
+ *     split would stall the kernel, so it is refused.  Rebuild the library
+ *     from source with the toolkit it targets (CUDA 13.0, sm_103a);
+ *   - (GEMMs on CTA pairs) a device on which no cluster of two CTAs of the
+ *     kernel can be resident.
+ */
+
 /* Output element type of the GEMMs. */
 typedef enum { FP8_OUT_F32 = 0, FP8_OUT_BF16 = 1 } fp8_out_t;
 
