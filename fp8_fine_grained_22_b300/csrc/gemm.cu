@@ -1198,8 +1198,12 @@ static int dispatch(const uint8_t* aq, int64_t a_rows, const uint8_t* bq, int64_
                 return launch<128, false, true, 0, 1>(aq, a_rows, bq, b_rows, p, tiles, stream);
             }
             // 256-wide tiles on CTA pairs: per SM and K block, shared memory
-            // moves A + B/2 each way instead of A + B
-            if (p.N % 256 == 0 && ceil_div(mblk_upper, kClusterM) * (p.N / 256) < (1LL << 30)) {
+            // moves A + B/2 each way instead of A + B.  A single 128-row
+            // block takes the one-CTA 128-wide kernel below instead: a pair
+            // would idle one of its CTAs, and the cluster set-up dominates
+            // such short launches (128 x 256 x 512: 8.5 us against 11.5 us)
+            if (p.N % 256 == 0 && mblk_upper > 1 &&
+                ceil_div(mblk_upper, kClusterM) * (p.N / 256) < (1LL << 30)) {
                 const int64_t tiles = ceil_div(mblk_upper, kClusterM) * (p.N / 256);
                 if (out_type == FP8_OUT_BF16)
                     return launch<256, true, false, 0, kClusterM>(aq, a_rows, bq, b_rows, p, tiles,

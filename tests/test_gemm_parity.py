@@ -73,9 +73,10 @@ def test_small_fp32_workload():
     _compare(out, aq, sa, bq, sw, 0)
 
 
-# N % 256 == 0 runs the dense kernel with two CTAs per cluster sharing B:
-# (1, 256, 128) and (257, 512, 384) give clusters whose second CTA has no
-# valid row, (640, 768, 256) an odd number of 128-row blocks.
+# N % 256 == 0 runs the dense kernel on CTA pairs when there is more than one
+# 128-row block: (257, 512, 384) gives a pair whose second CTA has no valid
+# row, (640, 768, 256) an odd number of 128-row blocks; (1, 256, 128), a
+# single row block, runs one CTA per 128 x 128 tile.
 SHAPES = [(1, 128, 128), (37, 384, 256), (130, 256, 1024), (257, 512, 384), (300, 640, 128),
           (1, 256, 128), (640, 768, 256)]
 
