@@ -99,6 +99,18 @@ def test_argument_checks():
     assert e.value.status == 2
 
 
+def test_more_chunks_than_resident_ctas():
+    """40000 tokens make 625 chunks of 64: more (chunk, K slice) CTAs than fit on
+    the GPU at once even with one K slice per chunk, so the pack launch runs in
+    more than one wave; skewed top-8 routing over 256 experts, 32 local."""
+    T, K = 40000, 256
+    g = torch.Generator().manual_seed(15)
+    x = inputs.act(T, K, g)
+    ids = inputs.moe_topk(T, 256, 8, g)
+    R = _check(x, ids.numpy(), 0, 32)
+    assert R > 1000
+
+
 def test_workspace_reused_without_initialisation():
     T, K = 400, 256
     g = torch.Generator().manual_seed(14)
